@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked gated delta rule on one or more GB300 GPUs.
+
+One step = one full pass of the hot path over one synthetic batch: gdn_chunk_fwd for the
+forward workloads (planner, context-parallel phase A + fix-up when used, output stage),
+gdn_chunk_fwd + gdn_chunk_bwd for the training-step workload.  Prints ONE JSON line on
+rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own copy of the workload (the
+(sequence, head) problems are independent, so there is no data-path collective; scaling is
+weak); value = tokens of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunked_prefill_gb300 import roofline as rl  # noqa: E402
+from chunked_prefill_gb300.inputs import WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "GDN chunked fwd & fwd+bwd ms at T=32768 (tokens/s), % of roofline"
+DEFAULT_WORKLOAD = "fwd_t32k_hqk2_hv8"
+# FlashQLA's published H200 forward latency for 1 x 32768 tokens, h_qk = 2, h_v = 8
+# (agentlenshq page, benchmark table, TP8 row): context only, another machine.
+PUBLISHED_MS = {"fwd_t32k_hqk2_hv8": 0.310, "fwd_t32k_hqk8_hv24": 0.659}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def lengths_of(inp):
+    if inp.cu_seqlens is None:
+        return [inp.meta["T"]] * inp.meta["B"]
+    cu = inp.cu_seqlens.tolist()
+    return [b - a for a, b in zip(cu[:-1], cu[1:])]
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.rows = []
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) == 7:
+                self.rows.append(f)
+
+    def summary(self):
+        rows = getattr(self, "rows", [])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def make_step(inp, dev, backward):
+    from chunked_prefill_gb300 import gdn
+    d = {n: (None if getattr(inp, n) is None else getattr(inp, n).to(dev).contiguous())
+         for n in ("q", "k", "v", "g", "beta", "h0", "dO", "dht")}
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
+    cu_host = inp.cu_seqlens
+    o = torch.empty_like(d["v"])
+    prob = gdn.Problem(d["q"], d["v"], inp.scale, cu, cu_host)
+    ht = torch.empty(prob.num_seqs, d["v"].shape[2], 128, 128, device=dev)
+    ws_f = torch.empty(max(gdn.gdn_chunk_fwd_workspace_size(prob), 16), dtype=torch.uint8, device=dev)
+    bufs = None
+    ws_b = None
+    if backward:
+        ws_b = torch.empty(max(gdn.gdn_chunk_bwd_workspace_size(prob), 16), dtype=torch.uint8,
+                           device=dev)
+        bufs = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
+                torch.empty_like(d["g"]), torch.empty_like(d["beta"]),
+                torch.empty_like(ht))
+
+    def step():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, h0=d["h0"],
+                          cu_seqlens=cu, cu_seqlens_host=cu_host, o=o, ht=ht, workspace=ws_f)
+        if backward:
+            gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, d["dO"],
+                              h0=d["h0"], dht=d["dht"], cu_seqlens=cu, cu_seqlens_host=cu_host,
+                              workspace=ws_b, out=bufs)
+    return step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs
+
+
+def time_steps(step, K, flush):
+    evs = []
+    for _ in range(K):
+        flush.zero_()  # overwrite a buffer larger than L2 between timed steps
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+def e2e_run(inp, dev, K, W, backward):
+    """The same step through the public API with HOST buffers: pinned host inputs copied in,
+    the call, the result copied out, all inside the timed region."""
+    from chunked_prefill_gb300 import gdn
+    names = ["q", "k", "v", "g", "beta", "h0"] + (["dO", "dht"] if backward else [])
+    host = {n: getattr(inp, n).pin_memory() for n in names if getattr(inp, n) is not None}
+    devb = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs = make_step(inp, dev, backward)
+    outs = [o, ht] if not backward else [o, ht] + [b for b in bufs if b is not None]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for n, t in host.items():
+            devb[n].copy_(t, non_blocking=True)
+        gdn.gdn_chunk_fwd(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"], inp.scale,
+                          h0=devb.get("h0"), cu_seqlens=cu, cu_seqlens_host=cu_host, o=o, ht=ht,
+                          workspace=ws_f)
+        if backward:
+            gdn.gdn_chunk_bwd(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"], inp.scale,
+                              devb["dO"], h0=devb.get("h0"), dht=devb.get("dht"), cu_seqlens=cu,
+                              cu_seqlens_host=cu_host, workspace=ws_b, out=bufs)
+        for src, dst in zip(outs, host_out):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(W):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        e2e_step()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / K, h2d, d2h
+
+
+def oracle_sample(inp, budget_s, backward, max_steps=1):
+    """Time the fp64 oracle on the first n tokens of every sequence, n sized so that one
+    call takes about budget_s seconds.  Returns (tokens/s, tokens, seconds, threads)."""
+    from oracle import oracle as orc
+    lens = lengths_of(inp)
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+
+    def sub(n):
+        idx = []
+        new_cu = [0]
+        for a, L in zip(cu[:-1], lens):
+            m = min(n, L)
+            idx.extend(range(a, a + m))
+            new_cu.append(new_cu[-1] + m)
+        it = torch.tensor(idx, dtype=torch.long)
+        f = lambda t: None if t is None else t.reshape((-1,) + tuple(t.shape[2:]))[it].unsqueeze(0)
+        return [f(inp.q), f(inp.k), f(inp.v), f(inp.g), f(inp.beta), f(inp.dO)], new_cu
+
+    def run(n):
+        (q, k, v, g, b, dO), c = sub(n)
+        t0 = time.perf_counter()
+        orc.fwd(q, k, v, g, b, inp.scale, h0=inp.h0, cu_seqlens=c)
+        if backward:
+            orc.bwd(q, k, v, g, b, inp.scale, dO, h0=inp.h0, dht=inp.dht, cu_seqlens=c)
+        return time.perf_counter() - t0, c[-1]
+
+    dt, toks = run(64)
+    n = 64
+    while dt < budget_s / 4 and n < max(lens):
+        n = min(max(lens), n * 4)
+        dt, toks = run(n)
+    if dt < budget_s and n < max(lens):
+        n = min(max(lens), int(n * budget_s / max(dt, 1e-3)))
+        dt, toks = run(n)
+    return toks / dt, toks, dt, orc.max_threads(), n
+
+
+def reference_arm(args, world, rank):
+    """The oracle as it stands, on the host cores: W untimed + K timed steps, each one call
+    on a fixed bounded sample of the workload (rank 0 only)."""
+    if rank != 0:
+        return
+    inp = workload_inputs(args.workload)
+    w = WORKLOADS[args.workload]
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    _, _, _, thr, n = oracle_sample(inp, per_step, w.backward)
+    lens = lengths_of(inp)
+    timed = []
+    for i in range(args.warmup + args.steps):
+        _, tk, d, thr, _ = oracle_sample_fixed(inp, n, w.backward)
+        if i >= args.warmup:
+            timed.append((tk, d))
+    tot_t = sum(d for _, d in timed)
+    value = sum(tk for tk, _ in timed) / tot_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * tot_t / len(timed), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(args.workload),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                         "sample": f"first {n} tokens of each of {len(lens)} sequence(s), all "
+                                   f"{w.Hv} v-heads, per step ({'fwd+bwd' if w.backward else 'fwd'})"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def oracle_sample_fixed(inp, n, backward):
+    from oracle import oracle as orc
+    lens = lengths_of(inp)
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    idx, new_cu = [], [0]
+    for a, L in zip(cu[:-1], lens):
+        m = min(n, L)
+        idx.extend(range(a, a + m))
+        new_cu.append(new_cu[-1] + m)
+    it = torch.tensor(idx, dtype=torch.long)
+    f = lambda t: None if t is None else t.reshape((-1,) + tuple(t.shape[2:]))[it].unsqueeze(0)
+    q, k, v, g, b, dO = (f(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta, inp.dO))
+    t0 = time.perf_counter()
+    orc.fwd(q, k, v, g, b, inp.scale, h0=inp.h0, cu_seqlens=new_cu)
+    if backward:
+        orc.bwd(q, k, v, g, b, inp.scale, dO, h0=inp.h0, dht=inp.dht, cu_seqlens=new_cu)
+    dt = time.perf_counter() - t0
+    return new_cu[-1] / dt, new_cu[-1], dt, orc.max_threads(), n
+
+
+def config_of(name):
+    w = WORKLOADS[name]
+    c = {"workload": name, "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv, "K": w.K, "V": w.V,
+         "chunk": 64, "pass": "fwd+bwd" if w.backward else "fwd",
+         "h0": w.h0_std > 0, "final_state": True,
+         "l2": "flushed between timed steps (256 MiB write)", "cp": "auto (exact)"}
+    if w.varlen_seqs:
+        c["varlen_seqs"] = w.varlen_seqs
+    return c
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup(args.gpus)
+
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+
+    from chunked_prefill_gb300 import build, gdn
+    build.build()
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    inp = workload_inputs(args.workload)
+    lens = lengths_of(inp)
+    tokens = sum(lens)
+    step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs = make_step(inp, dev, w.backward)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    gdn.gdn_timing_enable(True)
+    with ClockSampler(local) as clk:
+        ms_total = time_steps(step, args.steps, flush)
+    gdn.gdn_timing_enable(False)
+    kt = gdn.gdn_timing_collect()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_per_step = ms_total / args.steps
+    value = world * tokens / (ms_per_step / 1000.0)
+
+    pk, pk_kind = peaks()
+    fl = rl.fwd_flops(lens, w.Hqk, w.Hv) + (rl.bwd_flops(lens, w.Hqk, w.Hv) if w.backward else 0)
+    by = rl.fwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
+    if w.backward:
+        by += rl.bwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
+    t_roof = max(fl / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+
+    # dominant kernel and its roofline
+    launches = sum(v[0] for v in kt.values())
+    dom = max(kt.items(), key=lambda kv: kv[1][1]) if kt else ("none", (1, float("nan")))
+    dom_name, (dom_n, dom_ms) = dom
+    dom_avg_s = dom_ms / max(dom_n, 1) / 1000.0
+    if dom_name in ("fwd_phase_c",):
+        alg = rl.fwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
+        unit_note = "compulsory forward bytes (q,k,v,g,beta,h0 read; o,ht written)"
+    elif dom_name == "fwd_phase_a":
+        alg = (tokens * w.Hqk * 128 * 2 + tokens * w.Hv * (128 * 2 + 8))
+        unit_note = "k, v, g, beta of the sequence read once"
+    else:
+        alg = by
+        unit_note = "compulsory bytes of the step"
+    achieved = alg / dom_avg_s / 1e9
+    roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+            "peak_kind": pk_kind, "algorithmic_bytes_per_launch": alg, "bytes_counted": unit_note,
+            "avg_launch_ms": dom_avg_s * 1000.0,
+            "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items()}}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / (tokens / (PUBLISHED_MS[args.workload] / 1000.0))
+                        if args.workload in PUBLISHED_MS and world == 1 else None),
+        "dtype": "bf16", "data": "synthetic", "config": config_of(args.workload),
+        "roofline": roof,
+        "step_roofline": {"flops": fl, "bytes": by, "roofline_ms": t_roof * 1000.0,
+                          "frac": t_roof * 1000.0 / ms_per_step, "peak_kind": pk_kind},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_run(inp, dev, args.steps, args.warmup, w.backward)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        line["e2e"] = {"value": world * tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, toks, dt, thr, n = oracle_sample(inp, 10.0, w.backward)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": f"first {n} tokens of each of {len(lens)} sequence(s), "
+                                          f"all {w.Hv} v-heads ({toks} tokens, {dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

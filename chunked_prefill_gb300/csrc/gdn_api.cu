@@ -1,0 +1,257 @@
+// C ABI of the GDN library: argument validation, the host-side planner (segment length for
+// intra-GPU context parallelism), workspace layout and kernel launches.  Nothing here
+// allocates, frees or synchronises.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+gdn_status fail(gdn_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return n > 0 ? n : 148;
+}
+
+// Host plan of one call.
+struct HostPlan {
+    int N = 0;              // sequences
+    int C = 64;             // chunk size
+    int L = 1;              // chunks per segment
+    int warmup = 0;
+    int cp = gdn::CP_NONE;
+    int total_segs = 0;
+    int total_chunks = 0;
+    int max_nseg = 0;
+    int64_t total_tokens = 0;
+    // workspace layout (bytes)
+    size_t off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0, off_mbuf = 0,
+           off_end = 0;
+};
+
+constexpr size_t KVB = size_t(128) * 128 * 4;
+
+gdn_status validate_problem(const gdn_problem* p) {
+    if (!p) return fail(GDN_ERR_INVALID_ARG, "problem is NULL");
+    if (p->K <= 0 || p->V <= 0) return fail(GDN_ERR_INVALID_ARG, "K and V must be positive");
+    if (p->K != 128 || p->V != 128)
+        return fail(GDN_ERR_UNSUPPORTED, "only K = V = 128 is implemented (got K=%d V=%d)", p->K,
+                    p->V);
+    if (p->Hqk <= 0 || p->Hv <= 0) return fail(GDN_ERR_INVALID_ARG, "Hqk and Hv must be positive");
+    if (p->Hv % p->Hqk != 0)
+        return fail(GDN_ERR_INVALID_ARG, "Hv (%d) must be a multiple of Hqk (%d)", p->Hv, p->Hqk);
+    if (p->dtype != GDN_BF16 && p->dtype != GDN_FP32)
+        return fail(GDN_ERR_INVALID_ARG, "dtype must be GDN_BF16 or GDN_FP32");
+    if (!isfinite(p->scale)) return fail(GDN_ERR_INVALID_ARG, "scale must be finite");
+    if (p->T < 0 || p->B < 0) return fail(GDN_ERR_INVALID_ARG, "B and T must be >= 0");
+    if (p->cp_mode < GDN_CP_AUTO || p->cp_mode > GDN_CP_WARMUP)
+        return fail(GDN_ERR_INVALID_ARG, "unknown cp_mode %d", p->cp_mode);
+    if (p->cp_segment_chunks < 0 || p->warmup_chunks < 0 || !(p->cp_lambda >= 0.f))
+        return fail(GDN_ERR_INVALID_ARG, "cp_segment_chunks, warmup_chunks, cp_lambda must be >= 0");
+    if ((p->cu_seqlens == nullptr) != (p->cu_seqlens_host == nullptr))
+        return fail(GDN_ERR_INVALID_ARG, "cu_seqlens and cu_seqlens_host go together");
+    if (p->cu_seqlens) {
+        if (p->B != 1) return fail(GDN_ERR_INVALID_ARG, "varlen needs B == 1 (got %d)", p->B);
+        if (p->num_seqs < 1) return fail(GDN_ERR_INVALID_ARG, "num_seqs must be >= 1");
+        if (!aligned16(p->cu_seqlens) && (reinterpret_cast<uintptr_t>(p->cu_seqlens) & 3u))
+            return fail(GDN_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+        const int32_t* cu = p->cu_seqlens_host;
+        if (cu[0] != 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
+        for (int s = 0; s < p->num_seqs; ++s)
+            if (cu[s + 1] < cu[s])
+                return fail(GDN_ERR_INVALID_ARG, "cu_seqlens must be non-decreasing (at %d)", s);
+        if (cu[p->num_seqs] != p->T)
+            return fail(GDN_ERR_INVALID_ARG, "cu_seqlens[num_seqs] (%d) must equal T (%d)",
+                        cu[p->num_seqs], p->T);
+    }
+    return GDN_OK;
+}
+
+// Segment length: FlashQLA's AutoCP model L = lambda * sqrt(N) (N = chunks of a sequence,
+// L = chunks per CP rank), used only when sequences x heads leave SMs idle.
+void plan(const gdn_problem* p, HostPlan& h) {
+    h.C = gdn::fwd_chunk_size(p->dtype);
+    h.N = p->cu_seqlens ? p->num_seqs : p->B;
+    int nt_max = 0;
+    int64_t total_chunks = 0;
+    for (int s = 0; s < h.N; ++s) {
+        const int len = p->cu_seqlens ? p->cu_seqlens_host[s + 1] - p->cu_seqlens_host[s] : p->T;
+        const int nt = (len + h.C - 1) / h.C;
+        nt_max = std::max(nt_max, nt);
+        total_chunks += nt;
+    }
+    h.total_tokens = p->cu_seqlens ? p->T : int64_t(p->B) * p->T;
+    int L = std::max(nt_max, 1);
+    h.cp = gdn::CP_NONE;
+    const int units = h.N * p->Hv;
+    const float lam = p->cp_lambda > 0.f ? p->cp_lambda : 1.0f;
+    const int autoL = std::max(1, int(ceilf(lam * sqrtf(float(std::max(nt_max, 1))))));
+    switch (p->cp_mode) {
+        case GDN_CP_OFF:
+            break;
+        case GDN_CP_AUTO:
+            if (units < sm_count()) L = autoL;
+            break;
+        case GDN_CP_EXACT:
+        case GDN_CP_WARMUP:
+            L = p->cp_segment_chunks > 0 ? p->cp_segment_chunks : autoL;
+            break;
+    }
+    L = std::max(1, std::min(L, std::max(nt_max, 1)));
+    int total_segs = 0, max_nseg = 0;
+    for (int s = 0; s < h.N; ++s) {
+        const int len = p->cu_seqlens ? p->cu_seqlens_host[s + 1] - p->cu_seqlens_host[s] : p->T;
+        const int nt = (len + h.C - 1) / h.C;
+        const int ns = std::max(1, (nt + L - 1) / L);
+        total_segs += ns;
+        max_nseg = std::max(max_nseg, ns);
+    }
+    h.L = L;
+    h.total_segs = total_segs;
+    h.total_chunks = int(total_chunks);
+    h.max_nseg = max_nseg;
+    if (max_nseg > 1) h.cp = (p->cp_mode == GDN_CP_WARMUP) ? gdn::CP_WARMUP : gdn::CP_EXACT;
+    h.warmup = p->warmup_chunks > 0 ? p->warmup_chunks : 8;
+
+    size_t off = 0;
+    h.off_seg = off;
+    off = align_up(off + sizeof(int2) * size_t(total_segs), 256);
+    h.off_segoff = off;
+    off = align_up(off + sizeof(int) * size_t(h.N + 1), 256);
+    h.off_chunkoff = off;
+    off = align_up(off + sizeof(int) * size_t(h.N + 1), 256);
+    h.off_hin = off;
+    if (h.cp != gdn::CP_NONE) off += KVB * size_t(total_segs) * p->Hv;
+    h.off_mbuf = off;
+    if (h.cp == gdn::CP_EXACT) off += KVB * size_t(total_segs) * p->Hv;
+    h.off_end = align_up(off, 256);
+}
+
+void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Problem& P) {
+    P.plan.seg = reinterpret_cast<int2*>(ws + h.off_seg);
+    P.plan.seg_off = reinterpret_cast<int*>(ws + h.off_segoff);
+    P.plan.chunk_off = reinterpret_cast<int*>(ws + h.off_chunkoff);
+    P.hin = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_hin) : nullptr;
+    P.mbuf = h.cp == gdn::CP_EXACT ? reinterpret_cast<float*>(ws + h.off_mbuf) : nullptr;
+    P.cu = p->cu_seqlens;
+    P.N = h.N;
+    P.T = p->T;
+    P.Hqk = p->Hqk;
+    P.Hv = p->Hv;
+    P.total_segs = h.total_segs;
+    P.total_chunks = h.total_chunks;
+    P.L = h.L;
+    P.warmup = h.warmup;
+    P.cp = h.cp;
+    P.scale = p->scale;
+}
+
+gdn_status check_ptrs(std::initializer_list<const void*> required,
+                      std::initializer_list<const void*> optional) {
+    for (const void* x : required) {
+        if (!x) return fail(GDN_ERR_INVALID_ARG, "a required tensor pointer is NULL");
+        if (!aligned16(x)) return fail(GDN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    }
+    for (const void* x : optional)
+        if (x && !aligned16(x))
+            return fail(GDN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_last_error(void) { return g_err; }
+
+gdn_status gdn_chunk_fwd_workspace_size(const gdn_problem* p, size_t* bytes) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    if (!bytes) return fail(GDN_ERR_INVALID_ARG, "bytes is NULL");
+    HostPlan h;
+    plan(p, h);
+    *bytes = h.off_end;
+    g_err[0] = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* h0, void* o,
+                         float* ht, void* workspace, size_t workspace_bytes, void* stream) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    HostPlan h;
+    plan(p, h);
+    if (h.total_tokens > 0) {
+        st = check_ptrs({q, k, v, g, beta, o}, {h0, ht});
+    } else {
+        st = check_ptrs({}, {q, k, v, g, beta, o, h0, ht});
+    }
+    if (st != GDN_OK) return st;
+    if (h.N == 0) {
+        g_err[0] = 0;
+        return GDN_OK;
+    }
+    if (!workspace || workspace_bytes < h.off_end)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", h.off_end,
+                    workspace ? workspace_bytes : size_t(0));
+    if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    gdn::Problem P{};
+    P.q = q;
+    P.k = k;
+    P.v = v;
+    P.g = g;
+    P.beta = beta;
+    P.h0 = h0;
+    P.o = o;
+    P.ht = ht;
+    fill_problem(p, h, static_cast<char*>(workspace), P);
+    cudaError_t e = gdn::launch_fwd(P, p->dtype, false, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+    g_err[0] = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_bwd_workspace_size(const gdn_problem* p, size_t* bytes) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    if (!bytes) return fail(GDN_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = 0;
+    return fail(GDN_ERR_UNSUPPORTED, "backward not built yet");
+}
+
+gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* h0, const void* dO,
+                         const float* dht, void* dq, void* dk, void* dv, float* dg,
+                         float* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    (void)q; (void)k; (void)v; (void)g; (void)beta; (void)h0; (void)dO; (void)dht; (void)dq;
+    (void)dk; (void)dv; (void)dg; (void)dbeta; (void)dh0; (void)workspace; (void)workspace_bytes;
+    (void)stream;
+    return fail(GDN_ERR_UNSUPPORTED, "backward not built yet");
+}
+
+}  // extern "C"

@@ -1,0 +1,20 @@
+// Internal launch interface between the C ABI layer and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "gdn_plan.h"
+
+namespace gdn {
+
+// Chunk size of the kernels for a dtype (bf16: 64; fp32 test mode: 32).
+int fwd_chunk_size(int dtype);
+
+// Plan kernel + (phase A + fix-up when P.cp != CP_NONE) + phase C.  hist=true replaces
+// the output stage by a store of every chunk's entering state into P.hist.
+cudaError_t launch_fwd(const Problem& P, int dtype, bool hist, cudaStream_t st);
+
+// Per-kernel event timing hooks (no-ops unless gdn_timing_enable(1)).
+void timing_begin(const char* name, cudaStream_t st);
+void timing_end(cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,44 @@
+// Host/device shared description of one call's work decomposition.
+//
+// Each sequence s has NT_s = ceil(len_s / C) chunks, split into nseg_s = max(1,
+// ceil(NT_s / L)) segments of L chunks (FlashQLA pages, "AutoCP": CP ranks of L chunks
+// each).  Segments of all sequences are numbered globally; seg_off[s] is the first global
+// segment of sequence s and chunk_off[s] its first global chunk.
+#pragma once
+#include <stdint.h>
+
+namespace gdn {
+
+enum CpKind { CP_NONE = 0, CP_EXACT = 1, CP_WARMUP = 2 };
+
+struct PlanDev {
+    int2* seg;          // [total_segs] (sequence, local segment index)
+    int* seg_off;       // [N+1]
+    int* chunk_off;     // [N+1]
+};
+
+struct Problem {
+    // tensors
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    const float* h0;    // [N, Hv, K, V] or null
+    void* o;
+    float* ht;          // [N, Hv, K, V] or null
+    // workspace
+    float* hin;         // [total_segs, Hv, K, V]  entering state of each segment
+    float* mbuf;        // [total_segs, Hv, K, K]  segment transitions (exact CP)
+    void* hist;         // [total_chunks, Hv, K, V] entering state of every chunk (bwd)
+    PlanDev plan;
+    const int* cu;      // device cu_seqlens or null
+    int N, T, Hqk, Hv;
+    int total_segs, total_chunks;
+    int L;              // chunks per segment
+    int warmup;         // warm-up chunks (CP_WARMUP)
+    int cp;             // CpKind
+    float scale;
+};
+
+}  // namespace gdn

@@ -1,0 +1,253 @@
+"""Thin Python binding of libgdn.so (argument marshalling only; every step of the
+computation runs in the library's CUDA kernels).
+
+The names follow the C ABI (``gdn_chunk_fwd``, ``gdn_chunk_bwd``, ``*_workspace_size``)
+and, on top, the FlashQLA pages' high-level call (aisparkup page, "usage":
+``chunk_gated_delta_rule(q, k, v, g, beta, scale, initial_state, output_final_state,
+cu_seqlens) -> (o, final_state)``) as a ``torch.autograd.Function``.
+
+PyTorch supplies device memory and the stream; the library never allocates.  When
+libgdn.so is missing this module raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA = range(5)
+GDN_BF16, GDN_FP32 = 0, 1
+CP_AUTO, CP_OFF, CP_EXACT, CP_WARMUP = 0, 1, 2, 3
+_STATUS = {1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE",
+           4: "GDN_ERR_CUDA"}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class GdnProblem(ctypes.Structure):
+    """Mirror of ``gdn_problem`` in include/gdn.h."""
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Hqk", ctypes.c_int32),
+                ("Hv", ctypes.c_int32), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("cu_seqlens", ctypes.c_void_p), ("cu_seqlens_host", ctypes.c_void_p),
+                ("num_seqs", ctypes.c_int32), ("cp_mode", ctypes.c_int32),
+                ("cp_segment_chunks", ctypes.c_int32), ("warmup_chunks", ctypes.c_int32),
+                ("cp_lambda", ctypes.c_float)]
+
+
+class GdnKernelTime(ctypes.Structure):
+    """Mirror of ``gdn_kernel_time``."""
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int32),
+                ("total_ms", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libgdn.so (built in-tree by ``chunked_prefill_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m chunked_prefill_gb300.build` (no fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, P = ctypes.c_void_p, ctypes.POINTER(GdnProblem)
+        L.gdn_chunk_fwd_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+        L.gdn_chunk_bwd_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+        L.gdn_chunk_fwd.argtypes = [P] + [vp] * 9 + [ctypes.c_size_t, vp]
+        L.gdn_chunk_bwd.argtypes = [P] + [vp] * 15 + [ctypes.c_size_t, vp]
+        for f in ("gdn_chunk_fwd_workspace_size", "gdn_chunk_bwd_workspace_size",
+                  "gdn_chunk_fwd", "gdn_chunk_bwd"):
+            getattr(L, f).restype = ctypes.c_int
+        L.gdn_last_error.restype = ctypes.c_char_p
+        L.gdn_timing_enable.argtypes = [ctypes.c_int32]
+        L.gdn_timing_enable.restype = ctypes.c_int
+        L.gdn_timing_collect.argtypes = [ctypes.POINTER(GdnKernelTime), ctypes.c_int32,
+                                         ctypes.POINTER(ctypes.c_int32)]
+        L.gdn_timing_collect.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != GDN_OK:
+        raise GdnError(rc, lib().gdn_last_error().decode())
+
+
+def gdn_timing_enable(on: bool = True):
+    """Bracket every library kernel launch with CUDA events (see include/gdn.h)."""
+    _check(lib().gdn_timing_enable(1 if on else 0))
+
+
+def gdn_timing_collect() -> dict:
+    """{kernel name: (launches, total ms)} since the last collect; waits on the events."""
+    buf = (GdnKernelTime * 64)()
+    n = ctypes.c_int32(0)
+    _check(lib().gdn_timing_collect(buf, 64, ctypes.byref(n)))
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+            for i in range(min(n.value, 64))}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return GDN_BF16
+    if dt == torch.float32:
+        return GDN_FP32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {dt}")
+
+
+class Problem:
+    """A ``gdn_problem`` plus the host copy of cu_seqlens it points to (kept alive)."""
+
+    def __init__(self, q, v, scale, cu_seqlens=None, cu_seqlens_host=None, cp_mode=CP_AUTO,
+                 cp_segment_chunks=0, warmup_chunks=0, cp_lambda=0.0):
+        B, T, Hqk, K = q.shape
+        Hv, V = v.shape[2], v.shape[3]
+        p = GdnProblem(B=B, T=T, Hqk=Hqk, Hv=Hv, K=K, V=V, dtype=_dtype_code(q.dtype),
+                       scale=float(scale), cp_mode=cp_mode, cp_segment_chunks=cp_segment_chunks,
+                       warmup_chunks=warmup_chunks, cp_lambda=cp_lambda)
+        self._cu_host = None
+        self.num_seqs = B
+        if cu_seqlens is not None:
+            if cu_seqlens_host is None:
+                cu_seqlens_host = cu_seqlens.detach().to("cpu")
+            self._cu_host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+            self._cu_dev = cu_seqlens
+            p.cu_seqlens = cu_seqlens.data_ptr()
+            p.cu_seqlens_host = self._cu_host.data_ptr()
+            p.num_seqs = self._cu_host.numel() - 1
+            self.num_seqs = p.num_seqs
+        self.p = p
+        self.Hv, self.K, self.V = Hv, K, V
+
+    def ref(self):
+        return ctypes.byref(self.p)
+
+
+def gdn_chunk_fwd_workspace_size(prob: Problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().gdn_chunk_fwd_workspace_size(prob.ref(), ctypes.byref(n)))
+    return n.value
+
+
+def gdn_chunk_bwd_workspace_size(prob: Problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().gdn_chunk_bwd_workspace_size(prob.ref(), ctypes.byref(n)))
+    return n.value
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is not None and workspace.numel() * workspace.element_size() >= nbytes:
+        return workspace
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def _validate_tensors(q, k, v, g, beta):
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if k.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q and k must match in shape; q, k, v in dtype")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise ValueError("g and beta must be float32")
+    if g.shape != v.shape[:3] or beta.shape != v.shape[:3]:
+        raise ValueError("g and beta must be [B, T, Hv]")
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, scale, h0=None, output_final_state=True, cu_seqlens=None,
+                  cu_seqlens_host=None, cp_mode=CP_AUTO, cp_segment_chunks=0, warmup_chunks=0,
+                  cp_lambda=0.0, o=None, ht=None, workspace=None, stream=None):
+    """Forward through the C ABI.  Returns (o, ht); ht is None unless requested."""
+    _validate_tensors(q, k, v, g, beta)
+    prob = Problem(q, v, scale, cu_seqlens, cu_seqlens_host, cp_mode, cp_segment_chunks,
+                   warmup_chunks, cp_lambda)
+    if o is None:
+        o = torch.empty_like(v)
+    if ht is None and output_final_state:
+        ht = torch.empty(prob.num_seqs, prob.Hv, prob.K, prob.V, device=q.device,
+                         dtype=torch.float32)
+    if h0 is not None:
+        h0 = h0.contiguous().float()
+    nbytes = gdn_chunk_fwd_workspace_size(prob)
+    ws = _workspace(nbytes, q.device, workspace)
+    _check(lib().gdn_chunk_fwd(prob.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               _ptr(h0), _ptr(o), _ptr(ht), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)))
+    return o, ht
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, scale, dO, h0=None, dht=None, cu_seqlens=None,
+                  cu_seqlens_host=None, cp_mode=CP_AUTO, cp_segment_chunks=0, warmup_chunks=0,
+                  cp_lambda=0.0, want_dh0=True, workspace=None, stream=None, out=None):
+    """Backward through the C ABI.  Returns (dq, dk, dv, dg, dbeta, dh0)."""
+    _validate_tensors(q, k, v, g, beta)
+    if dO.shape != v.shape or dO.dtype != v.dtype or not dO.is_contiguous():
+        raise ValueError("dO must be contiguous and match v")
+    prob = Problem(q, v, scale, cu_seqlens, cu_seqlens_host, cp_mode, cp_segment_chunks,
+                   warmup_chunks, cp_lambda)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dg, db = torch.empty_like(g), torch.empty_like(beta)
+        dh0 = (torch.empty(prob.num_seqs, prob.Hv, prob.K, prob.V, device=q.device)
+               if want_dh0 else None)
+    else:
+        dq, dk, dv, dg, db, dh0 = out
+    if h0 is not None:
+        h0 = h0.contiguous().float()
+    if dht is not None:
+        dht = dht.contiguous().float()
+    nbytes = gdn_chunk_bwd_workspace_size(prob)
+    ws = _workspace(nbytes, q.device, workspace)
+    _check(lib().gdn_chunk_bwd(prob.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               _ptr(h0), _ptr(dO), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv),
+                               _ptr(dg), _ptr(db), _ptr(dh0), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)))
+    return dq, dk, dv, dg, db, dh0
+
+
+class _ChunkGDN(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, h0, scale, output_final_state, cu_seqlens):
+        o, ht = gdn_chunk_fwd(q, k, v, g, beta, scale, h0=h0,
+                              output_final_state=output_final_state, cu_seqlens=cu_seqlens)
+        ctx.save_for_backward(q, k, v, g, beta, h0, cu_seqlens)
+        ctx.scale = scale
+        return o, ht
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        q, k, v, g, beta, h0, cu = ctx.saved_tensors
+        dq, dk, dv, dg, db, dh0 = gdn_chunk_bwd(q, k, v, g, beta, ctx.scale, do.contiguous(),
+                                                h0=h0, dht=dht, cu_seqlens=cu,
+                                                want_dh0=h0 is not None)
+        return dq, dk, dv, dg, db, dh0, None, None, None
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None,
+                           output_final_state=False, cu_seqlens=None):
+    """High-level call with the FlashQLA/FLA signature; differentiable.
+    q, k [B,T,Hqk,K]; v [B,T,Hv,V]; g, beta [B,T,Hv] (fp32); initial_state [N,Hv,K,V]."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    return _ChunkGDN.apply(q, k, v, g, beta, initial_state, scale, output_final_state,
+                           cu_seqlens)

@@ -1,0 +1,141 @@
+/*
+ * gdn.h -- C ABI of the chunked gated delta rule (GDN) prefill library for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation (FlashQLA pages: agentlenshq "GDN chunked prefill optimisation" and the
+ * aisparkup "usage" section, which gives the high-level call
+ * chunk_gated_delta_rule(q, k, v, g, beta, scale, initial_state, output_final_state,
+ * cu_seqlens) -> (o, final_state) and the low-level forward/backward entry points):
+ *
+ *   per sequence, per v-head j (q/k head j / G, G = Hv / Hqk), state S_t in R^{V x K}:
+ *     S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = scale * S_t q_t
+ *   S_0 = initial state (zero when absent); the final state is S after the last token.
+ *
+ * States cross this ABI transposed, as h = S^T stored [K][V] (row-major, V fastest).
+ *
+ * Tensor layouts (row-major, contiguous; "T_total" = B*T, or T when varlen):
+ *   q, k      [T_total, Hqk, K]   dtype (bf16 or fp32)
+ *   v, o, dO  [T_total, Hv,  V]   dtype
+ *   g, beta   [T_total, Hv]       fp32   (g: natural-log decay, beta: write strength)
+ *   h0, ht, dht, dh0  [N_seq, Hv, K, V]  fp32
+ *   dq, dk    like q;  dv like v;  dg, dbeta like g (fp32)
+ *
+ * Conventions, for every entry point:
+ *   - Pointers are DEVICE pointers unless the field says host.  Every device pointer must
+ *     be 16-byte aligned.  The caller owns all memory; the library never allocates, frees
+ *     or synchronises.  Work is enqueued on `stream` (a cudaStream_t; NULL = legacy stream)
+ *     and runs asynchronously.
+ *   - Arguments are validated before anything is launched; on a non-OK status nothing has
+ *     been written and gdn_last_error() (thread-local) says why.
+ *   - Results are deterministic: repeated calls give bitwise-identical outputs.
+ *   - K = V = 128 only (GDN_ERR_UNSUPPORTED otherwise).
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment or cu_seqlens */
+    GDN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. K != 128) */
+    GDN_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the *_workspace_size */
+    GDN_ERR_CUDA = 4           /* a CUDA launch or attribute call failed */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
+
+/* Intra-GPU context parallelism over chunk ranges (FlashQLA pages, "AutoCP" section: when
+ * batch * heads leaves SMs idle, each sequence's chunks are split into segments). */
+typedef enum {
+    GDN_CP_AUTO = 0,    /* planner picks segment length L = lambda * sqrt(chunks); exact */
+    GDN_CP_OFF = 1,     /* one segment per sequence: a plain serial chunk scan */
+    GDN_CP_EXACT = 2,   /* segments of cp_segment_chunks chunks; transition fix-up, exact */
+    GDN_CP_WARMUP = 3   /* opt-in approximation: each segment starts warmup_chunks chunks
+                           early from a zero state instead of the exact fix-up (FlashQLA
+                           pages, "warm-up" paragraph: 6-8 chunks); NOT exact */
+} gdn_cp_mode;
+
+typedef struct gdn_problem {
+    int32_t B;                        /* batch; must be 1 when cu_seqlens is given */
+    int32_t T;                        /* tokens per sequence (total tokens when varlen) */
+    int32_t Hqk;                      /* q/k heads */
+    int32_t Hv;                       /* v heads; multiple of Hqk */
+    int32_t K;                        /* key dim (128) */
+    int32_t V;                        /* value dim (128) */
+    int32_t dtype;                    /* gdn_dtype of q, k, v, o, dO, dq, dk, dv */
+    float scale;                      /* output scale (> 0); usually K^-0.5 */
+    const int32_t* cu_seqlens;        /* device [num_seqs+1] or NULL (then B sequences of T) */
+    const int32_t* cu_seqlens_host;   /* HOST copy with the same contents; required iff
+                                         cu_seqlens != NULL (sizes the launch grids) */
+    int32_t num_seqs;                 /* N_seq when varlen */
+    int32_t cp_mode;                  /* gdn_cp_mode */
+    int32_t cp_segment_chunks;        /* EXACT / WARMUP: chunks per segment (0 = auto) */
+    int32_t warmup_chunks;            /* WARMUP: warm-up chunks (0 = 8) */
+    float cp_lambda;                  /* AUTO: lambda in L = lambda sqrt(N) (0 = default) */
+} gdn_problem;
+
+/* Bytes of device workspace gdn_chunk_fwd needs for *p (written to *bytes). */
+gdn_status gdn_chunk_fwd_workspace_size(const gdn_problem* p, size_t* bytes);
+
+/*
+ * Forward (FlashQLA pages: the low-level forward of the aisparkup "usage" section; the
+ * chunk-local prep, the chunk-serial state scan and the output stage of the agentlenshq
+ * "GDN chunked prefill" section).
+ *   h0  : initial states or NULL (zero).       o  : output, written for every token.
+ *   ht  : final states or NULL (not returned).
+ *   workspace: device scratch of at least gdn_chunk_fwd_workspace_size bytes (contents
+ *   are overwritten; it may be reused across calls on the same stream).
+ */
+gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* h0, void* o,
+                         float* ht, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace gdn_chunk_bwd needs for *p (written to *bytes). */
+gdn_status gdn_chunk_bwd_workspace_size(const gdn_problem* p, size_t* bytes);
+
+/*
+ * Backward (FlashQLA pages, agentlenshq "backward pass" paragraph: the dv, dh-scan,
+ * dq/dk/dw/dg and WY-backward steps).  Gradients of
+ *   L = <o, dO> + <ht, dht>
+ * with respect to q, k, v, g, beta and h0, for the forward defined above with the same
+ * inputs.  The forward intermediates are recomputed from q, k, v, g, beta, h0.
+ *   dht : NULL = zero.   dh0 : NULL = not returned.
+ *   dq, dk are summed over the G v-heads that share each q/k head.
+ */
+gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* h0, const void* dO,
+                         const float* dht, void* dq, void* dk, void* dv, float* dg,
+                         float* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Per-kernel timing (instrumentation for benchmarks; not needed for computation).
+ * While enabled, every kernel the library launches is bracketed by two CUDA events
+ * recorded on the launching stream.  gdn_timing_collect waits for the recorded events
+ * (it synchronises on them), sums the elapsed time per kernel name, writes up to
+ * max_entries records, sets *n_entries to the number of distinct kernels, releases the
+ * events and clears the record.  Not thread-safe: time one thread's calls at a time.
+ * ------------------------------------------------------------------------------------ */
+typedef struct gdn_kernel_time {
+    char name[48];     /* kernel name, e.g. "fwd_phase_c" */
+    int32_t launches;  /* launches recorded since the last collect */
+    float total_ms;    /* summed event-to-event time of those launches */
+} gdn_kernel_time;
+
+gdn_status gdn_timing_enable(int32_t enable);
+gdn_status gdn_timing_collect(gdn_kernel_time* out, int32_t max_entries, int32_t* n_entries);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* gdn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H */

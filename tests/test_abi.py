@@ -1,0 +1,110 @@
+"""The C ABI without a GPU: libgdn.so builds, loads, exports every function include/gdn.h
+declares, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from chunked_prefill_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    from chunked_prefill_gb300 import gdn
+    return gdn
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gdn_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_chunk_fwd_workspace_size",
+            "gdn_chunk_bwd_workspace_size", "gdn_last_error"} <= set(names)
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def problem(L, **kw):
+    base = dict(B=1, T=256, Hqk=2, Hv=4, K=128, V=128, dtype=0, scale=128 ** -0.5,
+                cp_mode=L.CP_OFF)
+    base.update(kw)
+    return L.GdnProblem(**base)
+
+
+def fwd_status(L, p, ptrs=None, ws_bytes=1 << 30):
+    fake = ctypes.c_void_p(0x10000)
+    args = ptrs or [fake] * 5 + [None, fake, fake, fake]  # q k v g beta h0 o ht ws
+    lib = L.lib()
+    rc = lib.gdn_chunk_fwd(ctypes.byref(p), *args[:8], args[8], ws_bytes, None)
+    return rc, lib.gdn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=64, V=64), 2),          # unsupported head dim
+    (dict(K=0), 1),
+    (dict(Hv=3), 1),                # Hv not a multiple of Hqk
+    (dict(dtype=7), 1),
+    (dict(T=-1), 1),
+    (dict(cp_mode=9), 1),
+    (dict(scale=float("nan")), 1),
+])
+def test_rejects_bad_problems(L, kw, code):
+    rc, msg = fwd_status(L, problem(L, **kw))
+    assert rc == code and msg
+
+
+def test_rejects_bad_cu_seqlens(L):
+    for cu in ([0, 100, 90, 256], [1, 100, 256], [0, 100, 200]):
+        host = (ctypes.c_int32 * len(cu))(*cu)
+        p = problem(L, cu_seqlens=0x10000, cu_seqlens_host=ctypes.addressof(host),
+                    num_seqs=len(cu) - 1)
+        rc, msg = fwd_status(L, p)
+        assert rc == 1, (cu, rc, msg)
+    p = problem(L, B=2, cu_seqlens=0x10000, cu_seqlens_host=0x10000, num_seqs=1)
+    assert fwd_status(L, p)[0] == 1
+    p = problem(L, cu_seqlens=0x10000)  # device copy without the host copy
+    assert fwd_status(L, p)[0] == 1
+
+
+def test_rejects_misaligned_and_null(L):
+    fake = ctypes.c_void_p(0x10000)
+    bad = ctypes.c_void_p(0x10002)
+    rc, _ = fwd_status(L, problem(L), [bad] + [fake] * 4 + [None, fake, fake, fake])
+    assert rc == 1
+    rc, _ = fwd_status(L, problem(L), [None] + [fake] * 4 + [None, fake, fake, fake])
+    assert rc == 1
+
+
+def test_workspace_size_and_too_small_workspace(L):
+    p = problem(L, T=32768, Hqk=2, Hv=8, cp_mode=L.CP_EXACT, cp_segment_chunks=16)
+    n = ctypes.c_size_t(0)
+    assert L.lib().gdn_chunk_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    # 32 segments x 8 heads x (entering state + transition) of 64 KiB each, plus the plan
+    assert n.value >= 2 * 32 * 8 * 128 * 128 * 4
+    rc, msg = fwd_status(L, p, ws_bytes=n.value - 1)
+    assert rc == 3 and "workspace" in msg
+    # no context parallelism: only the small plan arrays
+    p2 = problem(L, T=32768, Hqk=2, Hv=8, cp_mode=L.CP_OFF)
+    assert L.lib().gdn_chunk_fwd_workspace_size(ctypes.byref(p2), ctypes.byref(n)) == 0
+    assert n.value < 4096
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from chunked_prefill_gb300 import gdn
+    monkeypatch.setattr(gdn, "_lib", None)
+    monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        gdn.lib()

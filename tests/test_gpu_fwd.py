@@ -1,0 +1,112 @@
+"""GPU parity of the forward (gdn_chunk_fwd through the C ABI) against the fp64 oracle.
+
+Tolerances: max|err| <= 1e-2 max|ref| per output tensor for bf16 inputs with fp32
+accumulation, <= 1e-4 max|ref| in the fp32 test mode."""
+import numpy as np
+import pytest
+import torch
+
+from chunked_prefill_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+from oracle import chunked
+from tests.gpu_util import BF16_TOL, FP32_TOL, gpu_fwd, oracle_fwd, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from chunked_prefill_gb300 import build
+    build.build()
+
+
+def check(inp, tol, **kw):
+    o, ht = gpu_fwd(inp, **kw)
+    ro, rht = oracle_fwd(inp)
+    eo, eh = rel_err(o, ro), rel_err(ht, rht)
+    assert eo <= tol, f"o rel err {eo}"
+    assert eh <= tol, f"ht rel err {eh}"
+    return eo, eh
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+def test_small_workload(dtype, tol):
+    """B=1, T=256, 2 q/k heads shared by 4 v heads, h0 = 0: the small workload."""
+    check(workload_inputs("fwd_t256_hqk2_hv4", dtype=dtype), tol)
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+@pytest.mark.parametrize("B,T,Hqk,Hv,h0", [
+    (1, 1, 1, 1, True), (1, 63, 1, 3, False), (2, 64, 2, 2, True), (1, 65, 1, 2, True),
+    (3, 200, 1, 4, True), (1, 129, 3, 6, False),
+])
+def test_odd_shapes(dtype, tol, B, T, Hqk, Hv, h0):
+    inp = make_inputs(B, T, Hqk, Hv, seed=T * 7 + Hv, dtype=dtype, h0_std=0.1 if h0 else 0.0)
+    check(inp, tol, cp_mode=1)
+    check(inp, tol)  # planner's choice
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+def test_varlen_with_empty_and_partial_sequences(dtype, tol):
+    lens = [0, 1, 63, 64, 65, 130, 0, 7, 300]
+    inp = make_inputs(1, sum(lens), 2, 4, seed=5, dtype=dtype, h0_std=0.1, lengths=lens)
+    check(inp, tol, cp_mode=1)
+    check(inp, tol, cp_mode=2, cp_segment_chunks=1)
+    check(inp, tol, cp_mode=2, cp_segment_chunks=2)
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+@pytest.mark.parametrize("seg", [1, 2, 3, 5, 64])
+def test_context_parallel_exact(dtype, tol, seg):
+    """Exact intra-GPU context parallelism: any segment length gives the serial result."""
+    inp = make_inputs(1, 64 * 13 + 17, 1, 2, seed=11, dtype=dtype, h0_std=0.1)
+    check(inp, tol, cp_mode=2, cp_segment_chunks=seg)
+
+
+def test_warmup_mode_matches_its_own_definition_fp32():
+    """The opt-in warm-up mode is not exact; in the fp32 test mode it must equal the fp64
+    chunk-form warm-up (same chunk size, segment length and window) to 1e-4."""
+    inp = make_inputs(1, 32 * 24, 1, 2, seed=12, dtype=torch.float32, h0_std=0.1)
+    inp.g.mul_(0.05)  # mild decay: the warm-up error is far above rounding
+    o, ht = gpu_fwd(inp, cp_mode=3, cp_segment_chunks=4, warmup_chunks=2)
+    cu = None
+    ro, rht = chunked.fwd_cp(inp.q.double().numpy(), inp.k.double().numpy(),
+                             inp.v.double().numpy(), inp.g.double().numpy(),
+                             inp.beta.double().numpy(), inp.scale, h0=inp.h0.double().numpy(),
+                             cu_seqlens=cu, chunk=32, seg_chunks=4, warmup=2)
+    assert rel_err(o, ro) <= FP32_TOL
+    assert rel_err(ht, rht) <= FP32_TOL
+    # and it differs measurably from the exact result
+    eo, _ = oracle_fwd(inp)
+    assert rel_err(o, eo) > 1e-3
+
+
+def test_warmup_mode_error_reported_on_default_gates():
+    inp = make_inputs(1, 64 * 40, 1, 2, seed=13, dtype=torch.bfloat16, h0_std=0.1)
+    o, ht = gpu_fwd(inp, cp_mode=3, cp_segment_chunks=5, warmup_chunks=8)
+    ro, rht = oracle_fwd(inp)
+    print(f"warm-up mode error: o {rel_err(o, ro):.3e}  ht {rel_err(ht, rht):.3e}")
+    assert rel_err(o, ro) <= BF16_TOL and rel_err(ht, rht) <= BF16_TOL
+
+
+def test_no_final_state_and_determinism():
+    inp = make_inputs(1, 777, 2, 4, seed=14, h0_std=0.1)
+    o1, ht = gpu_fwd(inp, output_final_state=False)
+    assert ht is None
+    o2, _ = gpu_fwd(inp, output_final_state=False)
+    assert np.array_equal(o1, o2)
+
+
+def test_extreme_decay_and_zero_beta():
+    """Strong decay (gamma over a chunk far below -80) and beta = 0 rows."""
+    inp = make_inputs(1, 300, 1, 2, seed=15, h0_std=0.1, gate_scale=8.0)
+    inp.beta[:, ::3] = 0.0
+    check(inp, BF16_TOL)
+
+
+@pytest.mark.parametrize("name", ["fwd_t32k_hqk2_hv8", "fwd_t32k_hqk8_hv24",
+                                  "fwd_varlen16_64k_hqk4_hv16"])
+def test_full_size_workloads(name):
+    """The full-size forward workloads in the benchmark's launch configuration (AUTO)."""
+    check(workload_inputs(name), BF16_TOL)
