@@ -344,10 +344,16 @@ def main():
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    gdn.gdn_timing_enable(True)
     with ClockSampler(local) as clk:
+        # keep the GPU busy (untimed) while nvidia-smi starts, so the sampled clocks are
+        # those under load and its start-up does not overlap the timed steps
+        t_busy = time.time() + 1.0
+        while time.time() < t_busy:
+            step()
+            torch.cuda.synchronize()
+        gdn.gdn_timing_enable(True)
         ms_total = time_steps(step, args.steps, flush)
-    gdn.gdn_timing_enable(False)
+        gdn.gdn_timing_enable(False)
     kt = gdn.gdn_timing_collect()
     torch.cuda.synchronize()
     barrier(world)
