@@ -181,6 +181,11 @@ gdn_status check_ptrs(std::initializer_list<const void*> required,
 
 }  // namespace
 
+namespace gdn {
+// Message for gdn_last_error() from entry points defined in other files.
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+}  // namespace gdn
+
 extern "C" {
 
 const char* gdn_last_error(void) { return g_err; }

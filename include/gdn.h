@@ -132,6 +132,33 @@ typedef struct gdn_kernel_time {
 gdn_status gdn_timing_enable(int32_t enable);
 gdn_status gdn_timing_collect(gdn_kernel_time* out, int32_t max_entries, int32_t* n_entries);
 
+/* ------------------------------------------------------------------------------------
+ * Allocation-free forward.  The FlashQLA pages have no counterpart to this entry point: it
+ * exists for callers that cannot allocate device memory themselves -- a runtime that has
+ * handed all device memory to its own pool, a latency-critical loop where cudaMalloc or
+ * cudaFree may synchronise the device, or a plug-in interface that passes only inputs and
+ * outputs.  It computes exactly what gdn_chunk_fwd computes, with the same arguments minus
+ * the workspace.
+ *
+ * Its scratch is one fixed device array of GDN_NOALLOC_SCRATCH_BYTES inside the library;
+ * every GPU that loads the library holds that memory until the process exits.  Problems
+ * whose gdn_chunk_fwd_workspace_size exceeds it are rejected with GDN_ERR_WORKSPACE and a
+ * message (nothing is launched); fewer context-parallel segments (cp_mode /
+ * cp_segment_chunks) shrink the need.  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.  All calls
+ * share the one array and it keeps the last call's contents (every byte a call reads is
+ * written earlier by the same call), so calls whose GPU work overlaps -- on different
+ * streams, or from different threads -- race on it and must be serialised by the caller.
+ * ------------------------------------------------------------------------------------ */
+#define GDN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* p, const void* q, const void* k,
+                                 const void* v, const float* g, const float* beta,
+                                 const float* h0, void* o, float* ht, void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* gdn_last_error(void);
 
