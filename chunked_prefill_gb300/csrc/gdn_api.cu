@@ -4,6 +4,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -46,8 +47,8 @@ struct HostPlan {
     int max_nseg = 0;
     int64_t total_tokens = 0;
     // workspace layout (bytes)
-    size_t off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0, off_mbuf = 0,
-           off_end = 0;
+    size_t off_err = 0, off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0,
+           off_mbuf = 0, off_end = 0;
 };
 
 constexpr size_t KVB = size_t(128) * 128 * 4;
@@ -135,6 +136,8 @@ void plan(const gdn_problem* p, HostPlan& h) {
     h.warmup = p->warmup_chunks > 0 ? p->warmup_chunks : 8;
 
     size_t off = 0;
+    h.off_err = off;
+    off = align_up(off + sizeof(int), 256);
     h.off_seg = off;
     off = align_up(off + sizeof(int2) * size_t(total_segs), 256);
     h.off_segoff = off;
@@ -149,6 +152,7 @@ void plan(const gdn_problem* p, HostPlan& h) {
 }
 
 void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Problem& P) {
+    P.err = reinterpret_cast<int*>(ws + h.off_err);
     P.plan.seg = reinterpret_cast<int2*>(ws + h.off_seg);
     P.plan.seg_off = reinterpret_cast<int*>(ws + h.off_segoff);
     P.plan.chunk_off = reinterpret_cast<int*>(ws + h.off_chunkoff);
@@ -165,6 +169,14 @@ void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Proble
     P.warmup = h.warmup;
     P.cp = h.cp;
     P.scale = p->scale;
+}
+
+// bf16 runs on the tcgen05 kernels; GDN_FWD_PATH=mma selects the mma.sync kernels instead
+// (kept for comparison benchmarks), and the fp32 test mode always uses the CUDA-core kernels.
+bool use_tensor_cores(int dtype) {
+    if (dtype != GDN_BF16) return false;
+    const char* env = getenv("GDN_FWD_PATH");
+    return !(env && strcmp(env, "mma") == 0);
 }
 
 gdn_status check_ptrs(std::initializer_list<const void*> required,
@@ -232,7 +244,9 @@ gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, con
     P.o = o;
     P.ht = ht;
     fill_problem(p, h, static_cast<char*>(workspace), P);
-    cudaError_t e = gdn::launch_fwd(P, p->dtype, false, static_cast<cudaStream_t>(stream));
+    cudaError_t e = use_tensor_cores(p->dtype)
+                        ? gdn::launch_fwd_tc(P, false, h.total_tokens, static_cast<cudaStream_t>(stream))
+                        : gdn::launch_fwd(P, p->dtype, false, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
     g_err[0] = 0;
     return GDN_OK;

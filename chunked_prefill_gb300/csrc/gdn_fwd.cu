@@ -496,6 +496,19 @@ __global__ void k_plan(const int* cu, int N, int T, int C, int L, int total_segs
     chunk_off[N] = acc_c;
 }
 
+void launch_plan(const Problem& P, int C, cudaStream_t st) {
+    timing_begin("fwd_plan", st);
+    k_plan<<<1, 256, 0, st>>>(P.cu, P.N, P.T, C, P.L, P.total_segs, P.plan.seg, P.plan.seg_off,
+                              P.plan.chunk_off);
+    timing_end(st);
+}
+
+void launch_fixup(const Problem& P, cudaStream_t st) {
+    timing_begin("fwd_fixup", st);
+    k_fixup<<<dim3(P.N, P.Hv, VD / 16), 256, 0, st>>>(P);
+    timing_end(st);
+}
+
 template <typename Op, int C>
 static cudaError_t launch_fwd_t(const Problem& P, bool hist, cudaStream_t st) {
     using S = FwdSmem<Op, C>;
@@ -510,20 +523,13 @@ static cudaError_t launch_fwd_t(const Problem& P, bool hist, cudaStream_t st) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
 
-    timing_begin("fwd_plan", st);
-    k_plan<<<1, 256, 0, st>>>(P.cu, P.N, P.T, C, P.L, P.total_segs, P.plan.seg, P.plan.seg_off,
-                              P.plan.chunk_off);
-    timing_end(st);
+    launch_plan(P, C, st);
     if (P.cp != CP_NONE) {
         dim3 ga(P.total_segs, P.Hv, P.cp == CP_EXACT ? 2 : 1);
         timing_begin("fwd_phase_a", st);
         k_phase_a<Op, C><<<ga, NTHREADS, smem, st>>>(P);
         timing_end(st);
-        if (P.cp == CP_EXACT) {
-            timing_begin("fwd_fixup", st);
-            k_fixup<<<dim3(P.N, P.Hv, VD / 16), 256, 0, st>>>(P);
-            timing_end(st);
-        }
+        if (P.cp == CP_EXACT) launch_fixup(P, st);
     }
     dim3 gc(P.total_segs, P.Hv);
     timing_begin(hist ? "fwd_recompute_states" : "fwd_phase_c", st);

@@ -1,6 +1,8 @@
 // Internal launch interface between the C ABI layer and the kernel files.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include "gdn_plan.h"
 
@@ -12,6 +14,18 @@ int fwd_chunk_size(int dtype);
 // Plan kernel + (phase A + fix-up when P.cp != CP_NONE) + phase C.  hist=true replaces
 // the output stage by a store of every chunk's entering state into P.hist.
 cudaError_t launch_fwd(const Problem& P, int dtype, bool hist, cudaStream_t st);
+
+// The plan kernel (work decomposition from the device cu_seqlens) and the serial fix-up of
+// the exact context-parallel mode, shared by the CUDA-core and tensor-core paths.
+void launch_plan(const Problem& P, int C, cudaStream_t st);
+void launch_fixup(const Problem& P, cudaStream_t st);
+
+// TMA descriptors of k, q, v for the tensor-core path.
+struct TcMaps {
+    CUtensorMap k, q, v;
+};
+// Tensor-core (tcgen05) forward for bf16: same phases as launch_fwd.
+cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStream_t st);
 
 // Per-kernel event timing hooks (no-ops unless gdn_timing_enable(1)).
 void timing_begin(const char* name, cudaStream_t st);

@@ -39,6 +39,7 @@ struct Problem {
     int warmup;         // warm-up chunks (CP_WARMUP)
     int cp;             // CpKind
     float scale;
+    int* err;           // device error word (bounded waits that timed out), or null
 };
 
 }  // namespace gdn
