@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "../../include/gdn.h"
 #include "gdn_internal.h"
@@ -89,8 +90,35 @@ gdn_status validate_problem(const gdn_problem* p) {
     return GDN_OK;
 }
 
-// Segment length: FlashQLA's AutoCP model L = lambda * sqrt(N) (N = chunks of a sequence,
-// L = chunks per CP rank), used only when sequences x heads leave SMs idle.
+// Estimated time of a segmentation with L chunks per segment, in units of one chunk step
+// of the output stage: the waves of the two chunk-scan launches (one CTA per SM) times the
+// chunks a CTA scans, plus the serial fix-up steps.  The step costs are measured ratios on
+// GB300 (segment-transition steps ~0.9 of an output step, a fix-up step ~0.1).
+double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int warmup) {
+    constexpr double tC = 1.0, tA = 0.9, tF = 0.1;
+    long segs = 0, actas = 0;
+    int maxn = 0;
+    for (int s = 0; s < N; ++s) {
+        const int ns = std::max(1, (nts[s] + L - 1) / L);
+        segs += ns;
+        maxn = std::max(maxn, ns);
+        if (ns > 1) actas += exact ? 2 * ns - 3 : ns - 1;
+    }
+    const long cw = (segs * Hv + sms - 1) / sms;
+    const long aw = (actas * Hv + sms - 1) / sms;
+    const int Lc = std::min(L, *std::max_element(nts, nts + N));
+    double cost = double(cw) * Lc * tC;
+    if (maxn > 1) {
+        cost += double(aw) * (exact ? Lc : std::min(warmup, Lc)) * tA;
+        if (exact) cost += std::max(0, maxn - 2) * tF;
+    }
+    return cost;
+}
+
+// Segment length.  FlashQLA's AutoCP picks the chunks per CP rank as L = lambda * sqrt(N)
+// (N = chunks of a sequence); an explicit cp_lambda keeps that rule.  By default the planner
+// instead minimises cp_cost over L, which accounts for the wave quantisation of the launches
+// on this GPU's SM count.
 void plan(const gdn_problem* p, HostPlan& h) {
     h.C = gdn::fwd_chunk_size(p->dtype);
     h.N = p->cu_seqlens ? p->num_seqs : p->B;
@@ -105,14 +133,34 @@ void plan(const gdn_problem* p, HostPlan& h) {
     h.total_tokens = p->cu_seqlens ? p->T : int64_t(p->B) * p->T;
     int L = std::max(nt_max, 1);
     h.cp = gdn::CP_NONE;
-    const int units = h.N * p->Hv;
-    const float lam = p->cp_lambda > 0.f ? p->cp_lambda : 1.0f;
-    const int autoL = std::max(1, int(ceilf(lam * sqrtf(float(std::max(nt_max, 1))))));
+    const int warm = p->warmup_chunks > 0 ? p->warmup_chunks : 8;
+    int autoL = L;
+    if (p->cp_mode != GDN_CP_OFF && nt_max > 1) {
+        if (p->cp_lambda > 0.f) {
+            autoL = std::max(1, int(ceilf(p->cp_lambda * sqrtf(float(nt_max)))));
+        } else {
+            std::vector<int> nts(h.N);
+            for (int s = 0; s < h.N; ++s) {
+                const int len = p->cu_seqlens ? p->cu_seqlens_host[s + 1] - p->cu_seqlens_host[s] : p->T;
+                nts[s] = (len + h.C - 1) / h.C;
+            }
+            const int sms = sm_count();
+            const bool exact = p->cp_mode != GDN_CP_WARMUP;
+            double best = 1e300;
+            for (int cand = nt_max; cand >= 1; --cand) {  // ties go to longer segments
+                const double c = cp_cost(cand, nts.data(), h.N, p->Hv, sms, exact, warm);
+                if (c < best - 1e-9) {
+                    best = c;
+                    autoL = cand;
+                }
+            }
+        }
+    }
     switch (p->cp_mode) {
         case GDN_CP_OFF:
             break;
         case GDN_CP_AUTO:
-            if (units < sm_count()) L = autoL;
+            L = autoL;
             break;
         case GDN_CP_EXACT:
         case GDN_CP_WARMUP:

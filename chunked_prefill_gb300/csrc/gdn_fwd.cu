@@ -370,8 +370,15 @@ __device__ void scan_chunks(const Problem& P, char* smem, int s, int j, int64_t 
 #pragma unroll
         for (int n = 0; n < 16; ++n) {
             const int r = 16 * w + gq, cc = 8 * n + 2 * tq;
-            *reinterpret_cast<float2*>(x_out + r * VD + cc) = make_float2(X[n][0], X[n][1]);
-            *reinterpret_cast<float2*>(x_out + (r + 8) * VD + cc) = make_float2(X[n][2], X[n][3]);
+            if (KIND == K_TRANS) {  // segment transitions are stored transposed (M^T)
+                x_out[cc * VD + r] = X[n][0];
+                x_out[(cc + 1) * VD + r] = X[n][1];
+                x_out[cc * VD + r + 8] = X[n][2];
+                x_out[(cc + 1) * VD + r + 8] = X[n][3];
+            } else {
+                *reinterpret_cast<float2*>(x_out + r * VD + cc) = make_float2(X[n][0], X[n][1]);
+                *reinterpret_cast<float2*>(x_out + (r + 8) * VD + cc) = make_float2(X[n][2], X[n][3]);
+            }
         }
     }
 }
@@ -434,42 +441,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_phase_c(Problem P) {
     scan_chunks<Op, C, KIND>(P, smem, s, j, t0, t1, cb, ce, x0, x_out, hb);
 }
 
-// Fix-up: hin[g0+j+1] = M_j hin[g0+j] + S_j for j = 1..nseg-2, serially; each CTA owns 16
-// state columns of one (sequence, head).  fp32.
+// Fix-up: hin[g0+j+1] = M_j hin[g0+j] + S_j for j = 1..nseg-2, serially; each CTA owns 8
+// state columns of one (sequence, head).  The transitions are stored transposed (M^T), so
+// thread `row` reads M[row][m] = M^T[m][row] coalesced across the warp.  fp32.
 __global__ void __launch_bounds__(256) k_fixup(Problem P) {
-    __shared__ float xs[KD][17];
-    const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * 16;
+    __shared__ __align__(16) float xs[KD][8];
+    const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * 8;
     const int g0 = P.plan.seg_off[s], nseg = P.plan.seg_off[s + 1] - g0;
     if (nseg <= 2) return;
-    const int row = threadIdx.x >> 1, half = threadIdx.x & 1, c0 = half * 8;
+    const int row = threadIdx.x & 127, c0 = (threadIdx.x >> 7) * 4;
     {
-        const float* src = P.hin + (int64_t(g0 + 1) * P.Hv + j) * KV + row * VD + cb + c0;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) xs[row][c0 + c] = src[c];
+        const float4 x = *reinterpret_cast<const float4*>(
+            P.hin + (int64_t(g0 + 1) * P.Hv + j) * KV + row * VD + cb + c0);
+        *reinterpret_cast<float4*>(&xs[row][c0]) = x;
     }
     __syncthreads();
     for (int lj = 1; lj <= nseg - 2; ++lj) {
-        const float4* M = reinterpret_cast<const float4*>(P.mbuf + (int64_t(g0 + lj) * P.Hv + j) * KV +
-                                                          row * KD);
-        float* dst = P.hin + (int64_t(g0 + lj + 1) * P.Hv + j) * KV + row * VD + cb + c0;
-        float acc[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[c] = dst[c];
-#pragma unroll 4
-        for (int m4 = 0; m4 < KD / 4; ++m4) {
-            const float4 mv = M[m4];
-            const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[c] = fmaf(mm[u], xs[4 * m4 + u][c0 + c], acc[c]);
+        const float* Mt = P.mbuf + (int64_t(g0 + lj) * P.Hv + j) * KV;
+        float4* dst = reinterpret_cast<float4*>(P.hin + (int64_t(g0 + lj + 1) * P.Hv + j) * KV +
+                                                row * VD + cb + c0);
+        float4 acc = *dst;  // S_j
+#pragma unroll 16
+        for (int m = 0; m < KD; ++m) {
+            const float a = Mt[m * KD + row];
+            const float4 xv = *reinterpret_cast<const float4*>(&xs[m][c0]);
+            acc.x = fmaf(a, xv.x, acc.x);
+            acc.y = fmaf(a, xv.y, acc.y);
+            acc.z = fmaf(a, xv.z, acc.z);
+            acc.w = fmaf(a, xv.w, acc.w);
         }
         __syncthreads();
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            xs[row][c0 + c] = acc[c];
-            dst[c] = acc[c];
-        }
+        *reinterpret_cast<float4*>(&xs[row][c0]) = acc;
+        *dst = acc;
         __syncthreads();
     }
 }
@@ -505,7 +508,7 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
-    k_fixup<<<dim3(P.N, P.Hv, VD / 16), 256, 0, st>>>(P);
+    k_fixup<<<dim3(P.N, P.Hv, VD / 8), 256, 0, st>>>(P);
     timing_end(st);
 }
 

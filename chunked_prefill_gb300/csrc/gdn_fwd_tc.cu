@@ -452,8 +452,15 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                     float xv[16];
                     tmem_ld16(tm + lb + T_XF + c0, xv);
                     tmem_ld_wait();
+                    if (KIND == TK_TRANS) {  // segment transitions are stored transposed (M^T)
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) x_out[(c0 + i) * VD + v] = xv[i];
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(x_out + v * VD + c0 + i) =
+                                make_float4(xv[i], xv[i + 1], xv[i + 2], xv[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) x_out[(c0 + i) * VD + v] = xv[i];
+                    }
                 }
             }
         }
