@@ -50,6 +50,8 @@ struct HostPlan {
     // workspace layout (bytes)
     size_t off_err = 0, off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0,
            off_mbuf = 0, off_end = 0;
+    // backward only
+    size_t off_hist = 0, off_dhist = 0, off_dhb = 0, off_dqp = 0, off_dkp = 0;
 };
 
 constexpr size_t KVB = size_t(128) * 128 * 4;
@@ -119,7 +121,7 @@ double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int wa
 // (N = chunks of a sequence); an explicit cp_lambda keeps that rule.  By default the planner
 // instead minimises cp_cost over L, which accounts for the wave quantisation of the launches
 // on this GPU's SM count.
-void plan(const gdn_problem* p, HostPlan& h) {
+void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
     h.C = gdn::fwd_chunk_size(p->dtype);
     h.N = p->cu_seqlens ? p->num_seqs : p->B;
     int nt_max = 0;
@@ -180,7 +182,8 @@ void plan(const gdn_problem* p, HostPlan& h) {
     h.total_segs = total_segs;
     h.total_chunks = int(total_chunks);
     h.max_nseg = max_nseg;
-    if (max_nseg > 1) h.cp = (p->cp_mode == GDN_CP_WARMUP) ? gdn::CP_WARMUP : gdn::CP_EXACT;
+    if (max_nseg > 1)
+        h.cp = (p->cp_mode == GDN_CP_WARMUP && !backward) ? gdn::CP_WARMUP : gdn::CP_EXACT;
     h.warmup = p->warmup_chunks > 0 ? p->warmup_chunks : 8;
 
     size_t off = 0;
@@ -196,6 +199,26 @@ void plan(const gdn_problem* p, HostPlan& h) {
     if (h.cp != gdn::CP_NONE) off += KVB * size_t(total_segs) * p->Hv;
     h.off_mbuf = off;
     if (h.cp == gdn::CP_EXACT) off += KVB * size_t(total_segs) * p->Hv;
+    off = align_up(off, 256);
+    if (backward) {
+        const size_t elem = p->dtype == GDN_BF16 ? 2 : 4;
+        const size_t per_chunk = size_t(128) * 128 * elem * p->Hv;
+        h.off_hist = off;
+        off = align_up(off + per_chunk * size_t(h.total_chunks), 256);
+        h.off_dhist = off;
+        off = align_up(off + per_chunk * size_t(h.total_chunks), 256);
+        h.off_dhb = off;
+        if (h.cp != gdn::CP_NONE) off = align_up(off + KVB * size_t(total_segs) * p->Hv, 256);
+        h.off_dqp = off;
+        if (p->Hv != p->Hqk) {
+            const size_t part = size_t(h.total_tokens) * p->Hv * 128 * 4;
+            off = align_up(off + part, 256);
+            h.off_dkp = off;
+            off = align_up(off + part, 256);
+        } else {
+            h.off_dkp = off;
+        }
+    }
     h.off_end = align_up(off, 256);
 }
 
@@ -304,8 +327,11 @@ gdn_status gdn_chunk_bwd_workspace_size(const gdn_problem* p, size_t* bytes) {
     gdn_status st = validate_problem(p);
     if (st != GDN_OK) return st;
     if (!bytes) return fail(GDN_ERR_INVALID_ARG, "bytes is NULL");
-    *bytes = 0;
-    return fail(GDN_ERR_UNSUPPORTED, "backward not built yet");
+    HostPlan h;
+    plan(p, h, true);
+    *bytes = h.off_end;
+    g_err[0] = 0;
+    return GDN_OK;
 }
 
 gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
@@ -315,10 +341,54 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, con
                          void* stream) {
     gdn_status st = validate_problem(p);
     if (st != GDN_OK) return st;
-    (void)q; (void)k; (void)v; (void)g; (void)beta; (void)h0; (void)dO; (void)dht; (void)dq;
-    (void)dk; (void)dv; (void)dg; (void)dbeta; (void)dh0; (void)workspace; (void)workspace_bytes;
-    (void)stream;
-    return fail(GDN_ERR_UNSUPPORTED, "backward not built yet");
+    HostPlan h;
+    plan(p, h, true);
+    if (h.total_tokens > 0)
+        st = check_ptrs({q, k, v, g, beta, dO, dq, dk, dv, dg, dbeta}, {h0, dht, dh0});
+    else
+        st = check_ptrs({}, {q, k, v, g, beta, dO, dq, dk, dv, dg, dbeta, h0, dht, dh0});
+    if (st != GDN_OK) return st;
+    if (h.N == 0) {
+        g_err[0] = 0;
+        return GDN_OK;
+    }
+    if (!workspace || workspace_bytes < h.off_end)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", h.off_end,
+                    workspace ? workspace_bytes : size_t(0));
+    if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    gdn::BwdProblem B{};
+    gdn::Problem& P = B.f;
+    P.q = q;
+    P.k = k;
+    P.v = v;
+    P.g = g;
+    P.beta = beta;
+    P.h0 = h0;
+    P.o = nullptr;
+    P.ht = nullptr;
+    fill_problem(p, h, ws, P);
+    P.hist = ws + h.off_hist;
+    B.dO = dO;
+    B.dht = dht;
+    B.dh0 = dh0;
+    B.dq = dq;
+    B.dk = dk;
+    B.dv = dv;
+    B.dg = dg;
+    B.dbeta = dbeta;
+    B.dhist = ws + h.off_dhist;
+    B.dhb = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_dhb) : nullptr;
+    B.dqp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dqp) : nullptr;
+    B.dkp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dkp) : nullptr;
+    // recompute the state entering every chunk, then the reverse scan and local gradients
+    cudaError_t e = use_tensor_cores(p->dtype) ? gdn::launch_fwd_tc(P, true, h.total_tokens, cs)
+                                               : gdn::launch_fwd(P, p->dtype, true, cs);
+    if (e == cudaSuccess) e = gdn::launch_bwd(B, p->dtype, cs);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+    g_err[0] = 0;
+    return GDN_OK;
 }
 
 }  // extern "C"

@@ -27,6 +27,11 @@ struct TcMaps {
 // Tensor-core (tcgen05) forward for bf16: same phases as launch_fwd.
 cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStream_t st);
 
+// Backward: reverse dh scan (with the same context-parallel segments as the forward) and
+// the chunk-parallel local gradients; expects the forward recompute (states per chunk in
+// B.f.hist, transitions in B.f.mbuf) to have run on the same stream.
+cudaError_t launch_bwd(const BwdProblem& B, int dtype, cudaStream_t st);
+
 // Per-kernel event timing hooks (no-ops unless gdn_timing_enable(1)).
 void timing_begin(const char* name, cudaStream_t st);
 void timing_end(cudaStream_t st);

@@ -42,4 +42,22 @@ struct Problem {
     int* err;           // device error word (bounded waits that timed out), or null
 };
 
+// Backward: the forward fields (recompute of the per-chunk states uses them) plus the
+// gradient tensors and the backward's own workspace.
+struct BwdProblem {
+    Problem f;
+    const void* dO;     // [T, Hv, V]
+    const float* dht;   // [N, Hv, K, V] or null (zero)
+    float* dh0;         // [N, Hv, K, V] or null (not returned)
+    void* dq;           // [T, Hqk, K]
+    void* dk;           // [T, Hqk, K]
+    void* dv;           // [T, Hv, V]
+    float* dg;          // [T, Hv]
+    float* dbeta;       // [T, Hv]
+    void* dhist;        // [total_chunks, Hv, K, V] gradient w.r.t. the state leaving each chunk
+    float* dhb;         // [total_segs, Hv, K, V] gradient entering each segment from the right
+    float* dqp;         // [T, Hv, K] per-v-head partial dq (G > 1) or null
+    float* dkp;         // [T, Hv, K] per-v-head partial dk (G > 1) or null
+};
+
 }  // namespace gdn

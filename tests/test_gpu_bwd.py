@@ -1,0 +1,118 @@
+"""GPU parity of the backward (gdn_chunk_bwd through the C ABI) against the fp64 oracle's
+hand-written reverse mode, on L = <o, dO> + <ht, dht>.
+
+Tolerances as for the forward: max|err| <= 1e-2 max|ref| per gradient tensor for bf16 inputs,
+<= 1e-4 max|ref| in the fp32 test mode."""
+import numpy as np
+import pytest
+import torch
+
+from chunked_prefill_gb300.inputs import make_inputs, workload_inputs
+from tests.gpu_util import BF16_TOL, FP32_TOL, gpu_bwd, oracle_bwd, rel_err
+
+pytestmark = pytest.mark.gpu
+NAMES = ["dq", "dk", "dv", "dg", "dbeta", "dh0"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from chunked_prefill_gb300 import build
+    build.build()
+
+
+def check(inp, tol, **kw):
+    got = gpu_bwd(inp, **kw)
+    ref = oracle_bwd(inp)
+    errs = {}
+    for name, a, b in zip(NAMES, got, ref):
+        if a is None:
+            continue
+        errs[name] = rel_err(a.reshape(b.shape), b)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"relative errors above {tol}: {bad} (all: {errs})"
+    return errs
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+def test_small_training_step(dtype, tol):
+    inp = make_inputs(1, 256, 2, 4, seed=40, dtype=dtype, h0_std=0.1, backward=True)
+    check(inp, tol)
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+@pytest.mark.parametrize("B,T,Hqk,Hv,h0", [
+    (1, 1, 1, 1, True), (1, 63, 1, 3, False), (2, 64, 2, 2, True), (1, 65, 1, 2, True),
+    (3, 200, 1, 3, True), (1, 129, 2, 2, False),
+])
+def test_odd_shapes(dtype, tol, B, T, Hqk, Hv, h0):
+    inp = make_inputs(B, T, Hqk, Hv, seed=T * 3 + Hv, dtype=dtype, h0_std=0.1 if h0 else 0.0,
+                      backward=True)
+    check(inp, tol, cp_mode=1)
+    check(inp, tol)
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+def test_varlen_with_empty_sequences(dtype, tol):
+    lens = [0, 5, 64, 130, 0, 77]
+    inp = make_inputs(1, sum(lens), 2, 4, seed=41, dtype=dtype, h0_std=0.1, lengths=lens,
+                      backward=True)
+    check(inp, tol, cp_mode=1)
+    check(inp, tol, cp_mode=2, cp_segment_chunks=1)
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+@pytest.mark.parametrize("seg", [1, 2, 3, 5])
+def test_context_parallel_exact(dtype, tol, seg):
+    inp = make_inputs(1, 64 * 11 + 9, 1, 2, seed=42, dtype=dtype, h0_std=0.1, backward=True)
+    check(inp, tol, cp_mode=2, cp_segment_chunks=seg)
+
+
+def test_without_final_state_gradient_or_initial_state():
+    inp = make_inputs(1, 300, 1, 2, seed=43, backward=True)
+    inp.dht = None
+    check(inp, BF16_TOL)
+
+
+def test_determinism():
+    inp = make_inputs(1, 500, 2, 4, seed=44, h0_std=0.1, backward=True)
+    a = gpu_bwd(inp)
+    b = gpu_bwd(inp)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_autograd_wrapper_matches_oracle():
+    from chunked_prefill_gb300 import gdn
+    inp = make_inputs(1, 200, 1, 2, seed=45, h0_std=0.1, backward=True)
+    xs = {n: getattr(inp, n).cuda().requires_grad_(True) for n in ("q", "k", "v", "g", "beta", "h0")}
+    o, ht = gdn.chunk_gated_delta_rule(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"],
+                                       scale=inp.scale, initial_state=xs["h0"],
+                                       output_final_state=True)
+    loss = (o.float() * inp.dO.cuda().float()).sum() + (ht * inp.dht.cuda()).sum()
+    loss.backward()
+    ref = oracle_bwd(inp)
+    for name, key, r in zip(NAMES, ["q", "k", "v", "g", "beta", "h0"], ref):
+        got = xs[key].grad.float().cpu().numpy()
+        assert rel_err(got.reshape(r.shape), r) <= BF16_TOL, name
+
+
+def test_full_size_training_step_sampled_heads():
+    """The 32K-token, 16/16-head training step in the benchmark's launch configuration; the
+    oracle checks a sample of heads (heads are independent when each q/k head has one v
+    head)."""
+    inp = workload_inputs("fwdbwd_t32k_hqk16_hv16")
+    got = gpu_bwd(inp)
+    heads = [0, 5, 10, 15]
+    sub = make_inputs(1, 16, 1, 1, backward=True)  # container; fields replaced below
+    sub.q, sub.k = inp.q[:, :, heads], inp.k[:, :, heads]
+    sub.v, sub.dO = inp.v[:, :, heads], inp.dO[:, :, heads]
+    sub.g, sub.beta = inp.g[:, :, heads], inp.beta[:, :, heads]
+    sub.h0, sub.dht = inp.h0[:, heads], inp.dht[:, heads]
+    sub.scale, sub.cu_seqlens = inp.scale, None
+    ref = oracle_bwd(sub)
+    idx = {"dq": 2, "dk": 2, "dv": 2, "dg": 2, "dbeta": 2, "dh0": 1}
+    for name, a, r in zip(NAMES, got, ref):
+        a = np.take(a, heads, axis=idx[name])
+        assert rel_err(a, r) <= BF16_TOL, name
