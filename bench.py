@@ -94,6 +94,8 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        if self.dev is None:
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
@@ -301,6 +303,26 @@ def oracle_sample_fixed(inp, n, backward):
     return new_cu[-1] / dt, new_cu[-1], dt, orc.max_threads(), n
 
 
+def kernel_bytes(name, tokens, nseq, w):
+    """Algorithmic HBM bytes of one launch of a kernel: the tensors its step of the method
+    must read or write once (bf16 activations, fp32 gates and states)."""
+    qk = tokens * w.Hqk * 128 * 2
+    vv = tokens * w.Hv * 128 * 2
+    gb = tokens * w.Hv * 4 * 2
+    st = nseq * w.Hv * 128 * 128 * 4
+    h0 = st if w.h0_std > 0 else 0
+    table = {
+        "fwd_phase_c": (2 * qk + 2 * vv + gb + h0 + st, "q,k,v,g,beta,h0 read; o,ht written"),
+        "fwd_phase_a": (qk + vv + gb + h0, "k,v,g,beta,h0 read"),
+        "fwd_recompute_states": (qk + vv + gb + h0, "k,v,g,beta,h0 read"),
+        "bwd_phase_a": (2 * qk + vv + gb + st, "q,k,dO,g,beta,dht read"),
+        "bwd_dh_scan": (2 * qk + vv + gb + 2 * st, "q,k,dO,g,beta,dht read; dh0 written"),
+        "bwd_local": (2 * qk + 2 * vv + gb + 2 * qk + vv + gb,
+                      "q,k,v,dO,g,beta read; dq,dk,dv,dg,dbeta written"),
+    }
+    return table.get(name, (0.0, "not counted"))
+
+
 def config_of(name):
     w = WORKLOADS[name]
     c = {"workload": name, "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv, "K": w.K, "V": w.V,
@@ -321,6 +343,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="for ncu: warm-up and timed steps only (no clock sampling, e2e or "
+                         "CPU baseline)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args.gpus)
@@ -344,10 +369,12 @@ def main():
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    if args.profile:
+        args.no_e2e = args.no_cpu_baseline = True
+    with ClockSampler(local if not args.profile else None) as clk:
         # keep the GPU busy (untimed) while nvidia-smi starts, so the sampled clocks are
         # those under load and its start-up does not overlap the timed steps
-        t_busy = time.time() + 1.0
+        t_busy = time.time() + (0.0 if args.profile else 1.0)
         while time.time() < t_busy:
             step()
             torch.cuda.synchronize()
@@ -373,15 +400,7 @@ def main():
     dom = max(kt.items(), key=lambda kv: kv[1][1]) if kt else ("none", (1, float("nan")))
     dom_name, (dom_n, dom_ms) = dom
     dom_avg_s = dom_ms / max(dom_n, 1) / 1000.0
-    if dom_name in ("fwd_phase_c",):
-        alg = rl.fwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
-        unit_note = "compulsory forward bytes (q,k,v,g,beta,h0 read; o,ht written)"
-    elif dom_name == "fwd_phase_a":
-        alg = (tokens * w.Hqk * 128 * 2 + tokens * w.Hv * (128 * 2 + 8))
-        unit_note = "k, v, g, beta of the sequence read once"
-    else:
-        alg = by
-        unit_note = "compulsory bytes of the step"
+    alg, unit_note = kernel_bytes(dom_name, tokens, len(lens), w)
     achieved = alg / dom_avg_s / 1e9
     roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
