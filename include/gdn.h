@@ -108,6 +108,8 @@ gdn_status gdn_chunk_bwd_workspace_size(const gdn_problem* p, size_t* bytes);
  * inputs.  The forward intermediates are recomputed from q, k, v, g, beta, h0.
  *   dht : NULL = zero.   dh0 : NULL = not returned.
  *   dq, dk are summed over the G v-heads that share each q/k head.
+ *   Context parallelism in the backward is always exact (GDN_CP_WARMUP is treated as
+ *   GDN_CP_EXACT here).
  */
 gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* h0, const void* dO,
