@@ -49,7 +49,7 @@ struct HostPlan {
     int64_t total_tokens = 0;
     // workspace layout (bytes)
     size_t off_err = 0, off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0,
-           off_mbuf = 0, off_end = 0;
+           off_mbuf = 0, off_prep = 0, off_end = 0;
     // backward only
     size_t off_hist = 0, off_dhist = 0, off_dhb = 0, off_dqp = 0, off_dkp = 0;
 };
@@ -200,6 +200,8 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
     h.off_mbuf = off;
     if (h.cp == gdn::CP_EXACT) off += KVB * size_t(total_segs) * p->Hv;
     off = align_up(off, 256);
+    h.off_prep = off;  // TW, TU, P tiles of every (chunk, v-head): tensor-core path only
+    if (p->dtype == GDN_BF16) off = align_up(off + size_t(3) * 8192 * h.total_chunks * p->Hv, 256);
     if (backward) {
         const size_t elem = p->dtype == GDN_BF16 ? 2 : 4;
         const size_t per_chunk = size_t(128) * 128 * elem * p->Hv;
@@ -229,6 +231,7 @@ void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Proble
     P.plan.chunk_off = reinterpret_cast<int*>(ws + h.off_chunkoff);
     P.hin = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_hin) : nullptr;
     P.mbuf = h.cp == gdn::CP_EXACT ? reinterpret_cast<float*>(ws + h.off_mbuf) : nullptr;
+    P.prep = p->dtype == GDN_BF16 ? ws + h.off_prep : nullptr;
     P.cu = p->cu_seqlens;
     P.N = h.N;
     P.T = p->T;

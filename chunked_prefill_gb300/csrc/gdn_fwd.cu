@@ -24,6 +24,7 @@
 // segment from a zero state.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "tc05.cuh"
 
 namespace gdn {
 
@@ -442,39 +443,62 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_phase_c(Problem P) {
 }
 
 // Fix-up: hin[g0+j+1] = M_j hin[g0+j] + S_j for j = 1..nseg-2, serially; each CTA owns 8
-// state columns of one (sequence, head).  The transitions are stored transposed (M^T), so
-// thread `row` reads M[row][m] = M^T[m][row] coalesced across the warp.  fp32.
+// state columns of one (sequence, head).  The transitions are stored transposed (M^T); each
+// one arrives in shared memory by a bulk copy issued one step ahead (double buffer), and
+// thread `row` reads M[row][m] = M^T[m][row] without bank conflicts.  fp32.
+constexpr int FIX_SMEM = 2 * KD * KD * 4 + KD * 8 * 4 + 64;
 __global__ void __launch_bounds__(256) k_fixup(Problem P) {
-    __shared__ __align__(16) float xs[KD][8];
+    extern __shared__ __align__(128) unsigned char fsm[];
+    float* Ms = reinterpret_cast<float*>(fsm);                       // 2 x 128 x 128
+    float* xs = reinterpret_cast<float*>(fsm + 2 * KD * KD * 4);     // 128 x 8
+    uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + 2 * KD * KD * 4 + KD * 8 * 4);
     const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * 8;
     const int g0 = P.plan.seg_off[s], nseg = P.plan.seg_off[s + 1] - g0;
     if (nseg <= 2) return;
     const int row = threadIdx.x & 127, c0 = (threadIdx.x >> 7) * 4;
+    auto mt = [&](int lj) { return P.mbuf + (int64_t(g0 + lj) * P.Hv + j) * KV; };
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar[0], 1);
+        tc::mbar_init(&bar[1], 1);
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tc::mbar_expect_tx(&bar[0], KD * KD * 4);
+        tc::bulk_load(Ms, mt(1), KD * KD * 4, &bar[0]);
+    }
     {
         const float4 x = *reinterpret_cast<const float4*>(
             P.hin + (int64_t(g0 + 1) * P.Hv + j) * KV + row * VD + cb + c0);
-        *reinterpret_cast<float4*>(&xs[row][c0]) = x;
+        *reinterpret_cast<float4*>(&xs[row * 8 + c0]) = x;
     }
-    __syncthreads();
+    bool ok = true;
     for (int lj = 1; lj <= nseg - 2; ++lj) {
-        const float* Mt = P.mbuf + (int64_t(g0 + lj) * P.Hv + j) * KV;
+        const int b = (lj - 1) & 1;
+        if (threadIdx.x == 0 && lj + 1 <= nseg - 2) {  // prefetch the next transition
+            tc::mbar_expect_tx(&bar[b ^ 1], KD * KD * 4);
+            tc::bulk_load(Ms + (b ^ 1) * KD * KD, mt(lj + 1), KD * KD * 4, &bar[b ^ 1]);
+        }
+        ok = ok && tc::mbar_wait(&bar[b], ((lj - 1) >> 1) & 1);
+        __syncthreads();  // also orders the previous step's xs update
+        const float* M = Ms + b * KD * KD;
         float4* dst = reinterpret_cast<float4*>(P.hin + (int64_t(g0 + lj + 1) * P.Hv + j) * KV +
                                                 row * VD + cb + c0);
         float4 acc = *dst;  // S_j
 #pragma unroll 16
         for (int m = 0; m < KD; ++m) {
-            const float a = Mt[m * KD + row];
-            const float4 xv = *reinterpret_cast<const float4*>(&xs[m][c0]);
+            const float a = M[m * KD + row];
+            const float4 xv = *reinterpret_cast<const float4*>(&xs[m * 8 + c0]);
             acc.x = fmaf(a, xv.x, acc.x);
             acc.y = fmaf(a, xv.y, acc.y);
             acc.z = fmaf(a, xv.z, acc.z);
             acc.w = fmaf(a, xv.w, acc.w);
         }
-        __syncthreads();
-        *reinterpret_cast<float4*>(&xs[row][c0]) = acc;
+        __syncthreads();  // every thread is done with xs and with buffer b
+        *reinterpret_cast<float4*>(&xs[row * 8 + c0]) = acc;
         *dst = acc;
-        __syncthreads();
     }
+    if (!ok && threadIdx.x == 0 && P.err) atomicOr(P.err, 1 << 30);
 }
 
 // Work decomposition on the device from the device cu_seqlens (same rule as the host).
@@ -508,7 +532,8 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
-    k_fixup<<<dim3(P.N, P.Hv, VD / 8), 256, 0, st>>>(P);
+    cudaFuncSetAttribute(k_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
+    k_fixup<<<dim3(P.N, P.Hv, VD / 8), 256, FIX_SMEM, st>>>(P);
     timing_end(st);
 }
 

@@ -39,26 +39,20 @@ constexpr int TCT = 512;  // threads (16 warps)
 constexpr int CH = 64;    // chunk
 
 // tensor-memory columns
-constexpr uint32_t T_XF = 0, T_XB = 128, T_D1 = 192, T_D2 = 256, T_D3 = 320, T_D4 = 384,
-                   T_D5 = 448;
+constexpr uint32_t T_XF = 0, T_XB = 128 /* 2 x 64: bf16 state copy, by chunk parity */,
+                   T_D2 = 256, T_D3 = 320, T_D4 = 384, T_D5 = 448;
 
 // shared-memory layout (offsets from a 1024-aligned base)
 constexpr uint32_t S_KQ = 0;            // 2 x 32 KB: rows 0-63 K, 64-127 Q, 2 column blocks
 constexpr uint32_t S_KQ_STRIDE = 32768;
 constexpr uint32_t S_V = 65536;         // 2 x 16 KB
 constexpr uint32_t S_V_STRIDE = 16384;
-constexpr uint32_t S_WT = 98304;        // 16 KB: W'^T [128 dk][64 i]
-constexpr uint32_t S_TW = 114688;       // 8 KB:  [64 i][64 j]
-constexpr uint32_t S_TU = 122880;       // 8 KB
-constexpr uint32_t S_P = 131072;        // 2 x 8 KB
-constexpr uint32_t S_P_STRIDE = 8192;
-constexpr int LDA = 68;                 // fp32 scratch row stride (floats)
-constexpr uint32_t S_A = 147456;        // fp32 64 x 68
-constexpr uint32_t S_T = S_A + 64 * LDA * 4;
-constexpr uint32_t S_TMP = S_T + 64 * LDA * 4;        // 4 warps x 16 x 20 fp32
-constexpr uint32_t S_GATE = S_TMP + 5120;             // NGATE gate buffers
+constexpr uint32_t S_PR = 98304;        // 2 x 24 KB: TW, TU, P tiles ([64 i][64 j] each)
+constexpr uint32_t S_PR_STRIDE = 24576;
+constexpr uint32_t S_WT = 147456;       // 16 KB: W'^T [128 dk][64 i]
+constexpr uint32_t S_GATE = 163840;     // NGATE gate buffers
 constexpr int NGATE = 4;
-constexpr uint32_t GATE_BYTES = 1600;
+constexpr uint32_t GATE_BYTES = 1088;
 constexpr int LDO = 136;                              // output staging row stride (bf16)
 constexpr uint32_t S_O = S_GATE + NGATE * GATE_BYTES; // 64 x 136 bf16 output staging
 constexpr uint32_t S_BAR = S_O + 64 * LDO * 2;        // mbarriers
@@ -69,18 +63,15 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 struct alignas(16) Gate {
     float gam[CH];
     float e[CH];     // exp(gamma)
-    float einv[CH];  // exp(-gamma)
     float kd[CH];    // exp(gamma_C - gamma)
-    float beta[CH];
-    float be[CH];    // beta * exp(gamma)
     float eC;
     int c;           // valid rows
-    int pairwise;    // gamma range too wide for the factorised exponentials
 };
 static_assert(sizeof(Gate) <= GATE_BYTES && sizeof(Gate) % 16 == 0, "gate buffer");
 
-enum Bar { B_FULL0 = 0, B_FULL1, B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GFREE0, B_GFREE1, B_GFREE2,
-           B_GFREE3, B_MMA1, B_MMA2, B_MMA3, B_MMA5, B_ET, B_EW, B_EX, B_EV, B_EPI, B_COUNT };
+enum Bar { B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GFREE0,
+           B_GFREE1, B_GFREE2, B_GFREE3, B_MMA2, B_MMA3, B_MMA5, B_MMA4, B_EW, B_EX, B_EV, B_EPI,
+           B_COUNT };
 
 enum TcKind { TK_STATE = 0, TK_TRANS = 1, TK_OUT = 2, TK_HIST = 3 };
 
@@ -128,10 +119,52 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bars, int b, uint32_t parity
     __syncwarp();
     return ok;
 }
-// wait that is uniform over the four prep warps (named barrier 1)
-__device__ __forceinline__ bool group_wait(uint64_t* bars, int b, uint32_t parity, int* errflag) {
-    const bool ok = warp_wait(bars, b, parity, errflag);
-    return named_and(1, 128, ok);
+
+// Entering state (fp32, [dk][v] in global memory; null = zero, or the identity for the
+// transition kind) into key columns [64 half, 64 half + 64) of the transposed TMEM state.
+template <int KIND>
+__device__ __forceinline__ void init_state_half(uint32_t tm, uint32_t lb, int half, int v,
+                                                const float* x0) {
+    float xv[16];
+    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int dk = c0 + i;
+            xv[i] = x0 ? x0[dk * VD + v] : ((KIND == TK_TRANS && dk == v) ? 1.f : 0.f);
+        }
+        tmem_st16(tm + lb + T_XF + c0, xv);
+    }
+    tmem_st_wait();
+}
+
+// One half (64 key columns) of the per-chunk state hand-off: read the fp32 state, write its
+// bf16 copy (the A operand of the V' and Q h products), store it for the backward when asked,
+// and decay the fp32 state by exp(gamma_C) before the chunk's update accumulates onto it.
+template <int KIND>
+__device__ __forceinline__ void convert_state_half(const Problem& P, uint32_t tm, uint32_t lb,
+                                                   uint32_t xb, int half, int v, float eC,
+                                                   int64_t chunk, int j) {
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+        const int c0 = 64 * half + 32 * q;
+        float x[32];
+        tmem_ld32(tm + lb + T_XF + c0, x);
+        tmem_ld_wait();
+        if (KIND == TK_HIST) {
+            __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(P.hist) + (chunk * P.Hv + j) * (KD * VD);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
+        }
+        float pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
+        tmem_st16(tm + lb + xb + c0 / 2, pk);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] *= eC;
+        tmem_st16(tm + lb + T_XF + c0, x);
+        tmem_st16(tm + lb + T_XF + c0 + 16, x + 16);
+    }
+    tmem_st_wait();
 }
 
 template <int KIND>
@@ -151,17 +184,18 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     if (tid == 0) {
         mbar_init(&bars[B_FULL0], 1);
         mbar_init(&bars[B_FULL1], 1);
+        mbar_init(&bars[B_EMPTY0], 1);
+        mbar_init(&bars[B_EMPTY1], 1);
         for (int b = 0; b < NGATE; ++b) {
             mbar_init(&bars[B_GATE0 + b], 1);
-            mbar_init(&bars[B_GFREE0 + b], OUT ? 12 : 8);
+            mbar_init(&bars[B_GFREE0 + b], OUT ? 8 : 4);
         }
-        mbar_init(&bars[B_MMA1], 1);
         mbar_init(&bars[B_MMA2], 1);
         mbar_init(&bars[B_MMA3], 1);
         mbar_init(&bars[B_MMA5], 1);
-        mbar_init(&bars[B_ET], 4);
+        mbar_init(&bars[B_MMA4], 1);
         mbar_init(&bars[B_EW], 4);
-        mbar_init(&bars[B_EX], 4);
+        mbar_init(&bars[B_EX], 8);
         mbar_init(&bars[B_EV], 4);
         mbar_init(&bars[B_EPI], 4);
         *errflag = 0;
@@ -176,20 +210,27 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     if (w == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint32_t bytes = 16384u + (OUT ? 16384u : 0u) + (NEEDU ? 16384u : 0u);
+            const uint32_t bytes = 16384u + (OUT ? 16384u : 0u) + (NEEDU ? 16384u : 0u) +
+                                   8192u * (1u + (NEEDU ? 1u : 0u) + (OUT ? 1u : 0u));
             int issued = 0;
             for (int k = 0; k < n; ++k) {
                 const int st = k & 1;
-                if (k >= 2 && !wait_bar(bars, B_MMA5, (k - 2) & 1, errflag)) break;
+                if (k >= 2 && !wait_bar(bars, B_EMPTY0 + st, ((k - 2) >> 1) & 1, errflag)) break;
                 const int tc = int(t0 + int64_t(cb + k) * CH);
                 uint64_t* full = &bars[B_FULL0 + st];
                 unsigned char* kq = sm + S_KQ + st * S_KQ_STRIDE;
+                unsigned char* pr = sm + S_PR + st * S_PR_STRIDE;
+                const unsigned char* src = static_cast<const unsigned char*>(P.prep) +
+                                           ((hist_base + cb + k) * P.Hv + j) * 3 * 8192;
                 mbar_expect_tx(full, bytes);
                 tma_load_3d(kq, &maps.k, full, 0, qh, tc);
                 tma_load_3d(kq + 16384, &maps.k, full, 64, qh, tc);
+                bulk_load(pr, src, 8192, full);                       // TW
+                if (NEEDU) bulk_load(pr + 8192, src + 8192, 8192, full);   // TU
                 if (OUT) {
                     tma_load_3d(kq + 8192, &maps.q, full, 0, qh, tc);
                     tma_load_3d(kq + 16384 + 8192, &maps.q, full, 64, qh, tc);
+                    bulk_load(pr + 16384, src + 16384, 8192, full);   // P
                 }
                 if (NEEDU) {
                     unsigned char* vt = sm + S_V + st * S_V_STRIDE;
@@ -206,73 +247,55 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     } else if (w == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t ID1 = make_idesc(128, 64, 0, 0);
             constexpr uint32_t ID2 = make_idesc(128, 64, 1, 0);
             constexpr uint32_t ID3 = make_idesc(128, 64, 0, 1);
             constexpr uint32_t ID4 = make_idesc(128, 64, 0, 0);
             constexpr uint32_t ID5 = make_idesc(128, 128, 0, 1);
             const uint32_t kq0 = smem_addr(sm + S_KQ), v0 = smem_addr(sm + S_V);
-            const uint32_t wt = smem_addr(sm + S_WT), tw = smem_addr(sm + S_TW),
-                           tu = smem_addr(sm + S_TU), p0 = smem_addr(sm + S_P);
+            const uint32_t wt = smem_addr(sm + S_WT), pr0 = smem_addr(sm + S_PR);
             bool ok = true;
-            int n_mma1 = 0;  // commits made on the MMA1 barrier
-            auto prep_mma1 = [&](int k) -> bool {
+            int n_mma2 = 0;
+            // W'^T = K^T TW^T for chunk k (needs the stage loaded and partial rows masked)
+            auto issue_w = [&](int k) -> bool {
                 const int st = k & 1;
                 if (!wait_bar(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) return false;
                 if (!wait_bar(bars, B_GATE0 + (k & (NGATE - 1)), (k >> 2) & 1, errflag)) return false;
                 fence_after_sync();
-                const uint32_t kq = kq0 + st * S_KQ_STRIDE;
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                    mma_bf16(tm + T_D1, kdesc(kq + off), kdesc(kq + off), ID1, s > 0);
-                }
-                commit(&bars[B_MMA1]);
-                ++n_mma1;
-                return true;
-            };
-            auto prep_mma2 = [&](int k) -> bool {
-                const int st = k & 1;
-                if (!wait_bar(bars, B_ET, k & 1, errflag)) return false;
-                fence_after_sync();
-                const uint32_t kq = kq0 + st * S_KQ_STRIDE;
+                const uint32_t kq = kq0 + st * S_KQ_STRIDE, tw = pr0 + st * S_PR_STRIDE;
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_bf16(tm + T_D2, mdesc(kq + s * 2048, 16384), kdesc(tw + s * 32), ID2, s > 0);
                 commit(&bars[B_MMA2]);
+                ++n_mma2;
                 return true;
             };
-            ok = prep_mma1(0) && prep_mma2(0) && wait_bar(bars, B_EW, 0, errflag);
+            ok = issue_w(0);
             for (int k = 0; ok && k < n; ++k) {
                 const int st = k & 1;
-                const uint32_t kq = kq0 + st * S_KQ_STRIDE;
+                const uint32_t kq = kq0 + st * S_KQ_STRIDE, pr = pr0 + st * S_PR_STRIDE;
+                const uint32_t xb = tm + T_XB + 64 * (k & 1);
                 TRACE(k, 0);
                 if (NEEDU) {
                     const uint32_t vt = v0 + st * S_V_STRIDE;
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma_bf16(tm + T_D3, mdesc(vt + s * 2048, 8192), kdesc(tu + s * 32), ID2, s > 0);
+                        mma_bf16(tm + T_D3, mdesc(vt + s * 2048, 8192), kdesc(pr + 8192 + s * 32), ID2, s > 0);
                 }
-                if (!wait_bar(bars, B_EX, k & 1, errflag)) { ok = false; break; }
+                if (!wait_bar(bars, B_EX, k & 1, errflag) || !wait_bar(bars, B_EW, k & 1, errflag)) {
+                    ok = false;
+                    break;
+                }
                 TRACE(k, 1);
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_bf16_ta(tm + T_D3, tm + T_XB + 8 * s, mdesc(wt + s * 2048, 16384), ID3,
+                    mma_bf16_ta(tm + T_D3, xb + 8 * s, mdesc(wt + s * 2048, 16384), ID3,
                                 (NEEDU || s > 0) ? 1u : 0u);
                 commit(&bars[B_MMA3]);
                 TRACE(k, 2);
-                if (OUT) {
-                    if (k >= 1 && !wait_bar(bars, B_EPI, (k - 1) & 1, errflag)) { ok = false; break; }
-                    fence_after_sync();
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t off = 8192 + (s >> 2) * 16384 + (s & 3) * 32;
-                        mma_bf16_ta(tm + T_D4, tm + T_XB + 8 * s, kdesc(kq + off), ID4, s > 0);
-                    }
-                }
-                TRACE(k, 30);
-                if (k + 1 < n && !prep_mma1(k + 1)) { ok = false; break; }
+                // W' of the next chunk while the state warps convert V' (D2 is free: W'^T of
+                // this chunk was read out before the MMA above was issued)
+                if (k + 1 < n && !issue_w(k + 1)) { ok = false; break; }
                 TRACE(k, 3);
                 if (!wait_bar(bars, B_EV, k & 1, errflag)) { ok = false; break; }
                 TRACE(k, 4);
@@ -280,24 +303,27 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_bf16_ta(tm + T_XF, tm + T_D3 + 32 + 8 * s, mdesc(kq + s * 2048, 16384), ID5, 1u);
-                if (OUT) {
-                    const uint32_t pp = p0 + (k & 1) * S_P_STRIDE;
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_bf16_ta(tm + T_D5, tm + T_D3 + 8 * s, kdesc(pp + s * 32), ID4, s > 0);
-                }
                 commit(&bars[B_MMA5]);
                 TRACE(k, 5);
-                if (k + 1 < n) {
-                    if (!prep_mma2(k + 1)) { ok = false; break; }
-                    TRACE(k, 6);
-                    if (!wait_bar(bars, B_EW, (k + 1) & 1, errflag)) { ok = false; break; }
-                    TRACE(k, 7);
+                if (OUT) {
+                    if (k >= 1 && !wait_bar(bars, B_EPI, (k - 1) & 1, errflag)) { ok = false; break; }
+                    fence_after_sync();
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t off = 8192 + (s >> 2) * 16384 + (s & 3) * 32;
+                        mma_bf16_ta(tm + T_D4, xb + 8 * s, kdesc(kq + off), ID4, s > 0);
+                    }
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_bf16_ta(tm + T_D5, tm + T_D3 + 8 * s, kdesc(pr + 16384 + s * 32), ID4, s > 0);
+                    commit(&bars[B_MMA4]);
                 }
+                commit(&bars[B_EMPTY0 + st]);  // every reader of this stage has been issued
+                TRACE(k, 7);
             }
             // drain: wait for every issued MMA before TMEM may be released
-            commit(&bars[B_MMA1]);
-            mbar_wait(&bars[B_MMA1], n_mma1 & 1);
+            commit(&bars[B_MMA2]);
+            mbar_wait(&bars[B_MMA2], n_mma2 & 1);
         }
         __syncwarp();
     } else if (w == 2) {
@@ -306,12 +332,11 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             const int st = k & 1, gs = k & (NGATE - 1);
             const int64_t tc = t0 + int64_t(cb + k) * CH;
             const int c = int((t1 - tc) < int64_t(CH) ? (t1 - tc) : int64_t(CH));
-            float gv[2], bv[2];
+            float gv[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {  // issue the global loads before waiting for a buffer
                 const int r = 2 * lane + u;
                 gv[u] = r < c ? P.g[(tc + r) * P.Hv + j] : 0.f;
-                bv[u] = r < c ? P.beta[(tc + r) * P.Hv + j] : 0.f;
             }
             TRACE(k, 21);
             if (k >= NGATE && !warp_wait(bars, B_GFREE0 + gs, ((k - NGATE) >> 2) & 1, errflag)) break;
@@ -330,18 +355,13 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int r = 2 * lane + u;
-                const float e = expf(gm[u]);
                 gb.gam[r] = gm[u];
-                gb.e[r] = e;
-                gb.einv[r] = expf(-gm[u]);
+                gb.e[r] = expf(gm[u]);
                 gb.kd[r] = expf(last - gm[u]);
-                gb.beta[r] = bv[u];
-                gb.be[r] = bv[u] * e;
             }
             if (lane == 0) {
                 gb.eC = expf(last);
                 gb.c = c;
-                gb.pairwise = (last < -80.f || !(last == last)) ? 1 : 0;
             }
             if (c < CH) {  // rows past the sequence end: zero them (they may hold other tokens)
                 if (!warp_wait(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) break;
@@ -366,18 +386,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         // ------------------------------------------------------------ state warps
         const int v = tid - 128;                     // TMEM lane = value column of h
         const uint32_t lb = uint32_t(32 * (w & 3)) << 16;
-        {
-            float xv[16];
-            for (int c0 = 0; c0 < 128; c0 += 16) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int dk = c0 + i;
-                    xv[i] = x0 ? x0[dk * VD + v] : ((KIND == TK_TRANS && dk == v) ? 1.f : 0.f);
-                }
-                tmem_st16(tm + lb + T_XF + c0, xv);
-            }
-            tmem_st_wait();
-        }
+        init_state_half<KIND>(tm, lb, 0, v, x0);
         bool ok = true;
         for (int k = 0; ok && k < n; ++k) {
             const int gs = k & (NGATE - 1);
@@ -389,28 +398,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 fence_after_sync();
             }
             if (v == 0) TRACE(k, 17);
-            const float eC = gb.eC;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-                float x[32];
-                tmem_ld32(tm + lb + T_XF + c0, x);
-                tmem_ld_wait();
-                if (KIND == TK_HIST) {
-                    __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(P.hist) +
-                                        ((hist_base + cb + k) * P.Hv + j) * (KD * VD);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
-                }
-                float pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
-                tmem_st16(tm + lb + T_XB + c0 / 2, pk);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] *= eC;
-                tmem_st16(tm + lb + T_XF + c0, x);
-                tmem_st16(tm + lb + T_XF + c0 + 16, x + 16);
-            }
-            tmem_st_wait();
+            convert_state_half<KIND>(P, tm, lb, T_XB + 64 * (k & 1), 0, v, gb.eC, hist_base + cb + k, j);
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_EX]);
@@ -465,170 +453,12 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             }
         }
     } else if (w >= 8 && w < 12) {
-        // ------------------------------------------------------------ prep warps
-        const int t = tid - 256;                     // TMEM lane
+        // ------------------------------------------------------------ W'^T + state warps
+        const int t = tid - 256;                     // TMEM lane: key row dk / value column v
         const uint32_t lb = uint32_t(32 * (w & 3)) << 16;
-        float* sA = reinterpret_cast<float*>(sm + S_A);
-        float* sT = reinterpret_cast<float*>(sm + S_T);
-        float* sTmp = reinterpret_cast<float*>(sm + S_TMP);
-        const int i = t & 63;
-        for (int k = 0; k < n; ++k) {
-            const int st = k & 1;
-            const int gs = k & (NGATE - 1);
-            const Gate& gb = gates[gs];
-            if (t == 0) TRACE(k, 8);
-            if (!group_wait(bars, B_GATE0 + gs, (k >> 2) & 1, errflag)) break;
-            if (!group_wait(bars, B_MMA1, k & 1, errflag)) break;
-            if (t == 0) TRACE(k, 9);
-            fence_after_sync();
-            // A (threads 0-63: rows of K K^T) and P (threads 64-127: rows of Q K^T)
-            {
-                const bool pw = gb.pairwise != 0;
-                const float gi = gb.gam[i];
-                const float ri = (t < 64) ? gb.be[i] : gb.e[i];   // row factor
-                const float bi = gb.beta[i];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float d[32];
-                    tmem_ld32(tm + lb + T_D1 + 32 * half, d);
-                    tmem_ld_wait();
-                    if (t == 0 && half == 0) TRACE(k, 28);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int jj = 32 * half + q;
-                        float f;
-                        if (!pw) {
-                            f = ri * gb.einv[jj];
-                        } else {
-                            f = expf(gi - gb.gam[jj]);
-                            if (t < 64) f *= bi;
-                        }
-                        const bool keep = (t < 64) ? (i > jj) : (i >= jj);
-                        d[q] = keep ? f * d[q] : 0.f;
-                    }
-                    if (t < 64) {
-#pragma unroll
-                        for (int q = 0; q < 32; q += 4)
-                            *reinterpret_cast<float4*>(sA + i * LDA + 32 * half + q) =
-                                make_float4(d[q], d[q + 1], d[q + 2], d[q + 3]);
-                    } else if (OUT) {
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch)
-                            st_chunk8(sm + S_P + st * S_P_STRIDE, i, 4 * half + ch, d + 8 * ch);
-                    }
-                }
-                if (OUT && t >= 64) fence_proxy_async_smem();
-            }
-            named_sync(1, 128);
-            if (t == 0) TRACE(k, 10);
-            // T = (I + A)^-1.  Diagonal 16 x 16 blocks by substitution: warp q inverts block q
-            // (lane = column) ...
-            const int q = w - 8;
-            if (lane < 16) {
-                const int b0 = 16 * q, col = lane;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-                    for (int m = 0; m < r; ++m) {
-                        if (m & 1) acc1 = fmaf(sA[(b0 + r) * LDA + b0 + m], x[m], acc1);
-                        else acc0 = fmaf(sA[(b0 + r) * LDA + b0 + m], x[m], acc0);
-                    }
-                    x[r] = (r == col) ? 1.f : (r < col ? 0.f : -(acc0 + acc1));
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) sT[(b0 + r) * LDA + b0 + col] = x[r];
-            }
-            named_sync(1, 128);
-            if (t == 0) TRACE(k, 24);
-            // ... then the off-diagonal blocks, one block sub-diagonal per step and one block
-            // per warp, on TF32 tensor-core tiles:  X = sum_{M=J}^{I-1} A_IM T_MJ,
-            // T_IJ = -T_II X.
-            {
-                const int g = lane >> 2, tq = lane & 3;
-                float* xs = sTmp + q * (16 * 20);
-#pragma unroll 1
-                for (int dd = 1; dd < 4; ++dd) {
-                    const int J = q, I = q + dd;
-                    if (I < 4) {
-                        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                        for (int M = J; M < I; ++M) {
-#pragma unroll
-                            for (int kk = 0; kk < 16; kk += 8) {
-                                const float* ar = sA + (16 * I + g) * LDA + 16 * M + kk + tq;
-                                const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * LDA]),
-                                               a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * LDA + 4]);
-#pragma unroll
-                                for (int nt = 0; nt < 2; ++nt) {
-                                    const float* br = sT + (16 * M + kk + tq) * LDA + 16 * J + 8 * nt + g;
-                                    mma_tf32(acc[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * LDA]));
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            xs[g * 20 + 8 * nt + 2 * tq] = acc[nt][0];
-                            xs[g * 20 + 8 * nt + 2 * tq + 1] = acc[nt][1];
-                            xs[(g + 8) * 20 + 8 * nt + 2 * tq] = acc[nt][2];
-                            xs[(g + 8) * 20 + 8 * nt + 2 * tq + 1] = acc[nt][3];
-                        }
-                        __syncwarp();
-                        float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                        for (int kk = 0; kk < 16; kk += 8) {
-                            const float* ar = sT + (16 * I + g) * LDA + 16 * I + kk + tq;
-                            const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * LDA]),
-                                           a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * LDA + 4]);
-#pragma unroll
-                            for (int nt = 0; nt < 2; ++nt) {
-                                const float* br = xs + (kk + tq) * 20 + 8 * nt + g;
-                                mma_tf32(acc2[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * 20]));
-                            }
-                        }
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            float* tr = sT + (16 * I + g) * LDA + 16 * J + 8 * nt + 2 * tq;
-                            tr[0] = -acc2[nt][0];
-                            tr[1] = -acc2[nt][1];
-                            tr[8 * LDA] = -acc2[nt][2];
-                            tr[8 * LDA + 1] = -acc2[nt][3];
-                        }
-                        __syncwarp();
-                    }
-                    named_sync(1, 128);
-                    if (t == 0) TRACE(k, 24 + dd);
-                }
-            }
-            if (t == 0) TRACE(k, 11);
-            // TW = -T diag(beta e) (threads 0-63), TU = T diag(beta) (threads 64-127)
-            if (t < 64 || NEEDU) {
-                const float* cf = (t < 64) ? gb.be : gb.beta;
-                const float sg = (t < 64) ? -1.f : 1.f;
-                unsigned char* tile = sm + ((t < 64) ? S_TW : S_TU);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    float row[8];
-#pragma unroll
-                    for (int q = 0; q < 8; q += 4) {
-                        const int jj = 8 * ch + q;
-                        const float4 tv = *reinterpret_cast<const float4*>(sT + i * LDA + jj);
-                        const float4 fv = *reinterpret_cast<const float4*>(cf + jj);
-                        row[q + 0] = (jj + 0 <= i) ? sg * tv.x * fv.x : 0.f;
-                        row[q + 1] = (jj + 1 <= i) ? sg * tv.y * fv.y : 0.f;
-                        row[q + 2] = (jj + 2 <= i) ? sg * tv.z * fv.z : 0.f;
-                        row[q + 3] = (jj + 3 <= i) ? sg * tv.w * fv.w : 0.f;
-                    }
-                    st_chunk8(tile, i, ch, row);
-                }
-                fence_proxy_async_smem();
-            }
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_ET]);
+        auto convert_w = [&](int k) -> bool {
+            if (!warp_wait(bars, B_MMA2, k & 1, errflag)) return false;
             if (t == 0) TRACE(k, 12);
-            // W'^T from D2 -> smem tile rows dk = t
-            if (!group_wait(bars, B_MMA2, k & 1, errflag)) break;
             fence_after_sync();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -641,11 +471,24 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             fence_proxy_async_smem();
             fence_before_sync();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[B_EW]);
-                mbar_arrive(&bars[B_GFREE0 + gs]);  // done with this chunk's gates
-            }
+            if (lane == 0) mbar_arrive(&bars[B_EW]);
             if (t == 0) TRACE(k, 13);
+            return true;
+        };
+        init_state_half<KIND>(tm, lb, 1, t, x0);
+        bool ok = convert_w(0);
+        for (int k = 0; ok && k < n; ++k) {
+            const Gate& gb = gates[k & (NGATE - 1)];
+            if (!warp_wait(bars, B_GATE0 + (k & (NGATE - 1)), (k >> 2) & 1, errflag)) break;
+            if (k >= 1) {
+                if (!warp_wait(bars, B_MMA5, (k - 1) & 1, errflag)) break;
+                fence_after_sync();
+            }
+            convert_state_half<KIND>(P, tm, lb, T_XB + 64 * (k & 1), 1, t, gb.eC, hist_base + cb + k, j);
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_EX]);
+            if (k + 1 < n) ok = convert_w(k + 1);
         }
     } else if (w >= 12 && OUT) {
         // ------------------------------------------------------------ output warps
@@ -655,7 +498,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         for (int k = 0; k < n; ++k) {
             const int gs = k & (NGATE - 1);
             const Gate& gb = gates[gs];
-            if (!named_and(2, 128, warp_wait(bars, B_MMA5, k & 1, errflag))) break;
+            if (!named_and(2, 128, warp_wait(bars, B_MMA4, k & 1, errflag))) break;
             if (v == 0) TRACE(k, 14);
             fence_after_sync();
             const float sc = P.scale;
@@ -744,19 +587,19 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
             float* out = P.hin + (int64_t(gseg + 1) * P.Hv + j) * KVN;
             const float* x0 = lj == 0 ? h0 : nullptr;
             if (ce <= cb) { copy_state(x0, out, false); return; }
-            tc_scan<TK_STATE>(P, maps, sm, j, t0, t1, cb, ce, x0, out, 0);
+            tc_scan<TK_STATE>(P, maps, sm, j, t0, t1, cb, ce, x0, out, P.plan.chunk_off[s]);
         } else {
             if (lj == 0) return;
             float* out = P.mbuf + (int64_t(gseg) * P.Hv + j) * KVN;
             if (ce <= cb) { copy_state(nullptr, out, true); return; }
-            tc_scan<TK_TRANS>(P, maps, sm, j, t0, t1, cb, ce, nullptr, out, 0);
+            tc_scan<TK_TRANS>(P, maps, sm, j, t0, t1, cb, ce, nullptr, out, P.plan.chunk_off[s]);
         }
     } else {
         if (lj == 0 || blockIdx.z != 0) return;
         const int cb = lj * P.L, w0 = cb - P.warmup;
         const float* x0 = w0 <= 0 ? h0 : nullptr;
         float* out = P.hin + (int64_t(gseg) * P.Hv + j) * KVN;
-        tc_scan<TK_STATE>(P, maps, sm, j, t0, t1, max(w0, 0), cb, x0, out, 0);
+        tc_scan<TK_STATE>(P, maps, sm, j, t0, t1, max(w0, 0), cb, x0, out, P.plan.chunk_off[s]);
     }
 }
 
@@ -826,6 +669,7 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
     e = cudaFuncSetAttribute(k_tc_phase_c<TK_HIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     launch_plan(P, CH, st);
+    launch_prep(P, st);
     if (P.cp != CP_NONE) {
         dim3 ga(P.total_segs, P.Hv, P.cp == CP_EXACT ? 2 : 1);
         timing_begin("fwd_phase_a", st);

@@ -20,6 +20,9 @@ cudaError_t launch_fwd(const Problem& P, int dtype, bool hist, cudaStream_t st);
 void launch_plan(const Problem& P, int C, cudaStream_t st);
 void launch_fixup(const Problem& P, cudaStream_t st);
 
+// Chunk-parallel preparation of the tensor-core path (TW, TU, P tiles into P.prep).
+void launch_prep(const Problem& P, cudaStream_t st);
+
 // TMA descriptors of k, q, v for the tensor-core path.
 struct TcMaps {
     CUtensorMap k, q, v;

@@ -31,6 +31,7 @@ struct Problem {
     float* hin;         // [total_segs, Hv, K, V]  entering state of each segment
     float* mbuf;        // [total_segs, Hv, K, K]  segment transitions (exact CP)
     void* hist;         // [total_chunks, Hv, K, V] entering state of every chunk (bwd)
+    void* prep;         // [total_chunks, Hv, 3] x 8 KB: TW, TU, P tiles (tensor-core path)
     PlanDev plan;
     const int* cu;      // device cu_seqlens or null
     int N, T, Hqk, Hv;

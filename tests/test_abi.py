@@ -96,10 +96,14 @@ def test_workspace_size_and_too_small_workspace(L):
     assert n.value >= 2 * 32 * 8 * 128 * 128 * 4
     rc, msg = fwd_status(L, p, ws_bytes=n.value - 1)
     assert rc == 3 and "workspace" in msg
-    # no context parallelism: only the small plan arrays
-    p2 = problem(L, T=32768, Hqk=2, Hv=8, cp_mode=L.CP_OFF)
+    # no context parallelism: the plan arrays, plus (bf16 tensor-core path) the TW, TU, P
+    # tiles of every (chunk, v-head): 3 x 8 KiB each
+    p2 = problem(L, T=32768, Hqk=2, Hv=8, cp_mode=L.CP_OFF, dtype=1)
     assert L.lib().gdn_chunk_fwd_workspace_size(ctypes.byref(p2), ctypes.byref(n)) == 0
     assert n.value < 4096
+    p3 = problem(L, T=32768, Hqk=2, Hv=8, cp_mode=L.CP_OFF, dtype=0)
+    assert L.lib().gdn_chunk_fwd_workspace_size(ctypes.byref(p3), ctypes.byref(n)) == 0
+    assert 512 * 8 * 3 * 8192 <= n.value < 512 * 8 * 3 * 8192 + 4096
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
