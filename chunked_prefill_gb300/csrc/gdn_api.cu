@@ -95,9 +95,9 @@ gdn_status validate_problem(const gdn_problem* p) {
 // Estimated time of a segmentation with L chunks per segment, in units of one chunk step
 // of the output stage: the waves of the two chunk-scan launches (one CTA per SM) times the
 // chunks a CTA scans, plus the serial fix-up steps.  The step costs are measured ratios on
-// GB300 (segment-transition steps ~0.9 of an output step, a fix-up step ~0.1).
+// GB300 (a segment-transition chunk step ~0.7 of an output chunk step, a fix-up step ~0.45).
 double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int warmup) {
-    constexpr double tC = 1.0, tA = 0.9, tF = 0.1;
+    constexpr double tC = 1.0, tA = 0.7, tF = 0.45;
     long segs = 0, actas = 0;
     int maxn = 0;
     for (int s = 0; s < N; ++s) {

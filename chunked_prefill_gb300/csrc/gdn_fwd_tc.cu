@@ -39,8 +39,11 @@ constexpr int TCT = 512;  // threads (16 warps)
 constexpr int CH = 64;    // chunk
 
 // tensor-memory columns
+// D3 (U^T, then V'^T) is double-buffered by chunk parity at columns 320 and 448; D4 holds
+// O^T = (diag(e) Q h)^T + (P V')^T (the decay e is folded into the Q tile in shared memory).
 constexpr uint32_t T_XF = 0, T_XB = 128 /* 2 x 64: bf16 state copy, by chunk parity */,
-                   T_D2 = 256, T_D3 = 320, T_D4 = 384, T_D5 = 448;
+                   T_D2 = 256, T_D4 = 384;
+__device__ __forceinline__ uint32_t t_d3(int k) { return (k & 1) ? 448u : 320u; }
 
 // shared-memory layout (offsets from a 1024-aligned base)
 constexpr uint32_t S_KQ = 0;            // 2 x 32 KB: rows 0-63 K, 64-127 Q, 2 column blocks
@@ -71,7 +74,7 @@ static_assert(sizeof(Gate) <= GATE_BYTES && sizeof(Gate) % 16 == 0, "gate buffer
 
 enum Bar { B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GFREE0,
            B_GFREE1, B_GFREE2, B_GFREE3, B_MMA2, B_MMA3, B_MMA5, B_MMA4, B_EW, B_EX, B_EV, B_EPI,
-           B_COUNT };
+           B_QS0, B_QS1, B_COUNT };
 
 enum TcKind { TK_STATE = 0, TK_TRANS = 1, TK_OUT = 2, TK_HIST = 3 };
 
@@ -111,10 +114,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bars, int b, uint32_t parity,
     atomicOr(errflag, 1 << b);
     return false;
 }
+// a wait of a role that is not on the state chain: it backs off between tries
+__device__ __forceinline__ bool wait_bar_lazy(uint64_t* bars, int b, uint32_t parity, int* errflag) {
+    if (mbar_wait_sleep(&bars[b], parity, 64)) return true;
+    atomicOr(errflag, 1 << b);
+    return false;
+}
 // warp-uniform wait: lane 0 waits, the result is broadcast, then the warp synchronises
+template <bool LAZY = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bars, int b, uint32_t parity, int* errflag) {
     bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bars, b, parity, errflag);
+    if ((threadIdx.x & 31) == 0)
+        ok = LAZY ? wait_bar_lazy(bars, b, parity, errflag) : wait_bar(bars, b, parity, errflag);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     __syncwarp();
     return ok;
@@ -198,6 +209,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         mbar_init(&bars[B_EX], 8);
         mbar_init(&bars[B_EV], 4);
         mbar_init(&bars[B_EPI], 4);
+        mbar_init(&bars[B_QS0], 1);  // per stage: cannot run two phases ahead of its waiter
+        mbar_init(&bars[B_QS1], 1);
         *errflag = 0;
         mbar_fence_init();
     }
@@ -215,7 +228,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             int issued = 0;
             for (int k = 0; k < n; ++k) {
                 const int st = k & 1;
-                if (k >= 2 && !wait_bar(bars, B_EMPTY0 + st, ((k - 2) >> 1) & 1, errflag)) break;
+                if (k >= 2 && !wait_bar_lazy(bars, B_EMPTY0 + st, ((k - 2) >> 1) & 1, errflag)) break;
                 const int tc = int(t0 + int64_t(cb + k) * CH);
                 uint64_t* full = &bars[B_FULL0 + st];
                 unsigned char* kq = sm + S_KQ + st * S_KQ_STRIDE;
@@ -253,6 +266,13 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             constexpr uint32_t ID5 = make_idesc(128, 128, 0, 1);
             const uint32_t kq0 = smem_addr(sm + S_KQ), v0 = smem_addr(sm + S_V);
             const uint32_t wt = smem_addr(sm + S_WT), pr0 = smem_addr(sm + S_PR);
+            // descriptors are built once; a byte offset `off` within a tile is added to the
+            // start-address field as off >> 4 (addresses stay below 2^18, no carry out)
+            const uint64_t dKm[2] = {mdesc(kq0, 16384), mdesc(kq0 + S_KQ_STRIDE, 16384)};
+            const uint64_t dKk[2] = {kdesc(kq0), kdesc(kq0 + S_KQ_STRIDE)};
+            const uint64_t dV[2] = {mdesc(v0, 8192), mdesc(v0 + S_V_STRIDE, 8192)};
+            const uint64_t dPr[2] = {kdesc(pr0), kdesc(pr0 + S_PR_STRIDE)};
+            const uint64_t dWT = mdesc(wt, 16384);
             bool ok = true;
             int n_mma2 = 0;
             // W'^T = K^T TW^T for chunk k (needs the stage loaded and partial rows masked)
@@ -261,26 +281,30 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 if (!wait_bar(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) return false;
                 if (!wait_bar(bars, B_GATE0 + (k & (NGATE - 1)), (k >> 2) & 1, errflag)) return false;
                 fence_after_sync();
-                const uint32_t kq = kq0 + st * S_KQ_STRIDE, tw = pr0 + st * S_PR_STRIDE;
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_bf16(tm + T_D2, mdesc(kq + s * 2048, 16384), kdesc(tw + s * 32), ID2, s > 0);
+                    mma_bf16(tm + T_D2, (st ? dKm[1] : dKm[0]) + (s * 2048 >> 4), (st ? dPr[1] : dPr[0]) + (s * 32 >> 4), ID2, s > 0);
                 commit(&bars[B_MMA2]);
                 ++n_mma2;
                 return true;
             };
+            // U^T = V^T TU^T for chunk k into D3[k & 1] (needs the stage loaded; issue_w waited)
+            auto issue_u = [&](int k) {
+                const int st = k & 1;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tm + t_d3(k), (st ? dV[1] : dV[0]) + (s * 2048 >> 4),
+                             (st ? dPr[1] : dPr[0]) + ((8192 + s * 32) >> 4), ID2, s > 0);
+            };
             ok = issue_w(0);
+            if (ok && NEEDU) issue_u(0);
+            // Tensor-pipe order per chunk k: V' (MMA-3), W' of k+1, the state update (MMA-5),
+            // U of k+1, then the output products of k -- the state chain never waits behind
+            // the output products.
             for (int k = 0; ok && k < n; ++k) {
                 const int st = k & 1;
-                const uint32_t kq = kq0 + st * S_KQ_STRIDE, pr = pr0 + st * S_PR_STRIDE;
-                const uint32_t xb = tm + T_XB + 64 * (k & 1);
+                const uint32_t xb = tm + T_XB + 64 * (k & 1), d3 = tm + t_d3(k);
                 TRACE(k, 0);
-                if (NEEDU) {
-                    const uint32_t vt = v0 + st * S_V_STRIDE;
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_bf16(tm + T_D3, mdesc(vt + s * 2048, 8192), kdesc(pr + 8192 + s * 32), ID2, s > 0);
-                }
                 if (!wait_bar(bars, B_EX, k & 1, errflag) || !wait_bar(bars, B_EW, k & 1, errflag)) {
                     ok = false;
                     break;
@@ -289,12 +313,9 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_bf16_ta(tm + T_D3, xb + 8 * s, mdesc(wt + s * 2048, 16384), ID3,
-                                (NEEDU || s > 0) ? 1u : 0u);
+                    mma_bf16_ta(d3, xb + 8 * s, dWT + (s * 2048 >> 4), ID3, (NEEDU || s > 0) ? 1u : 0u);
                 commit(&bars[B_MMA3]);
                 TRACE(k, 2);
-                // W' of the next chunk while the state warps convert V' (D2 is free: W'^T of
-                // this chunk was read out before the MMA above was issued)
                 if (k + 1 < n && !issue_w(k + 1)) { ok = false; break; }
                 TRACE(k, 3);
                 if (!wait_bar(bars, B_EV, k & 1, errflag)) { ok = false; break; }
@@ -302,20 +323,24 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_bf16_ta(tm + T_XF, tm + T_D3 + 32 + 8 * s, mdesc(kq + s * 2048, 16384), ID5, 1u);
+                    mma_bf16_ta(tm + T_XF, d3 + 32 + 8 * s, (st ? dKm[1] : dKm[0]) + (s * 2048 >> 4), ID5, 1u);
                 commit(&bars[B_MMA5]);
                 TRACE(k, 5);
+                if (NEEDU && k + 1 < n) issue_u(k + 1);
                 if (OUT) {
                     if (k >= 1 && !wait_bar(bars, B_EPI, (k - 1) & 1, errflag)) { ok = false; break; }
+                    TRACE(k, 25);
+                    if (!wait_bar(bars, B_QS0 + st, (k >> 1) & 1, errflag)) { ok = false; break; }
+                    TRACE(k, 26);
                     fence_after_sync();
 #pragma unroll
                     for (int s = 0; s < 8; ++s) {
                         const uint32_t off = 8192 + (s >> 2) * 16384 + (s & 3) * 32;
-                        mma_bf16_ta(tm + T_D4, xb + 8 * s, kdesc(kq + off), ID4, s > 0);
+                        mma_bf16_ta(tm + T_D4, xb + 8 * s, (st ? dKk[1] : dKk[0]) + (off >> 4), ID4, s > 0);
                     }
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma_bf16_ta(tm + T_D5, tm + T_D3 + 8 * s, kdesc(pr + 16384 + s * 32), ID4, s > 0);
+                        mma_bf16_ta(tm + T_D4, d3 + 8 * s, (st ? dPr[1] : dPr[0]) + ((16384 + s * 32) >> 4), ID4, 1u);
                     commit(&bars[B_MMA4]);
                 }
                 commit(&bars[B_EMPTY0 + st]);  // every reader of this stage has been issued
@@ -339,7 +364,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 gv[u] = r < c ? P.g[(tc + r) * P.Hv + j] : 0.f;
             }
             TRACE(k, 21);
-            if (k >= NGATE && !warp_wait(bars, B_GFREE0 + gs, ((k - NGATE) >> 2) & 1, errflag)) break;
+            if (k >= NGATE && !warp_wait<true>(bars, B_GFREE0 + gs, ((k - NGATE) >> 2) & 1, errflag)) break;
             TRACE(k, 22);
             Gate& gb = gates[gs];
             float run0 = gv[0], run1 = gv[0] + gv[1];
@@ -363,24 +388,51 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 gb.eC = expf(last);
                 gb.c = c;
             }
-            if (c < CH) {  // rows past the sequence end: zero them (they may hold other tokens)
-                if (!warp_wait(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) break;
-                unsigned char* kq = sm + S_KQ + st * S_KQ_STRIDE;
-                unsigned char* vt = sm + S_V + st * S_V_STRIDE;
-                const int rows = CH - c;
-                for (int idx = lane; idx < rows * 16; idx += 32) {
-                    const int r = c + idx / 16, ch = idx % 16;
-                    const int blk = ch >> 3, cc = ch & 7;
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(kq + blk * 16384 + r * 128 + cc * 16) = z;
-                    if (OUT) *reinterpret_cast<uint4*>(kq + blk * 16384 + 8192 + r * 128 + cc * 16) = z;
-                    if (NEEDU) *reinterpret_cast<uint4*>(vt + blk * 8192 + r * 128 + cc * 16) = z;
-                }
-                fence_proxy_async_smem();
-            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_GATE0 + gs]);
             TRACE(k, 23);
+        }
+    } else if (w == 3 && OUT) {
+        // ------------------------------------------------------------ Q scaling warp
+        // Q row i <- exp(gamma_i) Q row i in place, after the stage landed and the gate warp
+        // zeroed rows past the sequence end; O = scale (Q~ h + P V') then needs one accumulator.
+        for (int k = 0; k < n; ++k) {
+            const int st = k & 1, gs = k & (NGATE - 1);
+            if (!warp_wait<true>(bars, B_GATE0 + gs, (k >> 2) & 1, errflag)) break;
+            if (!warp_wait<true>(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) break;
+            TRACE(k, 27);
+            const Gate& gb = gates[gs];
+            unsigned char* kq = sm + S_KQ + st * S_KQ_STRIDE;
+            // lane covers 16-byte piece (lane & 15) of rows 2i + (lane >> 4); eight pieces are
+            // loaded before any is rescaled so the shared-memory latency overlaps
+#pragma unroll
+            for (int b = 0; b < CH / 16; ++b) {
+                uint4 u[8];
+                float e[8];
+                uint4* p[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = (b * 8 + i) * 2 + (lane >> 4), ch = lane & 15;
+                    p[i] = reinterpret_cast<uint4*>(kq + (ch >> 3) * 16384 + 8192 + r * 128 + (ch & 7) * 16);
+                    u[i] = *p[i];
+                    e[i] = gb.e[r];
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t* w4 = reinterpret_cast<uint32_t*>(&u[i]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w4[q]);
+                        w4[q] = pack_bf16(e[i] * __low2float(h), e[i] * __high2float(h));
+                    }
+                    *p[i] = u[i];
+                }
+            }
+            TRACE(k, 29);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_QS0 + st]);
+            TRACE(k, 24);
         }
     } else if (w >= 4 && w < 8) {
         // ------------------------------------------------------------ state warps
@@ -408,8 +460,9 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             if (v == 0) TRACE(k, 19);
             fence_after_sync();
             float vp[64];
-            tmem_ld32(tm + lb + T_D3, vp);
-            tmem_ld32(tm + lb + T_D3 + 32, vp + 32);
+            const uint32_t d3 = t_d3(k);
+            tmem_ld32(tm + lb + d3, vp);
+            tmem_ld32(tm + lb + d3 + 32, vp + 32);
             tmem_ld_wait();
             float p1[16], p2[16], h1[16], h2[16];
 #pragma unroll
@@ -420,10 +473,10 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 h2[i] = __uint_as_float(pack_bf16(vp[32 + 2 * i] * gb.kd[32 + 2 * i],
                                                   vp[32 + 2 * i + 1] * gb.kd[32 + 2 * i + 1]));
             }
-            tmem_st16(tm + lb + T_D3, p1);
-            tmem_st16(tm + lb + T_D3 + 16, p2);
-            tmem_st16(tm + lb + T_D3 + 32, h1);
-            tmem_st16(tm + lb + T_D3 + 48, h2);
+            tmem_st16(tm + lb + d3, p1);
+            tmem_st16(tm + lb + d3 + 16, p2);
+            tmem_st16(tm + lb + d3 + 32, h1);
+            tmem_st16(tm + lb + d3 + 48, h2);
             tmem_st_wait();
             fence_before_sync();
             __syncwarp();
@@ -498,25 +551,25 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         for (int k = 0; k < n; ++k) {
             const int gs = k & (NGATE - 1);
             const Gate& gb = gates[gs];
-            if (!named_and(2, 128, warp_wait(bars, B_MMA4, k & 1, errflag))) break;
+            if (!named_and(2, 128, warp_wait<true>(bars, B_MMA4, k & 1, errflag))) break;
             if (v == 0) TRACE(k, 14);
             fence_after_sync();
             const float sc = P.scale;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float d4[32], d5[32];
+                float d4[32];
                 tmem_ld32(tm + lb + T_D4 + 32 * half, d4);
-                tmem_ld32(tm + lb + T_D5 + 32 * half, d5);
                 tmem_ld_wait();
                 if (half == 1) {
                     fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[B_EPI]);
+                    if (v == 0) TRACE(k, 28);
                 }
 #pragma unroll
                 for (int qq = 0; qq < 32; ++qq) {
                     const int ii = 32 * half + qq;
-                    sO[ii * LDO + v] = __float2bfloat16_rn(sc * fmaf(gb.e[ii], d4[qq], d5[qq]));
+                    sO[ii * LDO + v] = __float2bfloat16_rn(sc * d4[qq]);
                 }
             }
             named_sync(2, 128);

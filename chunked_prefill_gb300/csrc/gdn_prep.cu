@@ -141,15 +141,13 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
         warp_mma<8, false, true>(acc1, Ab, LDK, sK, LDK, rb + 16, 0, KD);
         __syncthreads();  // K and Q tiles consumed: A and T may overwrite them
         const bool pw = *sFlag != 0;
-        unsigned char* ptile = static_cast<unsigned char*>(P.prep) +
-                               ((int64_t(gch) * P.Hv + j) * 3 + 2) * 8192;
+        float* sP32 = sT;  // P in fp32 until it leaves; T overwrites it afterwards
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float(&acc)[8][4] = half ? acc1 : acc0;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int i = rb + 16 * half + gq + 8 * hh;
-                float pv[8][2];  // P values of the two columns 8n + 2t, 8n + 2t + 1
 #pragma unroll
                 for (int n = 0; n < 8; ++n) {
 #pragma unroll
@@ -158,22 +156,23 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
                         const float v = acc[n][2 * hh + u];
                         const float d = pw ? expf(sGam[i] - sGam[jj]) : sE[i] * sEi[jj];
                         if (!qrows) sA[i * LDA + jj] = (i > jj) ? sBeta[i] * d * v : 0.f;
-                        pv[n][u] = (i >= jj) ? d * v : 0.f;
-                    }
-                }
-                if (qrows) {
-                    // the four lanes of a quad hold two columns each of every 8-column chunk:
-                    // gather a chunk through shuffles and let one lane store it
-#pragma unroll
-                    for (int n = 0; n < 8; ++n) {
-                        float ch8[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            ch8[u] = __shfl_sync(0xffffffffu, pv[n][u & 1], (lane & ~3) | (u >> 1));
-                        if (tq == (n & 3)) st_chunk8g(ptile, i, n, ch8);
+                        else sP32[i * LDA + jj] = (i >= jj) ? d * v : 0.f;
                     }
                 }
             }
+        }
+    }
+    __syncthreads();
+    // P leaves as a pre-swizzled bf16 tile: eight threads per 128-byte row
+    {
+        unsigned char* ptile = static_cast<unsigned char*>(P.prep) +
+                               ((int64_t(gch) * P.Hv + j) * 3 + 2) * 8192;
+        for (int it = tid; it < CH * 8; it += PT) {
+            const int r = it >> 3, c8 = it & 7;
+            const float4 a = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
+            const float4 b = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8 + 4);
+            const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            st_chunk8g(ptile, r, c8, x);
         }
     }
     __syncthreads();
@@ -250,23 +249,23 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
             __syncthreads();
         }
     }
-    // TW (threads 0-63) and TU (threads 64-127), row i = tid & 63
+    // TW = -T diag(beta e) and TU = T diag(beta): eight threads per 128-byte row
     {
-        const int i = tid & 63;
-        const bool tw = tid < 64;
-        const float* cf = tw ? sBe : sBeta;
-        const float sg = tw ? -1.f : 1.f;
-        unsigned char* tile = static_cast<unsigned char*>(P.prep) +
-                              ((int64_t(gch) * P.Hv + j) * 3 + (tw ? 0 : 1)) * 8192;
+        unsigned char* base = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * 3 * 8192;
+        for (int it = tid; it < 2 * CH * 8; it += PT) {
+            const int tile = it >> 9, r = (it >> 3) & 63, c8 = it & 7;
+            const float* cf = tile == 0 ? sBe : sBeta;
+            const float sg = tile == 0 ? -1.f : 1.f;
+            const float4 t0 = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
+            const float4 t1 = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8 + 4);
+            const float4 f0 = *reinterpret_cast<const float4*>(cf + 8 * c8);
+            const float4 f1 = *reinterpret_cast<const float4*>(cf + 8 * c8 + 4);
+            const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+            const float fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+            float x[8];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            float row[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int jj = 8 * cc + u;
-                row[u] = (jj <= i) ? sg * sT[i * LDA + jj] * cf[jj] : 0.f;
-            }
-            st_chunk8g(tile, i, cc, row);
+            for (int u = 0; u < 8; ++u) x[u] = (8 * c8 + u <= r) ? sg * tv[u] * fv[u] : 0.f;
+            st_chunk8g(base + tile * 8192, r, c8, x);
         }
     }
 }

@@ -136,11 +136,13 @@ __device__ __forceinline__ void mbar_fence_init() {
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
     uint32_t ok;
+    // the suspend-time hint lets the hardware park the thread until the phase completes
+    // (or ~20 us pass) instead of spinning on issue slots other warps need
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.b32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(phase)
+        : "r"(smem_addr(bar)), "r"(phase), "r"(20000u)
         : "memory");
     return ok != 0;
 }
@@ -157,8 +159,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
 #pragma unroll 1
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < 4; ++i)
             if (mbar_try_wait(bar, phase)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+// The same bounded wait for threads off the critical path: between tries the warp sleeps
+// for sleep_ns so that it leaves the issue slots to the warps doing work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t phase, uint32_t sleep_ns,
+                                                uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, phase)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, phase)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
