@@ -200,8 +200,9 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
     h.off_mbuf = off;
     if (h.cp == gdn::CP_EXACT) off += KVB * size_t(total_segs) * p->Hv;
     off = align_up(off, 256);
-    h.off_prep = off;  // TW, TU, P tiles of every (chunk, v-head): tensor-core path only
-    if (p->dtype == GDN_BF16) off = align_up(off + size_t(3) * 8192 * h.total_chunks * p->Hv, 256);
+    h.off_prep = off;  // W', TU, P tiles of every (chunk, v-head): tensor-core path only
+    if (p->dtype == GDN_BF16)
+        off = align_up(off + size_t(gdn::PREP_TILE_BYTES) * h.total_chunks * p->Hv, 256);
     if (backward) {
         const size_t elem = p->dtype == GDN_BF16 ? 2 : 4;
         const size_t per_chunk = size_t(128) * 128 * elem * p->Hv;

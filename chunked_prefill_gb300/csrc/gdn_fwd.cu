@@ -443,50 +443,63 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_phase_c(Problem P) {
 }
 
 // Fix-up: hin[g0+j+1] = M_j hin[g0+j] + S_j for j = 1..nseg-2, serially; each CTA owns 8
-// state columns of one (sequence, head).  The transitions are stored transposed (M^T); each
-// one arrives in shared memory by a bulk copy issued one step ahead (double buffer), and
-// thread `row` reads M[row][m] = M^T[m][row] without bank conflicts.  fp32.
-constexpr int FIX_SMEM = 2 * KD * KD * 4 + KD * 8 * 4 + 64;
-__global__ void __launch_bounds__(256) k_fixup(Problem P) {
+// state columns of one (sequence, head).  The transitions are stored transposed (M^T); they
+// arrive in shared memory by bulk copies issued two steps ahead (three buffers), and thread
+// `row` reads M[row][m] = M^T[m][row] without bank conflicts.  512 threads: (row, group of 4
+// columns, half of the inner index m), the two halves summed through shared memory; S_j of
+// the next step is read into registers one step early.  fp32.
+constexpr int FIX_NB = 3;
+constexpr int FIX_SMEM = FIX_NB * KD * KD * 4 + KD * 8 * 4 + 256 * 16 + 64;
+__global__ void __launch_bounds__(512) k_fixup(Problem P) {
     extern __shared__ __align__(128) unsigned char fsm[];
-    float* Ms = reinterpret_cast<float*>(fsm);                       // 2 x 128 x 128
-    float* xs = reinterpret_cast<float*>(fsm + 2 * KD * KD * 4);     // 128 x 8
-    uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + 2 * KD * KD * 4 + KD * 8 * 4);
+    float* Ms = reinterpret_cast<float*>(fsm);                                // FIX_NB x 128 x 128
+    float* xs = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4);         // 128 x 8
+    float4* part = reinterpret_cast<float4*>(fsm + FIX_NB * KD * KD * 4 + KD * 8 * 4);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + FIX_NB * KD * KD * 4 + KD * 8 * 4 + 256 * 16);
     const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * 8;
     const int g0 = P.plan.seg_off[s], nseg = P.plan.seg_off[s + 1] - g0;
     if (nseg <= 2) return;
-    const int row = threadIdx.x & 127, c0 = (threadIdx.x >> 7) * 4;
+    const int last = nseg - 2;  // steps 1..last
+    const int t = threadIdx.x & 255, kh = threadIdx.x >> 8;
+    const int row = t & 127, c0 = (t >> 7) * 4;
     auto mt = [&](int lj) { return P.mbuf + (int64_t(g0 + lj) * P.Hv + j) * KV; };
+    auto hp = [&](int lj) {
+        return reinterpret_cast<float4*>(P.hin + (int64_t(g0 + lj) * P.Hv + j) * KV + row * VD + cb + c0);
+    };
     if (threadIdx.x == 0) {
-        tc::mbar_init(&bar[0], 1);
-        tc::mbar_init(&bar[1], 1);
+        for (int b = 0; b < FIX_NB; ++b) tc::mbar_init(&bar[b], 1);
         tc::mbar_fence_init();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        tc::mbar_expect_tx(&bar[0], KD * KD * 4);
-        tc::bulk_load(Ms, mt(1), KD * KD * 4, &bar[0]);
+        for (int q = 1; q <= min(last, FIX_NB - 1); ++q) {
+            const int b = (q - 1) % FIX_NB;
+            tc::mbar_expect_tx(&bar[b], KD * KD * 4);
+            tc::bulk_load(Ms + b * KD * KD, mt(q), KD * KD * 4, &bar[b]);
+        }
     }
-    {
-        const float4 x = *reinterpret_cast<const float4*>(
-            P.hin + (int64_t(g0 + 1) * P.Hv + j) * KV + row * VD + cb + c0);
-        *reinterpret_cast<float4*>(&xs[row * 8 + c0]) = x;
+    float4 snext = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kh == 0) {
+        *reinterpret_cast<float4*>(&xs[row * 8 + c0]) = *hp(1);
+        snext = *hp(2);
     }
     bool ok = true;
-    for (int lj = 1; lj <= nseg - 2; ++lj) {
-        const int b = (lj - 1) & 1;
-        if (threadIdx.x == 0 && lj + 1 <= nseg - 2) {  // prefetch the next transition
-            tc::mbar_expect_tx(&bar[b ^ 1], KD * KD * 4);
-            tc::bulk_load(Ms + (b ^ 1) * KD * KD, mt(lj + 1), KD * KD * 4, &bar[b ^ 1]);
+    for (int lj = 1; lj <= last; ++lj) {
+        const int q = lj - 1, b = q % FIX_NB;
+        if (threadIdx.x == 0 && lj + FIX_NB - 1 <= last) {  // into the buffer step lj-1 used
+            const int bn = (lj + FIX_NB - 2) % FIX_NB;
+            tc::mbar_expect_tx(&bar[bn], KD * KD * 4);
+            tc::bulk_load(Ms + bn * KD * KD, mt(lj + FIX_NB - 1), KD * KD * 4, &bar[bn]);
         }
-        ok = ok && tc::mbar_wait(&bar[b], ((lj - 1) >> 1) & 1);
+        ok = ok && tc::mbar_wait(&bar[b], (q / FIX_NB) & 1);
         __syncthreads();  // also orders the previous step's xs update
+        const float4 sj = snext;
+        if (kh == 0 && lj + 1 <= last) snext = *hp(lj + 2);
         const float* M = Ms + b * KD * KD;
-        float4* dst = reinterpret_cast<float4*>(P.hin + (int64_t(g0 + lj + 1) * P.Hv + j) * KV +
-                                                row * VD + cb + c0);
-        float4 acc = *dst;  // S_j
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int m0 = kh * (KD / 2);
 #pragma unroll 16
-        for (int m = 0; m < KD; ++m) {
+        for (int m = m0; m < m0 + KD / 2; ++m) {
             const float a = M[m * KD + row];
             const float4 xv = *reinterpret_cast<const float4*>(&xs[m * 8 + c0]);
             acc.x = fmaf(a, xv.x, acc.x);
@@ -494,9 +507,17 @@ __global__ void __launch_bounds__(256) k_fixup(Problem P) {
             acc.z = fmaf(a, xv.z, acc.z);
             acc.w = fmaf(a, xv.w, acc.w);
         }
-        __syncthreads();  // every thread is done with xs and with buffer b
-        *reinterpret_cast<float4*>(&xs[row * 8 + c0]) = acc;
-        *dst = acc;
+        if (kh == 1) part[t] = acc;
+        __syncthreads();  // partial sums visible; everyone is done with xs and buffer b
+        if (kh == 0) {
+            const float4 p = part[t];
+            acc.x = sj.x + (acc.x + p.x);
+            acc.y = sj.y + (acc.y + p.y);
+            acc.z = sj.z + (acc.z + p.z);
+            acc.w = sj.w + (acc.w + p.w);
+            *reinterpret_cast<float4*>(&xs[row * 8 + c0]) = acc;
+            *hp(lj + 1) = acc;
+        }
     }
     if (!ok && threadIdx.x == 0 && P.err) atomicOr(P.err, 1 << 30);
 }
@@ -533,7 +554,7 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
     cudaFuncSetAttribute(k_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
-    k_fixup<<<dim3(P.N, P.Hv, VD / 8), 256, FIX_SMEM, st>>>(P);
+    k_fixup<<<dim3(P.N, P.Hv, VD / 8), 512, FIX_SMEM, st>>>(P);
     timing_end(st);
 }
 

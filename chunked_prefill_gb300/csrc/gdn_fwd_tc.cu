@@ -6,23 +6,23 @@
 // what changes is where the data live and who moves them:
 //
 //   * the state is kept TRANSPOSED in tensor memory, Xt[v][dk] = h[dk][v] (fp32 master,
-//     128 columns) plus a bf16 copy (64 columns) that is the A operand of the V' and Q.h
+//     128 columns) plus a bf16 copy (64 columns) that is the A operand of the V' and Q h
 //     products straight from TMEM;
-//   * K, Q, V chunk tiles arrive by TMA (128-byte swizzle) into a 2-stage ring;
+//   * K, Q, V chunk tiles arrive by TMA (128-byte swizzle) and the chunk-local TW, TU, P
+//     tiles of the preparation kernel by bulk copies, into a 2-stage ring;
 //   * per chunk of 64 tokens (i, j tokens; dk key dim; v value dim):
-//       D1  = [K;Q] K^T                 (128 x 64)    -> A (strictly lower) and P
-//       T   = (I + A)^-1 on CUDA cores                -> TW = -T diag(beta e), TU = T diag(beta)
-//       D2  = K^T TW^T   = W'^T          (dk x i)      -> smem tile (B operand)
+//       D2  = K^T TW^T   = W'^T          (dk x i)      -> shared-memory tile (B operand)
 //       D3  = V^T TU^T + Xt W'^T = V'^T  (v x i)       -> bf16 V'^T and diag(kd) V'^T in TMEM
-//       D4  = Xt Q^T     = (Q h)^T       (v x i)
-//       D5  = V'^T P^T   = (P V')^T      (v x i)       -> O = scale (e * D4 + D5)
-//       Xt += (diag(kd) V')^T K          (v x dk)      after Xt was scaled by e^{gamma_C}
+//       D4a = Xt Q^T     = (Q h)^T       (v x i)
+//       D4b = V'^T P^T   = (P V')^T      (v x i)       -> O = scale (e * D4a + D4b)
+//       Xt  = e^{gamma_C} Xt + (diag(kd) V')^T K       (v x dk)
 //
-// Warp roles (12 warps): 0 TMA producer, 1 MMA issuer (one thread), 2 gates (cumsum of g,
-// exponentials, partial-chunk row masking), 4-7 state warps (TMEM round trips of the state
-// and of V'), 8-11 prep/epilogue warps (A, P, the triangular inverse, TW/TU, W'^T, O).
-// Every wait on an mbarrier is bounded; on a timeout the kernel records an error word and
-// winds down.
+// Warp roles (16 warps): 0 TMA producer; 1 state-chain MMA issuer (W', U, V', state update);
+// 2 gates (cumsum of g and its exponentials); 3 output MMA issuer (D4a, D4b); 4-11 state
+// warps, one warpgroup per half of the key columns (state hand-off, V' conversion; the second
+// also moves W'^T to shared memory); 12-15 output warps.  The two issuers run independently:
+// the state chain never queues behind the output products.  Every wait on an mbarrier is
+// bounded; on a timeout the kernel records an error word and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -38,28 +38,38 @@ using namespace tc;
 constexpr int TCT = 512;  // threads (16 warps)
 constexpr int CH = 64;    // chunk
 
-// tensor-memory columns
-// D3 (U^T, then V'^T) is double-buffered by chunk parity at columns 320 and 448; D4 holds
-// O^T = (diag(e) Q h)^T + (P V')^T (the decay e is folded into the Q tile in shared memory).
-constexpr uint32_t T_XF = 0, T_XB = 128 /* 2 x 64: bf16 state copy, by chunk parity */,
-                   T_D2 = 256, T_D4 = 384;
-__device__ __forceinline__ uint32_t t_d3(int k) { return (k & 1) ? 448u : 320u; }
+// tensor-memory columns: Xt (fp32 state, transposed), its bf16 copy, two chunk buffers DD
+// (by chunk parity) and D4b.  A DD buffer holds [V'^T | (Q h)^T] (64 + 64 columns): U^T is
+// written first (the (Q h)^T half is zero: the output warps clear it after reading it), then
+// one MMA over [W'; Q] adds Xt W'^T and Xt Q^T.  D4b = (P V')^T; the output warps combine
+// O = scale (e (Q h) + P V').
+constexpr uint32_t T_XF = 0, T_XB = 128, T_D4B = 448;
+__device__ __forceinline__ uint32_t t_dd(int k) { return (k & 1) ? 320u : 192u; }
+// converted V' in a DD buffer: tokens [0,32) at columns [0,16) (V'^T) and [16,32)
+// (diag(kd) V'^T), tokens [32,64) at [32,48) and [48,64); K step s covers 16 tokens
+__device__ __forceinline__ uint32_t p_col(int s) { return uint32_t((s >> 1) * 32 + (s & 1) * 8); }
+__device__ __forceinline__ uint32_t kd_col(int s) { return uint32_t((s >> 1) * 32 + 16 + (s & 1) * 8); }
 
-// shared-memory layout (offsets from a 1024-aligned base)
-constexpr uint32_t S_KQ = 0;            // 2 x 32 KB: rows 0-63 K, 64-127 Q, 2 column blocks
-constexpr uint32_t S_KQ_STRIDE = 32768;
-constexpr uint32_t S_V = 65536;         // 2 x 16 KB
-constexpr uint32_t S_V_STRIDE = 16384;
-constexpr uint32_t S_PR = 98304;        // 2 x 24 KB: TW, TU, P tiles ([64 i][64 j] each)
-constexpr uint32_t S_PR_STRIDE = 24576;
-constexpr uint32_t S_WT = 147456;       // 16 KB: W'^T [128 dk][64 i]
-constexpr uint32_t S_GATE = 163840;     // NGATE gate buffers
+// shared-memory layout (offsets from a 1024-aligned base), two stages of
+//   K     [64 tok][128 dk]          2 x 8 KB column blocks (MN-major B of the state update)
+//   WQ    [W' 64 rows; Q 64 rows]   2 column blocks of 16 KB (K-major B of the V'/Qh MMA)
+//   V     [64 tok][128 v]           MN-major A of the U MMA
+//   TU    [64 i][64 j]              K-major B of the U MMA
+// and a ring of NP P tiles ([64 i][64 j], K-major B of the P V' MMA) that the output issuer
+// fills and drains on its own, so the output side never holds back the stage ring.
+constexpr uint32_t S_K = 0, S_K_STRIDE = 16384;
+constexpr uint32_t S_WQ = 32768, S_WQ_STRIDE = 32768;
+constexpr uint32_t S_V = 98304, S_V_STRIDE = 16384;
+constexpr uint32_t S_TU = 131072, S_TU_STRIDE = 8192;
+constexpr uint32_t S_P = 147456, S_P_STRIDE = 8192;
+constexpr int NP = 4;
+constexpr uint32_t S_GATE = 180224;     // NGATE gate buffers
 constexpr int NGATE = 4;
 constexpr uint32_t GATE_BYTES = 1088;
 constexpr int LDO = 136;                              // output staging row stride (bf16)
 constexpr uint32_t S_O = S_GATE + NGATE * GATE_BYTES; // 64 x 136 bf16 output staging
 constexpr uint32_t S_BAR = S_O + 64 * LDO * 2;        // mbarriers
-constexpr uint32_t S_END = S_BAR + 256;
+constexpr uint32_t S_END = S_BAR + 512;              // B_COUNT barriers, TMEM slot, error word
 constexpr uint32_t SMEM_BYTES = S_END + 1024;         // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
@@ -73,8 +83,10 @@ struct alignas(16) Gate {
 static_assert(sizeof(Gate) <= GATE_BYTES && sizeof(Gate) % 16 == 0, "gate buffer");
 
 enum Bar { B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GFREE0,
-           B_GFREE1, B_GFREE2, B_GFREE3, B_MMA2, B_MMA3, B_MMA5, B_MMA4, B_EW, B_EX, B_EV, B_EPI,
-           B_QS0, B_QS1, B_COUNT };
+           B_GFREE1, B_GFREE2, B_GFREE3, B_MMA3, B_MMA5, B_MMA4_0, B_MMA4_1, B_DRAIN, B_EX, B_EV0,
+           B_EV1, B_EPI0, B_EPI1, B_FULLP0, B_EMPTYP0 = B_FULLP0 + NP, B_COUNT = B_EMPTYP0 + NP };
+
+static_assert(B_COUNT * 8 + 8 <= 512, "barrier area");
 
 enum TcKind { TK_STATE = 0, TK_TRANS = 1, TK_OUT = 2, TK_HIST = 3 };
 
@@ -184,6 +196,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                         int64_t hist_base) {
     constexpr bool OUT = KIND == TK_OUT;
     constexpr bool NEEDU = KIND != TK_TRANS;
+    constexpr int NDD = OUT ? 128 : 64;  // columns of a DD buffer the MMAs write
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + B_COUNT * 8);
@@ -195,22 +208,26 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     if (tid == 0) {
         mbar_init(&bars[B_FULL0], 1);
         mbar_init(&bars[B_FULL1], 1);
-        mbar_init(&bars[B_EMPTY0], 1);
+        mbar_init(&bars[B_EMPTY0], 1);  // released by the state-chain issuer
         mbar_init(&bars[B_EMPTY1], 1);
+        for (int b = 0; b < NP; ++b) {
+            mbar_init(&bars[B_FULLP0 + b], 1);
+            mbar_init(&bars[B_EMPTYP0 + b], 1);
+        }
         for (int b = 0; b < NGATE; ++b) {
             mbar_init(&bars[B_GATE0 + b], 1);
-            mbar_init(&bars[B_GFREE0 + b], OUT ? 8 : 4);
+            mbar_init(&bars[B_GFREE0 + b], OUT ? 12 : 8);  // 8 state warps (+ 4 output warps)
         }
-        mbar_init(&bars[B_MMA2], 1);
         mbar_init(&bars[B_MMA3], 1);
         mbar_init(&bars[B_MMA5], 1);
-        mbar_init(&bars[B_MMA4], 1);
-        mbar_init(&bars[B_EW], 4);
+        mbar_init(&bars[B_MMA4_0], 1);
+        mbar_init(&bars[B_MMA4_1], 1);
+        mbar_init(&bars[B_DRAIN], OUT ? 2 : 1);
         mbar_init(&bars[B_EX], 8);
-        mbar_init(&bars[B_EV], 4);
-        mbar_init(&bars[B_EPI], 4);
-        mbar_init(&bars[B_QS0], 1);  // per stage: cannot run two phases ahead of its waiter
-        mbar_init(&bars[B_QS1], 1);
+        mbar_init(&bars[B_EV0], 8);
+        mbar_init(&bars[B_EV1], 8);
+        mbar_init(&bars[B_EPI0], 4);
+        mbar_init(&bars[B_EPI1], 4);
         *errflag = 0;
         mbar_fence_init();
     }
@@ -219,36 +236,52 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = *tmem_slot;
+    if (OUT) {  // the (Q h)^T halves of both DD buffers start at zero
+        if (w >= 12) {
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+            const uint32_t lb = uint32_t(32 * (w & 3)) << 16;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                tmem_st32(tm + lb + t_dd(b) + 64, z);
+                tmem_st32(tm + lb + t_dd(b) + 96, z);
+            }
+            tmem_st_wait();
+        }
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
 
     if (w == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint32_t bytes = 16384u + (OUT ? 16384u : 0u) + (NEEDU ? 16384u : 0u) +
-                                   8192u * (1u + (NEEDU ? 1u : 0u) + (OUT ? 1u : 0u));
+            const uint32_t bytes = 16384u + 16384u + (OUT ? 16384u : 0u) + (NEEDU ? 16384u + 8192u : 0u);
             int issued = 0;
             for (int k = 0; k < n; ++k) {
                 const int st = k & 1;
                 if (k >= 2 && !wait_bar_lazy(bars, B_EMPTY0 + st, ((k - 2) >> 1) & 1, errflag)) break;
                 const int tc = int(t0 + int64_t(cb + k) * CH);
                 uint64_t* full = &bars[B_FULL0 + st];
-                unsigned char* kq = sm + S_KQ + st * S_KQ_STRIDE;
-                unsigned char* pr = sm + S_PR + st * S_PR_STRIDE;
-                const unsigned char* src = static_cast<const unsigned char*>(P.prep) +
-                                           ((hist_base + cb + k) * P.Hv + j) * 3 * 8192;
+                unsigned char* kt = sm + S_K + st * S_K_STRIDE;
+                unsigned char* wq = sm + S_WQ + st * S_WQ_STRIDE;
+                const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
+                                           ((hist_base + cb + k) * P.Hv + j) * PREP_TILE_BYTES;
                 mbar_expect_tx(full, bytes);
-                tma_load_3d(kq, &maps.k, full, 0, qh, tc);
-                tma_load_3d(kq + 16384, &maps.k, full, 64, qh, tc);
-                bulk_load(pr, src, 8192, full);                       // TW
-                if (NEEDU) bulk_load(pr + 8192, src + 8192, 8192, full);   // TU
+                tma_load_3d(kt, &maps.k, full, 0, qh, tc);
+                tma_load_3d(kt + 8192, &maps.k, full, 64, qh, tc);
+                bulk_load(wq, rec + PREP_W, 8192, full);                // W' columns 0-63
+                bulk_load(wq + 16384, rec + PREP_W + 8192, 8192, full); // W' columns 64-127
                 if (OUT) {
-                    tma_load_3d(kq + 8192, &maps.q, full, 0, qh, tc);
-                    tma_load_3d(kq + 16384 + 8192, &maps.q, full, 64, qh, tc);
-                    bulk_load(pr + 16384, src + 16384, 8192, full);   // P
+                    tma_load_3d(wq + 8192, &maps.q, full, 0, qh, tc);
+                    tma_load_3d(wq + 16384 + 8192, &maps.q, full, 64, qh, tc);
                 }
                 if (NEEDU) {
                     unsigned char* vt = sm + S_V + st * S_V_STRIDE;
                     tma_load_3d(vt, &maps.v, full, 0, j, tc);
                     tma_load_3d(vt + 8192, &maps.v, full, 64, j, tc);
+                    bulk_load(sm + S_TU + st * S_TU_STRIDE, rec + PREP_TU, 8192, full);
                 }
                 issued = k + 1;
             }
@@ -258,103 +291,88 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         }
         __syncwarp();
     } else if (w == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ state-chain MMA issuer
+        // per chunk k: [V'|Qh] (one MMA over [W'; Q]), the state update, then U of k+1 --
+        // only the reuse of a DD buffer two chunks later waits for the output side.
         if (lane == 0) {
-            constexpr uint32_t ID2 = make_idesc(128, 64, 1, 0);
-            constexpr uint32_t ID3 = make_idesc(128, 64, 0, 1);
-            constexpr uint32_t ID4 = make_idesc(128, 64, 0, 0);
+            constexpr uint32_t IDU = make_idesc(128, 64, 1, 0);
+            constexpr uint32_t IDV = make_idesc(128, NDD, 0, 0);
             constexpr uint32_t ID5 = make_idesc(128, 128, 0, 1);
-            const uint32_t kq0 = smem_addr(sm + S_KQ), v0 = smem_addr(sm + S_V);
-            const uint32_t wt = smem_addr(sm + S_WT), pr0 = smem_addr(sm + S_PR);
-            // descriptors are built once; a byte offset `off` within a tile is added to the
-            // start-address field as off >> 4 (addresses stay below 2^18, no carry out)
-            const uint64_t dKm[2] = {mdesc(kq0, 16384), mdesc(kq0 + S_KQ_STRIDE, 16384)};
-            const uint64_t dKk[2] = {kdesc(kq0), kdesc(kq0 + S_KQ_STRIDE)};
-            const uint64_t dV[2] = {mdesc(v0, 8192), mdesc(v0 + S_V_STRIDE, 8192)};
-            const uint64_t dPr[2] = {kdesc(pr0), kdesc(pr0 + S_PR_STRIDE)};
-            const uint64_t dWT = mdesc(wt, 16384);
-            bool ok = true;
-            int n_mma2 = 0;
-            // W'^T = K^T TW^T for chunk k (needs the stage loaded and partial rows masked)
-            auto issue_w = [&](int k) -> bool {
-                const int st = k & 1;
-                if (!wait_bar(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) return false;
-                if (!wait_bar(bars, B_GATE0 + (k & (NGATE - 1)), (k >> 2) & 1, errflag)) return false;
-                fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tm + T_D2, (st ? dKm[1] : dKm[0]) + (s * 2048 >> 4), (st ? dPr[1] : dPr[0]) + (s * 32 >> 4), ID2, s > 0);
-                commit(&bars[B_MMA2]);
-                ++n_mma2;
-                return true;
-            };
-            // U^T = V^T TU^T for chunk k into D3[k & 1] (needs the stage loaded; issue_w waited)
+            const uint32_t k0a = smem_addr(sm + S_K), wq0 = smem_addr(sm + S_WQ);
+            const uint32_t v0a = smem_addr(sm + S_V), tu0 = smem_addr(sm + S_TU);
+            const uint64_t dK[2] = {mdesc(k0a, 8192), mdesc(k0a + S_K_STRIDE, 8192)};
+            const uint64_t dWQ[2] = {kdesc(wq0), kdesc(wq0 + S_WQ_STRIDE)};
+            const uint64_t dV[2] = {mdesc(v0a, 8192), mdesc(v0a + S_V_STRIDE, 8192)};
+            const uint64_t dTU[2] = {kdesc(tu0), kdesc(tu0 + S_TU_STRIDE)};
+            // U^T = V^T TU^T for chunk k into the V' half of its DD buffer
             auto issue_u = [&](int k) {
                 const int st = k & 1;
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_bf16(tm + t_d3(k), (st ? dV[1] : dV[0]) + (s * 2048 >> 4),
-                             (st ? dPr[1] : dPr[0]) + ((8192 + s * 32) >> 4), ID2, s > 0);
+                    mma_bf16(tm + t_dd(k), (st ? dV[1] : dV[0]) + (s * 2048 >> 4),
+                             (st ? dTU[1] : dTU[0]) + (s * 32 >> 4), IDU, s > 0);
             };
-            ok = issue_w(0);
-            if (ok && NEEDU) issue_u(0);
-            // Tensor-pipe order per chunk k: V' (MMA-3), W' of k+1, the state update (MMA-5),
-            // U of k+1, then the output products of k -- the state chain never waits behind
-            // the output products.
+            bool ok = true;
+            if (NEEDU) {
+                ok = wait_bar(bars, B_FULL0, 0, errflag);
+                if (ok) {
+                    fence_after_sync();
+                    issue_u(0);
+                }
+            }
             for (int k = 0; ok && k < n; ++k) {
                 const int st = k & 1;
-                const uint32_t xb = tm + T_XB + 64 * (k & 1), d3 = tm + t_d3(k);
+                const uint32_t dd = tm + t_dd(k);
                 TRACE(k, 0);
-                if (!wait_bar(bars, B_EX, k & 1, errflag) || !wait_bar(bars, B_EW, k & 1, errflag)) {
+                if ((!NEEDU && !wait_bar(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) ||
+                    !wait_bar(bars, B_EX, k & 1, errflag)) {
                     ok = false;
                     break;
                 }
                 TRACE(k, 1);
                 fence_after_sync();
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_bf16_ta(d3, xb + 8 * s, dWT + (s * 2048 >> 4), ID3, (NEEDU || s > 0) ? 1u : 0u);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_bf16_ta(dd, tm + T_XB + 8 * s, (st ? dWQ[1] : dWQ[0]) + (off >> 4), IDV,
+                                (NEEDU || s > 0) ? 1u : 0u);
+                }
                 commit(&bars[B_MMA3]);
                 TRACE(k, 2);
-                if (k + 1 < n && !issue_w(k + 1)) { ok = false; break; }
-                TRACE(k, 3);
-                if (!wait_bar(bars, B_EV, k & 1, errflag)) { ok = false; break; }
+                if (!wait_bar(bars, B_EV0 + (k & 1), (k >> 1) & 1, errflag)) { ok = false; break; }
                 TRACE(k, 4);
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_bf16_ta(tm + T_XF, d3 + 32 + 8 * s, (st ? dKm[1] : dKm[0]) + (s * 2048 >> 4), ID5, 1u);
+                    mma_bf16_ta(tm + T_XF, dd + kd_col(s), (st ? dK[1] : dK[0]) + (s * 2048 >> 4), ID5, 1u);
                 commit(&bars[B_MMA5]);
+                commit(&bars[B_EMPTY0 + st]);  // last reader of this stage on this issuer
                 TRACE(k, 5);
-                if (NEEDU && k + 1 < n) issue_u(k + 1);
-                if (OUT) {
-                    if (k >= 1 && !wait_bar(bars, B_EPI, (k - 1) & 1, errflag)) { ok = false; break; }
-                    TRACE(k, 25);
-                    if (!wait_bar(bars, B_QS0 + st, (k >> 1) & 1, errflag)) { ok = false; break; }
-                    TRACE(k, 26);
-                    fence_after_sync();
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t off = 8192 + (s >> 2) * 16384 + (s & 3) * 32;
-                        mma_bf16_ta(tm + T_D4, xb + 8 * s, (st ? dKk[1] : dKk[0]) + (off >> 4), ID4, s > 0);
+                if (NEEDU && k + 1 < n) {
+                    if (!wait_bar(bars, B_FULL0 + ((k + 1) & 1), ((k + 1) >> 1) & 1, errflag)) {
+                        ok = false;
+                        break;
                     }
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_bf16_ta(tm + T_D4, d3 + 8 * s, (st ? dPr[1] : dPr[0]) + ((16384 + s * 32) >> 4), ID4, 1u);
-                    commit(&bars[B_MMA4]);
+                    // DD[(k+1) & 1] last held chunk k-1, read by its output warps
+                    if (OUT && k >= 1 &&
+                        !wait_bar(bars, B_EPI0 + ((k - 1) & 1), ((k - 1) >> 1) & 1, errflag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after_sync();
+                    issue_u(k + 1);
                 }
-                commit(&bars[B_EMPTY0 + st]);  // every reader of this stage has been issued
                 TRACE(k, 7);
             }
-            // drain: wait for every issued MMA before TMEM may be released
-            commit(&bars[B_MMA2]);
-            mbar_wait(&bars[B_MMA2], n_mma2 & 1);
+            // drain: every MMA issued here has completed before TMEM may be released
+            commit(&bars[B_DRAIN]);
+            mbar_wait(&bars[B_DRAIN], 0);
         }
         __syncwarp();
     } else if (w == 2) {
         // ------------------------------------------------------------ gates
         for (int k = 0; k < n; ++k) {
-            const int st = k & 1, gs = k & (NGATE - 1);
+            const int gs = k & (NGATE - 1);
             const int64_t tc = t0 + int64_t(cb + k) * CH;
             const int c = int((t1 - tc) < int64_t(CH) ? (t1 - tc) : int64_t(CH));
             float gv[2];
@@ -393,103 +411,114 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             TRACE(k, 23);
         }
     } else if (w == 3 && OUT) {
-        // ------------------------------------------------------------ Q scaling warp
-        // Q row i <- exp(gamma_i) Q row i in place, after the stage landed and the gate warp
-        // zeroed rows past the sequence end; O = scale (Q~ h + P V') then needs one accumulator.
-        for (int k = 0; k < n; ++k) {
-            const int st = k & 1, gs = k & (NGATE - 1);
-            if (!warp_wait<true>(bars, B_GATE0 + gs, (k >> 2) & 1, errflag)) break;
-            if (!warp_wait<true>(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) break;
-            TRACE(k, 27);
-            const Gate& gb = gates[gs];
-            unsigned char* kq = sm + S_KQ + st * S_KQ_STRIDE;
-            // lane covers 16-byte piece (lane & 15) of rows 2i + (lane >> 4); eight pieces are
-            // loaded before any is rescaled so the shared-memory latency overlaps
+        // ------------------------------------------------------------ output MMA issuer
+        // D4b = (P V')^T once V' of chunk k is converted and the output warps have read D4b
+        // of chunk k-1.
+        if (lane == 0) {
+            constexpr uint32_t ID4 = make_idesc(128, 64, 0, 0);
+            const uint32_t p0 = smem_addr(sm + S_P);
+            auto load_p = [&](int q) {  // P of chunk q into ring slot q % NP
+                const int b = q % NP;
+                const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
+                                           ((hist_base + cb + q) * P.Hv + j) * PREP_TILE_BYTES;
+                mbar_expect_tx(&bars[B_FULLP0 + b], 8192);
+                bulk_load(sm + S_P + b * S_P_STRIDE, rec + PREP_P, 8192, &bars[B_FULLP0 + b]);
+            };
+            int issued = 0, used = 0;
+            for (; issued < NP - 1 && issued < n; ++issued) load_p(issued);
+            for (int k = 0; k < n; ++k) {
+                const int b = k % NP;
+                if (!wait_bar(bars, B_FULLP0 + b, (k / NP) & 1, errflag)) break;
+                used = k + 1;
+                if (k >= 1 && !wait_bar(bars, B_EPI0 + ((k - 1) & 1), ((k - 1) >> 1) & 1, errflag)) break;
+                if (!wait_bar(bars, B_EV0 + (k & 1), (k >> 1) & 1, errflag)) break;
+                TRACE(k, 10);
+                fence_after_sync();
+                const uint32_t dd = tm + t_dd(k);
+                const uint64_t dP = kdesc(p0 + b * S_P_STRIDE);
 #pragma unroll
-            for (int b = 0; b < CH / 16; ++b) {
-                uint4 u[8];
-                float e[8];
-                uint4* p[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = (b * 8 + i) * 2 + (lane >> 4), ch = lane & 15;
-                    p[i] = reinterpret_cast<uint4*>(kq + (ch >> 3) * 16384 + 8192 + r * 128 + (ch & 7) * 16);
-                    u[i] = *p[i];
-                    e[i] = gb.e[r];
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    uint32_t* w4 = reinterpret_cast<uint32_t*>(&u[i]);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w4[q]);
-                        w4[q] = pack_bf16(e[i] * __low2float(h), e[i] * __high2float(h));
-                    }
-                    *p[i] = u[i];
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16_ta(tm + T_D4B, dd + p_col(s), dP + (s * 32 >> 4), ID4, s > 0);
+                commit(&bars[B_MMA4_0 + (k & 1)]);
+                commit(&bars[B_EMPTYP0 + b]);
+                TRACE(k, 11);
+                const int q = k + NP - 1;  // refill the slot chunk k-1 used
+                if (q < n) {
+                    if (q >= NP && !wait_bar(bars, B_EMPTYP0 + q % NP, ((q - NP) / NP) & 1, errflag)) break;
+                    load_p(q);
+                    issued = q + 1;
                 }
             }
-            TRACE(k, 29);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_QS0 + st]);
-            TRACE(k, 24);
+            for (int q = used; q < issued; ++q) mbar_wait(&bars[B_FULLP0 + q % NP], (q / NP) & 1);
+            commit(&bars[B_DRAIN]);
         }
-    } else if (w >= 4 && w < 8) {
+        __syncwarp();
+    } else if (w >= 4 && w < 12) {
         // ------------------------------------------------------------ state warps
-        const int v = tid - 128;                     // TMEM lane = value column of h
+        // two warpgroups, one per half of the key columns of the state (hf); each converts
+        // the V' columns of its half of the chunk's tokens
+        const int hf = w >= 8 ? 1 : 0;
+        const int v = tid - (hf ? 256 : 128);        // TMEM lane = value column
         const uint32_t lb = uint32_t(32 * (w & 3)) << 16;
-        init_state_half<KIND>(tm, lb, 0, v, x0);
+        init_state_half<KIND>(tm, lb, hf, v, x0);
         bool ok = true;
         for (int k = 0; ok && k < n; ++k) {
             const int gs = k & (NGATE - 1);
             const Gate& gb = gates[gs];
             if (!warp_wait(bars, B_GATE0 + gs, (k >> 2) & 1, errflag)) { ok = false; break; }
-            if (v == 0) TRACE(k, 16);
+            if (v == 0 && !hf) TRACE(k, 16);
             if (k >= 1) {
                 if (!warp_wait(bars, B_MMA5, (k - 1) & 1, errflag)) { ok = false; break; }
                 fence_after_sync();
             }
-            if (v == 0) TRACE(k, 17);
-            convert_state_half<KIND>(P, tm, lb, T_XB + 64 * (k & 1), 0, v, gb.eC, hist_base + cb + k, j);
+            if (v == 0 && !hf) TRACE(k, 17);
+            convert_state_half<KIND>(P, tm, lb, T_XB, hf, v, gb.eC, hist_base + cb + k, j);
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_EX]);
-            if (v == 0) TRACE(k, 18);
-            // V' = D3 -> bf16 V'^T (columns 0-31) and diag(kd) V'^T (columns 32-63)
+            if (v == 0 && !hf) TRACE(k, 18);
+            // V' of tokens [32 hf, 32 hf + 32): fp32 -> bf16 V'^T and bf16 diag(kd) V'^T, both
+            // inside the 32 columns just read (no other warp touches them)
             if (!warp_wait(bars, B_MMA3, k & 1, errflag)) { ok = false; break; }
-            if (v == 0) TRACE(k, 19);
+            if (v == 0 && !hf) TRACE(k, 19);
             fence_after_sync();
-            float vp[64];
-            const uint32_t d3 = t_d3(k);
-            tmem_ld32(tm + lb + d3, vp);
-            tmem_ld32(tm + lb + d3 + 32, vp + 32);
+            const uint32_t d3 = tm + lb + t_dd(k) + 32 * hf;
+            float vp[32];
+            tmem_ld32(d3, vp);
             tmem_ld_wait();
-            float p1[16], p2[16], h1[16], h2[16];
+            float p1[16], h1[16], kd[32];
+            {
+                const uint32_t ka = smem_addr(&gb.kd[32 * hf]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 f = lds128f(ka + 16 * i);
+                    kd[4 * i] = f.x;
+                    kd[4 * i + 1] = f.y;
+                    kd[4 * i + 2] = f.z;
+                    kd[4 * i + 3] = f.w;
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                p1[i] = __uint_as_float(pack_bf16(vp[2 * i], vp[2 * i + 1]));
-                p2[i] = __uint_as_float(pack_bf16(vp[32 + 2 * i], vp[32 + 2 * i + 1]));
-                h1[i] = __uint_as_float(pack_bf16(vp[2 * i] * gb.kd[2 * i], vp[2 * i + 1] * gb.kd[2 * i + 1]));
-                h2[i] = __uint_as_float(pack_bf16(vp[32 + 2 * i] * gb.kd[32 + 2 * i],
-                                                  vp[32 + 2 * i + 1] * gb.kd[32 + 2 * i + 1]));
+                const float a = vp[2 * i], b = vp[2 * i + 1];
+                p1[i] = __uint_as_float(pack_bf16(a, b));
+                h1[i] = __uint_as_float(pack_bf16(a * kd[2 * i], b * kd[2 * i + 1]));
             }
-            tmem_st16(tm + lb + d3, p1);
-            tmem_st16(tm + lb + d3 + 16, p2);
-            tmem_st16(tm + lb + d3 + 32, h1);
-            tmem_st16(tm + lb + d3 + 48, h2);
+            tmem_st16(d3, p1);
+            tmem_st16(d3 + 16, h1);
             tmem_st_wait();
             fence_before_sync();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&bars[B_EV]);
+                mbar_arrive(&bars[B_EV0 + (k & 1)]);
                 mbar_arrive(&bars[B_GFREE0 + gs]);  // done with this chunk's gates
             }
-            if (v == 0) TRACE(k, 20);
+            if (v == 0 && !hf) TRACE(k, 20);
         }
         if (ok && warp_wait(bars, B_MMA5, (n - 1) & 1, errflag)) {
             fence_after_sync();
             if (x_out) {
-                for (int c0 = 0; c0 < 128; c0 += 16) {
+                for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 16) {
                     float xv[16];
                     tmem_ld16(tm + lb + T_XF + c0, xv);
                     tmem_ld_wait();
@@ -505,71 +534,52 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 }
             }
         }
-    } else if (w >= 8 && w < 12) {
-        // ------------------------------------------------------------ W'^T + state warps
-        const int t = tid - 256;                     // TMEM lane: key row dk / value column v
-        const uint32_t lb = uint32_t(32 * (w & 3)) << 16;
-        auto convert_w = [&](int k) -> bool {
-            if (!warp_wait(bars, B_MMA2, k & 1, errflag)) return false;
-            if (t == 0) TRACE(k, 12);
-            fence_after_sync();
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float d[32];
-                tmem_ld32(tm + lb + T_D2 + 32 * half, d);
-                tmem_ld_wait();
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) st_chunk8(sm + S_WT, t, 4 * half + ch, d + 8 * ch);
-            }
-            fence_proxy_async_smem();
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_EW]);
-            if (t == 0) TRACE(k, 13);
-            return true;
-        };
-        init_state_half<KIND>(tm, lb, 1, t, x0);
-        bool ok = convert_w(0);
-        for (int k = 0; ok && k < n; ++k) {
-            const Gate& gb = gates[k & (NGATE - 1)];
-            if (!warp_wait(bars, B_GATE0 + (k & (NGATE - 1)), (k >> 2) & 1, errflag)) break;
-            if (k >= 1) {
-                if (!warp_wait(bars, B_MMA5, (k - 1) & 1, errflag)) break;
-                fence_after_sync();
-            }
-            convert_state_half<KIND>(P, tm, lb, T_XB + 64 * (k & 1), 1, t, gb.eC, hist_base + cb + k, j);
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_EX]);
-            if (k + 1 < n) ok = convert_w(k + 1);
-        }
     } else if (w >= 12 && OUT) {
         // ------------------------------------------------------------ output warps
+        // per chunk: read (Q h)^T (clearing it) and D4b, then O = scale (e (Q h) + P V')
         const int v = tid - 384;                     // TMEM lane = value column
         const uint32_t lb = uint32_t(32 * (w & 3)) << 16;
-        __nv_bfloat16* sO = reinterpret_cast<__nv_bfloat16*>(sm + S_O);
+        const uint32_t so = smem_addr(sm + S_O);
         for (int k = 0; k < n; ++k) {
             const int gs = k & (NGATE - 1);
             const Gate& gb = gates[gs];
-            if (!named_and(2, 128, warp_wait<true>(bars, B_MMA4, k & 1, errflag))) break;
+            if (!named_and(2, 128, warp_wait<true>(bars, B_GATE0 + gs, (k >> 2) & 1, errflag) &&
+                                   warp_wait<true>(bars, B_MMA4_0 + (k & 1), (k >> 1) & 1, errflag)))
+                break;
             if (v == 0) TRACE(k, 14);
             fence_after_sync();
             const float sc = P.scale;
+            const uint32_t dqa = tm + lb + t_dd(k) + 64;
 #pragma unroll
+            const uint32_t ge = smem_addr(&gb.e[0]);
             for (int half = 0; half < 2; ++half) {
-                float d4[32];
-                tmem_ld32(tm + lb + T_D4 + 32 * half, d4);
+                float qa[32], pb[32];
+                tmem_ld32(dqa + 32 * half, qa);
+                tmem_ld32(tm + lb + T_D4B + 32 * half, pb);
                 tmem_ld_wait();
+                {  // clear the output columns for the chunk that reuses this buffer
+                    float z[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+                    tmem_st32(dqa + 32 * half, z);
+                }
                 if (half == 1) {
+                    tmem_st_wait();
                     fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[B_EPI]);
+                    if (lane == 0) mbar_arrive(&bars[B_EPI0 + (k & 1)]);
                     if (v == 0) TRACE(k, 28);
                 }
 #pragma unroll
-                for (int qq = 0; qq < 32; ++qq) {
-                    const int ii = 32 * half + qq;
-                    sO[ii * LDO + v] = __float2bfloat16_rn(sc * d4[qq]);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 e4 = lds128f(ge + 4 * (32 * half + 4 * q4));
+                    const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int qq = 4 * q4 + u;
+                        sts16(so + ((32 * half + qq) * LDO + v) * 2,
+                              __bfloat16_as_ushort(__float2bfloat16_rn(sc * fmaf(ev[u], qa[qq], pb[qq]))));
+                    }
                 }
             }
             named_sync(2, 128);
@@ -580,8 +590,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             const int64_t rs = int64_t(P.Hv) * VD;
             for (int idx = v; idx < c * 16; idx += 128) {
                 const int r = idx >> 4, cv = idx & 15;
-                *reinterpret_cast<uint4*>(ob + r * rs + cv * 8) =
-                    *reinterpret_cast<const uint4*>(sO + r * LDO + cv * 8);
+                *reinterpret_cast<uint4*>(ob + r * rs + cv * 8) = lds128(so + (r * LDO + cv * 8) * 2);
             }
             named_sync(2, 128);
             if (lane == 0) mbar_arrive(&bars[B_GFREE0 + gs]);  // done with this chunk's gates

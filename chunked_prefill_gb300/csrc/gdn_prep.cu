@@ -5,10 +5,10 @@
 //     KK = K K^T, QK = Q K^T                        (bf16 mma.sync, fp32 accumulation)
 //     A  = diag(beta) (KK * Dm),  P = QK * D         (D_ij = exp(gamma_i - gamma_j), i >= j)
 //     T  = (I + A)^-1                                (fp32: substitution + TF32 block products)
-//     TW = -T diag(beta e),  TU = T diag(beta)
-// TW, TU and P leave as bf16 64 x 64 tiles already in the 128-byte-swizzled layout the
-// scan's tensor-core operands use, so the scan moves them with plain bulk copies.  Rows and
-// columns past the end of a sequence come out zero (g = beta = 0 and zero K/Q rows there).
+//     TU = T diag(beta),  W' = -T diag(beta e) K     (W' = -W of the pages' WY form)
+// W', TU and P leave as bf16 tiles already in the 128-byte-swizzled layout the scan's
+// tensor-core operands use, so the scan moves them with plain bulk copies.  Rows and columns
+// past the end of a sequence come out zero (g = beta = 0 and zero K/Q rows there).
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "tc05.cuh"
@@ -22,6 +22,7 @@ constexpr int PT = 128;  // threads
 constexpr int CH = 64;
 constexpr int LDK = KD + 8;  // bf16 operand rows
 constexpr int LDA = 68;      // fp32 scratch rows
+constexpr int LDW = 72;      // bf16 TW rows
 
 // The fp32 A and T scratch reuse the K and Q tiles once [K;Q] K^T is in registers (small
 // footprint: five CTAs per SM hide each other's latency).
@@ -33,6 +34,7 @@ struct PrepSmem {
                             oBe = oBeta + CH * 4, oFlag = oBe + CH * 4;
     static constexpr size_t bytes = oFlag + 16;
     static_assert(size_t(CH) * LDA * 4 <= TILE, "fp32 scratch fits a bf16 tile");
+    static_assert(size_t(CH) * LDW * 2 <= TILE && 16384 <= TILE, "TW and the W' staging fit a tile");
 };
 
 __device__ __forceinline__ void st_chunk8g(unsigned char* tile, int r, int ch, const float* x) {
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
     // P leaves as a pre-swizzled bf16 tile: eight threads per 128-byte row
     {
         unsigned char* ptile = static_cast<unsigned char*>(P.prep) +
-                               ((int64_t(gch) * P.Hv + j) * 3 + 2) * 8192;
+                               (int64_t(gch) * P.Hv + j) * PREP_TILE_BYTES + PREP_P;
         for (int it = tid; it < CH * 8; it += PT) {
             const int r = it >> 3, c8 = it & 7;
             const float4 a = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
@@ -249,25 +251,61 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
             __syncthreads();
         }
     }
-    // TW = -T diag(beta e) and TU = T diag(beta): eight threads per 128-byte row
-    {
-        unsigned char* base = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * 3 * 8192;
-        for (int it = tid; it < 2 * CH * 8; it += PT) {
-            const int tile = it >> 9, r = (it >> 3) & 63, c8 = it & 7;
-            const float* cf = tile == 0 ? sBe : sBeta;
-            const float sg = tile == 0 ? -1.f : 1.f;
-            const float4 t0 = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
-            const float4 t1 = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8 + 4);
-            const float4 f0 = *reinterpret_cast<const float4*>(cf + 8 * c8);
-            const float4 f1 = *reinterpret_cast<const float4*>(cf + 8 * c8 + 4);
-            const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-            const float fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-            float x[8];
+    // TU = T diag(beta) leaves as a swizzled bf16 tile (eight threads per 128-byte row);
+    // TW = -T diag(beta e) goes to shared memory (bf16, row stride LDW) over the dead A
+    unsigned char* rec = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * PREP_TILE_BYTES;
+    __nv_bfloat16* sTW = reinterpret_cast<__nv_bfloat16*>(smem + S::oK);
+    for (int it = tid; it < CH * 8; it += PT) {
+        const int r = it >> 3, c8 = it & 7;
+        const float4 t0 = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
+        const float4 t1 = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8 + 4);
+        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+        float xu[8], xw[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = (8 * c8 + u <= r) ? sg * tv[u] * fv[u] : 0.f;
-            st_chunk8g(base + tile * 8192, r, c8, x);
+        for (int u = 0; u < 8; ++u) {
+            const int c = 8 * c8 + u;
+            xu[u] = c <= r ? tv[u] * sBeta[c] : 0.f;
+            xw[u] = c <= r ? -tv[u] * sBe[c] : 0.f;
+        }
+        st_chunk8g(rec + PREP_TU, r, c8, xu);
+        uint4 w4;
+        w4.x = pack_bf16(xw[0], xw[1]);
+        w4.y = pack_bf16(xw[2], xw[3]);
+        w4.z = pack_bf16(xw[4], xw[5]);
+        w4.w = pack_bf16(xw[6], xw[7]);
+        *reinterpret_cast<uint4*>(sTW + r * LDW + 8 * c8) = w4;
+    }
+    __syncthreads();  // T is dead: K comes back (from L2) over it
+    __nv_bfloat16* sK2 = reinterpret_cast<__nv_bfloat16*>(smem + S::oT);
+    for (int idx = tid; idx < CH * 16; idx += PT) {
+        const int r = idx >> 4, cv = idx & 15;
+        uint4 a = make_uint4(0, 0, 0, 0);
+        if (r < c) a = *reinterpret_cast<const uint4*>(kb + r * qk_stride + cv * 8);
+        *reinterpret_cast<uint4*>(sK2 + r * LDK + cv * 8) = a;
+    }
+    __syncthreads();
+    // W' = TW K (64 x 128): warp w owns rows 16w..16w+15; TW is lower triangular, so only the
+    // first 16(w+1) inner indices contribute
+    float acc[16][4];
+    zero_acc(acc);
+    warp_mma<16, false, false>(acc, sTW, LDW, sK2, LDK, 16 * w, 0, 16 * (w + 1));
+    __syncthreads();  // TW consumed: the staging tile overwrites it
+    {
+        unsigned char* stg = reinterpret_cast<unsigned char*>(smem + S::oK);
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = 16 * w + gq + 8 * hh;
+                const uint32_t v2 = pack_bf16(acc[n][2 * hh], acc[n][2 * hh + 1]);
+                *reinterpret_cast<uint32_t*>(stg + (n >> 3) * 8192 + i * 128 + (((n & 7) ^ (i & 7)) << 4) +
+                                             4 * tq) = v2;
+            }
         }
     }
+    __syncthreads();
+    for (int it = tid; it < 16384 / 16; it += PT)
+        reinterpret_cast<uint4*>(rec + PREP_W)[it] = reinterpret_cast<const uint4*>(smem + S::oK)[it];
 }
 
 }  // namespace

@@ -103,7 +103,7 @@ def test_workspace_size_and_too_small_workspace(L):
     assert n.value < 4096
     p3 = problem(L, T=32768, Hqk=2, Hv=8, cp_mode=L.CP_OFF, dtype=0)
     assert L.lib().gdn_chunk_fwd_workspace_size(ctypes.byref(p3), ctypes.byref(n)) == 0
-    assert 512 * 8 * 3 * 8192 <= n.value < 512 * 8 * 3 * 8192 + 4096
+    assert 512 * 8 * 32768 <= n.value < 512 * 8 * 32768 + 4096
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
