@@ -147,7 +147,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bars, int b, uint32_t parity
 // transition kind) into key columns [64 half, 64 half + 64) of the transposed TMEM state.
 template <int KIND>
 __device__ __forceinline__ void init_state_half(uint32_t tm, uint32_t lb, int half, int v,
-                                                const float* x0) {
+                                                const float* x0, uint32_t xf = T_XF) {
     float xv[16];
     for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
 #pragma unroll
@@ -155,7 +155,7 @@ __device__ __forceinline__ void init_state_half(uint32_t tm, uint32_t lb, int ha
             const int dk = c0 + i;
             xv[i] = x0 ? x0[dk * VD + v] : ((KIND == TK_TRANS && dk == v) ? 1.f : 0.f);
         }
-        tmem_st16(tm + lb + T_XF + c0, xv);
+        tmem_st16(tm + lb + xf + c0, xv);
     }
     tmem_st_wait();
 }
@@ -166,12 +166,12 @@ __device__ __forceinline__ void init_state_half(uint32_t tm, uint32_t lb, int ha
 template <int KIND>
 __device__ __forceinline__ void convert_state_half(const Problem& P, uint32_t tm, uint32_t lb,
                                                    uint32_t xb, int half, int v, float eC,
-                                                   int64_t chunk, int j) {
+                                                   int64_t chunk, int j, uint32_t xf = T_XF) {
 #pragma unroll 1
     for (int q = 0; q < 2; ++q) {
         const int c0 = 64 * half + 32 * q;
         float x[32];
-        tmem_ld32(tm + lb + T_XF + c0, x);
+        tmem_ld32(tm + lb + xf + c0, x);
         tmem_ld_wait();
         if (KIND == TK_HIST) {
             __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(P.hist) + (chunk * P.Hv + j) * (KD * VD);
@@ -184,8 +184,8 @@ __device__ __forceinline__ void convert_state_half(const Problem& P, uint32_t tm
         tmem_st16(tm + lb + xb + c0 / 2, pk);
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] *= eC;
-        tmem_st16(tm + lb + T_XF + c0, x);
-        tmem_st16(tm + lb + T_XF + c0 + 16, x + 16);
+        tmem_st16(tm + lb + xf + c0, x);
+        tmem_st16(tm + lb + xf + c0 + 16, x + 16);
     }
     tmem_st_wait();
 }
@@ -344,7 +344,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_bf16_ta(tm + T_XF, dd + kd_col(s), (st ? dK[1] : dK[0]) + (s * 2048 >> 4), ID5, 1u);
+                    mma_bf16_ta(tm + T_XF, dd + (OUT ? kd_col(s) : p_col(s)), (st ? dK[1] : dK[0]) + (s * 2048 >> 4),
+                                ID5, 1u);
                 commit(&bars[B_MMA5]);
                 commit(&bars[B_EMPTY0 + st]);  // last reader of this stage on this issuer
                 TRACE(k, 5);
@@ -504,8 +505,12 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 p1[i] = __uint_as_float(pack_bf16(a, b));
                 h1[i] = __uint_as_float(pack_bf16(a * kd[2 * i], b * kd[2 * i + 1]));
             }
-            tmem_st16(d3, p1);
-            tmem_st16(d3 + 16, h1);
+            if (OUT) {
+                tmem_st16(d3, p1);
+                tmem_st16(d3 + 16, h1);
+            } else {  // only diag(kd) V' is read again (by the state update)
+                tmem_st16(d3, h1);
+            }
             tmem_st_wait();
             fence_before_sync();
             __syncwarp();
@@ -607,6 +612,288 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     }
 }
 
+// Exact context parallelism, first phase, for a segment past the first: the segment's state
+// from zero (S) and its transition (M, from the identity) share the chunk tiles and run as two
+// independent chains in one CTA, so that the tensor-core work of one chain overlaps the
+// CUDA-core hand-offs of the other.  Tensor memory: S chain at columns [0, 256), M chain at
+// [256, 512) (fp32 state, bf16 copy, one V' buffer each).
+//
+// Warp roles: 0 TMA producer; 1 MMA issuer of S (U, V', state update); 2 gates; 3 MMA issuer
+// of M (V', state update); 4-11 state warps of S (one warpgroup per half of the key columns);
+// 12-15 state warps of M (both halves).
+constexpr uint32_t PM = 256;  // tensor-memory column offset of the M chain
+__device__ void tc_scan_pair(const Problem& P, const TcMaps& maps, unsigned char* sm, int j,
+                             int64_t t0, int64_t t1, int cb, int ce, float* s_out, float* m_out,
+                             int64_t hist_base) {
+    enum PB { Q_FULL0 = 0, Q_FULL1, Q_EMPTY0, Q_EMPTY1, Q_GATE0, Q_GFREE0 = Q_GATE0 + NGATE,
+              Q_MMA3S = Q_GFREE0 + NGATE, Q_MMA5S, Q_MMA3M, Q_MMA5M, Q_EXS, Q_EVS, Q_EXM, Q_EVM,
+              Q_DRAIN, Q_COUNT };
+    static_assert(Q_COUNT * 8 + 8 <= 512, "barrier area");
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + Q_COUNT * 8);
+    int* errflag = reinterpret_cast<int*>(sm + S_BAR + Q_COUNT * 8 + 4);
+    Gate* gates = reinterpret_cast<Gate*>(sm + S_GATE);
+    const int G = P.Hv / P.Hqk, qh = j / G;
+    const int n = ce - cb;
+    constexpr uint32_t S_DD = 192, M_XF = PM + T_XF, M_XB = PM + T_XB, M_DD = PM + 192;
+
+    if (tid == 0) {
+        mbar_init(&bars[Q_FULL0], 1);
+        mbar_init(&bars[Q_FULL1], 1);
+        mbar_init(&bars[Q_EMPTY0], 2);  // released by both issuers
+        mbar_init(&bars[Q_EMPTY1], 2);
+        for (int b = 0; b < NGATE; ++b) {
+            mbar_init(&bars[Q_GATE0 + b], 1);
+            mbar_init(&bars[Q_GFREE0 + b], 12);
+        }
+        mbar_init(&bars[Q_MMA3S], 1);
+        mbar_init(&bars[Q_MMA5S], 1);
+        mbar_init(&bars[Q_MMA3M], 1);
+        mbar_init(&bars[Q_MMA5M], 1);
+        mbar_init(&bars[Q_EXS], 8);
+        mbar_init(&bars[Q_EVS], 8);
+        mbar_init(&bars[Q_EXM], 4);
+        mbar_init(&bars[Q_EVM], 4);
+        mbar_init(&bars[Q_DRAIN], 2);
+        *errflag = 0;
+        mbar_fence_init();
+    }
+    if (w == 0) tmem_alloc(tmem_slot, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+    const uint32_t k0a = smem_addr(sm + S_K), wq0 = smem_addr(sm + S_WQ);
+
+    if (w == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t bytes = 16384u + 16384u + 16384u + 8192u;
+            int issued = 0;
+            for (int k = 0; k < n; ++k) {
+                const int st = k & 1;
+                if (k >= 2 && !wait_bar_lazy(bars, Q_EMPTY0 + st, ((k - 2) >> 1) & 1, errflag)) break;
+                const int tc = int(t0 + int64_t(cb + k) * CH);
+                uint64_t* full = &bars[Q_FULL0 + st];
+                unsigned char* kt = sm + S_K + st * S_K_STRIDE;
+                unsigned char* wq = sm + S_WQ + st * S_WQ_STRIDE;
+                unsigned char* vt = sm + S_V + st * S_V_STRIDE;
+                const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
+                                           ((hist_base + cb + k) * P.Hv + j) * PREP_TILE_BYTES;
+                mbar_expect_tx(full, bytes);
+                tma_load_3d(kt, &maps.k, full, 0, qh, tc);
+                tma_load_3d(kt + 8192, &maps.k, full, 64, qh, tc);
+                bulk_load(wq, rec + PREP_W, 8192, full);
+                bulk_load(wq + 16384, rec + PREP_W + 8192, 8192, full);
+                tma_load_3d(vt, &maps.v, full, 0, j, tc);
+                tma_load_3d(vt + 8192, &maps.v, full, 64, j, tc);
+                bulk_load(sm + S_TU + st * S_TU_STRIDE, rec + PREP_TU, 8192, full);
+                issued = k + 1;
+            }
+            for (int k = max(0, issued - 2); k < issued; ++k)
+                mbar_wait(&bars[Q_FULL0 + (k & 1)], (k >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (w == 1 || w == 3) {
+        // ------------------------------------------------------------ MMA issuers (S: w1, M: w3)
+        if (lane == 0) {
+            const bool isS = w == 1;
+            constexpr uint32_t IDU = make_idesc(128, 64, 1, 0);
+            constexpr uint32_t IDV = make_idesc(128, 64, 0, 0);
+            constexpr uint32_t ID5 = make_idesc(128, 128, 0, 1);
+            const uint32_t v0a = smem_addr(sm + S_V), tu0 = smem_addr(sm + S_TU);
+            const uint64_t dK[2] = {mdesc(k0a, 8192), mdesc(k0a + S_K_STRIDE, 8192)};
+            const uint64_t dWQ[2] = {kdesc(wq0), kdesc(wq0 + S_WQ_STRIDE)};
+            const uint64_t dV[2] = {mdesc(v0a, 8192), mdesc(v0a + S_V_STRIDE, 8192)};
+            const uint64_t dTU[2] = {kdesc(tu0), kdesc(tu0 + S_TU_STRIDE)};
+            const uint32_t xf = tm + (isS ? T_XF : M_XF), xb = tm + (isS ? T_XB : M_XB);
+            const uint32_t dd = tm + (isS ? S_DD : M_DD);
+            const int bEX = isS ? Q_EXS : Q_EXM, bEV = isS ? Q_EVS : Q_EVM;
+            const int b3 = isS ? Q_MMA3S : Q_MMA3M, b5 = isS ? Q_MMA5S : Q_MMA5M;
+            auto issue_u = [&](int k) {
+                const int st = k & 1;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(dd, (st ? dV[1] : dV[0]) + (s * 2048 >> 4), (st ? dTU[1] : dTU[0]) + (s * 32 >> 4),
+                             IDU, s > 0);
+            };
+            bool ok = true;
+            if (isS) {
+                ok = wait_bar(bars, Q_FULL0, 0, errflag);
+                if (ok) {
+                    fence_after_sync();
+                    issue_u(0);
+                }
+            }
+            for (int k = 0; ok && k < n; ++k) {
+                const int st = k & 1;
+                if ((!isS && !wait_bar(bars, Q_FULL0 + st, (k >> 1) & 1, errflag)) ||
+                    !wait_bar(bars, bEX, k & 1, errflag)) {
+                    ok = false;
+                    break;
+                }
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_bf16_ta(dd, xb + 8 * s, (st ? dWQ[1] : dWQ[0]) + (off >> 4), IDV, (isS || s > 0) ? 1u : 0u);
+                }
+                commit(&bars[b3]);
+                if (!wait_bar(bars, bEV, k & 1, errflag)) { ok = false; break; }
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16_ta(xf, dd + p_col(s), (st ? dK[1] : dK[0]) + (s * 2048 >> 4), ID5, 1u);
+                commit(&bars[b5]);
+                commit(&bars[Q_EMPTY0 + st]);
+                if (isS && k + 1 < n) {
+                    if (!wait_bar(bars, Q_FULL0 + ((k + 1) & 1), ((k + 1) >> 1) & 1, errflag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after_sync();
+                    issue_u(k + 1);
+                }
+            }
+            commit(&bars[Q_DRAIN]);
+            if (isS) mbar_wait(&bars[Q_DRAIN], 0);
+        }
+        __syncwarp();
+    } else if (w == 2) {
+        // ------------------------------------------------------------ gates
+        for (int k = 0; k < n; ++k) {
+            const int gs = k & (NGATE - 1);
+            const int64_t tc = t0 + int64_t(cb + k) * CH;
+            const int c = int((t1 - tc) < int64_t(CH) ? (t1 - tc) : int64_t(CH));
+            float gv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = 2 * lane + u;
+                gv[u] = r < c ? P.g[(tc + r) * P.Hv + j] : 0.f;
+            }
+            if (k >= NGATE && !warp_wait<true>(bars, Q_GFREE0 + gs, ((k - NGATE) >> 2) & 1, errflag)) break;
+            Gate& gb = gates[gs];
+            float run0 = gv[0], run1 = gv[0] + gv[1];
+            float tot = run1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, tot, off);
+                if (lane >= off) tot += y;
+            }
+            const float excl = tot - run1;
+            const float last = __shfl_sync(0xffffffffu, tot, 31);
+            const float gm[2] = {run0 + excl, run1 + excl};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = 2 * lane + u;
+                gb.gam[r] = gm[u];
+                gb.e[r] = expf(gm[u]);
+                gb.kd[r] = expf(last - gm[u]);
+            }
+            if (lane == 0) {
+                gb.eC = expf(last);
+                gb.c = c;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[Q_GATE0 + gs]);
+        }
+    } else {
+        // ------------------------------------------------------------ state warps
+        // S: warps 4-11, one warpgroup per key half and per half of the chunk's tokens;
+        // M: warps 12-15, everything
+        const bool isS = w < 12;
+        const int hf = (w >= 8 && w < 12) ? 1 : 0;
+        const int v = tid & 127;                     // TMEM lane = value column
+        const uint32_t lb = uint32_t(32 * (w & 3)) << 16;
+        const uint32_t xf = isS ? T_XF : M_XF, xb = isS ? T_XB : M_XB, ddc = isS ? S_DD : M_DD;
+        const int bEX = isS ? Q_EXS : Q_EXM, bEV = isS ? Q_EVS : Q_EVM;
+        const int b3 = isS ? Q_MMA3S : Q_MMA3M, b5 = isS ? Q_MMA5S : Q_MMA5M;
+        if (isS) {
+            init_state_half<TK_STATE>(tm, lb, hf, v, nullptr, xf);
+        } else {
+            init_state_half<TK_TRANS>(tm, lb, 0, v, nullptr, xf);
+            init_state_half<TK_TRANS>(tm, lb, 1, v, nullptr, xf);
+        }
+        bool ok = true;
+        for (int k = 0; ok && k < n; ++k) {
+            const int gs = k & (NGATE - 1);
+            const Gate& gb = gates[gs];
+            if (!warp_wait(bars, Q_GATE0 + gs, (k >> 2) & 1, errflag)) { ok = false; break; }
+            if (k >= 1) {
+                if (!warp_wait(bars, b5, (k - 1) & 1, errflag)) { ok = false; break; }
+                fence_after_sync();
+            }
+            if (isS) {
+                convert_state_half<TK_STATE>(P, tm, lb, xb, hf, v, gb.eC, 0, j, xf);
+            } else {
+                convert_state_half<TK_TRANS>(P, tm, lb, xb, 0, v, gb.eC, 0, j, xf);
+                convert_state_half<TK_TRANS>(P, tm, lb, xb, 1, v, gb.eC, 0, j, xf);
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[bEX]);
+            if (!warp_wait(bars, b3, k & 1, errflag)) { ok = false; break; }
+            fence_after_sync();
+            // diag(kd) V' in bf16 over the fp32 V' of the same tokens (S: one half of them)
+            for (int th = isS ? hf : 0; th < (isS ? hf + 1 : 2); ++th) {
+                const uint32_t d3 = tm + lb + ddc + 32 * th;
+                float vp[32], h1[16];
+                tmem_ld32(d3, vp);
+                const uint32_t ka = smem_addr(&gb.kd[32 * th]);
+                float kd[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 f = lds128f(ka + 16 * i);
+                    kd[4 * i] = f.x;
+                    kd[4 * i + 1] = f.y;
+                    kd[4 * i + 2] = f.z;
+                    kd[4 * i + 3] = f.w;
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    h1[i] = __uint_as_float(pack_bf16(vp[2 * i] * kd[2 * i], vp[2 * i + 1] * kd[2 * i + 1]));
+                tmem_st16(d3, h1);
+            }
+            tmem_st_wait();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars[bEV]);
+                mbar_arrive(&bars[Q_GFREE0 + gs]);
+            }
+        }
+        if (ok && warp_wait(bars, b5, (n - 1) & 1, errflag)) {
+            fence_after_sync();
+            float* out = isS ? s_out : m_out;
+            const int c_lo = isS ? 64 * hf : 0, c_hi = isS ? 64 * hf + 64 : 128;
+            for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+                float xv[16];
+                tmem_ld16(tm + lb + xf + c0, xv);
+                tmem_ld_wait();
+                if (!isS) {  // transitions are stored transposed (M^T)
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4*>(out + v * VD + c0 + i) =
+                            make_float4(xv[i], xv[i + 1], xv[i + 2], xv[i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) out[(c0 + i) * VD + v] = xv[i];
+                }
+            }
+        }
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (*errflag && tid == 0 && P.err) atomicOr(P.err, *errflag);
+    if (w == 0) {
+        fence_after_sync();
+        tmem_dealloc(tm, 512);
+    }
+}
+
 __device__ __forceinline__ unsigned char* aligned_smem() {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -645,19 +932,21 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
     if (P.cp == CP_EXACT) {
         if (lj >= nseg - 1) return;
         const int cb = lj * P.L, ce = min(cb + P.L, nt);
-        if (blockIdx.z == 0) {
-            float* out = P.hin + (int64_t(gseg + 1) * P.Hv + j) * KVN;
-            const float* x0 = lj == 0 ? h0 : nullptr;
-            if (ce <= cb) { copy_state(x0, out, false); return; }
-            tc_scan<TK_STATE>(P, maps, sm, j, t0, t1, cb, ce, x0, out, P.plan.chunk_off[s]);
+        float* out = P.hin + (int64_t(gseg + 1) * P.Hv + j) * KVN;
+        if (lj == 0) {  // the first segment starts from h0 and needs no transition
+            if (ce <= cb) { copy_state(h0, out, false); return; }
+            tc_scan<TK_STATE>(P, maps, sm, j, t0, t1, cb, ce, h0, out, P.plan.chunk_off[s]);
         } else {
-            if (lj == 0) return;
-            float* out = P.mbuf + (int64_t(gseg) * P.Hv + j) * KVN;
-            if (ce <= cb) { copy_state(nullptr, out, true); return; }
-            tc_scan<TK_TRANS>(P, maps, sm, j, t0, t1, cb, ce, nullptr, out, P.plan.chunk_off[s]);
+            float* mout = P.mbuf + (int64_t(gseg) * P.Hv + j) * KVN;
+            if (ce <= cb) {
+                copy_state(nullptr, out, false);
+                copy_state(nullptr, mout, true);
+                return;
+            }
+            tc_scan_pair(P, maps, sm, j, t0, t1, cb, ce, out, mout, P.plan.chunk_off[s]);
         }
     } else {
-        if (lj == 0 || blockIdx.z != 0) return;
+        if (lj == 0) return;
         const int cb = lj * P.L, w0 = cb - P.warmup;
         const float* x0 = w0 <= 0 ? h0 : nullptr;
         float* out = P.hin + (int64_t(gseg) * P.Hv + j) * KVN;
@@ -733,7 +1022,7 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
     launch_plan(P, CH, st);
     launch_prep(P, st);
     if (P.cp != CP_NONE) {
-        dim3 ga(P.total_segs, P.Hv, P.cp == CP_EXACT ? 2 : 1);
+        dim3 ga(P.total_segs, P.Hv);
         timing_begin("fwd_phase_a", st);
         k_tc_phase_a<<<ga, TCT, SMEM_BYTES, st>>>(P, maps);
         timing_end(st);
