@@ -1020,7 +1020,7 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
     e = cudaFuncSetAttribute(k_tc_phase_c<TK_HIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     launch_plan(P, CH, st);
-    launch_prep(P, st);
+    launch_prep(P, maps, st);
     if (P.cp != CP_NONE) {
         dim3 ga(P.total_segs, P.Hv);
         timing_begin("fwd_phase_a", st);

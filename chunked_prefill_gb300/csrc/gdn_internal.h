@@ -20,16 +20,17 @@ cudaError_t launch_fwd(const Problem& P, int dtype, bool hist, cudaStream_t st);
 void launch_plan(const Problem& P, int C, cudaStream_t st);
 void launch_fixup(const Problem& P, cudaStream_t st);
 
-// Chunk-parallel preparation of the tensor-core path into P.prep: per (chunk, v-head) one
-// PREP_TILE_BYTES record holding W' = -T diag(beta e) K (bf16 64 x 128, two 128-byte-swizzled
-// 64-column blocks), TU = T diag(beta) (bf16 64 x 64, swizzled) and P (bf16 64 x 64, swizzled).
-constexpr int PREP_W = 0, PREP_TU = 16384, PREP_P = 24576, PREP_TILE_BYTES = 32768;
-void launch_prep(const Problem& P, cudaStream_t st);
-
 // TMA descriptors of k, q, v for the tensor-core path.
 struct TcMaps {
     CUtensorMap k, q, v;
 };
+// Chunk-parallel preparation of the tensor-core path into P.prep: per (chunk, v-head) one
+// PREP_TILE_BYTES record holding W' = -T diag(beta e) K (bf16 64 x 128, two 128-byte-swizzled
+// 64-column blocks), TU = T diag(beta) (bf16 64 x 64, swizzled) and P (bf16 64 x 64, swizzled).
+constexpr int PREP_W = 0, PREP_TU = 16384, PREP_P = 24576, PREP_TILE_BYTES = 32768;
+void launch_prep(const Problem& P, const TcMaps& maps, cudaStream_t st);
+
+
 // Tensor-core (tcgen05) forward for bf16: same phases as launch_fwd.
 cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStream_t st);
 

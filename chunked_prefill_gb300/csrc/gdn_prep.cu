@@ -2,13 +2,16 @@
 //
 // Per chunk of 64 tokens (FlashQLA pages, agentlenshq "GDN chunked prefill optimisation":
 // the chunk-local W/U preparation): gamma = in-chunk cumsum of g, then
-//     KK = K K^T, QK = Q K^T                        (bf16 mma.sync, fp32 accumulation)
+//     [KK; QK] = [K; Q] K^T                        (tcgen05, fp32 accumulation in TMEM)
 //     A  = diag(beta) (KK * Dm),  P = QK * D         (D_ij = exp(gamma_i - gamma_j), i >= j)
 //     T  = (I + A)^-1                                (fp32: substitution + TF32 block products)
-//     TU = T diag(beta),  W' = -T diag(beta e) K     (W' = -W of the pages' WY form)
-// W', TU and P leave as bf16 tiles already in the 128-byte-swizzled layout the scan's
-// tensor-core operands use, so the scan moves them with plain bulk copies.  Rows and columns
-// past the end of a sequence come out zero (g = beta = 0 and zero K/Q rows there).
+//     TU = T diag(beta),  W' = -T diag(beta e) K     (W' = -W of the pages' WY form; tcgen05)
+// K and Q arrive by TMA; W', TU and P leave by bulk copies from shared-memory tiles already in
+// the 128-byte-swizzled layout the scan's tensor-core operands use.  Rows past the end of a
+// sequence hold whatever tokens follow (finite); beta = g = 0 there makes every product that
+// reaches the scan exactly zero in those rows and columns.
+#include <cuda.h>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "tc05.cuh"
@@ -20,37 +23,29 @@ using namespace tc;
 
 constexpr int PT = 128;  // threads
 constexpr int CH = 64;
-constexpr int LDK = KD + 8;  // bf16 operand rows
-constexpr int LDA = 68;      // fp32 scratch rows
-constexpr int LDW = 72;      // bf16 TW rows
+constexpr int LDA = 68;  // fp32 scratch rows
 
-// The fp32 A and T scratch reuse the K and Q tiles once [K;Q] K^T is in registers (small
-// footprint: five CTAs per SM hide each other's latency).
+// Shared memory (from a 1024-aligned base).  The [K; Q] tile's Q half later stages P, the A
+// scratch later holds the TU staging tile and the TW operand tile, and the whole [K; Q] tile
+// finally stages W'.
 struct PrepSmem {
-    static constexpr size_t TILE = size_t(CH) * LDK * 2;
-    static constexpr size_t oK = 0, oQ = oK + TILE, oA = oK, oT = oQ,
-                            oTmp = oQ + TILE, oGam = oTmp + 4 * 16 * 20 * 4,
-                            oE = oGam + CH * 4, oEi = oE + CH * 4, oBeta = oEi + CH * 4,
-                            oBe = oBeta + CH * 4, oFlag = oBe + CH * 4;
-    static constexpr size_t bytes = oFlag + 16;
-    static_assert(size_t(CH) * LDA * 4 <= TILE, "fp32 scratch fits a bf16 tile");
-    static_assert(size_t(CH) * LDW * 2 <= TILE && 16384 <= TILE, "TW and the W' staging fit a tile");
+    static constexpr uint32_t oKQ = 0;                    // 2 x 16 KB: rows 0-63 K, 64-127 Q
+    static constexpr uint32_t oA = 32768;                 // 64 x 68 fp32
+    static constexpr uint32_t oT = oA + CH * LDA * 4;     // 64 x 68 fp32
+    static constexpr uint32_t oTmp = oT + CH * LDA * 4;   // 4 x 16 x 20 fp32
+    static constexpr uint32_t oGam = oTmp + 4 * 16 * 20 * 4;
+    static constexpr uint32_t oE = oGam + CH * 4, oEi = oE + CH * 4, oBeta = oEi + CH * 4,
+                              oBe = oBeta + CH * 4, oFlag = oBe + CH * 4, oBar = oFlag + 16,
+                              oSlot = oBar + 3 * 8;
+    static constexpr uint32_t bytes = oSlot + 16 + 1024;  // + alignment slack
+    static_assert(oA % 1024 == 0 && CH * LDA * 4 >= 16384, "TU staging and TW tiles fit the A scratch");
 };
 
-__device__ __forceinline__ void st_chunk8g(unsigned char* tile, int r, int ch, const float* x) {
-    uint4 u;
-    u.x = pack_bf16(x[0], x[1]);
-    u.y = pack_bf16(x[2], x[3]);
-    u.z = pack_bf16(x[4], x[5]);
-    u.w = pack_bf16(x[6], x[7]);
-    *reinterpret_cast<uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4)) = u;
-}
-
-__global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
-    extern __shared__ __align__(128) char smem[];
+__global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant__ TcMaps maps) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using S = PrepSmem;
-    __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem + S::oK);
-    __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem + S::oQ);
     float* sA = reinterpret_cast<float*>(smem + S::oA);
     float* sT = reinterpret_cast<float*>(smem + S::oT);
     float* sTmp = reinterpret_cast<float*>(smem + S::oTmp);
@@ -60,8 +55,11 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
     float* sBeta = reinterpret_cast<float*>(smem + S::oBeta);
     float* sBe = reinterpret_cast<float*>(smem + S::oBe);
     int* sFlag = reinterpret_cast<int*>(smem + S::oFlag);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);  // load, [K;Q]K^T, W'
+    uint32_t* slot = reinterpret_cast<uint32_t*>(smem + S::oSlot);
 
     const int gch = blockIdx.x, j = blockIdx.y;
+    if (gch >= P.plan.chunk_off[P.N]) return;
     int lo = 0, hi = P.N - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -69,7 +67,6 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
         else hi = mid - 1;
     }
     const int s = lo;
-    if (gch >= P.plan.chunk_off[P.N]) return;
     const int ch = gch - P.plan.chunk_off[s];
     int64_t t0, t1;
     if (P.cu) {
@@ -85,19 +82,25 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
     const int G = P.Hv / P.Hqk, qh = j / G;
-    const int64_t qk_stride = int64_t(P.Hqk) * KD;
-    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(P.k) + qh * KD + tc * qk_stride;
-    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(P.q) + qh * KD + tc * qk_stride;
+    unsigned char* rec = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * PREP_TILE_BYTES;
+    const uint32_t kq = smem_addr(smem + S::oKQ);
+    int* err = P.err;
 
-    for (int idx = tid; idx < CH * 16; idx += PT) {
-        const int r = idx >> 4, cv = idx & 15;
-        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-        if (r < c) {
-            a = *reinterpret_cast<const uint4*>(kb + r * qk_stride + cv * 8);
-            b = *reinterpret_cast<const uint4*>(qb + r * qk_stride + cv * 8);
-        }
-        *reinterpret_cast<uint4*>(sK + r * LDK + cv * 8) = a;
-        *reinterpret_cast<uint4*>(sQ + r * LDK + cv * 8) = b;
+    if (tid == 0) {
+        for (int b = 0; b < 3; ++b) mbar_init(&bars[b], 1);
+        mbar_fence_init();
+    }
+    if (w == 0) tmem_alloc(slot, 128);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = *slot;
+    if (tid == 0) {
+        mbar_expect_tx(&bars[0], 32768);
+        tma_load_3d(smem + S::oKQ, &maps.k, &bars[0], 0, qh, int(tc));
+        tma_load_3d(smem + S::oKQ + 16384, &maps.k, &bars[0], 64, qh, int(tc));
+        tma_load_3d(smem + S::oKQ + 8192, &maps.q, &bars[0], 0, qh, int(tc));
+        tma_load_3d(smem + S::oKQ + 16384 + 8192, &maps.q, &bars[0], 64, qh, int(tc));
     }
     if (w == 0) {
         float gv[2], bv[2];
@@ -128,56 +131,78 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
             sBe[r] = bv[u] * e;
         }
         if (lane == 0) *sFlag = (last < -80.f || !(last == last)) ? 1 : 0;
-    }
-    __syncthreads();
-
-    // [K;Q] K^T: warp w owns rows 32w..32w+31 of the stacked 128 x 64 product
-    {
-        const bool qrows = w >= 2;
-        const __nv_bfloat16* Ab = qrows ? sQ : sK;
-        const int rb = 32 * (w & 1);
-        float acc0[8][4], acc1[8][4];
-        zero_acc(acc0);
-        zero_acc(acc1);
-        warp_mma<8, false, true>(acc0, Ab, LDK, sK, LDK, rb, 0, KD);
-        warp_mma<8, false, true>(acc1, Ab, LDK, sK, LDK, rb + 16, 0, KD);
-        __syncthreads();  // K and Q tiles consumed: A and T may overwrite them
-        const bool pw = *sFlag != 0;
-        float* sP32 = sT;  // P in fp32 until it leaves; T overwrites it afterwards
+        if (lane == 0) {
+            // [KK; QK] = [K; Q] K^T into TMEM columns [0, 64)
+            bool ok = mbar_wait(&bars[0], 0);
+            if (ok) {
+                constexpr uint32_t ID1 = make_idesc(128, 64, 0, 0);
+                const uint64_t d = make_desc(kq, 0, 1024);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float(&acc)[8][4] = half ? acc1 : acc0;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = rb + 16 * half + gq + 8 * hh;
-#pragma unroll
-                for (int n = 0; n < 8; ++n) {
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int jj = 8 * n + 2 * tq + u;
-                        const float v = acc[n][2 * hh + u];
-                        const float d = pw ? expf(sGam[i] - sGam[jj]) : sE[i] * sEi[jj];
-                        if (!qrows) sA[i * LDA + jj] = (i > jj) ? sBeta[i] * d * v : 0.f;
-                        else sP32[i * LDA + jj] = (i >= jj) ? d * v : 0.f;
-                    }
+                for (int st = 0; st < 8; ++st) {
+                    const uint32_t off = (st >> 2) * 16384 + (st & 3) * 32;
+                    mma_bf16(tm, d + (off >> 4), d + (off >> 4), ID1, st > 0);
                 }
+            } else if (err) {
+                atomicOr(err, 1 << 29);
             }
+            commit(&bars[1]);
         }
+        __syncwarp();
     }
-    __syncthreads();
-    // P leaves as a pre-swizzled bf16 tile: eight threads per 128-byte row
+    __syncthreads();  // gates visible
+
+    // A (rows of KK) and P (rows of QK): thread = one row of the stacked product
     {
-        unsigned char* ptile = static_cast<unsigned char*>(P.prep) +
-                               (int64_t(gch) * P.Hv + j) * PREP_TILE_BYTES + PREP_P;
-        for (int it = tid; it < CH * 8; it += PT) {
-            const int r = it >> 3, c8 = it & 7;
-            const float4 a = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
-            const float4 b = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8 + 4);
-            const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            st_chunk8g(ptile, r, c8, x);
+        const bool ok = warp_uniform_wait(&bars[1], 0);
+        fence_after_sync();
+        float raw[64];
+        tmem_ld32(tm + (uint32_t(32 * w) << 16), raw);
+        tmem_ld32(tm + (uint32_t(32 * w) << 16) + 32, raw + 32);
+        tmem_ld_wait();
+        const bool pw = *sFlag != 0;
+        const bool qrows = w >= 2;
+        const int i = 32 * (w & 1) + lane;
+        const float gi = sGam[i], ei = sE[i], bi = sBeta[i];
+        if (!ok && lane == 0 && err) atomicOr(err, 1 << 28);
+        if (!qrows) {
+#pragma unroll
+            for (int j4 = 0; j4 < 16; ++j4) {
+                float x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int jj = 4 * j4 + u;
+                    const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
+                    x[u] = jj < i ? bi * d * raw[jj] : 0.f;
+                }
+                *reinterpret_cast<float4*>(sA + i * LDA + 4 * j4) = make_float4(x[0], x[1], x[2], x[3]);
+            }
+        } else {
+            // P in bf16, rows swizzled like the scan's K-major operand tiles, over Q's dead half
+            unsigned char* pt = smem + S::oKQ + 8192;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int jj = 8 * c8 + u;
+                    const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
+                    x[u] = jj <= i ? d * raw[jj] : 0.f;
+                }
+                uint4 q4;
+                q4.x = pack_bf16(x[0], x[1]);
+                q4.y = pack_bf16(x[2], x[3]);
+                q4.z = pack_bf16(x[4], x[5]);
+                q4.w = pack_bf16(x[6], x[7]);
+                *reinterpret_cast<uint4*>(pt + i * 128 + ((c8 ^ (i & 7)) << 4)) = q4;
+            }
+            fence_proxy_async_smem();
         }
     }
     __syncthreads();
+    if (tid == 0) {
+        bulk_store(rec + PREP_P, smem + S::oKQ + 8192, 8192);
+        bulk_commit();
+    }
 
     // T = (I + A)^-1: diagonal blocks by substitution (warp q, lane = column) ...
     if (lane < 16) {
@@ -251,70 +276,89 @@ __global__ void __launch_bounds__(PT, 5) k_prep(Problem P) {
             __syncthreads();
         }
     }
-    // TU = T diag(beta) leaves as a swizzled bf16 tile (eight threads per 128-byte row);
-    // TW = -T diag(beta e) goes to shared memory (bf16, row stride LDW) over the dead A
-    unsigned char* rec = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * PREP_TILE_BYTES;
-    __nv_bfloat16* sTW = reinterpret_cast<__nv_bfloat16*>(smem + S::oK);
+    // TU = T diag(beta) and TW = -T diag(beta e) as swizzled bf16 tiles over the dead A
+    // scratch: TU leaves by a bulk copy, TW is the B operand of W'^T = K^T TW^T
     for (int it = tid; it < CH * 8; it += PT) {
         const int r = it >> 3, c8 = it & 7;
-        const float4 t0 = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
-        const float4 t1 = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8 + 4);
-        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+        const float4 t0v = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
+        const float4 t1v = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8 + 4);
+        const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
         float xu[8], xw[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int c = 8 * c8 + u;
-            xu[u] = c <= r ? tv[u] * sBeta[c] : 0.f;
-            xw[u] = c <= r ? -tv[u] * sBe[c] : 0.f;
+            const int cc = 8 * c8 + u;
+            xu[u] = cc <= r ? tv[u] * sBeta[cc] : 0.f;
+            xw[u] = cc <= r ? -tv[u] * sBe[cc] : 0.f;
         }
-        st_chunk8g(rec + PREP_TU, r, c8, xu);
-        uint4 w4;
-        w4.x = pack_bf16(xw[0], xw[1]);
-        w4.y = pack_bf16(xw[2], xw[3]);
-        w4.z = pack_bf16(xw[4], xw[5]);
-        w4.w = pack_bf16(xw[6], xw[7]);
-        *reinterpret_cast<uint4*>(sTW + r * LDW + 8 * c8) = w4;
+        uint4 a, b;
+        a.x = pack_bf16(xu[0], xu[1]);
+        a.y = pack_bf16(xu[2], xu[3]);
+        a.z = pack_bf16(xu[4], xu[5]);
+        a.w = pack_bf16(xu[6], xu[7]);
+        b.x = pack_bf16(xw[0], xw[1]);
+        b.y = pack_bf16(xw[2], xw[3]);
+        b.z = pack_bf16(xw[4], xw[5]);
+        b.w = pack_bf16(xw[6], xw[7]);
+        const uint32_t off = r * 128 + ((c8 ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(smem + S::oA + off) = a;
+        *reinterpret_cast<uint4*>(smem + S::oA + 8192 + off) = b;
     }
-    __syncthreads();  // T is dead: K comes back (from L2) over it
-    __nv_bfloat16* sK2 = reinterpret_cast<__nv_bfloat16*>(smem + S::oT);
-    for (int idx = tid; idx < CH * 16; idx += PT) {
-        const int r = idx >> 4, cv = idx & 15;
-        uint4 a = make_uint4(0, 0, 0, 0);
-        if (r < c) a = *reinterpret_cast<const uint4*>(kb + r * qk_stride + cv * 8);
-        *reinterpret_cast<uint4*>(sK2 + r * LDK + cv * 8) = a;
-    }
+    fence_proxy_async_smem();
     __syncthreads();
-    // W' = TW K (64 x 128): warp w owns rows 16w..16w+15; TW is lower triangular, so only the
-    // first 16(w+1) inner indices contribute
-    float acc[16][4];
-    zero_acc(acc);
-    warp_mma<16, false, false>(acc, sTW, LDW, sK2, LDK, 16 * w, 0, 16 * (w + 1));
-    __syncthreads();  // TW consumed: the staging tile overwrites it
+    if (tid == 0) {
+        bulk_store(rec + PREP_TU, smem + S::oA, 8192);
+        bulk_commit();
+        // W'^T [dk][i] = K^T TW^T into TMEM columns [64, 128)
+        constexpr uint32_t ID2 = make_idesc(128, 64, 1, 0);
+        const uint64_t da = make_desc(kq, 16384, 1024);
+        const uint64_t db = make_desc(smem_addr(smem + S::oA + 8192), 0, 1024);
+        fence_after_sync();
+#pragma unroll
+        for (int st = 0; st < 4; ++st) mma_bf16(tm + 64, da + (st * 2048 >> 4), db + (st * 32 >> 4), ID2, st > 0);
+        commit(&bars[2]);
+        bulk_wait_read0();  // P's staging (over Q) has been read: W' may take the tile
+    }
     {
-        unsigned char* stg = reinterpret_cast<unsigned char*>(smem + S::oK);
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = 16 * w + gq + 8 * hh;
-                const uint32_t v2 = pack_bf16(acc[n][2 * hh], acc[n][2 * hh + 1]);
-                *reinterpret_cast<uint32_t*>(stg + (n >> 3) * 8192 + i * 128 + (((n & 7) ^ (i & 7)) << 4) +
-                                             4 * tq) = v2;
-            }
-        }
+        const bool ok = warp_uniform_wait(&bars[2], 0);
+        if (!ok && lane == 0 && err) atomicOr(err, 1 << 27);
     }
     __syncthreads();
-    for (int it = tid; it < 16384 / 16; it += PT)
-        reinterpret_cast<uint4*>(rec + PREP_W)[it] = reinterpret_cast<const uint4*>(smem + S::oK)[it];
+    fence_after_sync();
+    {
+        // thread = key row dk; W' row i, column dk goes to the K-major staging tile
+        const int dk = tid;
+        float d[64];
+        tmem_ld32(tm + (uint32_t(32 * w) << 16) + 64, d);
+        tmem_ld32(tm + (uint32_t(32 * w) << 16) + 96, d + 32);
+        tmem_ld_wait();
+        const uint32_t base = smem_addr(smem + S::oKQ) + (dk >> 6) * 8192 + (dk & 7) * 2;
+        const int cch = (dk & 63) >> 3;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            sts16(base + i * 128 + ((cch ^ (i & 7)) << 4), __bfloat16_as_ushort(__float2bfloat16_rn(d[i])));
+        fence_proxy_async_smem();
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(rec + PREP_W, smem + S::oKQ, 16384);
+        bulk_commit();
+        bulk_wait0();
+    }
+    __syncthreads();
+    if (w == 0) {
+        fence_after_sync();
+        tmem_dealloc(tm, 128);
+    }
 }
 
 }  // namespace
 
-void launch_prep(const Problem& P, cudaStream_t st) {
+void launch_prep(const Problem& P, const TcMaps& maps, cudaStream_t st) {
     if (P.total_chunks <= 0) return;
     cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PrepSmem::bytes));
     timing_begin("fwd_prep", st);
-    k_prep<<<dim3(P.total_chunks, P.Hv), PT, PrepSmem::bytes, st>>>(P);
+    k_prep<<<dim3(P.total_chunks, P.Hv), PT, PrepSmem::bytes, st>>>(P, maps);
     timing_end(st);
 }
 

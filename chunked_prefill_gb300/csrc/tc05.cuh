@@ -119,6 +119,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
         "r"(__float_as_uint(v[15]))
         : "memory");
 }
+// 1-D bulk copy shared -> global in a bulk group of the issuing thread (16-byte aligned,
+// size % 16 == 0); the source must have been fenced to the async proxy by its writers
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(
+                     reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_addr(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// the issuing thread's bulk groups have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// ... and have completed
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // shared-memory accesses by 32-bit shared-window address (no generic-address resolution)
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
@@ -208,6 +224,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
             if (mbar_try_wait(bar, phase)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+// bounded wait by lane 0, result broadcast to the warp
+__device__ __forceinline__ bool warp_uniform_wait(uint64_t* bar, uint32_t phase) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, phase);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
 }
 // The same bounded wait for threads off the critical path: between tries the warp sleeps
 // for sleep_ns so that it leaves the issue slots to the warps doing work.
