@@ -303,15 +303,20 @@ def oracle_sample_fixed(inp, n, backward):
     return new_cu[-1] / dt, new_cu[-1], dt, orc.max_threads(), n
 
 
-def kernel_bytes(name, tokens, nseq, w):
+def kernel_bytes(name, tokens, lens, w):
     """Algorithmic HBM bytes of one launch of a kernel: the tensors its step of the method
-    must read or write once (bf16 activations, fp32 gates and states)."""
+    must read or write once (bf16 activations, fp32 gates and states; for the chunk-local
+    preparation also the 32 KB per (chunk, v-head) record it hands to the scan)."""
+    nseq = len(lens)
     qk = tokens * w.Hqk * 128 * 2
     vv = tokens * w.Hv * 128 * 2
     gb = tokens * w.Hv * 4 * 2
     st = nseq * w.Hv * 128 * 128 * 4
     h0 = st if w.h0_std > 0 else 0
+    chunks = sum((int(n) + 63) // 64 for n in lens)
+    rec = chunks * w.Hv * 32768
     table = {
+        "fwd_prep": (2 * qk + gb + rec, "q,k,g,beta read; W',TU,P records written"),
         "fwd_phase_c": (2 * qk + 2 * vv + gb + h0 + st, "q,k,v,g,beta,h0 read; o,ht written"),
         "fwd_phase_a": (qk + vv + gb + h0, "k,v,g,beta,h0 read"),
         "fwd_recompute_states": (qk + vv + gb + h0, "k,v,g,beta,h0 read"),
@@ -400,7 +405,7 @@ def main():
     dom = max(kt.items(), key=lambda kv: kv[1][1]) if kt else ("none", (1, float("nan")))
     dom_name, (dom_n, dom_ms) = dom
     dom_avg_s = dom_ms / max(dom_n, 1) / 1000.0
-    alg, unit_note = kernel_bytes(dom_name, tokens, len(lens), w)
+    alg, unit_note = kernel_bytes(dom_name, tokens, lens, w)
     achieved = alg / dom_avg_s / 1e9
     roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,

@@ -93,18 +93,19 @@ gdn_status validate_problem(const gdn_problem* p) {
 }
 
 // Estimated time of a segmentation with L chunks per segment, in units of one chunk step
-// of the output stage: the waves of the two chunk-scan launches (one CTA per SM) times the
-// chunks a CTA scans, plus the serial fix-up steps.  The step costs are measured ratios on
-// GB300 (a segment-transition chunk step ~0.7 of an output chunk step, a fix-up step ~0.45).
+// of the output stage: the waves of the two chunk-scan launches (one CTA per SM; the first
+// phase runs a segment's state and transition in one CTA) times the chunks a CTA scans, plus
+// the serial fix-up steps.  The step costs are measured ratios on GB300 (a first-phase chunk
+// step ~1.0 of an output chunk step, a fix-up step ~0.52).
 double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int warmup) {
-    constexpr double tC = 1.0, tA = 0.7, tF = 0.45;
+    constexpr double tC = 1.0, tA = 1.0, tF = 0.52;
     long segs = 0, actas = 0;
     int maxn = 0;
     for (int s = 0; s < N; ++s) {
         const int ns = std::max(1, (nts[s] + L - 1) / L);
         segs += ns;
         maxn = std::max(maxn, ns);
-        if (ns > 1) actas += exact ? 2 * ns - 3 : ns - 1;
+        if (ns > 1) actas += ns - 1;
     }
     const long cw = (segs * Hv + sms - 1) / sms;
     const long aw = (actas * Hv + sms - 1) / sms;
