@@ -443,83 +443,111 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_phase_c(Problem P) {
 }
 
 // Fix-up: hin[g0+j+1] = M_j hin[g0+j] + S_j for j = 1..nseg-2, serially; each CTA owns 8
-// state columns of one (sequence, head).  The transitions are stored transposed (M^T); they
-// arrive in shared memory by bulk copies issued two steps ahead (three buffers), and thread
-// `row` reads M[row][m] = M^T[m][row] without bank conflicts.  512 threads: (row, group of 4
-// columns, half of the inner index m), the two halves summed through shared memory; S_j of
-// the next step is read into registers one step early.  fp32.
-constexpr int FIX_NB = 3;
-constexpr int FIX_SMEM = FIX_NB * KD * KD * 4 + KD * 8 * 4 + 256 * 16 + 64;
-__global__ void __launch_bounds__(512) k_fixup(Problem P) {
+// state columns of one (sequence, head).  The transitions are stored transposed (M^T); each
+// arrives in shared memory by a bulk copy issued one step ahead (two buffers).  Thread t
+// accumulates a 4-row x 8-column block over 16 of the 128 inner indices (rows 4 (t % 32),
+// inner range 16 (t / 32)): one 16-byte load of M^T and two broadcast loads of the state per
+// 32 FMAs; the eight partial blocks meet in shared memory.  S_j of the next step is read into
+// registers one step early.  fp32.
+#ifdef GDN_TRACE
+__device__ unsigned long long g_fix_trace[64][4];  // debug builds: SM clock per fix-up step
+#define FTRACE(k, e)                                                                            \
+    do {                                                                                        \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 && (k) < 64) \
+            g_fix_trace[k][e] = clock64();                                                      \
+    } while (0)
+#else
+#define FTRACE(k, e) \
+    do {             \
+    } while (0)
+#endif
+constexpr int FIX_NB = 2, FIX_T = 256;
+constexpr int FIX_SMEM = FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * 8 * 4 + 64;
+__global__ void __launch_bounds__(FIX_T) k_fixup(Problem P) {
     extern __shared__ __align__(128) unsigned char fsm[];
     float* Ms = reinterpret_cast<float*>(fsm);                                // FIX_NB x 128 x 128
-    float* xs = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4);         // 128 x 8
-    float4* part = reinterpret_cast<float4*>(fsm + FIX_NB * KD * KD * 4 + KD * 8 * 4);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + FIX_NB * KD * KD * 4 + KD * 8 * 4 + 256 * 16);
+    float* red = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4);        // 8 x 32 x 32
+    float* xs = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4);  // 128 x 8
+    uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * 8 * 4);
     const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * 8;
     const int g0 = P.plan.seg_off[s], nseg = P.plan.seg_off[s + 1] - g0;
     if (nseg <= 2) return;
     const int last = nseg - 2;  // steps 1..last
-    const int t = threadIdx.x & 255, kh = threadIdx.x >> 8;
-    const int row = t & 127, c0 = (t >> 7) * 4;
+    const int t = threadIdx.x, rg = t & 31, ks = t >> 5;
+    const int orow = t >> 1, oc = (t & 1) * 4;  // the 4 outputs this thread finishes
     auto mt = [&](int lj) { return P.mbuf + (int64_t(g0 + lj) * P.Hv + j) * KV; };
     auto hp = [&](int lj) {
-        return reinterpret_cast<float4*>(P.hin + (int64_t(g0 + lj) * P.Hv + j) * KV + row * VD + cb + c0);
+        return reinterpret_cast<float4*>(P.hin + (int64_t(g0 + lj) * P.Hv + j) * KV + orow * VD + cb + oc);
     };
-    if (threadIdx.x == 0) {
+    if (t == 0) {
         for (int b = 0; b < FIX_NB; ++b) tc::mbar_init(&bar[b], 1);
         tc::mbar_fence_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int q = 1; q <= min(last, FIX_NB - 1); ++q) {
-            const int b = (q - 1) % FIX_NB;
-            tc::mbar_expect_tx(&bar[b], KD * KD * 4);
-            tc::bulk_load(Ms + b * KD * KD, mt(q), KD * KD * 4, &bar[b]);
-        }
+    if (t == 0) {
+        tc::mbar_expect_tx(&bar[0], KD * KD * 4);
+        tc::bulk_load(Ms, mt(1), KD * KD * 4, &bar[0]);
     }
-    float4 snext = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (kh == 0) {
-        *reinterpret_cast<float4*>(&xs[row * 8 + c0]) = *hp(1);
-        snext = *hp(2);
-    }
+    *reinterpret_cast<float4*>(&xs[orow * 8 + oc]) = *hp(1);
+    float4 snext = *hp(2);
     bool ok = true;
     for (int lj = 1; lj <= last; ++lj) {
-        const int q = lj - 1, b = q % FIX_NB;
-        if (threadIdx.x == 0 && lj + FIX_NB - 1 <= last) {  // into the buffer step lj-1 used
-            const int bn = (lj + FIX_NB - 2) % FIX_NB;
-            tc::mbar_expect_tx(&bar[bn], KD * KD * 4);
-            tc::bulk_load(Ms + bn * KD * KD, mt(lj + FIX_NB - 1), KD * KD * 4, &bar[bn]);
+        const int q = lj - 1, b = q & 1;
+        if (t == 0 && lj + 1 <= last) {  // into the buffer step lj-1 used
+            tc::mbar_expect_tx(&bar[b ^ 1], KD * KD * 4);
+            tc::bulk_load(Ms + (b ^ 1) * KD * KD, mt(lj + 1), KD * KD * 4, &bar[b ^ 1]);
         }
-        ok = ok && tc::mbar_wait(&bar[b], (q / FIX_NB) & 1);
+        FTRACE(lj, 0);
+        ok = ok && tc::mbar_wait(&bar[b], (q >> 1) & 1);
+        FTRACE(lj, 1);
         __syncthreads();  // also orders the previous step's xs update
+        FTRACE(lj, 2);
         const float4 sj = snext;
-        if (kh == 0 && lj + 1 <= last) snext = *hp(lj + 2);
+        if (lj + 1 <= last) snext = *hp(lj + 2);
         const float* M = Ms + b * KD * KD;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int m0 = kh * (KD / 2);
-#pragma unroll 16
-        for (int m = m0; m < m0 + KD / 2; ++m) {
-            const float a = M[m * KD + row];
-            const float4 xv = *reinterpret_cast<const float4*>(&xs[m * 8 + c0]);
-            acc.x = fmaf(a, xv.x, acc.x);
-            acc.y = fmaf(a, xv.y, acc.y);
-            acc.z = fmaf(a, xv.z, acc.z);
-            acc.w = fmaf(a, xv.w, acc.w);
+        float acc[4][8];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+#pragma unroll 4
+        for (int m = 16 * ks; m < 16 * ks + 16; ++m) {
+            const float4 a = *reinterpret_cast<const float4*>(M + m * KD + 4 * rg);
+            const float4 x0 = *reinterpret_cast<const float4*>(&xs[m * 8]);
+            const float4 x1 = *reinterpret_cast<const float4*>(&xs[m * 8 + 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], xv[c], acc[r][c]);
         }
-        if (kh == 1) part[t] = acc;
-        __syncthreads();  // partial sums visible; everyone is done with xs and buffer b
-        if (kh == 0) {
-            const float4 p = part[t];
-            acc.x = sj.x + (acc.x + p.x);
-            acc.y = sj.y + (acc.y + p.y);
-            acc.z = sj.z + (acc.z + p.z);
-            acc.w = sj.w + (acc.w + p.w);
-            *reinterpret_cast<float4*>(&xs[row * 8 + c0]) = acc;
-            *hp(lj + 1) = acc;
+        // partial block -> red[ks][rg][32], 16-byte pieces rotated by rg against bank conflicts
+        float* rp = red + (ks * 32 + rg) * 32;
+#pragma unroll
+        for (int pq = 0; pq < 8; ++pq) {
+            const int r = pq >> 1, c = (pq & 1) * 4;
+            *reinterpret_cast<float4*>(rp + ((pq ^ (rg & 7)) << 2)) =
+                make_float4(acc[r][c], acc[r][c + 1], acc[r][c + 2], acc[r][c + 3]);
+        }
+        FTRACE(lj, 3);
+        __syncthreads();  // partial blocks visible; everyone is done with xs and buffer b
+        {
+            const int org = orow >> 2, pq = ((orow & 3) << 1) | (oc >> 2);
+            float4 o = sj;
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {
+                const float4 p = *reinterpret_cast<const float4*>(red + (k2 * 32 + org) * 32 + ((pq ^ (org & 7)) << 2));
+                o.x += p.x;
+                o.y += p.y;
+                o.z += p.z;
+                o.w += p.w;
+            }
+            *reinterpret_cast<float4*>(&xs[orow * 8 + oc]) = o;
+            *hp(lj + 1) = o;
         }
     }
-    if (!ok && threadIdx.x == 0 && P.err) atomicOr(P.err, 1 << 30);
+    if (!ok && t == 0 && P.err) atomicOr(P.err, 1 << 30);
 }
 
 // Work decomposition on the device from the device cu_seqlens (same rule as the host).
@@ -554,7 +582,7 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
     cudaFuncSetAttribute(k_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
-    k_fixup<<<dim3(P.N, P.Hv, VD / 8), 512, FIX_SMEM, st>>>(P);
+    k_fixup<<<dim3(P.N, P.Hv, VD / 8), FIX_T, FIX_SMEM, st>>>(P);
     timing_end(st);
 }
 
@@ -598,3 +626,9 @@ cudaError_t launch_fwd(const Problem& P, int dtype, bool hist, cudaStream_t st) 
 int fwd_chunk_size(int dtype) { return dtype == 0 ? 64 : 32; }
 
 }  // namespace gdn
+
+#ifdef GDN_TRACE
+extern "C" int gdn_debug_fix_trace(unsigned long long* out) {
+    return int(cudaMemcpyFromSymbol(out, gdn::g_fix_trace, sizeof(gdn::g_fix_trace)));
+}
+#endif
