@@ -555,8 +555,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             fence_after_sync();
             const float sc = P.scale;
             const uint32_t dqa = tm + lb + t_dd(k) + 64;
-#pragma unroll
             const uint32_t ge = smem_addr(&gb.e[0]);
+#pragma unroll
             for (int half = 0; half < 2; ++half) {
                 float qa[32], pb[32];
                 tmem_ld32(dqa + 32 * half, qa);
