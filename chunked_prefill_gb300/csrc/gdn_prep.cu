@@ -21,6 +21,18 @@ namespace {
 
 using namespace tc;
 
+#ifdef GDN_TRACE
+__device__ unsigned long long g_prep_trace[16];  // debug builds: SM clock at phase ends
+#define PTRACE(e)                                                                               \
+    do {                                                                                        \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) g_prep_trace[e] = clock64(); \
+    } while (0)
+#else
+#define PTRACE(e) \
+    do {          \
+    } while (0)
+#endif
+
 constexpr int PT = 128;  // threads
 constexpr int CH = 64;
 constexpr int LDA = 68;  // fp32 scratch rows
@@ -95,6 +107,7 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = *slot;
+    PTRACE(0);
     if (tid == 0) {
         mbar_expect_tx(&bars[0], 32768);
         tma_load_3d(smem + S::oKQ, &maps.k, &bars[0], 0, qh, int(tc));
@@ -150,6 +163,7 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
         __syncwarp();
     }
     __syncthreads();  // gates visible
+    PTRACE(1);
 
     // A (rows of KK) and P (rows of QK): thread = one row of the stacked product
     {
@@ -199,6 +213,7 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
         }
     }
     __syncthreads();
+    PTRACE(2);
     if (tid == 0) {
         bulk_store(rec + PREP_P, smem + S::oKQ + 8192, 8192);
         bulk_commit();
@@ -276,6 +291,7 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
             __syncthreads();
         }
     }
+    PTRACE(3);
     // TU = T diag(beta) and TW = -T diag(beta e) as swizzled bf16 tiles over the dead A
     // scratch: TU leaves by a bulk copy, TW is the B operand of W'^T = K^T TW^T
     for (int it = tid; it < CH * 8; it += PT) {
@@ -305,6 +321,7 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
     }
     fence_proxy_async_smem();
     __syncthreads();
+    PTRACE(4);
     if (tid == 0) {
         bulk_store(rec + PREP_TU, smem + S::oA, 8192);
         bulk_commit();
@@ -323,6 +340,7 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
         if (!ok && lane == 0 && err) atomicOr(err, 1 << 27);
     }
     __syncthreads();
+    PTRACE(5);
     fence_after_sync();
     {
         // thread = key row dk; W' row i, column dk goes to the K-major staging tile
@@ -343,7 +361,9 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
     if (tid == 0) {
         bulk_store(rec + PREP_W, smem + S::oKQ, 16384);
         bulk_commit();
-        bulk_wait0();
+        PTRACE(6);
+        bulk_wait_read0();  // the staging tiles may go away with the CTA; the writes complete on their own
+        PTRACE(7);
     }
     __syncthreads();
     if (w == 0) {
@@ -363,3 +383,9 @@ void launch_prep(const Problem& P, const TcMaps& maps, cudaStream_t st) {
 }
 
 }  // namespace gdn
+
+#ifdef GDN_TRACE
+extern "C" int gdn_debug_prep_trace(unsigned long long* out) {
+    return int(cudaMemcpyFromSymbol(out, gdn::g_prep_trace, sizeof(gdn::g_prep_trace)));
+}
+#endif
