@@ -464,6 +464,8 @@ __device__ unsigned long long g_fix_trace[64][4];  // debug builds: SM clock per
 constexpr int FIX_NB = 2, FIX_T = 256;
 constexpr int FIX_SMEM = FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * 8 * 4 + 64;
 __global__ void __launch_bounds__(FIX_T) k_fixup(Problem P) {
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();
     extern __shared__ __align__(128) unsigned char fsm[];
     float* Ms = reinterpret_cast<float*>(fsm);                                // FIX_NB x 128 x 128
     float* red = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4);        // 8 x 32 x 32
@@ -553,6 +555,7 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(Problem P) {
 // Work decomposition on the device from the device cu_seqlens (same rule as the host).
 __global__ void k_plan(const int* cu, int N, int T, int C, int L, int total_segs, int2* seg,
                        int* seg_off, int* chunk_off) {
+    tc::pdl_launch_dependents();
     for (int i = threadIdx.x; i < total_segs; i += blockDim.x) seg[i] = make_int2(-1, -1);
     __syncthreads();
     if (threadIdx.x != 0) return;
@@ -582,7 +585,7 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
     cudaFuncSetAttribute(k_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
-    k_fixup<<<dim3(P.N, P.Hv, VD / 8), FIX_T, FIX_SMEM, st>>>(P);
+    launch_pdl(k_fixup, dim3(P.N, P.Hv, VD / 8), dim3(FIX_T), FIX_SMEM, st, P);
     timing_end(st);
 }
 

@@ -919,6 +919,8 @@ __device__ void copy_state(const float* x0, float* x_out, bool ident) {
 }
 
 __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_constant__ TcMaps maps) {
+    pdl_launch_dependents();
+    pdl_wait();
     unsigned char* sm = aligned_smem();
     const int gseg = blockIdx.x, j = blockIdx.y;
     const int2 sj = P.plan.seg[gseg];
@@ -956,6 +958,8 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
 
 template <int KIND>
 __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_constant__ TcMaps maps) {
+    pdl_launch_dependents();
+    pdl_wait();
     unsigned char* sm = aligned_smem();
     const int gseg = blockIdx.x, j = blockIdx.y;
     const int2 sj = P.plan.seg[gseg];
@@ -1024,16 +1028,18 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
     if (P.cp != CP_NONE) {
         dim3 ga(P.total_segs, P.Hv);
         timing_begin("fwd_phase_a", st);
-        k_tc_phase_a<<<ga, TCT, SMEM_BYTES, st>>>(P, maps);
+        e = launch_pdl(k_tc_phase_a, ga, dim3(TCT), SMEM_BYTES, st, P, maps);
+        if (e != cudaSuccess) return e;
         timing_end(st);
         if (P.cp == CP_EXACT) launch_fixup(P, st);
     }
     dim3 gc(P.total_segs, P.Hv);
     timing_begin(hist ? "fwd_recompute_states" : "fwd_phase_c", st);
     if (hist)
-        k_tc_phase_c<TK_HIST><<<gc, TCT, SMEM_BYTES, st>>>(P, maps);
+        e = launch_pdl(k_tc_phase_c<TK_HIST>, gc, dim3(TCT), SMEM_BYTES, st, P, maps);
     else
-        k_tc_phase_c<TK_OUT><<<gc, TCT, SMEM_BYTES, st>>>(P, maps);
+        e = launch_pdl(k_tc_phase_c<TK_OUT>, gc, dim3(TCT), SMEM_BYTES, st, P, maps);
+    if (e != cudaSuccess) return e;
     timing_end(st);
     return cudaGetLastError();
 }

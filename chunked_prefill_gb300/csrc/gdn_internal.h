@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "gdn_plan.h"
 
 namespace gdn {
@@ -42,5 +44,24 @@ cudaError_t launch_bwd(const BwdProblem& B, int dtype, cudaStream_t st);
 // Per-kernel event timing hooks (no-ops unless gdn_timing_enable(1)).
 void timing_begin(const char* name, cudaStream_t st);
 void timing_end(cudaStream_t st);
+
+// Launch with programmatic stream serialisation: the kernel may begin launching while the
+// previous kernel in the stream drains; it must call pdl_wait() (tc05.cuh) before touching
+// anything that kernel (or an earlier one) wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 }  // namespace gdn

@@ -70,6 +70,8 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);  // load, [K;Q]K^T, W'
     uint32_t* slot = reinterpret_cast<uint32_t*>(smem + S::oSlot);
 
+    pdl_launch_dependents();
+    pdl_wait();
     const int gch = blockIdx.x, j = blockIdx.y;
     if (gch >= P.plan.chunk_off[P.N]) return;
     int lo = 0, hi = P.N - 1;
@@ -378,7 +380,7 @@ void launch_prep(const Problem& P, const TcMaps& maps, cudaStream_t st) {
     if (P.total_chunks <= 0) return;
     cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PrepSmem::bytes));
     timing_begin("fwd_prep", st);
-    k_prep<<<dim3(P.total_chunks, P.Hv), PT, PrepSmem::bytes, st>>>(P, maps);
+    launch_pdl(k_prep, dim3(P.total_chunks, P.Hv), dim3(PT), PrepSmem::bytes, st, P, maps);
     timing_end(st);
 }
 

@@ -135,6 +135,14 @@ __device__ __forceinline__ void bulk_wait_read0() {
 // ... and have completed
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
+// Programmatic dependent launch: allow the next kernel of the stream to start launching, and
+// wait until the previous kernel has completed with its memory visible.  Without a
+// programmatic dependency both return at once.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // shared-memory accesses by 32-bit shared-window address (no generic-address resolution)
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
