@@ -35,31 +35,40 @@ __device__ unsigned long long g_prep_trace[16];  // debug builds: SM clock at ph
 
 constexpr int PT = 128;  // threads
 constexpr int CH = 64;
-constexpr int LDA = 68;  // fp32 scratch rows
 
-// Shared memory (from a 1024-aligned base).  The [K; Q] tile's Q half later stages P, the A
-// scratch later holds the TU staging tile and the TW operand tile, and the whole [K; Q] tile
-// finally stages W'.
+// The 64 x 64 lower-triangular A and T are kept as their ten nonzero 16 x 16 blocks (row
+// stride BLD), block (I, M), I >= M, at index I (I + 1) / 2 + M.
+constexpr int BLD = 20, BLKF = 16 * BLD;  // floats per block row / per block
+__device__ __forceinline__ int tri(int I, int M) { return I * (I + 1) / 2 + M; }
+
+// Shared memory (from a 1024-aligned base), small enough for four CTAs per SM.  Once
+// [K;Q] K^T is in TMEM the two Q halves of the operand tile hold A's blocks (six, then four),
+// and after the inverse the TU staging tile and the TW operand tile; P is staged in the T
+// region before the inverse writes there; the whole [K;Q] tile finally stages W'.
 struct PrepSmem {
     static constexpr uint32_t oKQ = 0;                    // 2 x 16 KB: rows 0-63 K, 64-127 Q
-    static constexpr uint32_t oA = 32768;                 // 64 x 68 fp32
-    static constexpr uint32_t oT = oA + CH * LDA * 4;     // 64 x 68 fp32
-    static constexpr uint32_t oTmp = oT + CH * LDA * 4;   // 4 x 16 x 20 fp32
+    static constexpr uint32_t oQ0 = 8192, oQ1 = 24576;    // the Q halves
+    static constexpr uint32_t oT = 32768;                 // 10 blocks (12.5 KB), P staging first
+    static constexpr uint32_t oTmp = oT + 10 * BLKF * 4;  // 4 x 16 x 20 fp32
     static constexpr uint32_t oGam = oTmp + 4 * 16 * 20 * 4;
     static constexpr uint32_t oE = oGam + CH * 4, oEi = oE + CH * 4, oBeta = oEi + CH * 4,
                               oBe = oBeta + CH * 4, oFlag = oBe + CH * 4, oBar = oFlag + 16,
                               oSlot = oBar + 3 * 8;
     static constexpr uint32_t bytes = oSlot + 16 + 1024;  // + alignment slack
-    static_assert(oA % 1024 == 0 && CH * LDA * 4 >= 16384, "TU staging and TW tiles fit the A scratch");
+    static_assert(6 * BLKF * 4 <= 8192 && 4 * BLKF * 4 <= 8192, "A blocks fit the Q halves");
+    static_assert(10 * BLKF * 4 >= 8192, "P staging fits the T region");
 };
 
-__global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant__ TcMaps maps) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using S = PrepSmem;
-    float* sA = reinterpret_cast<float*>(smem + S::oA);
     float* sT = reinterpret_cast<float*>(smem + S::oT);
+    auto ablk = [&](int b) {
+        return reinterpret_cast<float*>(smem + (b < 6 ? S::oQ0 + b * BLKF * 4 : S::oQ1 + (b - 6) * BLKF * 4));
+    };
+    auto tblk = [&](int b) { return sT + b * BLKF; };
     float* sTmp = reinterpret_cast<float*>(smem + S::oTmp);
     float* sGam = reinterpret_cast<float*>(smem + S::oGam);
     float* sE = reinterpret_cast<float*>(smem + S::oE);
@@ -167,76 +176,87 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
     __syncthreads();  // gates visible
     PTRACE(1);
 
-    // A (rows of KK) and P (rows of QK): thread = one row of the stacked product
+    // A (rows of KK) and P (rows of QK): thread = one row of the stacked product, in two
+    // halves of 32 columns
     {
         const bool ok = warp_uniform_wait(&bars[1], 0);
         fence_after_sync();
-        float raw[64];
-        tmem_ld32(tm + (uint32_t(32 * w) << 16), raw);
-        tmem_ld32(tm + (uint32_t(32 * w) << 16) + 32, raw + 32);
-        tmem_ld_wait();
         const bool pw = *sFlag != 0;
         const bool qrows = w >= 2;
         const int i = 32 * (w & 1) + lane;
         const float gi = sGam[i], ei = sE[i], bi = sBeta[i];
         if (!ok && lane == 0 && err) atomicOr(err, 1 << 28);
-        if (!qrows) {
+        unsigned char* pt = smem + S::oT;  // P staging (bf16, swizzled rows)
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+            float raw[32];
+            tmem_ld32(tm + (uint32_t(32 * w) << 16) + 32 * hh, raw);
+            tmem_ld_wait();
+            if (!qrows) {
+                const int I = i >> 4, r = i & 15;
 #pragma unroll
-            for (int j4 = 0; j4 < 16; ++j4) {
-                float x[4];
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const int j0 = 32 * hh + 4 * j4, M = j0 >> 4;
+                    if (M > I) continue;  // above the diagonal blocks: not stored
+                    float x[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int jj = 4 * j4 + u;
-                    const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
-                    x[u] = jj < i ? bi * d * raw[jj] : 0.f;
+                    for (int u = 0; u < 4; ++u) {
+                        const int jj = j0 + u;
+                        const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
+                        x[u] = jj < i ? bi * d * raw[4 * j4 + u] : 0.f;
+                    }
+                    *reinterpret_cast<float4*>(ablk(tri(I, M)) + r * BLD + (j0 & 15)) =
+                        make_float4(x[0], x[1], x[2], x[3]);
                 }
-                *reinterpret_cast<float4*>(sA + i * LDA + 4 * j4) = make_float4(x[0], x[1], x[2], x[3]);
-            }
-        } else {
-            // P in bf16, rows swizzled like the scan's K-major operand tiles, over Q's dead half
-            unsigned char* pt = smem + S::oKQ + 8192;
+            } else {
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                float x[8];
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int c8 = 4 * hh + c4;
+                    float x[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int jj = 8 * c8 + u;
-                    const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
-                    x[u] = jj <= i ? d * raw[jj] : 0.f;
+                    for (int u = 0; u < 8; ++u) {
+                        const int jj = 8 * c8 + u;
+                        const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
+                        x[u] = jj <= i ? d * raw[8 * c4 + u] : 0.f;
+                    }
+                    uint4 q4;
+                    q4.x = pack_bf16(x[0], x[1]);
+                    q4.y = pack_bf16(x[2], x[3]);
+                    q4.z = pack_bf16(x[4], x[5]);
+                    q4.w = pack_bf16(x[6], x[7]);
+                    *reinterpret_cast<uint4*>(pt + i * 128 + ((c8 ^ (i & 7)) << 4)) = q4;
                 }
-                uint4 q4;
-                q4.x = pack_bf16(x[0], x[1]);
-                q4.y = pack_bf16(x[2], x[3]);
-                q4.z = pack_bf16(x[4], x[5]);
-                q4.w = pack_bf16(x[6], x[7]);
-                *reinterpret_cast<uint4*>(pt + i * 128 + ((c8 ^ (i & 7)) << 4)) = q4;
             }
-            fence_proxy_async_smem();
         }
+        if (qrows) fence_proxy_async_smem();
     }
     __syncthreads();
     PTRACE(2);
     if (tid == 0) {
-        bulk_store(rec + PREP_P, smem + S::oKQ + 8192, 8192);
+        bulk_store(rec + PREP_P, smem + S::oT, 8192);
         bulk_commit();
+        bulk_wait_read0();  // the T region is free again
     }
+    __syncthreads();
 
     // T = (I + A)^-1: diagonal blocks by substitution (warp q, lane = column) ...
     if (lane < 16) {
-        const int b0 = 16 * w, col = lane;
+        const int col = lane;
+        const float* ab = ablk(tri(w, w));
+        float* tb = tblk(tri(w, w));
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int m = 0; m < r; ++m) {
-                if (m & 1) a1 = fmaf(sA[(b0 + r) * LDA + b0 + m], x[m], a1);
-                else a0 = fmaf(sA[(b0 + r) * LDA + b0 + m], x[m], a0);
+                if (m & 1) a1 = fmaf(ab[r * BLD + m], x[m], a1);
+                else a0 = fmaf(ab[r * BLD + m], x[m], a0);
             }
             x[r] = (r == col) ? 1.f : (r < col ? 0.f : -(a0 + a1));
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(b0 + r) * LDA + b0 + col] = x[r];
+        for (int r = 0; r < 16; ++r) tb[r * BLD + col] = x[r];
     }
     __syncthreads();
     // ... then the off-diagonal blocks on TF32 tiles, one block sub-diagonal per step
@@ -250,13 +270,13 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
                 for (int M = J; M < I; ++M) {
 #pragma unroll
                     for (int kk = 0; kk < 16; kk += 8) {
-                        const float* ar = sA + (16 * I + gq) * LDA + 16 * M + kk + tq;
-                        const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * LDA]),
-                                       a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * LDA + 4]);
+                        const float* ar = ablk(tri(I, M)) + gq * BLD + kk + tq;
+                        const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * BLD]),
+                                       a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * BLD + 4]);
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
-                            const float* br = sT + (16 * M + kk + tq) * LDA + 16 * J + 8 * nt + gq;
-                            mma_tf32(acc[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * LDA]));
+                            const float* br = tblk(tri(M, J)) + (kk + tq) * BLD + 8 * nt + gq;
+                            mma_tf32(acc[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * BLD]));
                         }
                     }
                 }
@@ -271,9 +291,9 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
                 float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int kk = 0; kk < 16; kk += 8) {
-                    const float* ar = sT + (16 * I + gq) * LDA + 16 * I + kk + tq;
-                    const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * LDA]),
-                                   a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * LDA + 4]);
+                    const float* ar = tblk(tri(I, I)) + gq * BLD + kk + tq;
+                    const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * BLD]),
+                                   a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * BLD + 4]);
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         const float* br = xs + (kk + tq) * 20 + 8 * nt + gq;
@@ -282,11 +302,11 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
                 }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    float* tr = sT + (16 * I + gq) * LDA + 16 * J + 8 * nt + 2 * tq;
+                    float* tr = tblk(tri(I, J)) + gq * BLD + 8 * nt + 2 * tq;
                     tr[0] = -acc2[nt][0];
                     tr[1] = -acc2[nt][1];
-                    tr[8 * LDA] = -acc2[nt][2];
-                    tr[8 * LDA + 1] = -acc2[nt][3];
+                    tr[8 * BLD] = -acc2[nt][2];
+                    tr[8 * BLD + 1] = -acc2[nt][3];
                 }
                 __syncwarp();
             }
@@ -298,8 +318,12 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
     // scratch: TU leaves by a bulk copy, TW is the B operand of W'^T = K^T TW^T
     for (int it = tid; it < CH * 8; it += PT) {
         const int r = it >> 3, c8 = it & 7;
-        const float4 t0v = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8);
-        const float4 t1v = *reinterpret_cast<const float4*>(sT + r * LDA + 8 * c8 + 4);
+        float4 t0v = make_float4(0.f, 0.f, 0.f, 0.f), t1v = t0v;
+        if ((c8 >> 1) <= (r >> 4)) {
+            const float* tp = tblk(tri(r >> 4, c8 >> 1)) + (r & 15) * BLD + (c8 & 1) * 8;
+            t0v = *reinterpret_cast<const float4*>(tp);
+            t1v = *reinterpret_cast<const float4*>(tp + 4);
+        }
         const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
         float xu[8], xw[8];
 #pragma unroll
@@ -318,24 +342,24 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
         b.z = pack_bf16(xw[4], xw[5]);
         b.w = pack_bf16(xw[6], xw[7]);
         const uint32_t off = r * 128 + ((c8 ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(smem + S::oA + off) = a;
-        *reinterpret_cast<uint4*>(smem + S::oA + 8192 + off) = b;
+        *reinterpret_cast<uint4*>(smem + S::oQ0 + off) = a;  // TU staging over A's blocks
+        *reinterpret_cast<uint4*>(smem + S::oQ1 + off) = b;  // TW operand tile
     }
     fence_proxy_async_smem();
     __syncthreads();
     PTRACE(4);
     if (tid == 0) {
-        bulk_store(rec + PREP_TU, smem + S::oA, 8192);
+        bulk_store(rec + PREP_TU, smem + S::oQ0, 8192);
         bulk_commit();
         // W'^T [dk][i] = K^T TW^T into TMEM columns [64, 128)
         constexpr uint32_t ID2 = make_idesc(128, 64, 1, 0);
         const uint64_t da = make_desc(kq, 16384, 1024);
-        const uint64_t db = make_desc(smem_addr(smem + S::oA + 8192), 0, 1024);
+        const uint64_t db = make_desc(smem_addr(smem + S::oQ1), 0, 1024);
         fence_after_sync();
 #pragma unroll
         for (int st = 0; st < 4; ++st) mma_bf16(tm + 64, da + (st * 2048 >> 4), db + (st * 32 >> 4), ID2, st > 0);
         commit(&bars[2]);
-        bulk_wait_read0();  // P's staging (over Q) has been read: W' may take the tile
+        bulk_wait_read0();  // TU's staging (over Q) has been read: W' may take the tile
     }
     {
         const bool ok = warp_uniform_wait(&bars[2], 0);
@@ -347,15 +371,19 @@ __global__ void __launch_bounds__(PT, 3) k_prep(Problem P, const __grid_constant
     {
         // thread = key row dk; W' row i, column dk goes to the K-major staging tile
         const int dk = tid;
-        float d[64];
-        tmem_ld32(tm + (uint32_t(32 * w) << 16) + 64, d);
-        tmem_ld32(tm + (uint32_t(32 * w) << 16) + 96, d + 32);
-        tmem_ld_wait();
         const uint32_t base = smem_addr(smem + S::oKQ) + (dk >> 6) * 8192 + (dk & 7) * 2;
         const int cch = (dk & 63) >> 3;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+            float d[32];
+            tmem_ld32(tm + (uint32_t(32 * w) << 16) + 64 + 32 * hh, d);
+            tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-            sts16(base + i * 128 + ((cch ^ (i & 7)) << 4), __bfloat16_as_ushort(__float2bfloat16_rn(d[i])));
+            for (int ii = 0; ii < 32; ++ii) {
+                const int i = 32 * hh + ii;
+                sts16(base + i * 128 + ((cch ^ (i & 7)) << 4), __bfloat16_as_ushort(__float2bfloat16_rn(d[ii])));
+            }
+        }
         fence_proxy_async_smem();
     }
     fence_before_sync();
