@@ -157,6 +157,8 @@ __device__ void bwd_scan(const BwdProblem& B, char* smem, int j, int64_t t0, int
     using S = ScanSmem<Op, C>;
     constexpr int LDK = S::LDK, LDC = S::LDC, LDF = S::LDF;
     const Problem& P = B.f;
+    // bf16: the chunk-local W' and P are read from the forward's preparation records
+    constexpr bool RECS = sizeof(Op) == 2;
     Op* sK = reinterpret_cast<Op*>(smem + S::oK);
     Op* sQ = reinterpret_cast<Op*>(smem + S::oQ);
     Op* sDO = reinterpret_cast<Op*>(smem + S::oDO);
@@ -234,6 +236,29 @@ __device__ void bwd_scan(const BwdProblem& B, char* smem, int j, int64_t t0, int
         }
         __syncthreads();
         if (w == 0) gates_warp0<C>(sGam, sE, sKd);
+        if (RECS) {
+            // W' = -W and P come from the forward's chunk records (bf16, 128-byte swizzled
+            // rows): unswizzle them into the padded operand tiles of this kernel
+            const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
+                                       ((hist_base + ch) * Hv + j) * PREP_TILE_BYTES;
+            for (int q = tid; q < 1024 + 512; q += NT) {
+                if (q < 1024) {
+                    const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
+                    *reinterpret_cast<uint4*>(sW + r * LDK + blk * 64 + cc * 8) =
+                        *reinterpret_cast<const uint4*>(rec + PREP_W + q * 16);
+                } else {
+                    const int q2 = q - 1024, r = q2 >> 3, cc = (q2 & 7) ^ (r & 7);
+                    *reinterpret_cast<uint4*>(sP + r * LDC + cc * 8) =
+                        *reinterpret_cast<const uint4*>(rec + PREP_P + q2 * 16);
+                }
+            }
+            __syncthreads();  // gates
+            for (int idx = tid; idx < C * KD; idx += NT) {
+                const int i = idx / KD, v = idx % KD;
+                sDOe[i * LDK + v] = from_f<Op>(sc * sE[i] * to_f(sDO[i * LDK + v]));
+            }
+            __syncthreads();
+        } else {
         {
             float acc[NTk][4];
             zero_acc(acc);
@@ -280,6 +305,7 @@ __device__ void bwd_scan(const BwdProblem& B, char* smem, int j, int64_t t0, int
                 st2(sW + (m0 + gq) * LDK + cc, wacc[n][0], wacc[n][1]);
                 st2(sW + (m0 + gq + 8) * LDK + cc, wacc[n][2], wacc[n][3]);
             }
+        }
         }
         {  // dV' = scale P^T dO + diag(kd) K dh
             float a1[NTC][4], a2[NTC][4];
@@ -342,7 +368,8 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_phase_a(BwdProblem B) {
     const int nt = int((t1 - t0 + C - 1) / C);
     const int cb = lj * P.L, ce = min(cb + P.L, nt);
     const float* x0 = (lj == nseg - 1 && B.dht) ? B.dht + (int64_t(s) * P.Hv + j) * KVN : nullptr;
-    bwd_scan<Op, C, false>(B, smem, j, t0, t1, cb, ce, x0, B.dhb + (int64_t(gseg) * P.Hv + j) * KVN, 0);
+    bwd_scan<Op, C, false>(B, smem, j, t0, t1, cb, ce, x0, B.dhb + (int64_t(gseg) * P.Hv + j) * KVN,
+                           P.plan.chunk_off[s]);
 }
 
 // Phase C: every segment from its true right-end gradient, storing dh for every chunk; the
