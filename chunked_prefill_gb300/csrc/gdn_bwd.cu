@@ -1044,16 +1044,28 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
     const int fix_smem = (KD * 129 + KD * 8) * 4;
     e = cudaFuncSetAttribute(k_bwd_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, fix_smem);
     if (e != cudaSuccess) return e;
+    constexpr bool TC = sizeof(Op) == 2;  // bf16: tensor-core reverse scan
+    const int64_t T_total = P.cu ? P.T : int64_t(P.N) * P.T;
     if (P.cp != CP_NONE) {
         timing_begin("bwd_phase_a", st);
-        k_bwd_phase_a<Op, C><<<dim3(P.total_segs, P.Hv), NT, SS::bytes, st>>>(B);
+        if (TC) {
+            e = launch_bwd_scan_tc(B, 0, T_total, st);
+            if (e != cudaSuccess) return e;
+        } else {
+            k_bwd_phase_a<Op, C><<<dim3(P.total_segs, P.Hv), NT, SS::bytes, st>>>(B);
+        }
         timing_end(st);
         timing_begin("bwd_fixup", st);
         k_bwd_fixup<<<dim3(P.N, P.Hv, VD / 8), 256, fix_smem, st>>>(B);
         timing_end(st);
     }
     timing_begin("bwd_dh_scan", st);
-    k_bwd_phase_c<Op, C><<<dim3(P.total_segs, P.Hv), NT, SS::bytes, st>>>(B);
+    if (TC) {
+        e = launch_bwd_scan_tc(B, 1, T_total, st);
+        if (e != cudaSuccess) return e;
+    } else {
+        k_bwd_phase_c<Op, C><<<dim3(P.total_segs, P.Hv), NT, SS::bytes, st>>>(B);
+    }
     timing_end(st);
     if (P.total_chunks > 0) {
         timing_begin("bwd_local", st);
@@ -1061,7 +1073,6 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
         timing_end(st);
     }
     if (B.dqp) {
-        const int64_t T_total = P.cu ? P.T : int64_t(P.N) * P.T;
         const int64_t n = T_total * P.Hqk * (KD / 2);
         const int blocks = int(std::min<int64_t>((n + 255) / 256, 4096));
         if (blocks > 0) {

@@ -93,6 +93,15 @@ enum TcKind { TK_STATE = 0, TK_TRANS = 1, TK_OUT = 2, TK_HIST = 3 };
 #ifdef GDN_TRACE
 // debug builds only: SM-clock timestamps of the pipeline events of CTA (0, 0)
 __device__ unsigned long long g_trace[64][32];
+__device__ unsigned long long g_cta_trace[2][512][4];  // [phase A, C][cta]: globaltimer at entry, scan start, scan end, exit
+#define CTRACE(ph, e)                                                                          \
+    do {                                                                                       \
+        if (threadIdx.x == 0 && blockIdx.x * gridDim.y + blockIdx.y < 512) {                   \
+            unsigned long long t_;                                                             \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                             \
+            g_cta_trace[ph][blockIdx.x * gridDim.y + blockIdx.y][e] = t_;                      \
+        }                                                                                      \
+    } while (0)
 #define TRACE(k, ev)                                                                           \
     do {                                                                                       \
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (k) >= 0 && (k) < 64)     \
@@ -101,6 +110,9 @@ __device__ unsigned long long g_trace[64][32];
 #else
 #define TRACE(k, ev) \
     do {             \
+    } while (0)
+#define CTRACE(ph, e) \
+    do {              \
     } while (0)
 #endif
 
@@ -235,6 +247,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    CTRACE(OUT || KIND == TK_HIST ? 1 : 0, 2);
     const uint32_t tm = *tmem_slot;
     if (OUT) {  // the (Q h)^T halves of both DD buffers start at zero
         if (w >= 12) {
@@ -663,6 +676,7 @@ __device__ void tc_scan_pair(const Problem& P, const TcMaps& maps, unsigned char
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    CTRACE(0, 2);
     const uint32_t tm = *tmem_slot;
     const uint32_t k0a = smem_addr(sm + S_K), wq0 = smem_addr(sm + S_WQ);
 
@@ -919,8 +933,10 @@ __device__ void copy_state(const float* x0, float* x_out, bool ident) {
 }
 
 __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_constant__ TcMaps maps) {
+    CTRACE(0, 0);
     pdl_launch_dependents();
     pdl_wait();
+    CTRACE(0, 1);
     unsigned char* sm = aligned_smem();
     const int gseg = blockIdx.x, j = blockIdx.y;
     const int2 sj = P.plan.seg[gseg];
@@ -946,6 +962,7 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
                 return;
             }
             tc_scan_pair(P, maps, sm, j, t0, t1, cb, ce, out, mout, P.plan.chunk_off[s]);
+            CTRACE(0, 3);
         }
     } else {
         if (lj == 0) return;
@@ -958,8 +975,10 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
 
 template <int KIND>
 __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_constant__ TcMaps maps) {
+    CTRACE(1, 0);
     pdl_launch_dependents();
     pdl_wait();
+    CTRACE(1, 1);
     unsigned char* sm = aligned_smem();
     const int gseg = blockIdx.x, j = blockIdx.y;
     const int2 sj = P.plan.seg[gseg];
@@ -975,6 +994,373 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_c
     float* x_out = (lj == nseg - 1 && P.ht) ? P.ht + (int64_t(s) * P.Hv + j) * KVN : nullptr;
     if (ce <= cb) { copy_state(x0, x_out, false); return; }
     tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce, x0, x_out, P.plan.chunk_off[s]);
+    CTRACE(1, 3);
+}
+
+// =====================================================================================
+// Backward: the reverse dh scan on the tensor cores (bf16).  Per chunk, in reverse order,
+// with dOs = scale dO, W' = -W and P from the forward's chunk records:
+//     dV'^T   = dOs^T P + (dh^T K^T) diag(kd)                 (D_a off the chain, D_b on it)
+//     dh_in^T = e_C dh^T + dOs^T diag(e) Q + dV'^T W'
+// The state is kept transposed in TMEM (Xt[v][dk] = dh[dk][v], fp32 + bf16 copy), exactly like
+// the forward scan.  Warp roles: 0 TMA producer; 1 MMA issuer; 2 gates; 4-11 state warps (one
+// warpgroup per half of the key columns / of the chunk's tokens); 12-15 scale dO rows by
+// scale e_i into the operand of the dOs^T diag(e) Q product (rows past the sequence end -> 0).
+// =====================================================================================
+constexpr uint32_t R_K = 0, R_Q = 32768, R_DO = 65536, R_DOE = 98304, R_W = 131072, R_P = 163840;
+static_assert(R_P + 2 * 8192 <= S_GATE, "backward scan stages fit below the gate buffers");
+constexpr uint32_t T_DB = 192, T_DA = 256;
+
+template <bool HIST>
+__device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUtensorMap* mdo,
+                            unsigned char* sm, int j, int64_t t0, int64_t t1, int cb, int ce,
+                            const float* x0, float* x_out, int64_t gbase) {
+    enum RB { R_FULL0 = 0, R_FULL1, R_EMPTY0, R_EMPTY1, R_GATE0, R_GFREE0 = R_GATE0 + NGATE,
+              R_MMA3 = R_GFREE0 + NGATE, R_MMA5, R_EX, R_EV, R_DOE0, R_DOE1, R_DRAIN, R_COUNT };
+    static_assert(R_COUNT * 8 + 8 <= 512, "barrier area");
+    const Problem& P = B.f;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + R_COUNT * 8);
+    int* errflag = reinterpret_cast<int*>(sm + S_BAR + R_COUNT * 8 + 4);
+    Gate* gates = reinterpret_cast<Gate*>(sm + S_GATE);
+    const int G = P.Hv / P.Hqk, qh = j / G;
+    const int n = ce - cb;
+    const float sc = P.scale;
+    auto chunk_of = [&](int k) { return ce - 1 - k; };  // reverse order
+
+    if (tid == 0) {
+        mbar_init(&bars[R_FULL0], 1);
+        mbar_init(&bars[R_FULL1], 1);
+        mbar_init(&bars[R_EMPTY0], 1);
+        mbar_init(&bars[R_EMPTY1], 1);
+        for (int b = 0; b < NGATE; ++b) {
+            mbar_init(&bars[R_GATE0 + b], 1);
+            mbar_init(&bars[R_GFREE0 + b], 12);  // 8 state warps + 4 dO-scaling warps
+        }
+        mbar_init(&bars[R_MMA3], 1);
+        mbar_init(&bars[R_MMA5], 1);
+        mbar_init(&bars[R_EX], 8);
+        mbar_init(&bars[R_EV], 8);
+        mbar_init(&bars[R_DOE0], 4);
+        mbar_init(&bars[R_DOE1], 4);
+        mbar_init(&bars[R_DRAIN], 1);
+        *errflag = 0;
+        mbar_fence_init();
+    }
+    if (w == 0) tmem_alloc(tmem_slot, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+
+    if (w == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t bytes = 16384u * 4u + 8192u;
+            int issued = 0;
+            for (int k = 0; k < n; ++k) {
+                const int st = k & 1;
+                if (k >= 2 && !wait_bar_lazy(bars, R_EMPTY0 + st, ((k - 2) >> 1) & 1, errflag)) break;
+                const int ch = chunk_of(k);
+                const int tc = int(t0 + int64_t(ch) * CH);
+                uint64_t* full = &bars[R_FULL0 + st];
+                const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
+                                           ((gbase + ch) * P.Hv + j) * PREP_TILE_BYTES;
+                unsigned char* kt = sm + R_K + st * 16384;
+                unsigned char* qt = sm + R_Q + st * 16384;
+                unsigned char* dt = sm + R_DO + st * 16384;
+                unsigned char* wt = sm + R_W + st * 16384;
+                mbar_expect_tx(full, bytes);
+                tma_load_3d(kt, &maps.k, full, 0, qh, tc);
+                tma_load_3d(kt + 8192, &maps.k, full, 64, qh, tc);
+                tma_load_3d(qt, &maps.q, full, 0, qh, tc);
+                tma_load_3d(qt + 8192, &maps.q, full, 64, qh, tc);
+                tma_load_3d(dt, mdo, full, 0, j, tc);
+                tma_load_3d(dt + 8192, mdo, full, 64, j, tc);
+                bulk_load(wt, rec + PREP_W, 8192, full);
+                bulk_load(wt + 8192, rec + PREP_W + 8192, 8192, full);
+                bulk_load(sm + R_P + st * 8192, rec + PREP_P, 8192, full);
+                issued = k + 1;
+            }
+            for (int k = max(0, issued - 2); k < issued; ++k)
+                mbar_wait(&bars[R_FULL0 + (k & 1)], (k >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (w == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDA = make_idesc(128, 64, 1, 1);   // dO^T P
+            constexpr uint32_t IDB = make_idesc(128, 64, 0, 0);   // Xt_bf16 K^T
+            constexpr uint32_t IDX = make_idesc(128, 128, 1, 1);  // dOe^T Q
+            constexpr uint32_t IDW = make_idesc(128, 128, 0, 1);  // dV'^T W'
+            const uint32_t k0 = smem_addr(sm + R_K), q0 = smem_addr(sm + R_Q), d0 = smem_addr(sm + R_DO),
+                           e0 = smem_addr(sm + R_DOE), w0 = smem_addr(sm + R_W), p0 = smem_addr(sm + R_P);
+            const uint64_t dK[2] = {kdesc(k0), kdesc(k0 + 16384)};
+            const uint64_t dQ[2] = {mdesc(q0, 8192), mdesc(q0 + 16384, 8192)};
+            const uint64_t dD[2] = {mdesc(d0, 8192), mdesc(d0 + 16384, 8192)};
+            const uint64_t dE[2] = {mdesc(e0, 8192), mdesc(e0 + 16384, 8192)};
+            const uint64_t dW[2] = {mdesc(w0, 8192), mdesc(w0 + 16384, 8192)};
+            const uint64_t dP[2] = {mdesc(p0, 8192), mdesc(p0 + 8192, 8192)};
+            auto issue_da = [&](int k) {
+                const int st = k & 1;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tm + T_DA, (st ? dD[1] : dD[0]) + (s * 2048 >> 4), (st ? dP[1] : dP[0]) + (s * 2048 >> 4),
+                             IDA, s > 0);
+            };
+            bool ok = wait_bar(bars, R_FULL0, 0, errflag);
+            if (ok) {
+                fence_after_sync();
+                issue_da(0);
+            }
+            for (int k = 0; ok && k < n; ++k) {
+                const int st = k & 1;
+                if (!wait_bar(bars, R_EX, k & 1, errflag)) { ok = false; break; }
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32;
+                    mma_bf16_ta(tm + T_DB, tm + T_XB + 8 * s, (st ? dK[1] : dK[0]) + (off >> 4), IDB, s > 0);
+                }
+                commit(&bars[R_MMA3]);
+                if (!wait_bar(bars, R_DOE0 + st, (k >> 1) & 1, errflag)) { ok = false; break; }
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tm + T_XF, (st ? dE[1] : dE[0]) + (s * 2048 >> 4), (st ? dQ[1] : dQ[0]) + (s * 2048 >> 4),
+                             IDX, 1u);
+                if (!wait_bar(bars, R_EV, k & 1, errflag)) { ok = false; break; }
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16_ta(tm + T_XF, tm + T_DB + p_col(s), (st ? dW[1] : dW[0]) + (s * 2048 >> 4), IDW, 1u);
+                commit(&bars[R_MMA5]);
+                commit(&bars[R_EMPTY0 + st]);
+                if (k + 1 < n) {
+                    if (!wait_bar(bars, R_FULL0 + ((k + 1) & 1), ((k + 1) >> 1) & 1, errflag)) { ok = false; break; }
+                    fence_after_sync();
+                    issue_da(k + 1);
+                }
+            }
+            commit(&bars[R_DRAIN]);
+            mbar_wait(&bars[R_DRAIN], 0);
+        }
+        __syncwarp();
+    } else if (w == 2) {
+        // ------------------------------------------------------------ gates
+        for (int k = 0; k < n; ++k) {
+            const int gs = k & (NGATE - 1);
+            const int64_t tc = t0 + int64_t(chunk_of(k)) * CH;
+            const int c = int((t1 - tc) < int64_t(CH) ? (t1 - tc) : int64_t(CH));
+            float gv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = 2 * lane + u;
+                gv[u] = r < c ? P.g[(tc + r) * P.Hv + j] : 0.f;
+            }
+            if (k >= NGATE && !warp_wait<true>(bars, R_GFREE0 + gs, ((k - NGATE) >> 2) & 1, errflag)) break;
+            Gate& gb = gates[gs];
+            float run0 = gv[0], run1 = gv[0] + gv[1];
+            float tot = run1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, tot, off);
+                if (lane >= off) tot += y;
+            }
+            const float excl = tot - run1;
+            const float last = __shfl_sync(0xffffffffu, tot, 31);
+            const float gm[2] = {run0 + excl, run1 + excl};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = 2 * lane + u;
+                gb.gam[r] = gm[u];
+                gb.e[r] = expf(gm[u]);
+                gb.kd[r] = expf(last - gm[u]);
+            }
+            if (lane == 0) {
+                gb.eC = expf(last);
+                gb.c = c;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[R_GATE0 + gs]);
+        }
+    } else if (w >= 12) {
+        // ------------------------------------------------------------ dOe = scale e_i dO_i (i < c)
+        const int v = tid - 384;
+        for (int k = 0; k < n; ++k) {
+            const int st = k & 1, gs = k & (NGATE - 1);
+            if (!warp_wait<true>(bars, R_GATE0 + gs, (k >> 2) & 1, errflag) ||
+                !warp_wait<true>(bars, R_FULL0 + st, (k >> 1) & 1, errflag))
+                break;
+            const Gate& gb = gates[gs];
+            const uint32_t src = smem_addr(sm + R_DO + st * 16384), dst = smem_addr(sm + R_DOE + st * 16384);
+            const uint32_t ge = smem_addr(&gb.e[0]);
+            const int c = gb.c;
+            uint4 u[8];
+            float f[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {  // piece p: 16 bytes of row (p >> 3) & 63, block p >> 9
+                const int p = v + 128 * m, r = (p >> 3) & 63;
+                u[m] = lds128(src + 16 * p);
+                f[m] = r < c ? sc * lds32f(ge + 4 * r) : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                uint32_t* w4 = reinterpret_cast<uint32_t*>(&u[m]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w4[q]);
+                    w4[q] = pack_bf16(f[m] * __low2float(h), f[m] * __high2float(h));
+                }
+                sts128(dst + 16 * (v + 128 * m), u[m]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars[R_DOE0 + st]);
+                mbar_arrive(&bars[R_GFREE0 + gs]);
+            }
+        }
+    } else if (w >= 4) {
+        // ------------------------------------------------------------ state warps
+        const int hf = w >= 8 ? 1 : 0;
+        const int v = tid - (hf ? 256 : 128);
+        const uint32_t lb = uint32_t(32 * (w & 3)) << 16;
+        init_state_half<TK_STATE>(tm, lb, hf, v, x0);
+        bool ok = true;
+        for (int k = 0; ok && k < n; ++k) {
+            const int gs = k & (NGATE - 1);
+            const Gate& gb = gates[gs];
+            if (!warp_wait(bars, R_GATE0 + gs, (k >> 2) & 1, errflag)) { ok = false; break; }
+            if (k >= 1) {
+                if (!warp_wait(bars, R_MMA5, (k - 1) & 1, errflag)) { ok = false; break; }
+                fence_after_sync();
+            }
+            // hand-off: (store dh of the state leaving the chunk,) bf16 copy, decay by e_C
+#pragma unroll 1
+            for (int q = 0; q < 2; ++q) {
+                const int c0 = 64 * hf + 32 * q;
+                float x[32];
+                tmem_ld32(tm + lb + T_XF + c0, x);
+                tmem_ld_wait();
+                if (HIST) {
+                    __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(B.dhist) +
+                                        ((gbase + chunk_of(k)) * P.Hv + j) * (KD * VD);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
+                }
+                float pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
+                tmem_st16(tm + lb + T_XB + c0 / 2, pk);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] *= gb.eC;
+                tmem_st32(tm + lb + T_XF + c0, x);
+            }
+            tmem_st_wait();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[R_EX]);
+            // dV'^T of tokens [32 hf, 32 hf + 32) = scale D_a + kd D_b, packed bf16 in place
+            if (!warp_wait(bars, R_MMA3, k & 1, errflag)) { ok = false; break; }
+            fence_after_sync();
+            float da[32], db[32], kd[32];
+            tmem_ld32(tm + lb + T_DA + 32 * hf, da);
+            tmem_ld32(tm + lb + T_DB + 32 * hf, db);
+            {
+                const uint32_t ka = smem_addr(&gb.kd[32 * hf]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 f4 = lds128f(ka + 16 * i);
+                    kd[4 * i] = f4.x;
+                    kd[4 * i + 1] = f4.y;
+                    kd[4 * i + 2] = f4.z;
+                    kd[4 * i + 3] = f4.w;
+                }
+            }
+            tmem_ld_wait();
+            float pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = __uint_as_float(pack_bf16(fmaf(sc, da[2 * i], kd[2 * i] * db[2 * i]),
+                                                  fmaf(sc, da[2 * i + 1], kd[2 * i + 1] * db[2 * i + 1])));
+            tmem_st16(tm + lb + T_DB + 32 * hf, pk);
+            tmem_st_wait();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars[R_EV]);
+                mbar_arrive(&bars[R_GFREE0 + gs]);
+            }
+        }
+        if (ok && warp_wait(bars, R_MMA5, (n - 1) & 1, errflag)) {
+            fence_after_sync();
+            if (x_out) {
+                for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 16) {
+                    float xv[16];
+                    tmem_ld16(tm + lb + T_XF + c0, xv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) x_out[(c0 + i) * VD + v] = xv[i];
+                }
+            }
+        }
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (*errflag && tid == 0 && P.err) atomicOr(P.err, *errflag);
+    if (w == 0) {
+        fence_after_sync();
+        tmem_dealloc(tm, 512);
+    }
+}
+
+struct BwdMaps {
+    TcMaps f;
+    CUtensorMap dO;
+};
+
+// first phase of the reverse scan: the gradient entering segment lj >= 1 from its right end,
+// started from zero (or from dht for the last segment)
+__global__ void __launch_bounds__(TCT, 1) k_tc_bwd_a(BwdProblem B, const __grid_constant__ BwdMaps maps) {
+    unsigned char* sm = aligned_smem();
+    const Problem& P = B.f;
+    const int gseg = blockIdx.x, j = blockIdx.y;
+    const int2 sj = P.plan.seg[gseg];
+    const int s = sj.x, lj = sj.y;
+    if (s < 0 || s >= P.N || lj == 0) return;
+    const int nseg = P.plan.seg_off[s + 1] - P.plan.seg_off[s];
+    int64_t t0, t1;
+    seq_range(P, s, t0, t1);
+    const int nt = int((t1 - t0 + CH - 1) / CH);
+    const int cb = lj * P.L, ce = min(cb + P.L, nt);
+    const float* x0 = (lj == nseg - 1 && B.dht) ? B.dht + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    float* out = B.dhb + (int64_t(gseg) * P.Hv + j) * KVN;
+    if (ce <= cb) { copy_state(x0, out, false); return; }
+    tc_bwd_scan<false>(B, maps.f, &maps.dO, sm, j, t0, t1, cb, ce, x0, out, P.plan.chunk_off[s]);
+}
+
+// rerun of every segment from its true right-end gradient, storing dh for every chunk; the
+// first segment's result is dh0
+__global__ void __launch_bounds__(TCT, 1) k_tc_bwd_c(BwdProblem B, const __grid_constant__ BwdMaps maps) {
+    unsigned char* sm = aligned_smem();
+    const Problem& P = B.f;
+    const int gseg = blockIdx.x, j = blockIdx.y;
+    const int2 sj = P.plan.seg[gseg];
+    const int s = sj.x, lj = sj.y;
+    if (s < 0 || s >= P.N) return;
+    const int nseg = P.plan.seg_off[s + 1] - P.plan.seg_off[s];
+    int64_t t0, t1;
+    seq_range(P, s, t0, t1);
+    const int nt = int((t1 - t0 + CH - 1) / CH);
+    const int cb = lj * P.L, ce = min(cb + P.L, nt);
+    const float* x0 = (lj == nseg - 1) ? (B.dht ? B.dht + (int64_t(s) * P.Hv + j) * KVN : nullptr)
+                                       : B.dhb + (int64_t(gseg + 1) * P.Hv + j) * KVN;
+    float* x_out = (lj == 0 && B.dh0) ? B.dh0 + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    if (ce <= cb) { copy_state(x0, x_out, false); return; }
+    tc_bwd_scan<true>(B, maps.f, &maps.dO, sm, j, t0, t1, cb, ce, x0, x_out, P.plan.chunk_off[s]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1009,6 +1395,9 @@ bool make_map(CUtensorMap* m, const void* base, int H, int64_t T_total) {
 extern "C" int gdn_debug_trace(unsigned long long* out) {
     return int(cudaMemcpyFromSymbol(out, g_trace, sizeof(g_trace)));
 }
+extern "C" int gdn_debug_cta_trace(unsigned long long* out) {
+    return int(cudaMemcpyFromSymbol(out, g_cta_trace, sizeof(g_cta_trace)));
+}
 #endif
 
 cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStream_t st) {
@@ -1041,6 +1430,21 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
         e = launch_pdl(k_tc_phase_c<TK_OUT>, gc, dim3(TCT), SMEM_BYTES, st, P, maps);
     if (e != cudaSuccess) return e;
     timing_end(st);
+    return cudaGetLastError();
+}
+
+// The two reverse-scan launches of the backward (bf16): first phase, then (after the caller's
+// fix-up) the rerun that stores dh per chunk.  `which` = 0 first phase, 1 rerun.
+cudaError_t launch_bwd_scan_tc(const BwdProblem& B, int which, int64_t T_total, cudaStream_t st) {
+    const Problem& P = B.f;
+    BwdMaps maps;
+    if (!make_map(&maps.f.k, P.k, P.Hqk, T_total) || !make_map(&maps.f.q, P.q, P.Hqk, T_total) ||
+        !make_map(&maps.f.v, P.v, P.Hv, T_total) || !make_map(&maps.dO, B.dO, P.Hv, T_total))
+        return cudaErrorInvalidValue;
+    auto kern = which == 0 ? k_tc_bwd_a : k_tc_bwd_c;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(P.total_segs, P.Hv), TCT, SMEM_BYTES, st>>>(B, maps);
     return cudaGetLastError();
 }
 

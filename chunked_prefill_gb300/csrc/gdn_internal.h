@@ -35,6 +35,9 @@ void launch_prep(const Problem& P, const TcMaps& maps, cudaStream_t st);
 
 // Tensor-core (tcgen05) forward for bf16: same phases as launch_fwd.
 cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStream_t st);
+// Tensor-core reverse dh scan of the backward (bf16; needs the forward's chunk records):
+// which = 0 first context-parallel phase, 1 the rerun storing dh per chunk.
+cudaError_t launch_bwd_scan_tc(const BwdProblem& B, int which, int64_t T_total, cudaStream_t st);
 
 // Backward: reverse dh scan (with the same context-parallel segments as the forward) and
 // the chunk-parallel local gradients; expects the forward recompute (states per chunk in

@@ -8,8 +8,9 @@
 //     TU = T diag(beta),  W' = -T diag(beta e) K     (W' = -W of the pages' WY form; tcgen05)
 // K and Q arrive by TMA; W', TU and P leave by bulk copies from shared-memory tiles already in
 // the 128-byte-swizzled layout the scan's tensor-core operands use.  Rows past the end of a
-// sequence hold whatever tokens follow (finite); beta = g = 0 there makes every product that
-// reaches the scan exactly zero in those rows and columns.
+// sequence hold whatever tokens follow (finite); beta = g = 0 there makes T's rows and the
+// columns of TU and W' for them exactly zero, and P's rows for them are written as zeros (the
+// backward's dO^T P must not see them).
 #include <cuda.h>
 
 #include "gdn_common.cuh"
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                     for (int u = 0; u < 8; ++u) {
                         const int jj = 8 * c8 + u;
                         const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
-                        x[u] = jj <= i ? d * raw[8 * c4 + u] : 0.f;
+                        x[u] = (jj <= i && i < c) ? d * raw[8 * c4 + u] : 0.f;
                     }
                     uint4 q4;
                     q4.x = pack_bf16(x[0], x[1]);
