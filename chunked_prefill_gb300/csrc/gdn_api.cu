@@ -47,6 +47,7 @@ struct HostPlan {
     int total_chunks = 0;
     int max_nseg = 0;
     int64_t total_tokens = 0;
+    int64_t prep_stride = 0;  // bytes per (chunk, v-head) preparation record
     // workspace layout (bytes)
     size_t off_err = 0, off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0,
            off_mbuf = 0, off_prep = 0, off_end = 0;
@@ -201,9 +202,9 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
     h.off_mbuf = off;
     if (h.cp == gdn::CP_EXACT) off += KVB * size_t(total_segs) * p->Hv;
     off = align_up(off, 256);
-    h.off_prep = off;  // W', TU, P tiles of every (chunk, v-head): tensor-core path only
-    if (p->dtype == GDN_BF16)
-        off = align_up(off + size_t(gdn::PREP_TILE_BYTES) * h.total_chunks * p->Hv, 256);
+    h.off_prep = off;  // W', TU, P (and T) tiles of every (chunk, v-head): tensor-core path only
+    h.prep_stride = backward ? gdn::PREP_BWD_BYTES : gdn::PREP_FWD_BYTES;
+    if (p->dtype == GDN_BF16) off = align_up(off + size_t(h.prep_stride) * h.total_chunks * p->Hv, 256);
     if (backward) {
         const size_t elem = p->dtype == GDN_BF16 ? 2 : 4;
         const size_t per_chunk = size_t(128) * 128 * elem * p->Hv;
@@ -234,6 +235,7 @@ void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Proble
     P.hin = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_hin) : nullptr;
     P.mbuf = h.cp == gdn::CP_EXACT ? reinterpret_cast<float*>(ws + h.off_mbuf) : nullptr;
     P.prep = p->dtype == GDN_BF16 ? ws + h.off_prep : nullptr;
+    P.prep_stride = h.prep_stride;
     P.cu = p->cu_seqlens;
     P.N = h.N;
     P.T = p->T;

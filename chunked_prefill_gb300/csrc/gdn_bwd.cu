@@ -240,7 +240,7 @@ __device__ void bwd_scan(const BwdProblem& B, char* smem, int j, int64_t t0, int
             // W' = -W and P come from the forward's chunk records (bf16, 128-byte swizzled
             // rows): unswizzle them into the padded operand tiles of this kernel
             const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
-                                       ((hist_base + ch) * Hv + j) * PREP_TILE_BYTES;
+                                       ((hist_base + ch) * Hv + j) * P.prep_stride;
             for (int q = tid; q < 1024 + 512; q += NT) {
                 if (q < 1024) {
                     const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
@@ -561,6 +561,45 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
     if (w == 0) gates_warp0<C>(sGam, sE, sKd);
+    float acc[NTC][4];
+    if (S::BF) {
+        // bf16: P, T, TU and W' = -T diag(beta e) K come from the forward's chunk records
+        // (128-byte-swizzled bf16 rows, unswizzled here into the padded operand tiles); only
+        // the decayed K K^T (for the dbeta and dgamma terms) and U = TU V are recomputed
+        const unsigned char* rec = static_cast<const unsigned char*>(P.prep) + (int64_t(gch) * Hv + j) * P.prep_stride;
+        for (int q = tid; q < 1024 + 3 * 512; q += NT) {
+            if (q < 1024) {
+                const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
+                *reinterpret_cast<uint4*>(tW + r * LDK + blk * 64 + cc * 8) =
+                    *reinterpret_cast<const uint4*>(rec + PREP_W + q * 16);
+            } else {
+                const int t3 = (q - 1024) >> 9, q2 = (q - 1024) & 511, r = q2 >> 3, cc = (q2 & 7) ^ (r & 7);
+                Op* dst = t3 == 0 ? oP : (t3 == 1 ? oT : oTU);
+                const int off = t3 == 0 ? PREP_P : (t3 == 1 ? PREP_T : PREP_TU);
+                *reinterpret_cast<uint4*>(dst + r * LDC + cc * 8) = *reinterpret_cast<const uint4*>(rec + off + q2 * 16);
+            }
+        }
+        {
+            float a1[NTS][4];
+            zero_acc(a1);
+            warp_mma<NTS, false, true>(a1, tK, LDK, tK, LDK, m0, s0, KD);
+#pragma unroll
+            for (int n = 0; n < NTS; ++n) {
+                const int cc = s0 + 8 * n + 2 * tq;
+                fDB[r0 * LDF + cc] = a1[n][0];
+                fDB[r0 * LDF + cc + 1] = a1[n][1];
+                fDB[r1 * LDF + cc] = a1[n][2];
+                fDB[r1 * LDF + cc + 1] = a1[n][3];
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < C * C; idx += NT) {
+            const int i = idx / C, jj = idx % C;
+            fDB[i * LDF + jj] = (i > jj) ? expf(sGam[i] - sGam[jj]) * fDB[i * LDF + jj] : 0.f;  // Dm * Bm
+        }
+        zero_acc(acc);
+        warp_mma<NTC, false, false>(acc, oTU, LDC, tV, LDK, m0, n0, C);
+    } else {
     {
         float a1[NTS][4], a2[NTS][4];
         zero_acc(a1);
@@ -601,7 +640,6 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     __syncthreads();
 
     // ---- phase 2: W' = -T diag(beta e) K, U = T diag(beta) V, V' = U + W' h
-    float acc[NTC][4];
     {
         float wacc[NTC][4];
         zero_acc(wacc);
@@ -614,6 +652,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         }
         zero_acc(acc);
         warp_mma<NTC, false, false>(acc, oTU, LDC, tV, LDK, m0, n0, C);
+    }
     }
     __syncthreads();  // TW, TU consumed: the h tile may overwrite them
     if (S::BF) load_rows<Op, KD>(const_cast<Op*>(sH), LDK, hsrc, VD, KD);

@@ -280,7 +280,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 unsigned char* kt = sm + S_K + st * S_K_STRIDE;
                 unsigned char* wq = sm + S_WQ + st * S_WQ_STRIDE;
                 const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
-                                           ((hist_base + cb + k) * P.Hv + j) * PREP_TILE_BYTES;
+                                           ((hist_base + cb + k) * P.Hv + j) * P.prep_stride;
                 mbar_expect_tx(full, bytes);
                 tma_load_3d(kt, &maps.k, full, 0, qh, tc);
                 tma_load_3d(kt + 8192, &maps.k, full, 64, qh, tc);
@@ -434,7 +434,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             auto load_p = [&](int q) {  // P of chunk q into ring slot q % NP
                 const int b = q % NP;
                 const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
-                                           ((hist_base + cb + q) * P.Hv + j) * PREP_TILE_BYTES;
+                                           ((hist_base + cb + q) * P.Hv + j) * P.prep_stride;
                 mbar_expect_tx(&bars[B_FULLP0 + b], 8192);
                 bulk_load(sm + S_P + b * S_P_STRIDE, rec + PREP_P, 8192, &bars[B_FULLP0 + b]);
             };
@@ -694,7 +694,7 @@ __device__ void tc_scan_pair(const Problem& P, const TcMaps& maps, unsigned char
                 unsigned char* wq = sm + S_WQ + st * S_WQ_STRIDE;
                 unsigned char* vt = sm + S_V + st * S_V_STRIDE;
                 const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
-                                           ((hist_base + cb + k) * P.Hv + j) * PREP_TILE_BYTES;
+                                           ((hist_base + cb + k) * P.Hv + j) * P.prep_stride;
                 mbar_expect_tx(full, bytes);
                 tma_load_3d(kt, &maps.k, full, 0, qh, tc);
                 tma_load_3d(kt + 8192, &maps.k, full, 64, qh, tc);
@@ -1066,7 +1066,7 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
                 const int tc = int(t0 + int64_t(ch) * CH);
                 uint64_t* full = &bars[R_FULL0 + st];
                 const unsigned char* rec = static_cast<const unsigned char*>(P.prep) +
-                                           ((gbase + ch) * P.Hv + j) * PREP_TILE_BYTES;
+                                           ((gbase + ch) * P.Hv + j) * P.prep_stride;
                 unsigned char* kt = sm + R_K + st * 16384;
                 unsigned char* qt = sm + R_Q + st * 16384;
                 unsigned char* dt = sm + R_DO + st * 16384;

@@ -27,9 +27,11 @@ struct TcMaps {
     CUtensorMap k, q, v;
 };
 // Chunk-parallel preparation of the tensor-core path into P.prep: per (chunk, v-head) one
-// PREP_TILE_BYTES record holding W' = -T diag(beta e) K (bf16 64 x 128, two 128-byte-swizzled
-// 64-column blocks), TU = T diag(beta) (bf16 64 x 64, swizzled) and P (bf16 64 x 64, swizzled).
-constexpr int PREP_W = 0, PREP_TU = 16384, PREP_P = 24576, PREP_TILE_BYTES = 32768;
+// record of P.prep_stride bytes holding W' = -T diag(beta e) K (bf16 64 x 128, two
+// 128-byte-swizzled 64-column blocks), TU = T diag(beta) and P (bf16 64 x 64, swizzled), and
+// for the backward also T itself (bf16 64 x 64, swizzled).
+constexpr int PREP_W = 0, PREP_TU = 16384, PREP_P = 24576, PREP_T = 32768;
+constexpr int PREP_FWD_BYTES = 32768, PREP_BWD_BYTES = 40960;
 void launch_prep(const Problem& P, const TcMaps& maps, cudaStream_t st);
 
 

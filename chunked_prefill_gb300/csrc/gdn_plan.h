@@ -31,7 +31,8 @@ struct Problem {
     float* hin;         // [total_segs, Hv, K, V]  entering state of each segment
     float* mbuf;        // [total_segs, Hv, K, K]  segment transitions (exact CP)
     void* hist;         // [total_chunks, Hv, K, V] entering state of every chunk (bwd)
-    void* prep;         // [total_chunks, Hv, 3] x 8 KB: TW, TU, P tiles (tensor-core path)
+    void* prep;         // [total_chunks, Hv] records of prep_stride bytes (tensor-core path)
+    int64_t prep_stride;  // 32 KB (W', TU, P), or 40 KB with T as well (the backward needs it)
     PlanDev plan;
     const int* cu;      // device cu_seqlens or null
     int N, T, Hqk, Hv;

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
     const int G = P.Hv / P.Hqk, qh = j / G;
-    unsigned char* rec = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * PREP_TILE_BYTES;
+    unsigned char* rec = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * P.prep_stride;
     const uint32_t kq = smem_addr(smem + S::oKQ);
     int* err = P.err;
 
@@ -369,6 +369,26 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     __syncthreads();
     PTRACE(5);
     fence_after_sync();
+    const bool want_t = P.prep_stride >= PREP_BWD_BYTES;
+    if (want_t) {  // the backward also needs T itself: staged over the consumed TW tile
+        for (int it = tid; it < CH * 8; it += PT) {
+            const int r = it >> 3, c8 = it & 7;
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = 0.f;
+            if ((c8 >> 1) <= (r >> 4)) {
+                const float* tp = tblk(tri(r >> 4, c8 >> 1)) + (r & 15) * BLD + (c8 & 1) * 8;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = (8 * c8 + u <= r) ? tp[u] : 0.f;
+            }
+            uint4 q4;
+            q4.x = pack_bf16(x[0], x[1]);
+            q4.y = pack_bf16(x[2], x[3]);
+            q4.z = pack_bf16(x[4], x[5]);
+            q4.w = pack_bf16(x[6], x[7]);
+            *reinterpret_cast<uint4*>(smem + S::oQ1 + r * 128 + ((c8 ^ (r & 7)) << 4)) = q4;
+        }
+    }
     {
         // thread = key row dk; W' row i, column dk goes to the K-major staging tile
         const int dk = tid;
@@ -391,6 +411,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     __syncthreads();
     if (tid == 0) {
         bulk_store(rec + PREP_W, smem + S::oKQ, 16384);
+        if (want_t) bulk_store(rec + PREP_T, smem + S::oQ1, 8192);
         bulk_commit();
         PTRACE(6);
         bulk_wait_read0();  // the staging tiles may go away with the CTA; the writes complete on their own
