@@ -29,6 +29,18 @@
 namespace gdn {
 namespace {
 
+#ifdef GDN_TRACE
+__device__ unsigned long long g_loc_trace[16];  // debug builds: SM clock at phase starts of CTA (0, 0)
+#define LTRACE(e)                                                                               \
+    do {                                                                                        \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) g_loc_trace[e] = clock64(); \
+    } while (0)
+#else
+#define LTRACE(e) \
+    do {          \
+    } while (0)
+#endif
+
 constexpr int NT = 256;
 constexpr int64_t KVN = int64_t(KD) * VD;
 
@@ -548,10 +560,46 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     const int cgrp = w / RB, rgrp = w % RB;
     const int r0 = m0 + gq, r1 = m0 + gq + 8;
 
+    LTRACE(0);
     // ---- phase 1: tiles, gates, K K^T, Q K^T, A, P, T
-    load_rows<Op, C>(tK, LDK, reinterpret_cast<const Op*>(P.k) + qh * KD + tc * qk_stride, qk_stride, c);
-    load_rows<Op, C>(tQ, LDK, reinterpret_cast<const Op*>(P.q) + qh * KD + tc * qk_stride, qk_stride, c);
-    load_rows<Op, C>(tV, LDK, reinterpret_cast<const Op*>(P.v) + j * VD + tc * v_stride, v_stride, c);
+    if (S::BF) {
+        // bf16: every tile the first phases read is requested at once (asynchronous copies):
+        // K, Q, V (rows past the sequence end zero), the chunk record (W' -> its tile, P, T,
+        // TU -> the dQk tile, free until phase 3), the entering state h and the gradient dh
+        const Op* kg = reinterpret_cast<const Op*>(P.k) + qh * KD + tc * qk_stride;
+        const Op* qg = reinterpret_cast<const Op*>(P.q) + qh * KD + tc * qk_stride;
+        const Op* vg = reinterpret_cast<const Op*>(P.v) + j * VD + tc * v_stride;
+        for (int idx = tid; idx < C * 16; idx += NT) {
+            const int r = idx >> 4, cv = idx & 15;
+            const bool ok = r < c;
+            const int rr = ok ? r : 0;
+            cp_async16(tK + r * LDK + cv * 8, kg + rr * qk_stride + cv * 8, ok);
+            cp_async16(tQ + r * LDK + cv * 8, qg + rr * qk_stride + cv * 8, ok);
+            cp_async16(tV + r * LDK + cv * 8, vg + rr * v_stride + cv * 8, ok);
+        }
+        const unsigned char* rec = static_cast<const unsigned char*>(P.prep) + (int64_t(gch) * Hv + j) * P.prep_stride;
+        for (int q = tid; q < 1024 + 3 * 512; q += NT) {
+            if (q < 1024) {
+                const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
+                cp_async16(tW + r * LDK + blk * 64 + cc * 8, rec + PREP_W + q * 16, true);
+            } else {
+                const int t3 = (q - 1024) >> 9, q2 = (q - 1024) & 511, r = q2 >> 3, cc = (q2 & 7) ^ (r & 7);
+                Op* dst = t3 == 0 ? oP : (t3 == 1 ? oT : oX1);
+                const int off = t3 == 0 ? PREP_P : (t3 == 1 ? PREP_T : PREP_TU);
+                cp_async16(dst + r * LDC + cc * 8, rec + off + q2 * 16, true);
+            }
+        }
+        for (int idx = tid; idx < KD * 16; idx += NT) {
+            const int r = idx >> 4, cv = idx & 15;
+            cp_async16(const_cast<Op*>(sH) + r * LDK + cv * 8, hsrc + r * VD + cv * 8, true);
+            cp_async16(const_cast<Op*>(sDH) + r * LDK + cv * 8, dhsrc + r * VD + cv * 8, true);
+        }
+        cp_async_commit();
+    } else {
+        load_rows<Op, C>(tK, LDK, reinterpret_cast<const Op*>(P.k) + qh * KD + tc * qk_stride, qk_stride, c);
+        load_rows<Op, C>(tQ, LDK, reinterpret_cast<const Op*>(P.q) + qh * KD + tc * qk_stride, qk_stride, c);
+        load_rows<Op, C>(tV, LDK, reinterpret_cast<const Op*>(P.v) + j * VD + tc * v_stride, v_stride, c);
+    }
     for (int i = tid; i < C; i += NT) {
         const bool ok = i < c;
         sGam[i] = ok ? P.g[(tc + i) * Hv + j] : 0.f;
@@ -563,22 +611,11 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     if (w == 0) gates_warp0<C>(sGam, sE, sKd);
     float acc[NTC][4];
     if (S::BF) {
-        // bf16: P, T, TU and W' = -T diag(beta e) K come from the forward's chunk records
-        // (128-byte-swizzled bf16 rows, unswizzled here into the padded operand tiles); only
-        // the decayed K K^T (for the dbeta and dgamma terms) and U = TU V are recomputed
-        const unsigned char* rec = static_cast<const unsigned char*>(P.prep) + (int64_t(gch) * Hv + j) * P.prep_stride;
-        for (int q = tid; q < 1024 + 3 * 512; q += NT) {
-            if (q < 1024) {
-                const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
-                *reinterpret_cast<uint4*>(tW + r * LDK + blk * 64 + cc * 8) =
-                    *reinterpret_cast<const uint4*>(rec + PREP_W + q * 16);
-            } else {
-                const int t3 = (q - 1024) >> 9, q2 = (q - 1024) & 511, r = q2 >> 3, cc = (q2 & 7) ^ (r & 7);
-                Op* dst = t3 == 0 ? oP : (t3 == 1 ? oT : oTU);
-                const int off = t3 == 0 ? PREP_P : (t3 == 1 ? PREP_T : PREP_TU);
-                *reinterpret_cast<uint4*>(dst + r * LDC + cc * 8) = *reinterpret_cast<const uint4*>(rec + off + q2 * 16);
-            }
-        }
+        // bf16: P, T, TU and W' = -T diag(beta e) K came from the forward's chunk records
+        // (unswizzled by the copies above); only the decayed K K^T (for the dbeta and dgamma
+        // terms) and U = TU V are recomputed
+        cp_async_wait_all();
+        __syncthreads();
         {
             float a1[NTS][4];
             zero_acc(a1);
@@ -598,7 +635,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
             fDB[i * LDF + jj] = (i > jj) ? expf(sGam[i] - sGam[jj]) * fDB[i * LDF + jj] : 0.f;  // Dm * Bm
         }
         zero_acc(acc);
-        warp_mma<NTC, false, false>(acc, oTU, LDC, tV, LDK, m0, n0, C);
+        warp_mma<NTC, false, false>(acc, oX1, LDC, tV, LDK, m0, n0, C);
     } else {
     {
         float a1[NTS][4], a2[NTS][4];
@@ -639,6 +676,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
 
+    LTRACE(1);
     // ---- phase 2: W' = -T diag(beta e) K, U = T diag(beta) V, V' = U + W' h
     {
         float wacc[NTC][4];
@@ -655,7 +693,6 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     }
     __syncthreads();  // TW, TU consumed: the h tile may overwrite them
-    if (S::BF) load_rows<Op, KD>(const_cast<Op*>(sH), LDK, hsrc, VD, KD);
     __syncthreads();
     warp_mma<NTC, false, false>(acc, tW, LDK, sH, LDS, m0, n0, KD);
 #pragma unroll
@@ -666,9 +703,20 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();  // W' consumed: dO may overwrite it; T fp32 consumed: dh may overwrite it
 
+    LTRACE(2);
     // ---- phase 3: dO, dh; dV' = scale P^T dO + diag(kd) K dh
-    load_rows<Op, C>(tDO, LDK, reinterpret_cast<const Op*>(B.dO) + j * VD + tc * v_stride, v_stride, c);
-    if (S::BF) load_rows<Op, KD>(const_cast<Op*>(sDH), LDK, dhsrc, VD, KD);
+    if (S::BF) {  // dh arrived with the first copies; dO lands while K dh is formed
+        const Op* dg = reinterpret_cast<const Op*>(B.dO) + j * VD + tc * v_stride;
+        for (int idx = tid; idx < C * 16; idx += NT) {
+            const int r = idx >> 4, cv = idx & 15;
+            const bool ok = r < c;
+            cp_async16(tDO + r * LDK + cv * 8, dg + (ok ? r : 0) * v_stride + cv * 8, ok);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+    } else {
+        load_rows<Op, C>(tDO, LDK, reinterpret_cast<const Op*>(B.dO) + j * VD + tc * v_stride, v_stride, c);
+    }
     __syncthreads();
     {
         float a1[NTC][4], a2[NTC][4];
@@ -740,6 +788,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
 
+    LTRACE(3);
     // ---- phase 4: dQ = scale diag(e) dO h^T + dQk K; e_i <dOs_i, (Q h)_i>; <dh, h>
     {
         float a1[NTC][4], a2[NTC][4];
@@ -802,6 +851,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
 
+    LTRACE(4);
     // ---- phase 5: dK = dQk^T Q + diag(kd) (V' dh^T) (+ later terms); r_i
     float dk[NTC][4];
     {
@@ -842,6 +892,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
 
+    LTRACE(5);
     // ---- phase 6: dW = -dV' h^T -> tile (reuses the Q tile)
     {
         float a1[NTC][4];
@@ -857,6 +908,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
 
+    LTRACE(6);
     // ---- phase 7: dT = (dW K^T) diag(beta e) + (dV' V^T) diag(beta) -> fA (fp32) -> oX2
     {
         float a1[NTS][4], a2[NTS][4];
@@ -875,6 +927,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
 
+    LTRACE(7);
     // ---- phase 8: dYW = T^T dW, dYU = T^T dV'; dV = diag(beta) dYU; dK += diag(beta e) dYW
     {
         float yw[NTC][4], yu[NTC][4];
@@ -923,6 +976,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
 
+    LTRACE(8);
     // ---- phase 9: Z = dT T^T; dA = strictly-lower(-T^T Z); dB = diag(beta) dA * Dm
     {
         float z[NTS][4];
@@ -998,6 +1052,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
 
+    LTRACE(9);
     // ---- phase 10: dK += (dB + dB^T) K; store dK
     warp_mma<NTC, false, false>(dk, oX2, LDC, tK, LDK, m0, n0, C);
     {
@@ -1015,6 +1070,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
             }
         }
     }
+    LTRACE(10);
     // ---- dg = reverse in-chunk cumsum of dgamma; dbeta
     if (w == 0) {
         constexpr int PER = C / 32;
@@ -1131,3 +1187,9 @@ cudaError_t launch_bwd(const BwdProblem& B, int dtype, cudaStream_t st) {
 }
 
 }  // namespace gdn
+
+#ifdef GDN_TRACE
+extern "C" int gdn_debug_loc_trace(unsigned long long* out) {
+    return int(cudaMemcpyFromSymbol(out, gdn::g_loc_trace, sizeof(gdn::g_loc_trace)));
+}
+#endif

@@ -139,4 +139,14 @@ __device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
     for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 }
 
+// 16-byte asynchronous global -> shared copy (zero fill when !valid; src must still be a
+// valid address), committed and awaited in groups by the issuing thread
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc, bool valid) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(sdst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(gsrc), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 }  // namespace gdn
