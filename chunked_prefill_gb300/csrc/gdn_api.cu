@@ -50,7 +50,7 @@ struct HostPlan {
     int64_t prep_stride = 0;  // bytes per (chunk, v-head) preparation record
     // workspace layout (bytes)
     size_t off_err = 0, off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0,
-           off_mbuf = 0, off_prep = 0, off_end = 0;
+           off_mbuf = 0, off_mbuf_t = 0, off_prep = 0, off_end = 0;
     // backward only
     size_t off_hist = 0, off_dhist = 0, off_dhb = 0, off_dqp = 0, off_dkp = 0;
 };
@@ -201,6 +201,8 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
     if (h.cp != gdn::CP_NONE) off += KVB * size_t(total_segs) * p->Hv;
     h.off_mbuf = off;
     if (h.cp == gdn::CP_EXACT) off += KVB * size_t(total_segs) * p->Hv;
+    h.off_mbuf_t = off;  // the backward's reverse fix-up reads the transitions untransposed
+    if (h.cp == gdn::CP_EXACT && backward && p->dtype == GDN_BF16) off += KVB * size_t(total_segs) * p->Hv;
     off = align_up(off, 256);
     h.off_prep = off;  // W', TU, P (and T) tiles of every (chunk, v-head): tensor-core path only
     h.prep_stride = backward ? gdn::PREP_BWD_BYTES : gdn::PREP_FWD_BYTES;
@@ -234,6 +236,9 @@ void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Proble
     P.plan.chunk_off = reinterpret_cast<int*>(ws + h.off_chunkoff);
     P.hin = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_hin) : nullptr;
     P.mbuf = h.cp == gdn::CP_EXACT ? reinterpret_cast<float*>(ws + h.off_mbuf) : nullptr;
+    P.mbuf_t = (h.cp == gdn::CP_EXACT && h.prep_stride == gdn::PREP_BWD_BYTES && p->dtype == GDN_BF16)
+                   ? reinterpret_cast<float*>(ws + h.off_mbuf_t)
+                   : nullptr;
     P.prep = p->dtype == GDN_BF16 ? ws + h.off_prep : nullptr;
     P.prep_stride = h.prep_stride;
     P.cu = p->cu_seqlens;

@@ -1151,7 +1151,10 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
         }
         timing_end(st);
         timing_begin("bwd_fixup", st);
-        k_bwd_fixup<<<dim3(P.N, P.Hv, VD / 8), 256, fix_smem, st>>>(B);
+        if (TC && P.mbuf_t)
+            launch_bwd_fixup_tc(B, st);
+        else
+            k_bwd_fixup<<<dim3(P.N, P.Hv, VD / 8), 256, fix_smem, st>>>(B);
         timing_end(st);
     }
     timing_begin("bwd_dh_scan", st);

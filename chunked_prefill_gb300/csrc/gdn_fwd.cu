@@ -463,7 +463,13 @@ __device__ unsigned long long g_fix_trace[64][4];  // debug builds: SM clock per
 #endif
 constexpr int FIX_NB = 2, FIX_T = 256;
 constexpr int FIX_SMEM = FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * 8 * 4 + 64;
-__global__ void __launch_bounds__(FIX_T) k_fixup(Problem P) {
+// REV = false: the forward, hin[g0+lj+1] = M_lj hin[g0+lj] + S_lj for lj = 1..nseg-2, reading
+// M^T (the transposed store).  REV = true: the backward, dhb[g0+lj] = M_lj^T dhb[g0+lj+1] +
+// dhb[g0+lj] for lj = nseg-2..1, reading M (the untransposed store).  In both the shared
+// tile holds A^T for the step's matrix A, and xbuf[g] is read as S and overwritten in place.
+template <bool REV>
+__global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float* mats, float* xbuf,
+                                                 int Hv, int* err) {
     tc::pdl_launch_dependents();
     tc::pdl_wait();
     extern __shared__ __align__(128) unsigned char fsm[];
@@ -472,14 +478,18 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(Problem P) {
     float* xs = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4);  // 128 x 8
     uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * 8 * 4);
     const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * 8;
-    const int g0 = P.plan.seg_off[s], nseg = P.plan.seg_off[s + 1] - g0;
+    const int g0 = seg_off[s], nseg = seg_off[s + 1] - g0;
     if (nseg <= 2) return;
     const int last = nseg - 2;  // steps 1..last
     const int t = threadIdx.x, rg = t & 31, ks = t >> 5;
     const int orow = t >> 1, oc = (t & 1) * 4;  // the 4 outputs this thread finishes
-    auto mt = [&](int lj) { return P.mbuf + (int64_t(g0 + lj) * P.Hv + j) * KV; };
-    auto hp = [&](int lj) {
-        return reinterpret_cast<float4*>(P.hin + (int64_t(g0 + lj) * P.Hv + j) * KV + orow * VD + cb + oc);
+    auto seg_of = [&](int q) { return REV ? nseg - 2 - q : 1 + q; };  // step q -> segment lj
+    auto mt = [&](int q) { return mats + (int64_t(g0 + seg_of(q)) * Hv + j) * KV; };
+    // x entering step q, and the S / result slot of step q
+    auto xin = [&](int q) { return REV ? g0 + seg_of(q) + 1 : g0 + seg_of(q); };
+    auto xout = [&](int q) { return REV ? g0 + seg_of(q) : g0 + seg_of(q) + 1; };
+    auto hp = [&](int g) {
+        return reinterpret_cast<float4*>(xbuf + (int64_t(g) * Hv + j) * KV + orow * VD + cb + oc);
     };
     if (t == 0) {
         for (int b = 0; b < FIX_NB; ++b) tc::mbar_init(&bar[b], 1);
@@ -488,24 +498,24 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(Problem P) {
     __syncthreads();
     if (t == 0) {
         tc::mbar_expect_tx(&bar[0], KD * KD * 4);
-        tc::bulk_load(Ms, mt(1), KD * KD * 4, &bar[0]);
+        tc::bulk_load(Ms, mt(0), KD * KD * 4, &bar[0]);
     }
-    *reinterpret_cast<float4*>(&xs[orow * 8 + oc]) = *hp(1);
-    float4 snext = *hp(2);
+    *reinterpret_cast<float4*>(&xs[orow * 8 + oc]) = *hp(xin(0));
+    float4 snext = *hp(xout(0));
     bool ok = true;
-    for (int lj = 1; lj <= last; ++lj) {
-        const int q = lj - 1, b = q & 1;
-        if (t == 0 && lj + 1 <= last) {  // into the buffer step lj-1 used
+    for (int q = 0; q < last; ++q) {
+        const int b = q & 1;
+        if (t == 0 && q + 1 < last) {  // into the buffer step q-1 used
             tc::mbar_expect_tx(&bar[b ^ 1], KD * KD * 4);
-            tc::bulk_load(Ms + (b ^ 1) * KD * KD, mt(lj + 1), KD * KD * 4, &bar[b ^ 1]);
+            tc::bulk_load(Ms + (b ^ 1) * KD * KD, mt(q + 1), KD * KD * 4, &bar[b ^ 1]);
         }
-        FTRACE(lj, 0);
+        FTRACE(q + 1, 0);
         ok = ok && tc::mbar_wait(&bar[b], (q >> 1) & 1);
-        FTRACE(lj, 1);
+        FTRACE(q + 1, 1);
         __syncthreads();  // also orders the previous step's xs update
-        FTRACE(lj, 2);
+        FTRACE(q + 1, 2);
         const float4 sj = snext;
-        if (lj + 1 <= last) snext = *hp(lj + 2);
+        if (q + 1 < last) snext = *hp(xout(q + 1));
         const float* M = Ms + b * KD * KD;
         float acc[4][8];
 #pragma unroll
@@ -532,7 +542,7 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(Problem P) {
             *reinterpret_cast<float4*>(rp + ((pq ^ (rg & 7)) << 2)) =
                 make_float4(acc[r][c], acc[r][c + 1], acc[r][c + 2], acc[r][c + 3]);
         }
-        FTRACE(lj, 3);
+        FTRACE(q + 1, 3);
         __syncthreads();  // partial blocks visible; everyone is done with xs and buffer b
         {
             const int org = orow >> 2, pq = ((orow & 3) << 1) | (oc >> 2);
@@ -546,10 +556,10 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(Problem P) {
                 o.w += p.w;
             }
             *reinterpret_cast<float4*>(&xs[orow * 8 + oc]) = o;
-            *hp(lj + 1) = o;
+            *hp(xout(q)) = o;
         }
     }
-    if (!ok && t == 0 && P.err) atomicOr(P.err, 1 << 30);
+    if (!ok && t == 0 && err) atomicOr(err, 1 << 30);
 }
 
 // Work decomposition on the device from the device cu_seqlens (same rule as the host).
@@ -584,9 +594,16 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
-    cudaFuncSetAttribute(k_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
-    launch_pdl(k_fixup, dim3(P.N, P.Hv, VD / 8), dim3(FIX_T), FIX_SMEM, st, P);
+    cudaFuncSetAttribute(k_fixup<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
+    launch_pdl(k_fixup<false>, dim3(P.N, P.Hv, VD / 8), dim3(FIX_T), FIX_SMEM, st,
+               static_cast<const int*>(P.plan.seg_off), static_cast<const float*>(P.mbuf), P.hin, P.Hv, P.err);
     timing_end(st);
+}
+
+void launch_bwd_fixup_tc(const BwdProblem& B, cudaStream_t st) {
+    const Problem& P = B.f;
+    cudaFuncSetAttribute(k_fixup<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
+    k_fixup<true><<<dim3(P.N, P.Hv, VD / 8), FIX_T, FIX_SMEM, st>>>(P.plan.seg_off, P.mbuf_t, B.dhb, P.Hv, P.err);
 }
 
 template <typename Op, int C>

@@ -637,7 +637,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
 constexpr uint32_t PM = 256;  // tensor-memory column offset of the M chain
 __device__ void tc_scan_pair(const Problem& P, const TcMaps& maps, unsigned char* sm, int j,
                              int64_t t0, int64_t t1, int cb, int ce, float* s_out, float* m_out,
-                             int64_t hist_base) {
+                             float* m_out_t, int64_t hist_base) {
     enum PB { Q_FULL0 = 0, Q_FULL1, Q_EMPTY0, Q_EMPTY1, Q_GATE0, Q_GFREE0 = Q_GATE0 + NGATE,
               Q_MMA3S = Q_GFREE0 + NGATE, Q_MMA5S, Q_MMA3M, Q_MMA5M, Q_EXS, Q_EVS, Q_EXM, Q_EVM,
               Q_DRAIN, Q_COUNT };
@@ -886,11 +886,15 @@ __device__ void tc_scan_pair(const Problem& P, const TcMaps& maps, unsigned char
                 float xv[16];
                 tmem_ld16(tm + lb + xf + c0, xv);
                 tmem_ld_wait();
-                if (!isS) {  // transitions are stored transposed (M^T)
+                if (!isS) {  // transitions are stored transposed (M^T), and for the backward also as M
 #pragma unroll
                     for (int i = 0; i < 16; i += 4)
                         *reinterpret_cast<float4*>(out + v * VD + c0 + i) =
                             make_float4(xv[i], xv[i + 1], xv[i + 2], xv[i + 3]);
+                    if (m_out_t) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) m_out_t[(c0 + i) * VD + v] = xv[i];
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) out[(c0 + i) * VD + v] = xv[i];
@@ -956,12 +960,14 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
             tc_scan<TK_STATE>(P, maps, sm, j, t0, t1, cb, ce, h0, out, P.plan.chunk_off[s]);
         } else {
             float* mout = P.mbuf + (int64_t(gseg) * P.Hv + j) * KVN;
+            float* mout_t = P.mbuf_t ? P.mbuf_t + (int64_t(gseg) * P.Hv + j) * KVN : nullptr;
             if (ce <= cb) {
                 copy_state(nullptr, out, false);
                 copy_state(nullptr, mout, true);
+                if (mout_t) copy_state(nullptr, mout_t, true);
                 return;
             }
-            tc_scan_pair(P, maps, sm, j, t0, t1, cb, ce, out, mout, P.plan.chunk_off[s]);
+            tc_scan_pair(P, maps, sm, j, t0, t1, cb, ce, out, mout, mout_t, P.plan.chunk_off[s]);
             CTRACE(0, 3);
         }
     } else {

@@ -21,6 +21,8 @@ cudaError_t launch_fwd(const Problem& P, int dtype, bool hist, cudaStream_t st);
 // the exact context-parallel mode, shared by the CUDA-core and tensor-core paths.
 void launch_plan(const Problem& P, int C, cudaStream_t st);
 void launch_fixup(const Problem& P, cudaStream_t st);
+// The backward's reverse fix-up (bf16 path: reads the untransposed transitions P.mbuf_t).
+void launch_bwd_fixup_tc(const BwdProblem& B, cudaStream_t st);
 
 // TMA descriptors of k, q, v for the tensor-core path.
 struct TcMaps {

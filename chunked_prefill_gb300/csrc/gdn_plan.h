@@ -29,7 +29,8 @@ struct Problem {
     float* ht;          // [N, Hv, K, V] or null
     // workspace
     float* hin;         // [total_segs, Hv, K, V]  entering state of each segment
-    float* mbuf;        // [total_segs, Hv, K, K]  segment transitions (exact CP)
+    float* mbuf;        // [total_segs, Hv, K, K]  segment transitions, stored transposed (exact CP)
+    float* mbuf_t;      // the same transitions untransposed (bf16 backward only), or null
     void* hist;         // [total_chunks, Hv, K, V] entering state of every chunk (bwd)
     void* prep;         // [total_chunks, Hv] records of prep_stride bytes (tensor-core path)
     int64_t prep_stride;  // 32 KB (W', TU, P), or 40 KB with T as well (the backward needs it)
