@@ -798,6 +798,14 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         warp_mma<NTC, false, false>(a2, oX1, LDC, tK, LDK, m0, n0, C);
         const float e0 = sc * sE[r0], e1 = sc * sE[r1];
         float* dqp = B.dqp;
+        // <dO_i, (Q h)_i> = <Q_i, (dO h^T)_i>: row sums of Q * (dO h^T), no Q h product needed
+        float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+        for (int n = 0; n < NTC; ++n) {
+            const int cc = n0 + 8 * n + 2 * tq;
+            rs0 += a1[n][0] * to_f(tQ[r0 * LDK + cc]) + a1[n][1] * to_f(tQ[r0 * LDK + cc + 1]);
+            rs1 += a1[n][2] * to_f(tQ[r1 * LDK + cc]) + a1[n][3] * to_f(tQ[r1 * LDK + cc + 1]);
+        }
 #pragma unroll
         for (int n = 0; n < NTC; ++n) {
             const int cc = n0 + 8 * n + 2 * tq;
@@ -811,16 +819,6 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
                 if (r0 < c) st2(dq + (tc + r0) * qk_stride + cc, q00, q01);
                 if (r1 < c) st2(dq + (tc + r1) * qk_stride + cc, q10, q11);
             }
-        }
-        // (Q h) . dO row sums
-        zero_acc(a1);
-        warp_mma<NTC, false, false>(a1, tQ, LDK, sH, LDS, m0, n0, KD);
-        float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-        for (int n = 0; n < NTC; ++n) {
-            const int cc = n0 + 8 * n + 2 * tq;
-            rs0 += a1[n][0] * to_f(tDO[r0 * LDK + cc]) + a1[n][1] * to_f(tDO[r0 * LDK + cc + 1]);
-            rs1 += a1[n][2] * to_f(tDO[r1 * LDK + cc]) + a1[n][3] * to_f(tDO[r1 * LDK + cc + 1]);
         }
         rs0 = quad_sum(rs0);
         rs1 = quad_sum(rs1);
