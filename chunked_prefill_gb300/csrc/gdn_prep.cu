@@ -42,6 +42,8 @@ constexpr int CH = 64;
 constexpr int BLD = 20, BLKF = 16 * BLD;  // floats per block row / per block
 __device__ __forceinline__ int tri(int I, int M) { return I * (I + 1) / 2 + M; }
 
+// One CTA per (chunk, q/k head, slice of at most GMAX v-heads of its group): K and Q are
+// loaded and [K;Q] K^T formed once, then each v-head's gating, inverse and W' follow in turn.
 // Shared memory (from a 1024-aligned base), small enough for four CTAs per SM.  Once
 // [K;Q] K^T is in TMEM the two Q halves of the operand tile hold A's blocks (six, then four),
 // and after the inverse the TU staging tile and the TW operand tile; P is staged in the T
@@ -55,7 +57,9 @@ struct PrepSmem {
     static constexpr uint32_t oE = oGam + CH * 4, oEi = oE + CH * 4, oBeta = oEi + CH * 4,
                               oBe = oBeta + CH * 4, oFlag = oBe + CH * 4, oBar = oFlag + 16,
                               oSlot = oBar + 3 * 8;
-    static constexpr uint32_t bytes = oSlot + 16 + 1024;  // + alignment slack
+    static constexpr int GMAX = 8;                        // v-heads per CTA (q/k group slice)
+    static constexpr uint32_t oGin = oSlot + 16;          // g, beta of those heads: [GMAX][2][64]
+    static constexpr uint32_t bytes = oGin + GMAX * 2 * CH * 4 + 1024;  // + alignment slack
     static_assert(6 * BLKF * 4 <= 8192 && 4 * BLKF * 4 <= 8192, "A blocks fit the Q halves");
     static_assert(10 * BLKF * 4 >= 8192, "P staging fits the T region");
 };
@@ -77,13 +81,18 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     float* sBeta = reinterpret_cast<float*>(smem + S::oBeta);
     float* sBe = reinterpret_cast<float*>(smem + S::oBe);
     int* sFlag = reinterpret_cast<int*>(smem + S::oFlag);
+    float* sGin = reinterpret_cast<float*>(smem + S::oGin);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);  // load, [K;Q]K^T, W'
     uint32_t* slot = reinterpret_cast<uint32_t*>(smem + S::oSlot);
 
     pdl_launch_dependents();
     pdl_wait();
-    const int gch = blockIdx.x, j = blockIdx.y;
+    const int gch = blockIdx.x;
     if (gch >= P.plan.chunk_off[P.N]) return;
+    const int G = P.Hv / P.Hqk;
+    const int nsl = (G + S::GMAX - 1) / S::GMAX;          // slices of a q/k group
+    const int qh = blockIdx.y / nsl, j0 = qh * G + (blockIdx.y % nsl) * S::GMAX;
+    const int nh = min(S::GMAX, qh * G + G - j0);         // v-heads of this CTA
     int lo = 0, hi = P.N - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -105,10 +114,9 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     const int c = int((t1 - tc) < int64_t(CH) ? (t1 - tc) : int64_t(CH));
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
-    const int G = P.Hv / P.Hqk, qh = j / G;
-    unsigned char* rec = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * P.prep_stride;
     const uint32_t kq = smem_addr(smem + S::oKQ);
     int* err = P.err;
+    const bool want_t = P.prep_stride >= PREP_BWD_BYTES;
 
     if (tid == 0) {
         for (int b = 0; b < 3; ++b) mbar_init(&bars[b], 1);
@@ -127,295 +135,314 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         tma_load_3d(smem + S::oKQ + 8192, &maps.q, &bars[0], 0, qh, int(tc));
         tma_load_3d(smem + S::oKQ + 16384 + 8192, &maps.q, &bars[0], 64, qh, int(tc));
     }
-    if (w == 0) {
-        float gv[2], bv[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int r = 2 * lane + u;
-            gv[u] = r < c ? P.g[(tc + r) * P.Hv + j] : 0.f;
-            bv[u] = r < c ? P.beta[(tc + r) * P.Hv + j] : 0.f;
-        }
-        const float run0 = gv[0], run1 = gv[0] + gv[1];
-        float tot = run1;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, tot, off);
-            if (lane >= off) tot += y;
-        }
-        const float excl = tot - run1;
-        const float last = __shfl_sync(0xffffffffu, tot, 31);
-        const float gm[2] = {run0 + excl, run1 + excl};
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int r = 2 * lane + u;
-            const float e = expf(gm[u]);
-            sGam[r] = gm[u];
-            sE[r] = e;
-            sEi[r] = expf(-gm[u]);
-            sBeta[r] = bv[u];
-            sBe[r] = bv[u] * e;
-        }
-        if (lane == 0) *sFlag = (last < -80.f || !(last == last)) ? 1 : 0;
-        if (lane == 0) {
-            // [KK; QK] = [K; Q] K^T into TMEM columns [0, 64)
-            bool ok = mbar_wait(&bars[0], 0);
-            if (ok) {
-                constexpr uint32_t ID1 = make_idesc(128, 64, 0, 0);
-                const uint64_t d = make_desc(kq, 0, 1024);
-#pragma unroll
-                for (int st = 0; st < 8; ++st) {
-                    const uint32_t off = (st >> 2) * 16384 + (st & 3) * 32;
-                    mma_bf16(tm, d + (off >> 4), d + (off >> 4), ID1, st > 0);
-                }
-            } else if (err) {
-                atomicOr(err, 1 << 29);
-            }
-            commit(&bars[1]);
-        }
-        __syncwarp();
+    // g and beta of every v-head of this CTA (rows past the sequence end 0)
+    for (int idx = tid; idx < nh * CH; idx += PT) {
+        const int hh = idx / CH, r = idx % CH;
+        const bool ok = r < c;
+        sGin[(hh * 2) * CH + r] = ok ? P.g[(tc + r) * P.Hv + j0 + hh] : 0.f;
+        sGin[(hh * 2 + 1) * CH + r] = ok ? P.beta[(tc + r) * P.Hv + j0 + hh] : 0.f;
     }
-    __syncthreads();  // gates visible
-    PTRACE(1);
-
-    // A (rows of KK) and P (rows of QK): thread = one row of the stacked product, in two
-    // halves of 32 columns
+    if (tid == 0) {
+        // [KK; QK] = [K; Q] K^T into TMEM columns [0, 64), shared by the v-heads
+        bool ok = mbar_wait(&bars[0], 0);
+        if (ok) {
+            constexpr uint32_t ID1 = make_idesc(128, 64, 0, 0);
+            const uint64_t d = make_desc(kq, 0, 1024);
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+                const uint32_t off = (st >> 2) * 16384 + (st & 3) * 32;
+                mma_bf16(tm, d + (off >> 4), d + (off >> 4), ID1, st > 0);
+            }
+        } else if (err) {
+            atomicOr(err, 1 << 29);
+        }
+        commit(&bars[1]);
+    }
+    __syncthreads();  // g, beta staged
     {
         const bool ok = warp_uniform_wait(&bars[1], 0);
-        fence_after_sync();
-        const bool pw = *sFlag != 0;
-        const bool qrows = w >= 2;
-        const int i = 32 * (w & 1) + lane;
-        const float gi = sGam[i], ei = sE[i], bi = sBeta[i];
         if (!ok && lane == 0 && err) atomicOr(err, 1 << 28);
-        unsigned char* pt = smem + S::oT;  // P staging (bf16, swizzled rows)
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-            float raw[32];
-            tmem_ld32(tm + (uint32_t(32 * w) << 16) + 32 * hh, raw);
-            tmem_ld_wait();
-            if (!qrows) {
-                const int I = i >> 4, r = i & 15;
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const int j0 = 32 * hh + 4 * j4, M = j0 >> 4;
-                    if (M > I) continue;  // above the diagonal blocks: not stored
-                    float x[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int jj = j0 + u;
-                        const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
-                        x[u] = jj < i ? bi * d * raw[4 * j4 + u] : 0.f;
-                    }
-                    *reinterpret_cast<float4*>(ablk(tri(I, M)) + r * BLD + (j0 & 15)) =
-                        make_float4(x[0], x[1], x[2], x[3]);
-                }
-            } else {
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const int c8 = 4 * hh + c4;
-                    float x[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int jj = 8 * c8 + u;
-                        const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
-                        x[u] = (jj <= i && i < c) ? d * raw[8 * c4 + u] : 0.f;
-                    }
-                    uint4 q4;
-                    q4.x = pack_bf16(x[0], x[1]);
-                    q4.y = pack_bf16(x[2], x[3]);
-                    q4.z = pack_bf16(x[4], x[5]);
-                    q4.w = pack_bf16(x[6], x[7]);
-                    *reinterpret_cast<uint4*>(pt + i * 128 + ((c8 ^ (i & 7)) << 4)) = q4;
-                }
-            }
-        }
-        if (qrows) fence_proxy_async_smem();
     }
-    __syncthreads();
-    PTRACE(2);
-    if (tid == 0) {
-        bulk_store(rec + PREP_P, smem + S::oT, 8192);
-        bulk_commit();
-        bulk_wait_read0();  // the T region is free again
-    }
-    __syncthreads();
+    fence_after_sync();
 
-    // T = (I + A)^-1: diagonal blocks by substitution (warp q, lane = column) ...
-    if (lane < 16) {
-        const int col = lane;
-        const float* ab = ablk(tri(w, w));
-        float* tb = tblk(tri(w, w));
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < r; ++m) {
-                if (m & 1) a1 = fmaf(ab[r * BLD + m], x[m], a1);
-                else a0 = fmaf(ab[r * BLD + m], x[m], a0);
-            }
-            x[r] = (r == col) ? 1.f : (r < col ? 0.f : -(a0 + a1));
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) tb[r * BLD + col] = x[r];
-    }
-    __syncthreads();
-    // ... then the off-diagonal blocks on TF32 tiles, one block sub-diagonal per step
-    {
-        float* xs = sTmp + w * (16 * 20);
 #pragma unroll 1
-        for (int dd = 1; dd < 4; ++dd) {
-            const int J = w, I = w + dd;
-            if (I < 4) {
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                for (int M = J; M < I; ++M) {
+    for (int hh = 0; hh < nh; ++hh) {
+        const int j = j0 + hh;
+        unsigned char* rec = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * P.prep_stride;
+        if (w == 0) {  // in-chunk gates of this v-head
+            const float gv[2] = {sGin[(hh * 2) * CH + 2 * lane], sGin[(hh * 2) * CH + 2 * lane + 1]};
+            const float bv[2] = {sGin[(hh * 2 + 1) * CH + 2 * lane], sGin[(hh * 2 + 1) * CH + 2 * lane + 1]};
+            const float run0 = gv[0], run1 = gv[0] + gv[1];
+            float tot = run1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, tot, off);
+                if (lane >= off) tot += y;
+            }
+            const float excl = tot - run1;
+            const float last = __shfl_sync(0xffffffffu, tot, 31);
+            const float gm[2] = {run0 + excl, run1 + excl};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = 2 * lane + u;
+                const float e = expf(gm[u]);
+                sGam[r] = gm[u];
+                sE[r] = e;
+                sEi[r] = expf(-gm[u]);
+                sBeta[r] = bv[u];
+                sBe[r] = bv[u] * e;
+            }
+            if (lane == 0) *sFlag = (last < -80.f || !(last == last)) ? 1 : 0;
+        }
+        __syncthreads();  // gates visible; the previous head's staging has been read
+        PTRACE(1);
+
+        // A (rows of KK) and P (rows of QK): thread = one row of the stacked product, in two
+        // halves of 32 columns
+        {
+            const bool pw = *sFlag != 0;
+            const bool qrows = w >= 2;
+            const int i = 32 * (w & 1) + lane;
+            const float gi = sGam[i], ei = sE[i], bi = sBeta[i];
+            unsigned char* pt = smem + S::oT;  // P staging (bf16, swizzled rows)
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float raw[32];
+                tmem_ld32(tm + (uint32_t(32 * w) << 16) + 32 * h2, raw);
+                tmem_ld_wait();
+                if (!qrows) {
+                    const int I = i >> 4, r = i & 15;
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const int jb = 32 * h2 + 4 * j4, M = jb >> 4;
+                        if (M > I) continue;  // above the diagonal blocks: not stored
+                        float x[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int jj = jb + u;
+                            const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
+                            x[u] = jj < i ? bi * d * raw[4 * j4 + u] : 0.f;
+                        }
+                        *reinterpret_cast<float4*>(ablk(tri(I, M)) + r * BLD + (jb & 15)) =
+                            make_float4(x[0], x[1], x[2], x[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int c8 = 4 * h2 + c4;
+                        float x[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int jj = 8 * c8 + u;
+                            const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
+                            x[u] = (jj <= i && i < c) ? d * raw[8 * c4 + u] : 0.f;
+                        }
+                        uint4 q4;
+                        q4.x = pack_bf16(x[0], x[1]);
+                        q4.y = pack_bf16(x[2], x[3]);
+                        q4.z = pack_bf16(x[4], x[5]);
+                        q4.w = pack_bf16(x[6], x[7]);
+                        *reinterpret_cast<uint4*>(pt + i * 128 + ((c8 ^ (i & 7)) << 4)) = q4;
+                    }
+                }
+            }
+            if (qrows) fence_proxy_async_smem();
+        }
+        __syncthreads();
+        PTRACE(2);
+        if (tid == 0) {
+            bulk_store(rec + PREP_P, smem + S::oT, 8192);
+            bulk_commit();
+            bulk_wait_read0();  // the T region is free again
+        }
+        __syncthreads();
+
+        // T = (I + A)^-1: diagonal blocks by substitution (warp q, lane = column) ...
+        if (lane < 16) {
+            const int col = lane;
+            const float* ab = ablk(tri(w, w));
+            float* tb = tblk(tri(w, w));
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) {
+                    if (m & 1) a1 = fmaf(ab[r * BLD + m], x[m], a1);
+                    else a0 = fmaf(ab[r * BLD + m], x[m], a0);
+                }
+                x[r] = (r == col) ? 1.f : (r < col ? 0.f : -(a0 + a1));
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) tb[r * BLD + col] = x[r];
+        }
+        __syncthreads();
+        // ... then the off-diagonal blocks on TF32 tiles, one block sub-diagonal per step
+        {
+            float* xs = sTmp + w * (16 * 20);
+#pragma unroll 1
+            for (int dd = 1; dd < 4; ++dd) {
+                const int J = w, I = w + dd;
+                if (I < 4) {
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int M = J; M < I; ++M) {
+#pragma unroll
+                        for (int kk = 0; kk < 16; kk += 8) {
+                            const float* ar = ablk(tri(I, M)) + gq * BLD + kk + tq;
+                            const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * BLD]),
+                                           a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * BLD + 4]);
+#pragma unroll
+                            for (int nt = 0; nt < 2; ++nt) {
+                                const float* br = tblk(tri(M, J)) + (kk + tq) * BLD + 8 * nt + gq;
+                                mma_tf32(acc[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * BLD]));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        xs[gq * 20 + 8 * nt + 2 * tq] = acc[nt][0];
+                        xs[gq * 20 + 8 * nt + 2 * tq + 1] = acc[nt][1];
+                        xs[(gq + 8) * 20 + 8 * nt + 2 * tq] = acc[nt][2];
+                        xs[(gq + 8) * 20 + 8 * nt + 2 * tq + 1] = acc[nt][3];
+                    }
+                    __syncwarp();
+                    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                     for (int kk = 0; kk < 16; kk += 8) {
-                        const float* ar = ablk(tri(I, M)) + gq * BLD + kk + tq;
+                        const float* ar = tblk(tri(I, I)) + gq * BLD + kk + tq;
                         const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * BLD]),
                                        a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * BLD + 4]);
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
-                            const float* br = tblk(tri(M, J)) + (kk + tq) * BLD + 8 * nt + gq;
-                            mma_tf32(acc[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * BLD]));
+                            const float* br = xs + (kk + tq) * 20 + 8 * nt + gq;
+                            mma_tf32(acc2[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * 20]));
                         }
                     }
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    xs[gq * 20 + 8 * nt + 2 * tq] = acc[nt][0];
-                    xs[gq * 20 + 8 * nt + 2 * tq + 1] = acc[nt][1];
-                    xs[(gq + 8) * 20 + 8 * nt + 2 * tq] = acc[nt][2];
-                    xs[(gq + 8) * 20 + 8 * nt + 2 * tq + 1] = acc[nt][3];
-                }
-                __syncwarp();
-                float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int kk = 0; kk < 16; kk += 8) {
-                    const float* ar = tblk(tri(I, I)) + gq * BLD + kk + tq;
-                    const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * BLD]),
-                                   a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * BLD + 4]);
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        const float* br = xs + (kk + tq) * 20 + 8 * nt + gq;
-                        mma_tf32(acc2[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * 20]));
+                        float* tr = tblk(tri(I, J)) + gq * BLD + 8 * nt + 2 * tq;
+                        tr[0] = -acc2[nt][0];
+                        tr[1] = -acc2[nt][1];
+                        tr[8 * BLD] = -acc2[nt][2];
+                        tr[8 * BLD + 1] = -acc2[nt][3];
                     }
+                    __syncwarp();
                 }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    float* tr = tblk(tri(I, J)) + gq * BLD + 8 * nt + 2 * tq;
-                    tr[0] = -acc2[nt][0];
-                    tr[1] = -acc2[nt][1];
-                    tr[8 * BLD] = -acc2[nt][2];
-                    tr[8 * BLD + 1] = -acc2[nt][3];
-                }
-                __syncwarp();
+                __syncthreads();
             }
-            __syncthreads();
         }
-    }
-    PTRACE(3);
-    // TU = T diag(beta) and TW = -T diag(beta e) as swizzled bf16 tiles over the dead A
-    // scratch: TU leaves by a bulk copy, TW is the B operand of W'^T = K^T TW^T
-    for (int it = tid; it < CH * 8; it += PT) {
-        const int r = it >> 3, c8 = it & 7;
-        float4 t0v = make_float4(0.f, 0.f, 0.f, 0.f), t1v = t0v;
-        if ((c8 >> 1) <= (r >> 4)) {
-            const float* tp = tblk(tri(r >> 4, c8 >> 1)) + (r & 15) * BLD + (c8 & 1) * 8;
-            t0v = *reinterpret_cast<const float4*>(tp);
-            t1v = *reinterpret_cast<const float4*>(tp + 4);
-        }
-        const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
-        float xu[8], xw[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int cc = 8 * c8 + u;
-            xu[u] = cc <= r ? tv[u] * sBeta[cc] : 0.f;
-            xw[u] = cc <= r ? -tv[u] * sBe[cc] : 0.f;
-        }
-        uint4 a, b;
-        a.x = pack_bf16(xu[0], xu[1]);
-        a.y = pack_bf16(xu[2], xu[3]);
-        a.z = pack_bf16(xu[4], xu[5]);
-        a.w = pack_bf16(xu[6], xu[7]);
-        b.x = pack_bf16(xw[0], xw[1]);
-        b.y = pack_bf16(xw[2], xw[3]);
-        b.z = pack_bf16(xw[4], xw[5]);
-        b.w = pack_bf16(xw[6], xw[7]);
-        const uint32_t off = r * 128 + ((c8 ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(smem + S::oQ0 + off) = a;  // TU staging over A's blocks
-        *reinterpret_cast<uint4*>(smem + S::oQ1 + off) = b;  // TW operand tile
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    PTRACE(4);
-    if (tid == 0) {
-        bulk_store(rec + PREP_TU, smem + S::oQ0, 8192);
-        bulk_commit();
-        // W'^T [dk][i] = K^T TW^T into TMEM columns [64, 128)
-        constexpr uint32_t ID2 = make_idesc(128, 64, 1, 0);
-        const uint64_t da = make_desc(kq, 16384, 1024);
-        const uint64_t db = make_desc(smem_addr(smem + S::oQ1), 0, 1024);
-        fence_after_sync();
-#pragma unroll
-        for (int st = 0; st < 4; ++st) mma_bf16(tm + 64, da + (st * 2048 >> 4), db + (st * 32 >> 4), ID2, st > 0);
-        commit(&bars[2]);
-        bulk_wait_read0();  // TU's staging (over Q) has been read: W' may take the tile
-    }
-    {
-        const bool ok = warp_uniform_wait(&bars[2], 0);
-        if (!ok && lane == 0 && err) atomicOr(err, 1 << 27);
-    }
-    __syncthreads();
-    PTRACE(5);
-    fence_after_sync();
-    const bool want_t = P.prep_stride >= PREP_BWD_BYTES;
-    if (want_t) {  // the backward also needs T itself: staged over the consumed TW tile
+        PTRACE(3);
+        // TU = T diag(beta) and TW = -T diag(beta e) as swizzled bf16 tiles over the dead A
+        // blocks: TU leaves by a bulk copy, TW is the B operand of W'^T = K^T TW^T
         for (int it = tid; it < CH * 8; it += PT) {
             const int r = it >> 3, c8 = it & 7;
-            float x[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = 0.f;
+            float4 t0v = make_float4(0.f, 0.f, 0.f, 0.f), t1v = t0v;
             if ((c8 >> 1) <= (r >> 4)) {
                 const float* tp = tblk(tri(r >> 4, c8 >> 1)) + (r & 15) * BLD + (c8 & 1) * 8;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = (8 * c8 + u <= r) ? tp[u] : 0.f;
+                t0v = *reinterpret_cast<const float4*>(tp);
+                t1v = *reinterpret_cast<const float4*>(tp + 4);
             }
-            uint4 q4;
-            q4.x = pack_bf16(x[0], x[1]);
-            q4.y = pack_bf16(x[2], x[3]);
-            q4.z = pack_bf16(x[4], x[5]);
-            q4.w = pack_bf16(x[6], x[7]);
-            *reinterpret_cast<uint4*>(smem + S::oQ1 + r * 128 + ((c8 ^ (r & 7)) << 4)) = q4;
-        }
-    }
-    {
-        // thread = key row dk; W' row i, column dk goes to the K-major staging tile
-        const int dk = tid;
-        const uint32_t base = smem_addr(smem + S::oKQ) + (dk >> 6) * 8192 + (dk & 7) * 2;
-        const int cch = (dk & 63) >> 3;
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-            float d[32];
-            tmem_ld32(tm + (uint32_t(32 * w) << 16) + 64 + 32 * hh, d);
-            tmem_ld_wait();
+            const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+            float xu[8], xw[8];
 #pragma unroll
-            for (int ii = 0; ii < 32; ++ii) {
-                const int i = 32 * hh + ii;
-                sts16(base + i * 128 + ((cch ^ (i & 7)) << 4), __bfloat16_as_ushort(__float2bfloat16_rn(d[ii])));
+            for (int u = 0; u < 8; ++u) {
+                const int cc = 8 * c8 + u;
+                xu[u] = cc <= r ? tv[u] * sBeta[cc] : 0.f;
+                xw[u] = cc <= r ? -tv[u] * sBe[cc] : 0.f;
             }
+            uint4 a, b;
+            a.x = pack_bf16(xu[0], xu[1]);
+            a.y = pack_bf16(xu[2], xu[3]);
+            a.z = pack_bf16(xu[4], xu[5]);
+            a.w = pack_bf16(xu[6], xu[7]);
+            b.x = pack_bf16(xw[0], xw[1]);
+            b.y = pack_bf16(xw[2], xw[3]);
+            b.z = pack_bf16(xw[4], xw[5]);
+            b.w = pack_bf16(xw[6], xw[7]);
+            const uint32_t off = r * 128 + ((c8 ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(smem + S::oQ0 + off) = a;  // TU staging
+            *reinterpret_cast<uint4*>(smem + S::oQ1 + off) = b;  // TW operand tile
         }
         fence_proxy_async_smem();
-    }
-    fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_store(rec + PREP_W, smem + S::oKQ, 16384);
-        if (want_t) bulk_store(rec + PREP_T, smem + S::oQ1, 8192);
-        bulk_commit();
-        PTRACE(6);
-        bulk_wait_read0();  // the staging tiles may go away with the CTA; the writes complete on their own
-        PTRACE(7);
+        __syncthreads();
+        PTRACE(4);
+        if (tid == 0) {
+            bulk_store(rec + PREP_TU, smem + S::oQ0, 8192);
+            bulk_commit();
+            // W'^T [dk][i] = K^T TW^T into TMEM columns [64, 128)
+            constexpr uint32_t ID2 = make_idesc(128, 64, 1, 0);
+            const uint64_t da = make_desc(kq, 16384, 1024);
+            const uint64_t db = make_desc(smem_addr(smem + S::oQ1), 0, 1024);
+            fence_after_sync();
+#pragma unroll
+            for (int st = 0; st < 4; ++st) mma_bf16(tm + 64, da + (st * 2048 >> 4), db + (st * 32 >> 4), ID2, st > 0);
+            commit(&bars[2]);
+        }
+        // T itself for the backward: held in registers, then staged in bf16 over the T region
+        float tkeep[32];
+        if (want_t) {
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                const int it = tid + PT * u4, r = it >> 3, c8 = it & 7;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) tkeep[8 * u4 + u] = 0.f;
+                if ((c8 >> 1) <= (r >> 4)) {
+                    const float* tp = tblk(tri(r >> 4, c8 >> 1)) + (r & 15) * BLD + (c8 & 1) * 8;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) tkeep[8 * u4 + u] = (8 * c8 + u <= r) ? tp[u] : 0.f;
+                }
+            }
+        }
+        {
+            const bool ok = warp_uniform_wait(&bars[2], hh & 1);
+            if (!ok && lane == 0 && err) atomicOr(err, 1 << 27);
+        }
+        if (tid == 0) bulk_wait_read0();  // TU's staging has been read: W' may take it
+        __syncthreads();
+        PTRACE(5);
+        fence_after_sync();
+        if (want_t) {
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                const int it = tid + PT * u4, r = it >> 3, c8 = it & 7;
+                uint4 q4;
+                q4.x = pack_bf16(tkeep[8 * u4 + 0], tkeep[8 * u4 + 1]);
+                q4.y = pack_bf16(tkeep[8 * u4 + 2], tkeep[8 * u4 + 3]);
+                q4.z = pack_bf16(tkeep[8 * u4 + 4], tkeep[8 * u4 + 5]);
+                q4.w = pack_bf16(tkeep[8 * u4 + 6], tkeep[8 * u4 + 7]);
+                *reinterpret_cast<uint4*>(smem + S::oT + r * 128 + ((c8 ^ (r & 7)) << 4)) = q4;
+            }
+        }
+        {
+            // thread = key row dk; W' row i, column dk goes to its K-major staging block
+            // (columns 0-63 over the TU staging, 64-127 over the consumed TW tile)
+            const int dk = tid;
+            const uint32_t base = smem_addr(smem + ((dk >> 6) ? S::oQ1 : S::oQ0)) + (dk & 7) * 2;
+            const int cch = (dk & 63) >> 3;
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float d[32];
+                tmem_ld32(tm + (uint32_t(32 * w) << 16) + 64 + 32 * h2, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) {
+                    const int i = 32 * h2 + ii;
+                    sts16(base + i * 128 + ((cch ^ (i & 7)) << 4), __bfloat16_as_ushort(__float2bfloat16_rn(d[ii])));
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store(rec + PREP_W, smem + S::oQ0, 8192);
+            bulk_store(rec + PREP_W + 8192, smem + S::oQ1, 8192);
+            if (want_t) bulk_store(rec + PREP_T, smem + S::oT, 8192);
+            bulk_commit();
+            PTRACE(6);
+            bulk_wait_read0();  // the next head (or the CTA's exit) may reuse the staging tiles
+            PTRACE(7);
+        }
     }
     __syncthreads();
     if (w == 0) {
@@ -429,8 +456,9 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
 void launch_prep(const Problem& P, const TcMaps& maps, cudaStream_t st) {
     if (P.total_chunks <= 0) return;
     cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PrepSmem::bytes));
+    const int G = P.Hv / P.Hqk, nsl = (G + PrepSmem::GMAX - 1) / PrepSmem::GMAX;
     timing_begin("fwd_prep", st);
-    launch_pdl(k_prep, dim3(P.total_chunks, P.Hv), dim3(PT), PrepSmem::bytes, st, P, maps);
+    launch_pdl(k_prep, dim3(P.total_chunks, P.Hqk * nsl), dim3(PT), PrepSmem::bytes, st, P, maps);
     timing_end(st);
 }
 
