@@ -123,15 +123,6 @@ __device__ __forceinline__ uint64_t mdesc(uint32_t addr, uint32_t lbo) {  // MN-
     return make_desc(addr, lbo, 1024);
 }
 
-// store 8 consecutive fp32 values as one 16-byte bf16 chunk of row r of an SW128 tile
-__device__ __forceinline__ void st_chunk8(unsigned char* tile, int r, int ch, const float* x) {
-    uint4 u;
-    u.x = pack_bf16(x[0], x[1]);
-    u.y = pack_bf16(x[2], x[3]);
-    u.z = pack_bf16(x[4], x[5]);
-    u.w = pack_bf16(x[6], x[7]);
-    *reinterpret_cast<uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4)) = u;
-}
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bars, int b, uint32_t parity, int* errflag) {
     if (mbar_wait(&bars[b], parity)) return true;
@@ -175,29 +166,32 @@ __device__ __forceinline__ void init_state_half(uint32_t tm, uint32_t lb, int ha
 // One half (64 key columns) of the per-chunk state hand-off: read the fp32 state, write its
 // bf16 copy (the A operand of the V' and Q h products), store it for the backward when asked,
 // and decay the fp32 state by exp(gamma_C) before the chunk's update accumulates onto it.
-template <int KIND>
+template <int KIND, bool WIDE = true>
 __device__ __forceinline__ void convert_state_half(const Problem& P, uint32_t tm, uint32_t lb,
                                                    uint32_t xb, int half, int v, float eC,
                                                    int64_t chunk, int j, uint32_t xf = T_XF) {
+    // WIDE: both 32-column loads in flight before the wait (64 registers); otherwise in turn
+    constexpr int W = WIDE ? 64 : 32;
 #pragma unroll 1
-    for (int q = 0; q < 2; ++q) {
-        const int c0 = 64 * half + 32 * q;
-        float x[32];
+    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += W) {
+        float x[W];
         tmem_ld32(tm + lb + xf + c0, x);
+        if (WIDE) tmem_ld32(tm + lb + xf + c0 + 32, x + (W - 32));
         tmem_ld_wait();
         if (KIND == TK_HIST) {
             __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(P.hist) + (chunk * P.Hv + j) * (KD * VD);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
+            for (int i = 0; i < W; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
         }
-        float pk[16];
+        float pk[W / 2];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
+        for (int i = 0; i < W / 2; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
         tmem_st16(tm + lb + xb + c0 / 2, pk);
+        if (WIDE) tmem_st16(tm + lb + xb + c0 / 2 + 16, pk + (W / 2 - 16));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] *= eC;
-        tmem_st16(tm + lb + xf + c0, x);
-        tmem_st16(tm + lb + xf + c0 + 16, x + 16);
+        for (int i = 0; i < W; ++i) x[i] *= eC;
+        tmem_st32(tm + lb + xf + c0, x);
+        if (WIDE) tmem_st32(tm + lb + xf + c0 + 32, x + (W - 32));
     }
     tmem_st_wait();
 }
@@ -841,8 +835,8 @@ __device__ void tc_scan_pair(const Problem& P, const TcMaps& maps, unsigned char
             if (isS) {
                 convert_state_half<TK_STATE>(P, tm, lb, xb, hf, v, gb.eC, 0, j, xf);
             } else {
-                convert_state_half<TK_TRANS>(P, tm, lb, xb, 0, v, gb.eC, 0, j, xf);
-                convert_state_half<TK_TRANS>(P, tm, lb, xb, 1, v, gb.eC, 0, j, xf);
+                convert_state_half<TK_TRANS, false>(P, tm, lb, xb, 0, v, gb.eC, 0, j, xf);
+                convert_state_half<TK_TRANS, false>(P, tm, lb, xb, 1, v, gb.eC, 0, j, xf);
             }
             fence_before_sync();
             __syncwarp();

@@ -277,59 +277,83 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
             for (int r = 0; r < 16; ++r) tb[r * BLD + col] = x[r];
         }
         __syncthreads();
-        // ... then the off-diagonal blocks on TF32 tiles, one block sub-diagonal per step
+        // ... then the off-diagonal blocks on TF32 tiles, by halves: with T_AA, T_BB the inverses
+        // of the two 32 x 32 diagonal halves, T_BA = -T_BB (A_BA T_AA).  Three rounds of at most
+        // two 16 x 16 products per warp; scratch blocks S0..S3 in sTmp.
         {
-            float* xs = sTmp + w * (16 * 20);
-#pragma unroll 1
-            for (int dd = 1; dd < 4; ++dd) {
-                const int J = w, I = w + dd;
-                if (I < 4) {
-                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int M = J; M < I; ++M) {
+            auto mm = [&](float (&acc)[2][4], const float* Am, const float* Bm) {  // acc += Am Bm
 #pragma unroll
-                        for (int kk = 0; kk < 16; kk += 8) {
-                            const float* ar = ablk(tri(I, M)) + gq * BLD + kk + tq;
-                            const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * BLD]),
-                                           a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * BLD + 4]);
-#pragma unroll
-                            for (int nt = 0; nt < 2; ++nt) {
-                                const float* br = tblk(tri(M, J)) + (kk + tq) * BLD + 8 * nt + gq;
-                                mma_tf32(acc[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * BLD]));
-                            }
-                        }
-                    }
+                for (int kk = 0; kk < 16; kk += 8) {
+                    const float* ar = Am + gq * BLD + kk + tq;
+                    const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * BLD]), a2 = f2tf32(ar[4]),
+                                   a3 = f2tf32(ar[8 * BLD + 4]);
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        xs[gq * 20 + 8 * nt + 2 * tq] = acc[nt][0];
-                        xs[gq * 20 + 8 * nt + 2 * tq + 1] = acc[nt][1];
-                        xs[(gq + 8) * 20 + 8 * nt + 2 * tq] = acc[nt][2];
-                        xs[(gq + 8) * 20 + 8 * nt + 2 * tq + 1] = acc[nt][3];
+                        const float* br = Bm + (kk + tq) * BLD + 8 * nt + gq;
+                        mma_tf32(acc[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * BLD]));
                     }
-                    __syncwarp();
-                    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                    for (int kk = 0; kk < 16; kk += 8) {
-                        const float* ar = tblk(tri(I, I)) + gq * BLD + kk + tq;
-                        const uint32_t a0 = f2tf32(ar[0]), a1 = f2tf32(ar[8 * BLD]),
-                                       a2 = f2tf32(ar[4]), a3 = f2tf32(ar[8 * BLD + 4]);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            const float* br = xs + (kk + tq) * 20 + 8 * nt + gq;
-                            mma_tf32(acc2[nt], a0, a1, a2, a3, f2tf32(br[0]), f2tf32(br[4 * 20]));
-                        }
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        float* tr = tblk(tri(I, J)) + gq * BLD + 8 * nt + 2 * tq;
-                        tr[0] = -acc2[nt][0];
-                        tr[1] = -acc2[nt][1];
-                        tr[8 * BLD] = -acc2[nt][2];
-                        tr[8 * BLD + 1] = -acc2[nt][3];
-                    }
-                    __syncwarp();
                 }
-                __syncthreads();
+            };
+            auto put = [&](float* D, const float (&acc)[2][4], float sg) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    float* tr = D + gq * BLD + 8 * nt + 2 * tq;
+                    tr[0] = sg * acc[nt][0];
+                    tr[1] = sg * acc[nt][1];
+                    tr[8 * BLD] = sg * acc[nt][2];
+                    tr[8 * BLD + 1] = sg * acc[nt][3];
+                }
+            };
+            auto slot = [&](int q) { return sTmp + q * (16 * BLD); };
+            float acc[2][4];
+            auto zero = [&]() {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            };
+            // round 1: T10 = -T11 (A10 T00), T32 = -T33 (A32 T22); Y21 = A21 T11, Y31 = A31 T11
+            zero();
+            if (w == 0 || w == 1) {
+                const int lo = 2 * w;  // 0 or 2
+                mm(acc, ablk(tri(lo + 1, lo)), tblk(tri(lo, lo)));
+                put(slot(w), acc, 1.f);
+                __syncwarp();
+                zero();
+                mm(acc, tblk(tri(lo + 1, lo + 1)), slot(w));
+                put(tblk(tri(lo + 1, lo)), acc, -1.f);
+            } else {
+                mm(acc, ablk(tri(w, 1)), tblk(tri(1, 1)));
+                put(slot(w), acc, 1.f);
             }
+            __syncthreads();
+            // round 2: Y20 = A20 T00 + A21 T10 (S0), Y30 = A30 T00 + A31 T10 (S1);
+            // T21 = -T22 Y21, T31 = -(T32 Y21 + T33 Y31)
+            zero();
+            if (w == 0 || w == 1) {
+                mm(acc, ablk(tri(w + 2, 0)), tblk(tri(0, 0)));
+                mm(acc, ablk(tri(w + 2, 1)), tblk(tri(1, 0)));
+                __syncwarp();
+                put(slot(w), acc, 1.f);
+            } else if (w == 2) {
+                mm(acc, tblk(tri(2, 2)), slot(2));
+                put(tblk(tri(2, 1)), acc, -1.f);
+            } else {
+                mm(acc, tblk(tri(3, 2)), slot(2));
+                mm(acc, tblk(tri(3, 3)), slot(3));
+                put(tblk(tri(3, 1)), acc, -1.f);
+            }
+            __syncthreads();
+            // round 3: T20 = -T22 Y20, T30 = -(T32 Y20 + T33 Y30)
+            if (w == 0) {
+                zero();
+                mm(acc, tblk(tri(2, 2)), slot(0));
+                put(tblk(tri(2, 0)), acc, -1.f);
+            } else if (w == 1) {
+                zero();
+                mm(acc, tblk(tri(3, 2)), slot(0));
+                mm(acc, tblk(tri(3, 3)), slot(1));
+                put(tblk(tri(3, 0)), acc, -1.f);
+            }
+            __syncthreads();
         }
         PTRACE(3);
         // TU = T diag(beta) and TW = -T diag(beta e) as swizzled bf16 tiles over the dead A

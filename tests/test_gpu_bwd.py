@@ -44,7 +44,7 @@ def test_small_training_step(dtype, tol):
 @pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
 @pytest.mark.parametrize("B,T,Hqk,Hv,h0", [
     (1, 1, 1, 1, True), (1, 63, 1, 3, False), (2, 64, 2, 2, True), (1, 65, 1, 2, True),
-    (3, 200, 1, 3, True), (1, 129, 2, 2, False),
+    (3, 200, 1, 3, True), (1, 129, 2, 2, False), (1, 200, 1, 10, True),
 ])
 def test_odd_shapes(dtype, tol, B, T, Hqk, Hv, h0):
     inp = make_inputs(B, T, Hqk, Hv, seed=T * 3 + Hv, dtype=dtype, h0_std=0.1 if h0 else 0.0,

@@ -40,6 +40,7 @@ def test_small_workload(dtype, tol):
 @pytest.mark.parametrize("B,T,Hqk,Hv,h0", [
     (1, 1, 1, 1, True), (1, 63, 1, 3, False), (2, 64, 2, 2, True), (1, 65, 1, 2, True),
     (3, 200, 1, 4, True), (1, 129, 3, 6, False),
+    (1, 300, 1, 12, True),  # a q/k group of 12 v-heads: the preparation splits it in two slices
 ])
 def test_odd_shapes(dtype, tol, B, T, Hqk, Hv, h0):
     inp = make_inputs(B, T, Hqk, Hv, seed=T * 7 + Hv, dtype=dtype, h0_std=0.1 if h0 else 0.0)
