@@ -489,8 +489,8 @@ __device__ __forceinline__ float col_sum8(float v) {
     return v;
 }
 
-template <typename Op, int C>
-__global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
+template <typename Op, int C, int NTL>
+__global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
     using S = LocSmem<Op, C>;
     constexpr int LDK = S::LDK, LDC = S::LDC, LDF = S::LDF;
     extern __shared__ __align__(128) char smem[];
@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     const Op* sDH = S::BF ? reinterpret_cast<const Op*>(smem + S::oDH) : dhsrc;
     constexpr int LDS = S::BF ? LDK : VD;
 
-    constexpr int RB = C / 16, WPR = 8 / RB, COLS = 128 / WPR, NTC = COLS / 8;
+    constexpr int RB = C / 16, WPR = (NTL / 32) / RB, COLS = 128 / WPR, NTC = COLS / 8;
     constexpr int CCOLS = C / WPR, NTS = CCOLS / 8;
     static_assert(NTS >= 1 && WPR <= 4 && RB <= 4, "warp tiling");
     const int m0 = 16 * (w % RB), n0 = COLS * (w / RB), s0 = CCOLS * (w / RB);
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         const Op* kg = reinterpret_cast<const Op*>(P.k) + qh * KD + tc * qk_stride;
         const Op* qg = reinterpret_cast<const Op*>(P.q) + qh * KD + tc * qk_stride;
         const Op* vg = reinterpret_cast<const Op*>(P.v) + j * VD + tc * v_stride;
-        for (int idx = tid; idx < C * 16; idx += NT) {
+        for (int idx = tid; idx < C * 16; idx += NTL) {
             const int r = idx >> 4, cv = idx & 15;
             const bool ok = r < c;
             const int rr = ok ? r : 0;
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
             cp_async16(tV + r * LDK + cv * 8, vg + rr * v_stride + cv * 8, ok);
         }
         const unsigned char* rec = static_cast<const unsigned char*>(P.prep) + (int64_t(gch) * Hv + j) * P.prep_stride;
-        for (int q = tid; q < 1024 + 3 * 512; q += NT) {
+        for (int q = tid; q < 1024 + 3 * 512; q += NTL) {
             if (q < 1024) {
                 const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
                 cp_async16(tW + r * LDK + blk * 64 + cc * 8, rec + PREP_W + q * 16, true);
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
                 cp_async16(dst + r * LDC + cc * 8, rec + off + q2 * 16, true);
             }
         }
-        for (int idx = tid; idx < KD * 16; idx += NT) {
+        for (int idx = tid; idx < KD * 16; idx += NTL) {
             const int r = idx >> 4, cv = idx & 15;
             cp_async16(const_cast<Op*>(sH) + r * LDK + cv * 8, hsrc + r * VD + cv * 8, true);
             cp_async16(const_cast<Op*>(sDH) + r * LDK + cv * 8, dhsrc + r * VD + cv * 8, true);
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         load_rows<Op, C>(tQ, LDK, reinterpret_cast<const Op*>(P.q) + qh * KD + tc * qk_stride, qk_stride, c);
         load_rows<Op, C>(tV, LDK, reinterpret_cast<const Op*>(P.v) + j * VD + tc * v_stride, v_stride, c);
     }
-    for (int i = tid; i < C; i += NT) {
+    for (int i = tid; i < C; i += NTL) {
         const bool ok = i < c;
         sGam[i] = ok ? P.g[(tc + i) * Hv + j] : 0.f;
         sBeta[i] = ok ? P.beta[(tc + i) * Hv + j] : 0.f;
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
             }
         }
         __syncthreads();
-        for (int idx = tid; idx < C * C; idx += NT) {
+        for (int idx = tid; idx < C * C; idx += NTL) {
             const int i = idx / C, jj = idx % C;
             fDB[i * LDF + jj] = (i > jj) ? expf(sGam[i] - sGam[jj]) * fDB[i * LDF + jj] : 0.f;  // Dm * Bm
         }
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         }
     }
     __syncthreads();
-    for (int idx = tid; idx < C * C; idx += NT) {
+    for (int idx = tid; idx < C * C; idx += NTL) {
         const int i = idx / C, jj = idx % C;
         const float d = expf(sGam[i] - sGam[jj]);
         const float db = (i > jj) ? d * fDB[i * LDF + jj] : 0.f;
@@ -667,7 +667,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     }
     __syncthreads();
     tri_inverse<C, LDF>(fA, fT, sTmp);
-    for (int idx = tid; idx < C * C; idx += NT) {
+    for (int idx = tid; idx < C * C; idx += NTL) {
         const int i = idx / C, jj = idx % C;
         const float t = (jj <= i) ? fT[i * LDF + jj] : 0.f;
         oT[i * LDC + jj] = from_f<Op>(t);
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
     // ---- phase 3: dO, dh; dV' = scale P^T dO + diag(kd) K dh
     if (S::BF) {  // dh arrived with the first copies; dO lands while K dh is formed
         const Op* dg = reinterpret_cast<const Op*>(B.dO) + j * VD + tc * v_stride;
-        for (int idx = tid; idx < C * 16; idx += NT) {
+        for (int idx = tid; idx < C * 16; idx += NTL) {
             const int r = idx >> 4, cv = idx & 15;
             const bool ok = r < c;
             cp_async16(tDO + r * LDK + cv * 8, dg + (ok ? r : 0) * v_stride + cv * 8, ok);
@@ -780,7 +780,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < C; i += NT) {  // fold the dP * P row/column sums into dgamma
+    for (int i = tid; i < C; i += NTL) {  // fold the dP * P row/column sums into dgamma
         float v = 0.f;
         for (int q = 0; q < WPR; ++q) v += rowp[q * C + i];
         for (int q = 0; q < RB; ++q) v -= colp[q * C + i];
@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         }
         // <dh, h>
         float hd = 0.f;
-        for (int idx = tid; idx < KD * VD; idx += NT) {
+        for (int idx = tid; idx < KD * VD; idx += NTL) {
             const int r = idx / VD, v = idx % VD;
             hd += to_f(sDH[r * LDS + v]) * to_f(sH[r * LDS + v]);
         }
@@ -837,14 +837,14 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         if (lane == 0) sRed[w] = hd;
     }
     __syncthreads();
-    for (int i = tid; i < C; i += NT) {
+    for (int i = tid; i < C; i += NTL) {
         float v = 0.f;
         for (int q = 0; q < WPR; ++q) v += rowp[q * C + i];
         sDg[i] += sc * sE[i] * v;
     }
     if (tid == 0) {
         float hd = 0.f;
-        for (int q = 0; q < NT / 32; ++q) hd += sRed[q];
+        for (int q = 0; q < NTL / 32; ++q) hd += sRed[q];
         sRed[8] = hd;
     }
     __syncthreads();
@@ -963,7 +963,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < C; i += NT) {
+    for (int i = tid; i < C; i += NTL) {
         float tw = 0.f, tu = 0.f;
         for (int q = 0; q < WPR; ++q) {
             tw += rowp[q * C + i];
@@ -1033,7 +1033,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < C; i += NT) {
+    for (int i = tid; i < C; i += NTL) {
         float ra = 0.f, ca = 0.f, rb = 0.f;
         for (int q = 0; q < WPR; ++q) {
             ra += rowp[q * C + i];
@@ -1044,7 +1044,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_local(BwdProblem B) {
         sDb[i] += rb;
     }
     // (dB + dB^T) as an MMA operand
-    for (int idx = tid; idx < C * C; idx += NT) {
+    for (int idx = tid; idx < C * C; idx += NTL) {
         const int i = idx / C, jj = idx % C;
         oX2[i * LDC + jj] = from_f<Op>(fT[i * LDF + jj] + fT[jj * LDF + i]);
     }
@@ -1132,7 +1132,8 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_bwd_phase_c<Op, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SS::bytes));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_bwd_local<Op, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(LS::bytes));
+    constexpr int NTL = NT;
+    e = cudaFuncSetAttribute(k_bwd_local<Op, C, NTL>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(LS::bytes));
     if (e != cudaSuccess) return e;
     const int fix_smem = (KD * 129 + KD * 8) * 4;
     e = cudaFuncSetAttribute(k_bwd_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, fix_smem);
@@ -1165,7 +1166,7 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
     timing_end(st);
     if (P.total_chunks > 0) {
         timing_begin("bwd_local", st);
-        k_bwd_local<Op, C><<<dim3(P.total_chunks, P.Hv), NT, LS::bytes, st>>>(B);
+        k_bwd_local<Op, C, NTL><<<dim3(P.total_chunks, P.Hv), NTL, LS::bytes, st>>>(B);
         timing_end(st);
     }
     if (B.dqp) {
