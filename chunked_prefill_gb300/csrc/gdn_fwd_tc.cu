@@ -84,7 +84,8 @@ static_assert(sizeof(Gate) <= GATE_BYTES && sizeof(Gate) % 16 == 0, "gate buffer
 
 enum Bar { B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GFREE0,
            B_GFREE1, B_GFREE2, B_GFREE3, B_MMA3, B_MMA5, B_MMA4_0, B_MMA4_1, B_DRAIN, B_EX, B_EV0,
-           B_EV1, B_EPI0, B_EPI1, B_FULLP0, B_EMPTYP0 = B_FULLP0 + NP, B_COUNT = B_EMPTYP0 + NP };
+           B_EV1, B_EPI0, B_EPI1, B_M5C0, B_M5C1, B_FULLP0, B_EMPTYP0 = B_FULLP0 + NP,
+           B_COUNT = B_EMPTYP0 + NP };
 
 static_assert(B_COUNT * 8 + 8 <= 512, "barrier area");
 
@@ -234,6 +235,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         mbar_init(&bars[B_EV1], 8);
         mbar_init(&bars[B_EPI0], 4);
         mbar_init(&bars[B_EPI1], 4);
+        mbar_init(&bars[B_M5C0], 1);  // per chunk parity: the state update has completed
+        mbar_init(&bars[B_M5C1], 1);
         *errflag = 0;
         mbar_fence_init();
     }
@@ -354,6 +357,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                     mma_bf16_ta(tm + T_XF, dd + (OUT ? kd_col(s) : p_col(s)), (st ? dK[1] : dK[0]) + (s * 2048 >> 4),
                                 ID5, 1u);
                 commit(&bars[B_MMA5]);
+                if (OUT) commit(&bars[B_M5C0 + (k & 1)]);
                 commit(&bars[B_EMPTY0 + st]);  // last reader of this stage on this issuer
                 TRACE(k, 5);
                 if (NEEDU && k + 1 < n) {
@@ -439,7 +443,9 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 if (!wait_bar(bars, B_FULLP0 + b, (k / NP) & 1, errflag)) break;
                 used = k + 1;
                 if (k >= 1 && !wait_bar(bars, B_EPI0 + ((k - 1) & 1), ((k - 1) >> 1) & 1, errflag)) break;
-                if (!wait_bar(bars, B_EV0 + (k & 1), (k >> 1) & 1, errflag)) break;
+                // after the state update of chunk k (so P V' never queues ahead of it); V' of
+                // chunk k is converted by then as well
+                if (!wait_bar(bars, B_M5C0 + (k & 1), (k >> 1) & 1, errflag)) break;
                 TRACE(k, 10);
                 fence_after_sync();
                 const uint32_t dd = tm + t_dd(k);
