@@ -92,7 +92,11 @@ static_assert(B_COUNT * 8 + 8 <= 512, "barrier area");
 enum TcKind { TK_STATE = 0, TK_TRANS = 1, TK_OUT = 2, TK_HIST = 3 };
 
 #ifdef GDN_TRACE
-// debug builds only: SM-clock timestamps of the pipeline events of CTA (0, 0)
+#ifndef GDN_TRACE_X
+#define GDN_TRACE_X 0
+#define GDN_TRACE_Y 0
+#endif
+// debug builds only: SM-clock timestamps of the pipeline events of one CTA
 __device__ unsigned long long g_trace[64][32];
 __device__ unsigned long long g_cta_trace[2][512][4];  // [phase A, C][cta]: globaltimer at entry, scan start, scan end, exit
 #define CTRACE(ph, e)                                                                          \
@@ -105,7 +109,7 @@ __device__ unsigned long long g_cta_trace[2][512][4];  // [phase A, C][cta]: glo
     } while (0)
 #define TRACE(k, ev)                                                                           \
     do {                                                                                       \
-        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (k) >= 0 && (k) < 64)     \
+        if (blockIdx.x == GDN_TRACE_X && blockIdx.y == GDN_TRACE_Y && blockIdx.z == 0 && (k) >= 0 && (k) < 64) \
             g_trace[(k)][(ev)] = clock64();                                                    \
     } while (0)
 #else
@@ -126,7 +130,7 @@ __device__ __forceinline__ uint64_t mdesc(uint32_t addr, uint32_t lbo) {  // MN-
 
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bars, int b, uint32_t parity, int* errflag) {
-    if (mbar_wait(&bars[b], parity)) return true;
+    if (mbar_wait_spin(&bars[b], parity)) return true;
     atomicOr(errflag, 1 << b);
     return false;
 }

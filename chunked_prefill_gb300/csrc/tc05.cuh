@@ -233,6 +233,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
+// The same bounded wait polling without suspension (for the waits on the serial chain, where
+// the wake-up latency of a suspended thread is on the critical path).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t phase,
+                                               uint64_t limit_ns = 2000000000ull) {
+    if (mbar_test(bar, phase)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_test(bar, phase)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
 // bounded wait by lane 0, result broadcast to the warp
 __device__ __forceinline__ bool warp_uniform_wait(uint64_t* bar, uint32_t phase) {
     bool ok = true;
