@@ -303,6 +303,11 @@ def oracle_sample_fixed(inp, n, backward):
     return new_cu[-1] / dt, new_cu[-1], dt, orc.max_threads(), n
 
 
+# DRAM bytes (read + write) of one launch, from the ncu capture summarised in profiles/
+# (fwd_prep_t32k_hqk2_hv8.md); None where no capture of the current kernel exists.
+NCU_TRAFFIC = {("fwd_t32k_hqk2_hv8", "fwd_prep"): 36.814848e6 + 73.433344e6}
+
+
 def kernel_bytes(name, tokens, lens, w):
     """Algorithmic HBM bytes of one launch of a kernel: the tensors its step of the method
     must read or write once (bf16 activations, fp32 gates and states; for the chunk-local
@@ -411,7 +416,8 @@ def main():
     alg, unit_note = kernel_bytes(dom_name, tokens, lens, w)
     achieved = alg / dom_avg_s / 1e9
     roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+            "traffic": NCU_TRAFFIC.get((args.workload, dom_name)),
             "peak_kind": pk_kind, "algorithmic_bytes_per_launch": alg, "bytes_counted": unit_note,
             "avg_launch_ms": dom_avg_s * 1000.0,
             "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items()}}
