@@ -344,6 +344,39 @@ def config_of(name):
     return c
 
 
+def sweep(args, local):
+    """Forward tokens/s and roofline fraction over the head / length sweep (inputs.SWEEP)."""
+    from chunked_prefill_gb300 import build, gdn
+    from chunked_prefill_gb300.inputs import SWEEP
+    build.build()
+    dev = torch.device("cuda", local)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    pk, pk_kind = peaks()
+    for name, w in SWEEP.items():
+        inp = workload_inputs(name)
+        lens = lengths_of(inp)
+        tokens = sum(lens)
+        step = make_step(inp, dev, False)[0]
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        ms = time_steps(step, args.steps, flush) / args.steps
+        gdn.gdn_timing_enable(True)
+        time_steps(step, args.steps, flush)
+        gdn.gdn_timing_enable(False)
+        kt = gdn.gdn_timing_collect()
+        fl = rl.fwd_flops(lens, w.Hqk, w.Hv)
+        by = rl.fwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
+        t_roof = max(fl / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+        print(json.dumps({
+            "sweep": True, "workload": name, "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv,
+            "ms_per_step": ms, "tokens_per_s": tokens / (ms / 1000.0),
+            "roofline_ms": t_roof * 1000.0, "frac": t_roof * 1000.0 / ms, "peak_kind": pk_kind,
+            "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items()}}), flush=True)
+        del inp, step
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -356,9 +389,15 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="for ncu: warm-up and timed steps only (no clock sampling, e2e or "
                          "CPU baseline)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="head / length sweep of the forward: one JSON line per point "
+                         "(an auxiliary report, not the benchmark line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args.gpus)
+    if args.sweep:
+        sweep(args, local)
+        return
 
     if args.impl == "reference":
         reference_arm(args, world, rank)

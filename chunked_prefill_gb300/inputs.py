@@ -48,6 +48,27 @@ WORKLOADS = {
 }
 
 
+# Head / length sweep (the pages benchmark the head settings h_v in {64, 48, 32, 24, 16, 8}
+# across tensor-parallel degrees 1-8 and several lengths; FlashQLA pages, "performance
+# benchmark" paragraph).  Reading: two model families with 16 q/k heads and 64 or 48 v-heads
+# split over TP = 1, 2, 4, 8, keeping the splits whose v-head count is in that set; lengths
+# 1 x 8192, 4 x 8192 and 1 x 32768 tokens.
+def _sweep() -> dict:
+    pts = []
+    for hqk_all, hv_all in ((16, 64), (16, 48)):
+        for tp in (1, 2, 4, 8):
+            hqk, hv = hqk_all // tp, hv_all // tp
+            if hv not in (64, 48, 32, 24, 16, 8):
+                continue
+            for B, T in ((1, 8192), (4, 8192), (1, 32768)):
+                pts.append(Workload(f"sweep_b{B}_t{T // 1024}k_hqk{hqk}_hv{hv}", T=T, Hqk=hqk, Hv=hv, B=B,
+                                    seed=2000 + len(pts)))
+    return {w.name: w for w in pts}
+
+
+SWEEP = _sweep()
+
+
 def varlen_lengths(gen: torch.Generator, n: int, total: int, lo: int, hi: int) -> list[int]:
     """n lengths drawn uniformly from [lo, hi], rescaled to sum to exactly ``total`` by the
     largest-remainder method (ties go to the lower index).  Lengths may leave [lo, hi]."""
@@ -127,7 +148,7 @@ def make_inputs(B: int, T: int, Hqk: int, Hv: int, K: int = 128, V: int = 128, *
 
 
 def workload_inputs(name: str, dtype: torch.dtype = torch.bfloat16) -> Inputs:
-    w = WORKLOADS[name]
+    w = WORKLOADS[name] if name in WORKLOADS else SWEEP[name]
     return make_inputs(w.B, w.T, w.Hqk, w.Hv, w.K, w.V, seed=w.seed, dtype=dtype,
                        h0_std=w.h0_std, backward=w.backward, varlen_seqs=w.varlen_seqs,
                        varlen_range=w.varlen_range)
