@@ -13,6 +13,15 @@
 #include "../../include/gdn.h"
 #include "gdn_internal.h"
 
+namespace gdn {
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return n > 0 ? n : 148;
+}
+}  // namespace gdn
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -29,12 +38,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-    return n > 0 ? n : 148;
-}
+using gdn::sm_count;
 
 // Host plan of one call.
 struct HostPlan {
@@ -97,9 +101,9 @@ gdn_status validate_problem(const gdn_problem* p) {
 // of the output stage: the waves of the two chunk-scan launches (one CTA per SM; the first
 // phase runs a segment's state and transition in one CTA) times the chunks a CTA scans, plus
 // the serial fix-up steps.  The step costs are measured ratios on GB300 (a first-phase chunk
-// step ~1.0 of an output chunk step, a fix-up step ~0.52).
+// step ~1.0 of an output chunk step; a fix-up step as below).
 double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int warmup) {
-    constexpr double tC = 1.0, tA = 1.0, tF = 0.52;
+    constexpr double tC = 1.0, tA = 1.0;
     long segs = 0, actas = 0;
     int maxn = 0;
     for (int s = 0; s < N; ++s) {
@@ -114,7 +118,14 @@ double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int wa
     double cost = double(cw) * Lc * tC;
     if (maxn > 1) {
         cost += double(aw) * (exact ? Lc : std::min(warmup, Lc)) * tA;
-        if (exact) cost += std::max(0, maxn - 2) * tF;
+        if (exact) {
+            // fix-up step: ~0.43 us fixed + ~0.53 us per column group of its CTAs, against
+            // ~1.84 us per chunk step; more chains than one wave holds repeat it
+            const int cg = gdn::fixup_groups(N * Hv);
+            const long fw = (long(N) * Hv * (128 / (8 * cg)) + sms - 1) / sms;
+            const double tF = (0.43 + 0.53 * cg) / 1.84;
+            cost += double(fw) * std::max(0, maxn - 2) * tF;
+        }
     }
     return cost;
 }

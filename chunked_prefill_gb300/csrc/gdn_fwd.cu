@@ -462,34 +462,43 @@ __device__ unsigned long long g_fix_trace[64][4];  // debug builds: SM clock per
     } while (0)
 #endif
 constexpr int FIX_NB = 2, FIX_T = 256;
-constexpr int FIX_SMEM = FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * 8 * 4 + 64;
+// Shared memory of a fix-up CTA with CG groups of 8 state columns: FIX_NB transition tiles, the
+// k-slice partial blocks (8 warps x 32 lanes x 32 floats whatever CG is) and the CTA's
+// columns of x.
+constexpr int fix_smem(int CG) { return FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * 8 * CG * 4 + 64; }
 // REV = false: the forward, hin[g0+lj+1] = M_lj hin[g0+lj] + S_lj for lj = 1..nseg-2, reading
 // M^T (the transposed store).  REV = true: the backward, dhb[g0+lj] = M_lj^T dhb[g0+lj+1] +
 // dhb[g0+lj] for lj = nseg-2..1, reading M (the untransposed store).  In both the shared
 // tile holds A^T for the step's matrix A, and xbuf[g] is read as S and overwritten in place.
-template <bool REV>
+// A CTA owns W = 8 CG columns of one (sequence, v-head) chain.  Its 8 warps split the
+// contraction into KS = 8 / CG slices; a thread accumulates a 4-row x 8-column block of one
+// column group over its slice, and the slices are summed through shared memory.  Few chains
+// take CG = 1 (short steps, many CTAs per chain); many chains take a wider CG so that all
+// chains run in one wave and each transition tile is read by fewer CTAs.
+template <bool REV, int CG>
 __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float* mats, float* xbuf,
                                                  int Hv, int* err) {
+    constexpr int W = 8 * CG, KS = 8 / CG, MS = KD / KS;
     tc::pdl_launch_dependents();
     tc::pdl_wait();
     extern __shared__ __align__(128) unsigned char fsm[];
     float* Ms = reinterpret_cast<float*>(fsm);                                // FIX_NB x 128 x 128
     float* red = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4);        // 8 x 32 x 32
-    float* xs = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4);  // 128 x 8
-    uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * 8 * 4);
-    const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * 8;
+    float* xs = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4);  // 128 x W
+    uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * W * 4);
+    const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * W;
     const int g0 = seg_off[s], nseg = seg_off[s + 1] - g0;
     if (nseg <= 2) return;
     const int last = nseg - 2;  // steps 1..last
-    const int t = threadIdx.x, rg = t & 31, ks = t >> 5;
-    const int orow = t >> 1, oc = (t & 1) * 4;  // the 4 outputs this thread finishes
+    const int t = threadIdx.x, rg = t & 31, ks = (t >> 5) / CG, cg = (t >> 5) % CG;
+    const int orow = t >> 1, oc = (t & 1) * 4;  // each thread finishes 4 columns of orow per group
     auto seg_of = [&](int q) { return REV ? nseg - 2 - q : 1 + q; };  // step q -> segment lj
     auto mt = [&](int q) { return mats + (int64_t(g0 + seg_of(q)) * Hv + j) * KV; };
     // x entering step q, and the S / result slot of step q
     auto xin = [&](int q) { return REV ? g0 + seg_of(q) + 1 : g0 + seg_of(q); };
     auto xout = [&](int q) { return REV ? g0 + seg_of(q) : g0 + seg_of(q) + 1; };
-    auto hp = [&](int g) {
-        return reinterpret_cast<float4*>(xbuf + (int64_t(g) * Hv + j) * KV + orow * VD + cb + oc);
+    auto hp = [&](int g, int c) {
+        return reinterpret_cast<float4*>(xbuf + (int64_t(g) * Hv + j) * KV + orow * VD + cb + 8 * c + oc);
     };
     if (t == 0) {
         for (int b = 0; b < FIX_NB; ++b) tc::mbar_init(&bar[b], 1);
@@ -500,8 +509,12 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
         tc::mbar_expect_tx(&bar[0], KD * KD * 4);
         tc::bulk_load(Ms, mt(0), KD * KD * 4, &bar[0]);
     }
-    *reinterpret_cast<float4*>(&xs[orow * 8 + oc]) = *hp(xin(0));
-    float4 snext = *hp(xout(0));
+    float4 snext[CG];
+#pragma unroll
+    for (int c = 0; c < CG; ++c) {
+        *reinterpret_cast<float4*>(&xs[orow * W + 8 * c + oc]) = *hp(xin(0), c);
+        snext[c] = *hp(xout(0), c);
+    }
     bool ok = true;
     for (int q = 0; q < last; ++q) {
         const int b = q & 1;
@@ -514,8 +527,12 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
         FTRACE(q + 1, 1);
         __syncthreads();  // also orders the previous step's xs update
         FTRACE(q + 1, 2);
-        const float4 sj = snext;
-        if (q + 1 < last) snext = *hp(xout(q + 1));
+        float4 sj[CG];
+#pragma unroll
+        for (int c = 0; c < CG; ++c) {
+            sj[c] = snext[c];
+            if (q + 1 < last) snext[c] = *hp(xout(q + 1), c);
+        }
         const float* M = Ms + b * KD * KD;
         float acc[4][8];
 #pragma unroll
@@ -523,10 +540,10 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
 #pragma unroll
             for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
 #pragma unroll 4
-        for (int m = 16 * ks; m < 16 * ks + 16; ++m) {
+        for (int m = MS * ks; m < MS * ks + MS; ++m) {
             const float4 a = *reinterpret_cast<const float4*>(M + m * KD + 4 * rg);
-            const float4 x0 = *reinterpret_cast<const float4*>(&xs[m * 8]);
-            const float4 x1 = *reinterpret_cast<const float4*>(&xs[m * 8 + 4]);
+            const float4 x0 = *reinterpret_cast<const float4*>(&xs[m * W + 8 * cg]);
+            const float4 x1 = *reinterpret_cast<const float4*>(&xs[m * W + 8 * cg + 4]);
             const float av[4] = {a.x, a.y, a.z, a.w};
             const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
@@ -534,8 +551,9 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
 #pragma unroll
                 for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], xv[c], acc[r][c]);
         }
-        // partial block -> red[ks][rg][32], 16-byte pieces rotated by rg against bank conflicts
-        float* rp = red + (ks * 32 + rg) * 32;
+        // partial block -> red[ks][rg][cg][32], 16-byte pieces rotated by rg against bank
+        // conflicts
+        float* rp = red + ((ks * 32 + rg) * CG + cg) * 32;
 #pragma unroll
         for (int pq = 0; pq < 8; ++pq) {
             const int r = pq >> 1, c = (pq & 1) * 4;
@@ -546,20 +564,51 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
         __syncthreads();  // partial blocks visible; everyone is done with xs and buffer b
         {
             const int org = orow >> 2, pq = ((orow & 3) << 1) | (oc >> 2);
-            float4 o = sj;
 #pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2) {
-                const float4 p = *reinterpret_cast<const float4*>(red + (k2 * 32 + org) * 32 + ((pq ^ (org & 7)) << 2));
-                o.x += p.x;
-                o.y += p.y;
-                o.z += p.z;
-                o.w += p.w;
+            for (int c = 0; c < CG; ++c) {
+                float4 o = sj[c];
+#pragma unroll
+                for (int k2 = 0; k2 < KS; ++k2) {
+                    const float4 p = *reinterpret_cast<const float4*>(
+                        red + ((k2 * 32 + org) * CG + c) * 32 + ((pq ^ (org & 7)) << 2));
+                    o.x += p.x;
+                    o.y += p.y;
+                    o.z += p.z;
+                    o.w += p.w;
+                }
+                *reinterpret_cast<float4*>(&xs[orow * W + 8 * c + oc]) = o;
+                *hp(xout(q), c) = o;
             }
-            *reinterpret_cast<float4*>(&xs[orow * 8 + oc]) = o;
-            *hp(xout(q)) = o;
         }
     }
     if (!ok && t == 0 && err) atomicOr(err, 1 << 30);
+}
+
+// Column groups per fix-up CTA: the narrowest that puts every chain of the launch in one wave
+// at one CTA per SM (the shared memory allows no more).
+int fixup_groups(int chains) {
+    const int sms = sm_count();
+    for (int cg = 1; cg < 8; cg *= 2)
+        if (int64_t(chains) * (VD / (8 * cg)) <= sms) return cg;
+    return 8;
+}
+
+template <bool REV>
+static void launch_fixup_cg(int N, int Hv, const int* seg_off, const float* mats, float* xbuf,
+                            int* err, bool pdl, cudaStream_t st) {
+    auto run = [&](auto kern, int cg) {
+        const int smem = fix_smem(cg);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        const dim3 grid(N, Hv, VD / (8 * cg));
+        if (pdl) launch_pdl(kern, grid, dim3(FIX_T), smem, st, seg_off, mats, xbuf, Hv, err);
+        else kern<<<grid, FIX_T, smem, st>>>(seg_off, mats, xbuf, Hv, err);
+    };
+    switch (fixup_groups(N * Hv)) {
+        case 1: run(k_fixup<REV, 1>, 1); break;
+        case 2: run(k_fixup<REV, 2>, 2); break;
+        case 4: run(k_fixup<REV, 4>, 4); break;
+        default: run(k_fixup<REV, 8>, 8); break;
+    }
 }
 
 // Work decomposition on the device from the device cu_seqlens (same rule as the host).
@@ -594,16 +643,13 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
-    cudaFuncSetAttribute(k_fixup<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
-    launch_pdl(k_fixup<false>, dim3(P.N, P.Hv, VD / 8), dim3(FIX_T), FIX_SMEM, st,
-               static_cast<const int*>(P.plan.seg_off), static_cast<const float*>(P.mbuf), P.hin, P.Hv, P.err);
+    launch_fixup_cg<false>(P.N, P.Hv, P.plan.seg_off, P.mbuf, P.hin, P.err, true, st);
     timing_end(st);
 }
 
 void launch_bwd_fixup_tc(const BwdProblem& B, cudaStream_t st) {
     const Problem& P = B.f;
-    cudaFuncSetAttribute(k_fixup<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
-    k_fixup<true><<<dim3(P.N, P.Hv, VD / 8), FIX_T, FIX_SMEM, st>>>(P.plan.seg_off, P.mbuf_t, B.dhb, P.Hv, P.err);
+    launch_fixup_cg<true>(P.N, P.Hv, P.plan.seg_off, P.mbuf_t, B.dhb, P.err, false, st);
 }
 
 template <typename Op, int C>

@@ -20,6 +20,10 @@ cudaError_t launch_fwd(const Problem& P, int dtype, bool hist, cudaStream_t st);
 // The plan kernel (work decomposition from the device cu_seqlens) and the serial fix-up of
 // the exact context-parallel mode, shared by the CUDA-core and tensor-core paths.
 void launch_plan(const Problem& P, int C, cudaStream_t st);
+// Multiprocessors of the current device.
+int sm_count();
+// Groups of 8 state columns per fix-up CTA for a launch over this many (sequence, head) chains.
+int fixup_groups(int chains);
 void launch_fixup(const Problem& P, cudaStream_t st);
 // The backward's reverse fix-up (bf16 path: reads the untransposed transitions P.mbuf_t).
 void launch_bwd_fixup_tc(const BwdProblem& B, cudaStream_t st);

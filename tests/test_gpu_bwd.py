@@ -116,3 +116,10 @@ def test_full_size_training_step_sampled_heads():
     for name, a, r in zip(NAMES, got, ref):
         a = np.take(a, heads, axis=idx[name])
         assert rel_err(a, r) <= BF16_TOL, name
+
+
+@pytest.mark.parametrize("Hqk,Hv", [(2, 12), (4, 24), (4, 48)])
+def test_context_parallel_many_heads(Hqk, Hv):
+    """Enough (sequence, v-head) chains that the fix-up runs 2, 4 or 8 column groups per CTA."""
+    inp = make_inputs(1, 64 * 12 + 5, Hqk, Hv, seed=46 + Hv, h0_std=0.1, backward=True)
+    check(inp, BF16_TOL, cp_mode=2, cp_segment_chunks=2)

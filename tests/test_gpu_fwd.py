@@ -65,6 +65,14 @@ def test_context_parallel_exact(dtype, tol, seg):
     check(inp, tol, cp_mode=2, cp_segment_chunks=seg)
 
 
+@pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
+@pytest.mark.parametrize("Hqk,Hv", [(2, 12), (4, 24), (4, 48)])
+def test_context_parallel_many_heads(dtype, tol, Hqk, Hv):
+    """Enough (sequence, v-head) chains that the fix-up runs 2, 4 or 8 column groups per CTA."""
+    inp = make_inputs(1, 64 * 12 + 5, Hqk, Hv, seed=12 + Hv, dtype=dtype, h0_std=0.1)
+    check(inp, tol, cp_mode=2, cp_segment_chunks=2)
+
+
 def test_warmup_mode_matches_its_own_definition_fp32():
     """The opt-in warm-up mode is not exact; in the fp32 test mode it must equal the fp64
     chunk-form warm-up (same chunk size, segment length and window) to 1e-4."""

@@ -21,7 +21,7 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("name", ["sweep_b4_t8k_hqk16_hv64", "sweep_b1_t32k_hqk8_hv24",
+@pytest.mark.parametrize("name", ["sweep_b4_t8k_hqk16_hv64", "sweep_b1_t8k_hqk16_hv64", "sweep_b1_t32k_hqk8_hv24",
                                   "sweep_b1_t8k_hqk2_hv8"])
 def test_sweep_point_sampled_groups(name):
     inp = workload_inputs(name)
