@@ -130,7 +130,7 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def make_step(inp, dev, backward):
+def make_step(inp, dev, backward, save_states=False):
     from chunked_prefill_gb300 import gdn
     d = {n: (None if getattr(inp, n) is None else getattr(inp, n).to(dev).contiguous())
          for n in ("q", "k", "v", "g", "beta", "h0", "dO", "dht")}
@@ -148,6 +148,22 @@ def make_step(inp, dev, backward):
         bufs = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
                 torch.empty_like(d["g"]), torch.empty_like(d["beta"]),
                 torch.empty_like(ht))
+
+    if backward and save_states:
+        # the forward keeps the state entering every chunk and the chunk records in ws_b; the
+        # backward reads them back instead of recomputing the forward
+        C, nchunks = gdn.gdn_chunk_layout(prob)
+        hbuf = torch.empty(nchunks, d["v"].shape[2], 128, 128, dtype=d["v"].dtype, device=dev)
+
+        def step():
+            gdn.gdn_chunk_fwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale,
+                                    h0=d["h0"], cu_seqlens=cu, cu_seqlens_host=cu_host,
+                                    want_g_cum=False, want_A=False, workspace=ws_b, o=o, ht=ht,
+                                    h=hbuf)
+            gdn.gdn_chunk_bwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, hbuf,
+                                    ws_b, d["dO"], dht=d["dht"], cu_seqlens=cu,
+                                    cu_seqlens_host=cu_host, out=bufs)
+        return step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs
 
     def step():
         gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, h0=d["h0"],
@@ -172,7 +188,7 @@ def time_steps(step, K, flush):
     return sum(a.elapsed_time(b) for a, b in evs)
 
 
-def e2e_run(inp, dev, K, W, backward):
+def e2e_run(inp, dev, K, W, backward, save_states=False):
     """The same step through the public API with HOST buffers: pinned host inputs copied in,
     the call, the result copied out, all inside the timed region."""
     from chunked_prefill_gb300 import gdn
@@ -181,6 +197,10 @@ def e2e_run(inp, dev, K, W, backward):
     devb = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
     step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs = make_step(inp, dev, backward)
     outs = [o, ht] if not backward else [o, ht] + [b for b in bufs if b is not None]
+    hbuf = None
+    if backward and save_states:
+        nchunks = gdn.gdn_chunk_layout(gdn.Problem(d["q"], d["v"], inp.scale, cu, cu_host))[1]
+        hbuf = torch.empty(nchunks, d["v"].shape[2], 128, 128, dtype=d["v"].dtype, device=dev)
     host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out)
@@ -188,6 +208,17 @@ def e2e_run(inp, dev, K, W, backward):
     def e2e_step():
         for n, t in host.items():
             devb[n].copy_(t, non_blocking=True)
+        if hbuf is not None:
+            gdn.gdn_chunk_fwd_saved(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"],
+                                    inp.scale, h0=devb.get("h0"), cu_seqlens=cu,
+                                    cu_seqlens_host=cu_host, want_g_cum=False, want_A=False,
+                                    workspace=ws_b, o=o, ht=ht, h=hbuf)
+            gdn.gdn_chunk_bwd_saved(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"],
+                                    inp.scale, hbuf, ws_b, devb["dO"], dht=devb.get("dht"),
+                                    cu_seqlens=cu, cu_seqlens_host=cu_host, out=bufs)
+            for src, dst in zip(outs, host_out):
+                dst.copy_(src, non_blocking=True)
+            return
         gdn.gdn_chunk_fwd(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"], inp.scale,
                           h0=devb.get("h0"), cu_seqlens=cu, cu_seqlens_host=cu_host, o=o, ht=ht,
                           workspace=ws_f)
@@ -389,6 +420,10 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="for ncu: warm-up and timed steps only (no clock sampling, e2e or "
                          "CPU baseline)")
+    ap.add_argument("--save-states", action="store_true",
+                    help="training workloads: the forward keeps the state entering every chunk "
+                         "for the backward (low-level saved pair) instead of the backward "
+                         "recomputing it")
     ap.add_argument("--sweep", action="store_true",
                     help="head / length sweep of the forward: one JSON line per point "
                          "(an auxiliary report, not the benchmark line)")
@@ -410,7 +445,8 @@ def main():
     inp = workload_inputs(args.workload)
     lens = lengths_of(inp)
     tokens = sum(lens)
-    step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs = make_step(inp, dev, w.backward)
+    save = args.save_states and w.backward
+    step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs = make_step(inp, dev, w.backward, save)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     for _ in range(args.warmup):
@@ -467,7 +503,8 @@ def main():
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / (tokens / (PUBLISHED_MS[args.workload] / 1000.0))
                         if args.workload in PUBLISHED_MS and world == 1 else None),
-        "dtype": "bf16", "data": "synthetic", "config": config_of(args.workload),
+        "dtype": "bf16", "data": "synthetic",
+        "config": dict(config_of(args.workload), **({"save_states": True} if save else {})),
         "roofline": roof,
         "step_roofline": {"flops": fl, "bytes": by, "roofline_ms": t_roof * 1000.0,
                           "frac": t_roof * 1000.0 / ms_per_step, "peak_kind": pk_kind},
@@ -475,7 +512,7 @@ def main():
         "clocks": clk.summary(),
     }
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = e2e_run(inp, dev, args.steps, args.warmup, w.backward)
+        e2e_ms, h2d, d2h = e2e_run(inp, dev, args.steps, args.warmup, w.backward, save)
         e2e_ms = max_over_ranks(e2e_ms, world)
         line["e2e"] = {"value": world * tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}

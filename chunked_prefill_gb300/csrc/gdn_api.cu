@@ -406,9 +406,118 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, con
     B.dqp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dqp) : nullptr;
     B.dkp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dkp) : nullptr;
     // recompute the state entering every chunk, then the reverse scan and local gradients
-    cudaError_t e = use_tensor_cores(p->dtype) ? gdn::launch_fwd_tc(P, true, h.total_tokens, cs)
-                                               : gdn::launch_fwd(P, p->dtype, true, cs);
+    // (bf16 always on the tensor-core forward: the reverse scan reads its chunk records)
+    cudaError_t e = p->dtype == GDN_BF16 ? gdn::launch_fwd_tc(P, true, h.total_tokens, cs)
+                                         : gdn::launch_fwd(P, p->dtype, true, cs);
     if (e == cudaSuccess) e = gdn::launch_bwd(B, p->dtype, cs);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+    g_err[0] = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_layout(const gdn_problem* p, int32_t* chunk_size, int64_t* total_chunks) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    if (!chunk_size || !total_chunks) return fail(GDN_ERR_INVALID_ARG, "output pointer is NULL");
+    HostPlan h;
+    plan(p, h, true);
+    *chunk_size = h.C;
+    *total_chunks = h.total_chunks;
+    g_err[0] = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd_saved(const gdn_problem* p, const void* q, const void* k, const void* v,
+                               const float* g, const float* beta, const float* h0, void* o,
+                               float* ht, float* g_cum, void* A, void* h_chunks, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    HostPlan h;
+    plan(p, h, true);  // the backward's plan: exact CP, chunk records with T, M untransposed
+    if (h.total_chunks > 0)
+        st = check_ptrs({q, k, v, g, beta, o, h_chunks}, {h0, ht, g_cum, A});
+    else
+        st = check_ptrs({}, {q, k, v, g, beta, o, h0, ht, g_cum, A, h_chunks});
+    if (st != GDN_OK) return st;
+    if (h.N == 0) {
+        g_err[0] = 0;
+        return GDN_OK;
+    }
+    if (!workspace || workspace_bytes < h.off_end)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", h.off_end,
+                    workspace ? workspace_bytes : size_t(0));
+    if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    gdn::Problem P{};
+    P.q = q;
+    P.k = k;
+    P.v = v;
+    P.g = g;
+    P.beta = beta;
+    P.h0 = h0;
+    P.o = o;
+    P.ht = ht;
+    fill_problem(p, h, static_cast<char*>(workspace), P);
+    P.hist = h_chunks;
+    P.gam_out = g_cum;
+    P.a_out = A;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = p->dtype == GDN_BF16 ? gdn::launch_fwd_tc(P, false, h.total_tokens, cs)
+                                         : gdn::launch_fwd(P, p->dtype, false, cs);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+    g_err[0] = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_bwd_saved(const gdn_problem* p, const void* q, const void* k, const void* v,
+                               const float* g, const float* beta, const void* h_chunks,
+                               const void* dO, const float* dht, void* dq, void* dk, void* dv,
+                               float* dg, float* dbeta, float* dh0, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    HostPlan h;
+    plan(p, h, true);
+    if (h.total_chunks > 0)
+        st = check_ptrs({q, k, v, g, beta, h_chunks, dO, dq, dk, dv, dg, dbeta}, {dht, dh0});
+    else
+        st = check_ptrs({}, {q, k, v, g, beta, h_chunks, dO, dq, dk, dv, dg, dbeta, dht, dh0});
+    if (st != GDN_OK) return st;
+    if (h.N == 0) {
+        g_err[0] = 0;
+        return GDN_OK;
+    }
+    if (!workspace || workspace_bytes < h.off_end)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", h.off_end,
+                    workspace ? workspace_bytes : size_t(0));
+    if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    gdn::BwdProblem B{};
+    gdn::Problem& P = B.f;
+    P.q = q;
+    P.k = k;
+    P.v = v;
+    P.g = g;
+    P.beta = beta;
+    fill_problem(p, h, ws, P);
+    P.hist = const_cast<void*>(h_chunks);
+    B.dO = dO;
+    B.dht = dht;
+    B.dh0 = dh0;
+    B.dq = dq;
+    B.dk = dk;
+    B.dv = dv;
+    B.dg = dg;
+    B.dbeta = dbeta;
+    B.dhist = ws + h.off_dhist;
+    B.dhb = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_dhb) : nullptr;
+    B.dqp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dqp) : nullptr;
+    B.dkp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dkp) : nullptr;
+    // the states, chunk records and segment transitions come from gdn_chunk_fwd_saved: only
+    // the work decomposition is rebuilt before the reverse scan and the local gradients
+    gdn::launch_plan(P, h.C, cs);
+    cudaError_t e = gdn::launch_bwd(B, p->dtype, cs);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
     g_err[0] = 0;
     return GDN_OK;

@@ -155,7 +155,7 @@ __device__ void scan_chunks(const Problem& P, char* smem, int s, int j, int64_t 
         const int64_t tc = t0 + int64_t(ch) * C;
         const int c = int((t1 - tc) < int64_t(C) ? (t1 - tc) : int64_t(C));
 
-        if (KIND == K_HIST) {  // entering state of this chunk, for the backward
+        if (KIND == K_HIST || (KIND == K_OUT && P.hist)) {  // entering state, for the backward
             Op* hp = reinterpret_cast<Op*>(P.hist) + (hist_base + ch) * Hv * (KD * VD) +
                      int64_t(j) * (KD * VD);
 #pragma unroll
@@ -280,12 +280,17 @@ __device__ void scan_chunks(const Problem& P, char* smem, int s, int j, int64_t 
             __syncthreads();
         }
 
-        // ---- -T diag(beta e) and T diag(beta) as MMA operands
+        // ---- -T diag(beta e) and T diag(beta) as MMA operands (and gamma, T when asked)
+        const bool lowlevel = KIND == K_OUT && (P.a_out || P.gam_out);
         for (int idx = tid; idx < C * C; idx += NTHREADS) {
             const int i = idx / C, jj = idx % C;
             const float t = (jj <= i) ? sT[i * LDF + jj] : 0.f;
             sTW[i * LDC + jj] = from_f<Op>(-t * sBeta[jj] * sE[jj]);
             if (kU) sTU[i * LDC + jj] = from_f<Op>(t * sBeta[jj]);
+            if (lowlevel && i < c) {
+                if (P.a_out) reinterpret_cast<Op*>(P.a_out)[((tc + i) * Hv + j) * C + jj] = from_f<Op>(t);
+                if (P.gam_out && jj == 0) P.gam_out[(tc + i) * Hv + j] = sGam[i];
+            }
         }
         __syncthreads();
 

@@ -169,7 +169,8 @@ __device__ __forceinline__ void init_state_half(uint32_t tm, uint32_t lb, int ha
 }
 
 // One half (64 key columns) of the per-chunk state hand-off: read the fp32 state, write its
-// bf16 copy (the A operand of the V' and Q h products), store it for the backward when asked,
+// bf16 copy (the A operand of the V' and Q h products), store it for the backward when asked
+// (the recompute kind always, the output kind when P.hist is set),
 // and decay the fp32 state by exp(gamma_C) before the chunk's update accumulates onto it.
 template <int KIND, bool WIDE = true>
 __device__ __forceinline__ void convert_state_half(const Problem& P, uint32_t tm, uint32_t lb,
@@ -183,7 +184,7 @@ __device__ __forceinline__ void convert_state_half(const Problem& P, uint32_t tm
         tmem_ld32(tm + lb + xf + c0, x);
         if (WIDE) tmem_ld32(tm + lb + xf + c0 + 32, x + (W - 32));
         tmem_ld_wait();
-        if (KIND == TK_HIST) {
+        if (KIND == TK_HIST || (KIND == TK_OUT && P.hist)) {
             __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(P.hist) + (chunk * P.Hv + j) * (KD * VD);
 #pragma unroll
             for (int i = 0; i < W; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);

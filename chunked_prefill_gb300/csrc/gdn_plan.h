@@ -31,7 +31,10 @@ struct Problem {
     float* hin;         // [total_segs, Hv, K, V]  entering state of each segment
     float* mbuf;        // [total_segs, Hv, K, K]  segment transitions, stored transposed (exact CP)
     float* mbuf_t;      // the same transitions untransposed (bf16 backward only), or null
-    void* hist;         // [total_chunks, Hv, K, V] entering state of every chunk (bwd)
+    void* hist;         // [total_chunks, Hv, K, V] entering state of every chunk (bwd); in the
+                        // output stage non-null asks for the same store next to the outputs
+    float* gam_out;     // [T, Hv] in-chunk cumulative gate gamma, or null (not returned)
+    void* a_out;        // [T, Hv, C] row of the chunk's T = (I + A)^-1 for every token, or null
     void* prep;         // [total_chunks, Hv] records of prep_stride bytes (tensor-core path)
     int64_t prep_stride;  // 32 KB (W', TU, P), or 40 KB with T as well (the backward needs it)
     PlanDev plan;

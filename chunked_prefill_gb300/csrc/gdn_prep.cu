@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     const int gq = lane >> 2, tq = lane & 3;
     const uint32_t kq = smem_addr(smem + S::oKQ);
     int* err = P.err;
-    const bool want_t = P.prep_stride >= PREP_BWD_BYTES;
+    const bool store_t = P.prep_stride >= PREP_BWD_BYTES;  // T in the record (backward)
+    const bool want_t = store_t || P.a_out != nullptr;
 
     if (tid == 0) {
         for (int b = 0; b < 3; ++b) mbar_init(&bars[b], 1);
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 sEi[r] = expf(-gm[u]);
                 sBeta[r] = bv[u];
                 sBe[r] = bv[u] * e;
+                if (P.gam_out && r < c) P.gam_out[(tc + r) * P.Hv + j] = gm[u];
             }
             if (lane == 0) *sFlag = (last < -80.f || !(last == last)) ? 1 : 0;
         }
@@ -434,7 +436,10 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 q4.y = pack_bf16(tkeep[8 * u4 + 2], tkeep[8 * u4 + 3]);
                 q4.z = pack_bf16(tkeep[8 * u4 + 4], tkeep[8 * u4 + 5]);
                 q4.w = pack_bf16(tkeep[8 * u4 + 6], tkeep[8 * u4 + 7]);
-                *reinterpret_cast<uint4*>(smem + S::oT + r * 128 + ((c8 ^ (r & 7)) << 4)) = q4;
+                if (store_t) *reinterpret_cast<uint4*>(smem + S::oT + r * 128 + ((c8 ^ (r & 7)) << 4)) = q4;
+                if (P.a_out && r < c)  // token tc + r: its row of T, 64 bf16 columns
+                    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.a_out) +
+                                              ((tc + r) * P.Hv + j) * CH + 8 * c8) = q4;
             }
         }
         {
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         if (tid == 0) {
             bulk_store(rec + PREP_W, smem + S::oQ0, 8192);
             bulk_store(rec + PREP_W + 8192, smem + S::oQ1, 8192);
-            if (want_t) bulk_store(rec + PREP_T, smem + S::oT, 8192);
+            if (store_t) bulk_store(rec + PREP_T, smem + S::oT, 8192);
             bulk_commit();
             PTRACE(6);
             bulk_wait_read0();  // the next head (or the CTA's exit) may reuse the staging tiles

@@ -65,8 +65,13 @@ def lib():
         L.gdn_chunk_bwd_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
         L.gdn_chunk_fwd.argtypes = [P] + [vp] * 9 + [ctypes.c_size_t, vp]
         L.gdn_chunk_bwd.argtypes = [P] + [vp] * 15 + [ctypes.c_size_t, vp]
+        L.gdn_chunk_layout.argtypes = [P, ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_int64)]
+        L.gdn_chunk_fwd_saved.argtypes = [P] + [vp] * 12 + [ctypes.c_size_t, vp]
+        L.gdn_chunk_bwd_saved.argtypes = [P] + [vp] * 15 + [ctypes.c_size_t, vp]
         for f in ("gdn_chunk_fwd_workspace_size", "gdn_chunk_bwd_workspace_size",
-                  "gdn_chunk_fwd", "gdn_chunk_bwd"):
+                  "gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_chunk_layout", "gdn_chunk_fwd_saved",
+                  "gdn_chunk_bwd_saved"):
             getattr(L, f).restype = ctypes.c_int
         L.gdn_last_error.restype = ctypes.c_char_p
         L.gdn_timing_enable.argtypes = [ctypes.c_int32]
@@ -225,29 +230,107 @@ def gdn_chunk_bwd(q, k, v, g, beta, scale, dO, h0=None, dht=None, cu_seqlens=Non
     return dq, dk, dv, dg, db, dh0
 
 
+def gdn_chunk_layout(prob: Problem):
+    """(chunk size C, chunks over all sequences) of the per-chunk saved outputs."""
+    c, n = ctypes.c_int32(0), ctypes.c_int64(0)
+    _check(lib().gdn_chunk_layout(prob.ref(), ctypes.byref(c), ctypes.byref(n)))
+    return c.value, n.value
+
+
+def gdn_chunk_fwd_saved(q, k, v, g, beta, scale, h0=None, output_final_state=True,
+                        cu_seqlens=None, cu_seqlens_host=None, cp_mode=CP_AUTO,
+                        cp_segment_chunks=0, cp_lambda=0.0, want_g_cum=True, want_A=True,
+                        workspace=None, stream=None, o=None, ht=None, h=None):
+    """Low-level forward through the C ABI.  Returns (g_cum, A, o, h, ht, ctx): the in-chunk
+    cumulative gate [B,T,Hv] (or None), every token's row of its chunk's (I + A)^-1
+    [B,T,Hv,C] (or None), the output, the state entering every chunk [total_chunks,Hv,K,V],
+    the final state (or None) and the workspace that gdn_chunk_bwd_saved reads back."""
+    _validate_tensors(q, k, v, g, beta)
+    prob = Problem(q, v, scale, cu_seqlens, cu_seqlens_host, cp_mode, cp_segment_chunks, 0,
+                   cp_lambda)
+    C, nchunks = gdn_chunk_layout(prob)
+    B, T, Hv = v.shape[:3]
+    if o is None:
+        o = torch.empty_like(v)
+    if ht is None and output_final_state:
+        ht = torch.empty(prob.num_seqs, Hv, prob.K, prob.V, device=q.device, dtype=torch.float32)
+    g_cum = torch.empty_like(g) if want_g_cum else None
+    A = torch.empty(B, T, Hv, C, device=q.device, dtype=q.dtype) if want_A else None
+    if h is None:
+        h = torch.empty(max(nchunks, 0), Hv, prob.K, prob.V, device=q.device, dtype=q.dtype)
+    if h0 is not None:
+        h0 = h0.contiguous().float()
+    nbytes = gdn_chunk_bwd_workspace_size(prob)
+    ws = _workspace(nbytes, q.device, workspace)
+    _check(lib().gdn_chunk_fwd_saved(prob.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(h0), _ptr(o), _ptr(ht), _ptr(g_cum), _ptr(A), _ptr(h),
+                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+    return g_cum, A, o, h, ht, ws
+
+
+def gdn_chunk_bwd_saved(q, k, v, g, beta, scale, h, ctx, dO, dht=None, cu_seqlens=None,
+                        cu_seqlens_host=None, cp_mode=CP_AUTO, cp_segment_chunks=0,
+                        cp_lambda=0.0, want_dh0=True, stream=None, out=None):
+    """Backward from the saved states h and workspace ctx of gdn_chunk_fwd_saved (same
+    problem arguments).  Returns (dq, dk, dv, dg, dbeta, dh0)."""
+    _validate_tensors(q, k, v, g, beta)
+    if dO.shape != v.shape or dO.dtype != v.dtype or not dO.is_contiguous():
+        raise ValueError("dO must be contiguous and match v")
+    prob = Problem(q, v, scale, cu_seqlens, cu_seqlens_host, cp_mode, cp_segment_chunks, 0,
+                   cp_lambda)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dg, db = torch.empty_like(g), torch.empty_like(beta)
+        dh0 = (torch.empty(prob.num_seqs, prob.Hv, prob.K, prob.V, device=q.device)
+               if want_dh0 else None)
+    else:
+        dq, dk, dv, dg, db, dh0 = out
+    if dht is not None:
+        dht = dht.contiguous().float()
+    _check(lib().gdn_chunk_bwd_saved(prob.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(h), _ptr(dO), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     _ptr(dg), _ptr(db), _ptr(dh0), _ptr(ctx),
+                                     ctx.numel() * ctx.element_size(), _stream(stream)))
+    return dq, dk, dv, dg, db, dh0
+
+
 class _ChunkGDN(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, h0, scale, output_final_state, cu_seqlens):
-        o, ht = gdn_chunk_fwd(q, k, v, g, beta, scale, h0=h0,
-                              output_final_state=output_final_state, cu_seqlens=cu_seqlens)
-        ctx.save_for_backward(q, k, v, g, beta, h0, cu_seqlens)
+    def forward(ctx, q, k, v, g, beta, h0, scale, output_final_state, cu_seqlens, save_states):
+        if save_states:
+            _, _, o, h, ht, ws = gdn_chunk_fwd_saved(q, k, v, g, beta, scale, h0=h0,
+                                                     output_final_state=output_final_state,
+                                                     cu_seqlens=cu_seqlens, want_g_cum=False,
+                                                     want_A=False)
+            ctx.save_for_backward(q, k, v, g, beta, h0, cu_seqlens, h, ws)
+        else:
+            o, ht = gdn_chunk_fwd(q, k, v, g, beta, scale, h0=h0,
+                                  output_final_state=output_final_state, cu_seqlens=cu_seqlens)
+            ctx.save_for_backward(q, k, v, g, beta, h0, cu_seqlens)
         ctx.scale = scale
+        ctx.save_states = save_states
         return o, ht
 
     @staticmethod
     def backward(ctx, do, dht):
-        q, k, v, g, beta, h0, cu = ctx.saved_tensors
-        dq, dk, dv, dg, db, dh0 = gdn_chunk_bwd(q, k, v, g, beta, ctx.scale, do.contiguous(),
-                                                h0=h0, dht=dht, cu_seqlens=cu,
-                                                want_dh0=h0 is not None)
-        return dq, dk, dv, dg, db, dh0, None, None, None
+        if ctx.save_states:
+            q, k, v, g, beta, h0, cu, h, ws = ctx.saved_tensors
+            grads = gdn_chunk_bwd_saved(q, k, v, g, beta, ctx.scale, h, ws, do.contiguous(),
+                                        dht=dht, cu_seqlens=cu, want_dh0=h0 is not None)
+        else:
+            q, k, v, g, beta, h0, cu = ctx.saved_tensors
+            grads = gdn_chunk_bwd(q, k, v, g, beta, ctx.scale, do.contiguous(), h0=h0, dht=dht,
+                                  cu_seqlens=cu, want_dh0=h0 is not None)
+        return (*grads, None, None, None, None)
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None,
-                           output_final_state=False, cu_seqlens=None):
+                           output_final_state=False, cu_seqlens=None, save_states=False):
     """High-level call with the FlashQLA/FLA signature; differentiable.
-    q, k [B,T,Hqk,K]; v [B,T,Hv,V]; g, beta [B,T,Hv] (fp32); initial_state [N,Hv,K,V]."""
+    q, k [B,T,Hqk,K]; v [B,T,Hv,V]; g, beta [B,T,Hv] (fp32); initial_state [N,Hv,K,V].
+    save_states=True keeps the state entering every chunk (and the chunk records) from the
+    forward for the backward, which then skips its recompute of the forward."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
     return _ChunkGDN.apply(q, k, v, g, beta, initial_state, scale, output_final_state,
-                           cu_seqlens)
+                           cu_seqlens, save_states)

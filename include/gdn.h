@@ -118,6 +118,48 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, con
                          void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Low-level forward / backward pair with saved intermediates (FlashQLA pages, aisparkup
+ * "usage" section: the low-level forward returns g, A, o, h and the final state, and the
+ * backward is called separately).  The pages name the tuple but do not define its members;
+ * this library reads them as
+ *   g_cum : [T_total, Hv] fp32, gamma, the cumulative sum of g within each chunk (it restarts
+ *           at every chunk start and at every sequence start);
+ *   A     : [T_total, Hv, C] dtype, for every token its row of its chunk's
+ *           T = (I + diag(beta) (K K^T * Dm))^-1 (unit lower triangular; Dm_ij =
+ *           exp(gamma_i - gamma_j) for i > j, else 0); column i of a token's row refers to
+ *           the chunk's i-th token, columns past the token's own position are 0;
+ *   h     : [total_chunks, Hv, K, V] dtype, the state h = S^T entering every chunk, chunks
+ *           numbered over all sequences in order (sequence s holds ceil(len_s / C) of them,
+ *           its first one being h0, or 0).
+ * C is the kernels' chunk size (64 for bf16, 32 in the fp32 test mode); gdn_chunk_layout
+ * reports it and total_chunks.
+ *
+ * gdn_chunk_fwd_saved computes what gdn_chunk_fwd computes and also writes g_cum and A (when
+ * non-NULL) and h (required).  It runs the backward's decomposition of the problem
+ * (context parallelism is exact; GDN_CP_WARMUP is treated as GDN_CP_EXACT) and leaves in
+ * the workspace the chunk records and segment transitions that the backward needs: the
+ * workspace must hold gdn_chunk_bwd_workspace_size bytes.
+ *
+ * gdn_chunk_bwd_saved computes what gdn_chunk_bwd computes for the same inputs, without
+ * recomputing the forward: it reads h and the workspace exactly as gdn_chunk_fwd_saved left
+ * them for the same problem (the caller keeps both unchanged between the two calls, and
+ * orders the calls, e.g. on one stream).  h0 is not needed (h holds it).  g_cum and A are
+ * outputs only; the backward does not read them.
+ * ------------------------------------------------------------------------------------ */
+gdn_status gdn_chunk_layout(const gdn_problem* p, int32_t* chunk_size, int64_t* total_chunks);
+
+gdn_status gdn_chunk_fwd_saved(const gdn_problem* p, const void* q, const void* k, const void* v,
+                               const float* g, const float* beta, const float* h0, void* o,
+                               float* ht, float* g_cum, void* A, void* h, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+gdn_status gdn_chunk_bwd_saved(const gdn_problem* p, const void* q, const void* k, const void* v,
+                               const float* g, const float* beta, const void* h, const void* dO,
+                               const float* dht, void* dq, void* dk, void* dv, float* dg,
+                               float* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Per-kernel timing (instrumentation for benchmarks; not needed for computation).
  * While enabled, every kernel the library launches is bracketed by two CUDA events
  * recorded on the launching stream.  gdn_timing_collect waits for the recorded events

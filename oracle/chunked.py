@@ -108,6 +108,44 @@ def fwd(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, chunk=64):
     return o.reshape(B, T, Hv, V), ht
 
 
+def fwd_lowlevel(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, chunk=64):
+    """Chunked forward that also returns the low-level intermediates of the pages' low-level
+    forward (FlashQLA pages, aisparkup "usage" section: g, A, o, h, final state), read as
+
+        gam [TT, Hv]        gamma, the in-chunk inclusive cumsum of g
+        A   [TT, Hv, chunk] each token's row of its chunk's T = (I + A)^-1, zero past the
+                            token's own column (and for the missing rows of a short chunk)
+        h   [NC, Hv, K, V]  the state entering every chunk, chunks of all sequences in order
+
+    with TT = B*T packed tokens.  Returns (gam, A, o, h, ht); o is [B, T, Hv, V]."""
+    B, T, q, k, v, g, beta, _ = _packed(q, k, v, g, beta)
+    Hqk, K = q.shape[1:]
+    Hv, V = v.shape[1:]
+    G = Hv // Hqk
+    cu = _cu(cu_seqlens, B, T)
+    N = len(cu) - 1
+    nchunks = [-(-int(cu[s + 1] - cu[s]) // chunk) for s in range(N)]
+    first = np.concatenate([[0], np.cumsum(nchunks)]).astype(np.int64)
+    o = np.zeros((B * T, Hv, V))
+    ht = np.zeros((N, Hv, K, V))
+    gam = np.zeros((B * T, Hv))
+    A = np.zeros((B * T, Hv, chunk))
+    hs = np.zeros((int(first[-1]), Hv, K, V))
+    for s in range(N):
+        for j in range(Hv):
+            h = np.zeros((K, V)) if h0 is None else np.array(h0[s, j], np.float64)
+            for n, (c0, c1, ch) in enumerate(_chunks_of(q, k, v, g, beta, cu[s], cu[s + 1],
+                                                        j // G, j, chunk)):
+                hs[first[s] + n, j] = h
+                gam[c0:c1, j] = ch.gam
+                A[c0:c1, j, :c1 - c0] = ch.T
+                vp = ch.vprime(h)
+                o[c0:c1, j] = ch.out(h, vp, scale)
+                h = ch.next_state(h, vp)
+            ht[s, j] = h
+    return gam, A.reshape(B * T, Hv, chunk), o.reshape(B, T, Hv, V), hs, ht
+
+
 def fwd_cp(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, chunk=64, seg_chunks=4,
            warmup=None):
     """Chunked forward with context parallelism over chunk ranges of ``seg_chunks`` chunks.

@@ -91,3 +91,74 @@ def test_chunked_backward_equals_recurrent_backward(chunk):
     got = chunked.bwd(q, k, v, g, beta, 0.7, dO, h0=h0, dht=dht, cu_seqlens=cu, chunk=chunk)
     for name, a, b in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], got, ref):
         np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-9, err_msg=name)
+
+
+# ---- the low-level forward's intermediates (gamma, T per token, state entering every chunk)
+
+def test_lowlevel_states_are_prefix_recurrences():
+    """h of chunk n of a sequence is the per-token recurrence's final state after the
+    sequence's first n*chunk tokens (h0 for n = 0); o and ht are the recurrence's."""
+    lens = [37, 0, 5, 64, 129]
+    C = 16
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q, k, v, g, beta, h0 = rnd(8, sum(lens), 2, 4, nseq=len(lens))
+    gam, A, o, hs, ht = chunked.fwd_lowlevel(q, k, v, g, beta, 0.6, h0=h0, cu_seqlens=cu, chunk=C)
+    ro, rht = orc.fwd(q, k, v, g, beta, 0.6, h0=h0, cu_seqlens=cu)
+    np.testing.assert_allclose(o, ro, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(ht, rht, rtol=1e-11, atol=1e-11)
+    n_all = 0
+    for s, L in enumerate(lens):
+        for n in range(-(-L // C)):
+            t0, t1 = cu[s], cu[s] + n * C
+            sl = lambda x: x[:, t0:t1]
+            _, pre = orc.fwd(sl(q), sl(k), sl(v), sl(g), sl(beta), 0.6, h0=h0[s:s + 1])
+            np.testing.assert_allclose(hs[n_all], pre[0], rtol=1e-11, atol=1e-11)
+            n_all += 1
+    assert hs.shape[0] == n_all
+
+
+def test_lowlevel_gamma_restarts_at_chunk_and_sequence_starts():
+    lens = [3, 20, 0, 9]
+    C = 8
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q, k, v, _, beta, _ = rnd(9, sum(lens), 1, 2, h0=False)
+    g = np.full(beta.shape, -0.1)
+    gam = chunked.fwd_lowlevel(q, k, v, g, beta, 1.0, cu_seqlens=cu, chunk=C)[0]
+    for s in range(len(lens)):
+        for t in range(cu[s], cu[s + 1]):
+            pos = (t - cu[s]) % C
+            np.testing.assert_allclose(gam[t], -0.1 * (pos + 1), rtol=1e-14)
+
+
+def test_lowlevel_T_closed_forms():
+    """Rows of T = (I + L)^-1 with L_ij = beta_i exp(g_{j+1} + ... + g_i) <k_i, k_j> (i > j):
+    for three tokens T_10 = -L_10, T_21 = -L_21, T_20 = -L_20 + L_21 L_10 (Neumann series
+    of a nilpotent L); the diagonal is 1 and everything past it 0."""
+    q, k, v, g, beta, _ = rnd(10, 3, 1, 1, h0=False)
+    A = chunked.fwd_lowlevel(q, k, v, g, beta, 1.0, chunk=64)[1][:, 0]
+    kk = lambda i, j: float(np.dot(k[0, i, 0], k[0, j, 0]))
+    Lm = lambda i, j: beta[0, i, 0] * np.exp(g[0, j + 1:i + 1, 0].sum()) * kk(i, j)
+    want = np.zeros((3, 64))
+    want[0, 0] = want[1, 1] = want[2, 2] = 1.0
+    want[1, 0] = -Lm(1, 0)
+    want[2, 1] = -Lm(2, 1)
+    want[2, 0] = -Lm(2, 0) + Lm(2, 1) * Lm(1, 0)
+    np.testing.assert_allclose(A, want, rtol=1e-12, atol=1e-14)
+
+
+def test_lowlevel_T_inverts_the_chunk_matrix_by_loops():
+    """(I + L) T = I on every chunk of a ragged sequence, L built entry by entry."""
+    T_len, C = 45, 16
+    q, k, v, g, beta, _ = rnd(11, T_len, 1, 2, h0=False)
+    A = chunked.fwd_lowlevel(q, k, v, g, beta, 1.0, chunk=C)[1]
+    for j in range(2):
+        for c0 in range(0, T_len, C):
+            c = min(C, T_len - c0)
+            Lc = np.eye(c)
+            for i in range(c):
+                for jj in range(i):
+                    dec = np.exp(sum(g[0, c0 + m, j] for m in range(jj + 1, i + 1)))
+                    Lc[i, jj] = beta[0, c0 + i, j] * dec * np.dot(k[0, c0 + i, 0], k[0, c0 + jj, 0])
+            Tc = A[c0:c0 + c, j, :c]
+            np.testing.assert_allclose(Lc @ Tc, np.eye(c), atol=1e-12)
+            assert np.all(A[c0:c0 + c, j, c:] == 0)
