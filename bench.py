@@ -408,6 +408,54 @@ def sweep(args, local):
         torch.cuda.empty_cache()
 
 
+def prologue_bench(args, local):
+    """Fused prologue forward and reverse on the q/k/gate shapes of two workloads: HBM bytes
+    each launch must move, CUDA-event time, fraction of the measured copy bandwidth."""
+    from chunked_prefill_gb300 import build, gdn
+    from chunked_prefill_gb300.inputs import make_prologue_inputs
+    build.build()
+    dev = torch.device("cuda", local)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    pk, pk_kind = peaks()
+    names = ("q_raw", "k_raw", "a", "b", "A_log", "dt_bias")
+    for wl in ("fwd_t32k_hqk2_hv8", "fwdbwd_t32k_hqk16_hv16"):
+        w = WORKLOADS[wl]
+        d = {n: t.to(dev) for n, t in make_prologue_inputs(w.B, w.T, w.Hqk, w.Hv,
+                                                           backward=True).items()}
+        tok = w.B * w.T
+        qk = 2 * tok * w.Hqk * 128 * 2
+        gt = tok * w.Hv * 4
+        legs = {
+            # read q_raw, k_raw, a, b; write q, k, g, beta
+            "prologue_fwd": (lambda: gdn.gdn_prologue_fwd(*(d[n] for n in names)),
+                             2 * qk + 4 * gt),
+            # read q_raw, k_raw, dq, dk, a, b, dg, dbeta; write dq_raw, dk_raw, da, db;
+            # the per-head sums re-read a, dg, da
+            "prologue_bwd": (lambda: gdn.gdn_prologue_bwd(*(d[n] for n in names), d["dq"], d["dk"],
+                                                          d["dg"], d["dbeta"]),
+                             3 * qk + 8 * gt + 3 * gt),
+        }
+        for leg, (fn, by) in legs.items():
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            ms = time_steps(fn, args.steps, flush) / args.steps
+            gdn.gdn_timing_enable(True)
+            time_steps(fn, args.steps, flush)
+            gdn.gdn_timing_enable(False)
+            kt = gdn.gdn_timing_collect()
+            kms = {k: v[1] / args.steps for k, v in kt.items()}
+            main_ms = sum(kms.values())  # kernel time (event pairs around each launch)
+            print(json.dumps({
+                "prologue": True, "workload": wl, "leg": leg, "ms_per_call": ms,
+                "kernels_ms_per_call": kms, "algorithmic_bytes": by,
+                "achieved_gbs": by / (main_ms / 1000.0) / 1e9,
+                "frac": by / (main_ms / 1000.0) / 1e9 / pk["hbm_gbs"], "peak_kind": pk_kind}),
+                flush=True)
+        del d
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -424,6 +472,9 @@ def main():
                     help="training workloads: the forward keeps the state entering every chunk "
                          "for the backward (low-level saved pair) instead of the backward "
                          "recomputing it")
+    ap.add_argument("--prologue", action="store_true",
+                    help="fused prologue forward / reverse: one JSON line per leg and shape "
+                         "(an auxiliary report, not the benchmark line)")
     ap.add_argument("--sweep", action="store_true",
                     help="head / length sweep of the forward: one JSON line per point "
                          "(an auxiliary report, not the benchmark line)")
@@ -432,6 +483,9 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     if args.sweep:
         sweep(args, local)
+        return
+    if args.prologue:
+        prologue_bench(args, local)
         return
 
     if args.impl == "reference":

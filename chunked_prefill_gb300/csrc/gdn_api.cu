@@ -523,4 +523,98 @@ gdn_status gdn_chunk_bwd_saved(const gdn_problem* p, const void* q, const void* 
     return GDN_OK;
 }
 
+namespace {
+gdn_status prologue_common(const gdn_problem* p, gdn::PrologueArgs& A) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    const int64_t T_total = p->cu_seqlens ? int64_t(p->T) : int64_t(p->B) * p->T;
+    A.dtype = p->dtype;
+    A.rows = T_total * p->Hqk;
+    A.gates = T_total * p->Hv;
+    A.Hv = p->Hv;
+    return GDN_OK;
+}
+}  // namespace
+
+gdn_status gdn_prologue_fwd(const gdn_problem* p, const void* q_raw, const void* k_raw,
+                            const float* a, const float* b, const float* A_log,
+                            const float* dt_bias, void* q, void* k, float* g, float* beta,
+                            void* stream) {
+    gdn::PrologueArgs A{};
+    gdn_status st = prologue_common(p, A);
+    if (st != GDN_OK) return st;
+    st = A.rows > 0 ? check_ptrs({q_raw, k_raw, a, b, A_log, dt_bias, q, k, g, beta}, {})
+                    : check_ptrs({A_log, dt_bias}, {q_raw, k_raw, a, b, q, k, g, beta});
+    if (st != GDN_OK) return st;
+    if (A.rows == 0) {
+        g_err[0] = 0;
+        return GDN_OK;
+    }
+    A.q_raw = q_raw;
+    A.k_raw = k_raw;
+    A.a = a;
+    A.b = b;
+    A.A_log = A_log;
+    A.dt_bias = dt_bias;
+    A.q = q;
+    A.k = k;
+    A.g = g;
+    A.beta = beta;
+    cudaError_t e = gdn::launch_prologue_fwd(A, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+    g_err[0] = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_prologue_bwd_workspace_size(const gdn_problem* p, size_t* bytes) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    if (!bytes) return fail(GDN_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = gdn::prologue_bwd_workspace(p->Hv);
+    g_err[0] = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void* k_raw,
+                            const float* a, const float* b, const float* A_log,
+                            const float* dt_bias, const void* dq, const void* dk,
+                            const float* dg, const float* dbeta, void* dq_raw, void* dk_raw,
+                            float* da, float* db, float* dA_log, float* ddt_bias,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    gdn::PrologueArgs A{};
+    gdn_status st = prologue_common(p, A);
+    if (st != GDN_OK) return st;
+    st = A.rows > 0 ? check_ptrs({q_raw, k_raw, a, b, A_log, dt_bias, dq, dk, dg, dbeta, dq_raw,
+                                  dk_raw, da, db, dA_log, ddt_bias}, {})
+                    : check_ptrs({A_log, dt_bias, dA_log, ddt_bias},
+                                 {q_raw, k_raw, a, b, dq, dk, dg, dbeta, dq_raw, dk_raw, da, db});
+    if (st != GDN_OK) return st;
+    const size_t need = gdn::prologue_bwd_workspace(p->Hv);
+    if (!workspace || workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : size_t(0));
+    if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    A.q_raw = q_raw;
+    A.k_raw = k_raw;
+    A.a = a;
+    A.b = b;
+    A.A_log = A_log;
+    A.dt_bias = dt_bias;
+    A.dq = dq;
+    A.dk = dk;
+    A.dg = dg;
+    A.dbeta = dbeta;
+    A.dq_raw = dq_raw;
+    A.dk_raw = dk_raw;
+    A.da = da;
+    A.db = db;
+    A.dA_log = dA_log;
+    A.ddt_bias = ddt_bias;
+    A.part = static_cast<float*>(workspace);
+    cudaError_t e = gdn::launch_prologue_bwd(A, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+    g_err[0] = 0;
+    return GDN_OK;
+}
+
 }  // extern "C"

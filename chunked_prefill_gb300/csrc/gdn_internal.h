@@ -52,6 +52,38 @@ cudaError_t launch_bwd_scan_tc(const BwdProblem& B, int which, int64_t T_total, 
 // B.f.hist, transitions in B.f.mbuf) to have run on the same stream.
 cudaError_t launch_bwd(const BwdProblem& B, int dtype, cudaStream_t st);
 
+// Fused prologue (q/k L2 norm, gate and beta activations) and its reverse mode.
+struct PrologueArgs {
+    int dtype;            // 0 bf16, 1 fp32 (q, k and their gradients)
+    int64_t rows;         // T_total * Hqk rows of 128 for q and for k
+    int64_t gates;        // T_total * Hv gate elements
+    int Hv;
+    const void* q_raw;
+    const void* k_raw;
+    const float* a;       // [T, Hv] gate pre-activation
+    const float* b;       // [T, Hv] beta pre-activation
+    const float* A_log;   // [Hv]
+    const float* dt_bias; // [Hv]
+    void* q;              // forward outputs
+    void* k;
+    float* g;
+    float* beta;
+    const void* dq;       // backward inputs
+    const void* dk;
+    const float* dg;
+    const float* dbeta;
+    void* dq_raw;         // backward outputs
+    void* dk_raw;
+    float* da;
+    float* db;
+    float* dA_log;
+    float* ddt_bias;
+    float* part;          // backward workspace (prologue_bwd_workspace bytes)
+};
+size_t prologue_bwd_workspace(int Hv);
+cudaError_t launch_prologue_fwd(const PrologueArgs& A, cudaStream_t st);
+cudaError_t launch_prologue_bwd(const PrologueArgs& A, cudaStream_t st);
+
 // Per-kernel event timing hooks (no-ops unless gdn_timing_enable(1)).
 void timing_begin(const char* name, cudaStream_t st);
 void timing_end(cudaStream_t st);

@@ -23,12 +23,21 @@ namespace {
 using namespace tc;
 
 #ifdef GDN_TRACE
-__device__ unsigned long long g_prep_trace[16];  // debug builds: SM clock at phase ends
-#define PTRACE(e)                                                                               \
+__device__ unsigned long long g_prep_trace[8 * 9];  // debug builds: SM clock at phase ends
+#ifndef GDN_PTRACE_X
+#define GDN_PTRACE_X 0
+#endif
+// per v-head slot (the CTA-level events go to slot 8)
+#define PTRACE_H(h, e)                                                                          \
     do {                                                                                        \
-        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) g_prep_trace[e] = clock64(); \
+        if (blockIdx.x == GDN_PTRACE_X && blockIdx.y == 0 && threadIdx.x == 0 && (h) < 9)       \
+            g_prep_trace[(h) * 8 + (e)] = clock64();                                            \
     } while (0)
+#define PTRACE(e) PTRACE_H(hh, e)
 #else
+#define PTRACE_H(h, e) \
+    do {               \
+    } while (0)
 #define PTRACE(e) \
     do {          \
     } while (0)
@@ -128,7 +137,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = *slot;
-    PTRACE(0);
+    PTRACE_H(8, 0);
     if (tid == 0) {
         mbar_expect_tx(&bars[0], 32768);
         tma_load_3d(smem + S::oKQ, &maps.k, &bars[0], 0, qh, int(tc));
@@ -169,6 +178,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
 #pragma unroll 1
     for (int hh = 0; hh < nh; ++hh) {
         const int j = j0 + hh;
+        PTRACE(0);
         unsigned char* rec = static_cast<unsigned char*>(P.prep) + (int64_t(gch) * P.Hv + j) * P.prep_stride;
         if (w == 0) {  // in-chunk gates of this v-head
             const float gv[2] = {sGin[(hh * 2) * CH + 2 * lane], sGin[(hh * 2) * CH + 2 * lane + 1]};

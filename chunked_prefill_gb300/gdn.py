@@ -69,9 +69,13 @@ def lib():
                                        ctypes.POINTER(ctypes.c_int64)]
         L.gdn_chunk_fwd_saved.argtypes = [P] + [vp] * 12 + [ctypes.c_size_t, vp]
         L.gdn_chunk_bwd_saved.argtypes = [P] + [vp] * 15 + [ctypes.c_size_t, vp]
+        L.gdn_prologue_fwd.argtypes = [P] + [vp] * 10 + [vp]
+        L.gdn_prologue_bwd_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+        L.gdn_prologue_bwd.argtypes = [P] + [vp] * 17 + [ctypes.c_size_t, vp]
         for f in ("gdn_chunk_fwd_workspace_size", "gdn_chunk_bwd_workspace_size",
                   "gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_chunk_layout", "gdn_chunk_fwd_saved",
-                  "gdn_chunk_bwd_saved"):
+                  "gdn_chunk_bwd_saved", "gdn_prologue_fwd", "gdn_prologue_bwd_workspace_size",
+                  "gdn_prologue_bwd"):
             getattr(L, f).restype = ctypes.c_int
         L.gdn_last_error.restype = ctypes.c_char_p
         L.gdn_timing_enable.argtypes = [ctypes.c_int32]
@@ -292,6 +296,81 @@ def gdn_chunk_bwd_saved(q, k, v, g, beta, scale, h, ctx, dO, dht=None, cu_seqlen
                                      _ptr(dg), _ptr(db), _ptr(dh0), _ptr(ctx),
                                      ctx.numel() * ctx.element_size(), _stream(stream)))
     return dq, dk, dv, dg, db, dh0
+
+
+def _prologue_problem(q_raw, a):
+    if q_raw.dim() != 4 or a.dim() != 3 or a.shape[:2] != q_raw.shape[:2]:
+        raise ValueError("q_raw must be [B,T,Hqk,K] and a [B,T,Hv]")
+    B, T, Hqk, K = q_raw.shape
+    Hv = a.shape[2]
+    return GdnProblem(B=B, T=T, Hqk=Hqk, Hv=Hv, K=K, V=K, dtype=_dtype_code(q_raw.dtype),
+                      scale=1.0, cp_mode=CP_AUTO)
+
+
+def _check_prologue_inputs(q_raw, k_raw, a, b, A_log, dt_bias):
+    for name, t in (("q_raw", q_raw), ("k_raw", k_raw), ("a", a), ("b", b), ("A_log", A_log),
+                    ("dt_bias", dt_bias)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k_raw.shape != q_raw.shape or k_raw.dtype != q_raw.dtype:
+        raise ValueError("q_raw and k_raw must match in shape and dtype")
+    for name, t in (("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias)):
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
+    if b.shape != a.shape or A_log.shape != (a.shape[2],) or dt_bias.shape != (a.shape[2],):
+        raise ValueError("b must match a; A_log and dt_bias must be [Hv]")
+
+
+def gdn_prologue_fwd(q_raw, k_raw, a, b, A_log, dt_bias, stream=None):
+    """Fused prologue through the C ABI: (q, k, g, beta) from the raw projections."""
+    _check_prologue_inputs(q_raw, k_raw, a, b, A_log, dt_bias)
+    p = _prologue_problem(q_raw, a)
+    q, k = torch.empty_like(q_raw), torch.empty_like(k_raw)
+    g, beta = torch.empty_like(a), torch.empty_like(b)
+    _check(lib().gdn_prologue_fwd(ctypes.byref(p), _ptr(q_raw), _ptr(k_raw), _ptr(a), _ptr(b),
+                                  _ptr(A_log), _ptr(dt_bias), _ptr(q), _ptr(k), _ptr(g),
+                                  _ptr(beta), _stream(stream)))
+    return q, k, g, beta
+
+
+def gdn_prologue_bwd(q_raw, k_raw, a, b, A_log, dt_bias, dq, dk, dg, dbeta, stream=None):
+    """Reverse mode of the prologue: (dq_raw, dk_raw, da, db, dA_log, ddt_bias)."""
+    _check_prologue_inputs(q_raw, k_raw, a, b, A_log, dt_bias)
+    p = _prologue_problem(q_raw, a)
+    dq, dk = dq.contiguous(), dk.contiguous()
+    dg, dbeta = dg.contiguous().float(), dbeta.contiguous().float()
+    dq_raw, dk_raw = torch.empty_like(q_raw), torch.empty_like(k_raw)
+    da, db = torch.empty_like(a), torch.empty_like(b)
+    dA_log, ddt_bias = torch.empty_like(A_log), torch.empty_like(dt_bias)
+    n = ctypes.c_size_t(0)
+    _check(lib().gdn_prologue_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)))
+    ws = torch.empty(max(n.value, 16), dtype=torch.uint8, device=q_raw.device)
+    _check(lib().gdn_prologue_bwd(ctypes.byref(p), _ptr(q_raw), _ptr(k_raw), _ptr(a), _ptr(b),
+                                  _ptr(A_log), _ptr(dt_bias), _ptr(dq), _ptr(dk), _ptr(dg),
+                                  _ptr(dbeta), _ptr(dq_raw), _ptr(dk_raw), _ptr(da), _ptr(db),
+                                  _ptr(dA_log), _ptr(ddt_bias), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)))
+    return dq_raw, dk_raw, da, db, dA_log, ddt_bias
+
+
+class _Prologue(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q_raw, k_raw, a, b, A_log, dt_bias):
+        ctx.save_for_backward(q_raw, k_raw, a, b, A_log, dt_bias)
+        return gdn_prologue_fwd(q_raw, k_raw, a, b, A_log, dt_bias)
+
+    @staticmethod
+    def backward(ctx, dq, dk, dg, dbeta):
+        q_raw, k_raw, a, b, A_log, dt_bias = ctx.saved_tensors
+        zero = lambda t, like: torch.zeros_like(like) if t is None else t
+        return gdn_prologue_bwd(q_raw, k_raw, a, b, A_log, dt_bias, zero(dq, q_raw),
+                                zero(dk, k_raw), zero(dg, a), zero(dbeta, b))
+
+
+def gated_delta_rule_prologue(q_raw, k_raw, a, b, A_log, dt_bias):
+    """Differentiable fused prologue: q, k L2-normalised over K; g = -exp(A_log)
+    softplus(a + dt_bias); beta = sigmoid(b).  Returns (q, k, g, beta)."""
+    return _Prologue.apply(q_raw, k_raw, a, b, A_log, dt_bias)
 
 
 class _ChunkGDN(torch.autograd.Function):

@@ -152,3 +152,26 @@ def workload_inputs(name: str, dtype: torch.dtype = torch.bfloat16) -> Inputs:
     return make_inputs(w.B, w.T, w.Hqk, w.Hv, w.K, w.V, seed=w.seed, dtype=dtype,
                        h0_std=w.h0_std, backward=w.backward, varlen_seqs=w.varlen_seqs,
                        varlen_range=w.varlen_range)
+
+
+def make_prologue_inputs(B: int, T: int, Hqk: int, Hv: int, K: int = 128, *, seed: int = 0,
+                         dtype: torch.dtype = torch.bfloat16, backward: bool = False) -> dict:
+    """Raw projections for the fused prologue, drawn on the CPU: q_raw, k_raw ~ N(0, 1)
+    [B, T, Hqk, K]; gate and beta pre-activations a, b ~ N(0, 1) [B, T, Hv]; per-head
+    A_log = log U[1, 16] and dt_bias ~ N(0, 1) [Hv]; with ``backward`` also upstream
+    gradients dq, dk ~ N(0, 1) and dg, dbeta ~ N(0, 1)."""
+    gen = torch.Generator().manual_seed(seed)
+    d = {
+        "q_raw": torch.randn(B, T, Hqk, K, generator=gen).to(dtype),
+        "k_raw": torch.randn(B, T, Hqk, K, generator=gen).to(dtype),
+        "a": torch.randn(B, T, Hv, generator=gen),
+        "b": torch.randn(B, T, Hv, generator=gen),
+        "A_log": torch.log(1 + 15 * torch.rand(Hv, generator=gen)),
+        "dt_bias": torch.randn(Hv, generator=gen),
+    }
+    if backward:
+        d["dq"] = torch.randn(B, T, Hqk, K, generator=gen).to(dtype)
+        d["dk"] = torch.randn(B, T, Hqk, K, generator=gen).to(dtype)
+        d["dg"] = torch.randn(B, T, Hv, generator=gen)
+        d["dbeta"] = torch.randn(B, T, Hv, generator=gen)
+    return d

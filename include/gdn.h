@@ -160,6 +160,40 @@ gdn_status gdn_chunk_bwd_saved(const gdn_problem* p, const void* q, const void* 
                                void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Fused prologue: the activations that turn a layer's raw projections into the inputs of
+ * gdn_chunk_fwd, in one pass (read once, write once), and their reverse mode.  The FlashQLA
+ * pages take q, k, g, beta as given (g a log-decay, beta a write strength, q and k the unit
+ * keys of the delta rule) and do not say how they are formed; this library reads them as
+ *   q = q_raw / sqrt(sum(q_raw^2) + 1e-6)  and  k likewise   (per token and q/k head, over K)
+ *   g = -exp(A_log[j]) * softplus(a + dt_bias[j])           (per token and v-head j)
+ *   beta = 1 / (1 + exp(-b))
+ * with softplus(x) = log(1 + exp(x)) (x itself above 20).
+ *
+ * Shapes from *p (B, T or varlen total T, Hqk, Hv, K = 128, dtype; cu_seqlens unused):
+ *   q_raw, k_raw, q, k, dq, dk, dq_raw, dk_raw   [T_total, Hqk, K]  dtype
+ *   a, b, g, beta, dg, dbeta, da, db             [T_total, Hv]      fp32
+ *   A_log, dt_bias, dA_log, ddt_bias             [Hv]               fp32
+ * gdn_prologue_fwd may run in place (q == q_raw, k == k_raw, g == a, beta == b).
+ * gdn_prologue_bwd takes dq, dk, dg, dbeta (the gradients gdn_chunk_bwd returns) and the
+ * forward's raw inputs, and writes the gradients of L with respect to q_raw, k_raw, a, b,
+ * A_log and dt_bias; dA_log and ddt_bias are sums over all tokens taken in a fixed order.
+ * Its workspace (gdn_prologue_bwd_workspace_size bytes) holds per-head partial sums.
+ * ------------------------------------------------------------------------------------ */
+gdn_status gdn_prologue_fwd(const gdn_problem* p, const void* q_raw, const void* k_raw,
+                            const float* a, const float* b, const float* A_log,
+                            const float* dt_bias, void* q, void* k, float* g, float* beta,
+                            void* stream);
+
+gdn_status gdn_prologue_bwd_workspace_size(const gdn_problem* p, size_t* bytes);
+
+gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void* k_raw,
+                            const float* a, const float* b, const float* A_log,
+                            const float* dt_bias, const void* dq, const void* dk,
+                            const float* dg, const float* dbeta, void* dq_raw, void* dk_raw,
+                            float* da, float* db, float* dA_log, float* ddt_bias,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Per-kernel timing (instrumentation for benchmarks; not needed for computation).
  * While enabled, every kernel the library launches is bracketed by two CUDA events
  * recorded on the launching stream.  gdn_timing_collect waits for the recorded events
