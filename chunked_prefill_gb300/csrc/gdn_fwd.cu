@@ -447,13 +447,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_phase_c(Problem P) {
     scan_chunks<Op, C, KIND>(P, smem, s, j, t0, t1, cb, ce, x0, x_out, hb);
 }
 
-// Fix-up: hin[g0+j+1] = M_j hin[g0+j] + S_j for j = 1..nseg-2, serially; each CTA owns 8
-// state columns of one (sequence, head).  The transitions are stored transposed (M^T); each
-// arrives in shared memory by a bulk copy issued one step ahead (two buffers).  Thread t
-// accumulates a 4-row x 8-column block over 16 of the 128 inner indices (rows 4 (t % 32),
-// inner range 16 (t / 32)): one 16-byte load of M^T and two broadcast loads of the state per
-// 32 FMAs; the eight partial blocks meet in shared memory.  S_j of the next step is read into
-// registers one step early.  fp32.
+// Fix-up: hin[g0+j+1] = M_j hin[g0+j] + S_j for j = 1..nseg-2, serially.  The transitions
+// are stored transposed (M^T); each arrives in shared memory by a bulk copy issued one step
+// ahead (two buffers).  Thread t accumulates a 4-row x 8-column block over a slice of the
+// inner index: one 16-byte load of M^T and two broadcast loads of the state per 16 packed
+// (two-lane) FMAs; the slices' partial blocks meet in shared memory.  S_j of the next step is
+// read into registers one step early.  fp32.  Measured on GB300 at 8 columns per CTA a step
+// takes ~2.8k cycles, most of it shared-memory traffic: the 64 KB transition tile, the
+// broadcast state loads and the 32 KB of partial blocks written and read back.
 #ifdef GDN_TRACE
 __device__ unsigned long long g_fix_trace[64][4];  // debug builds: SM clock per fix-up step
 #define FTRACE(k, e)                                                                            \
@@ -539,31 +540,35 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
             if (q + 1 < last) snext[c] = *hp(xout(q + 1), c);
         }
         const float* M = Ms + b * KD * KD;
-        float acc[4][8];
+        // acc[r][p]: row r, columns (2p, 2p + 1) as a packed pair (one packed FMA per pair)
+        uint64_t acc[4][4];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
-#pragma unroll 4
+            for (int p2 = 0; p2 < 4; ++p2) acc[r][p2] = 0ull;
+#pragma unroll 8
         for (int m = MS * ks; m < MS * ks + MS; ++m) {
             const float4 a = *reinterpret_cast<const float4*>(M + m * KD + 4 * rg);
-            const float4 x0 = *reinterpret_cast<const float4*>(&xs[m * W + 8 * cg]);
-            const float4 x1 = *reinterpret_cast<const float4*>(&xs[m * W + 8 * cg + 4]);
+            const ulonglong2 x0 = *reinterpret_cast<const ulonglong2*>(&xs[m * W + 8 * cg]);
+            const ulonglong2 x1 = *reinterpret_cast<const ulonglong2*>(&xs[m * W + 8 * cg + 4]);
             const float av[4] = {a.x, a.y, a.z, a.w};
-            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], xv[c], acc[r][c]);
+            for (int r = 0; r < 4; ++r) {
+                const uint64_t ar = tc::dup2(av[r]);
+                acc[r][0] = tc::ffma2(ar, x0.x, acc[r][0]);
+                acc[r][1] = tc::ffma2(ar, x0.y, acc[r][1]);
+                acc[r][2] = tc::ffma2(ar, x1.x, acc[r][2]);
+                acc[r][3] = tc::ffma2(ar, x1.y, acc[r][3]);
+            }
         }
         // partial block -> red[ks][rg][cg][32], 16-byte pieces rotated by rg against bank
         // conflicts
         float* rp = red + ((ks * 32 + rg) * CG + cg) * 32;
 #pragma unroll
         for (int pq = 0; pq < 8; ++pq) {
-            const int r = pq >> 1, c = (pq & 1) * 4;
-            *reinterpret_cast<float4*>(rp + ((pq ^ (rg & 7)) << 2)) =
-                make_float4(acc[r][c], acc[r][c + 1], acc[r][c + 2], acc[r][c + 3]);
+            const int r = pq >> 1, c2 = (pq & 1) * 2;
+            *reinterpret_cast<ulonglong2*>(rp + ((pq ^ (rg & 7)) << 2)) =
+                make_ulonglong2(acc[r][c2], acc[r][c2 + 1]);
         }
         FTRACE(q + 1, 3);
         __syncthreads();  // partial blocks visible; everyone is done with xs and buffer b
