@@ -229,10 +229,12 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                         const int jb = 32 * h2 + 4 * j4, M = jb >> 4;
                         if (M > I) continue;  // above the diagonal blocks: not stored
                         float x[4];
+                        const float4 ev = *reinterpret_cast<const float4*>(sEi + jb);
+                        const float evs[4] = {ev.x, ev.y, ev.z, ev.w};
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const int jj = jb + u;
-                            const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
+                            const float d = pw ? expf(gi - sGam[jj]) : ei * evs[u];
                             x[u] = jj < i ? bi * d * raw[4 * j4 + u] : 0.f;
                         }
                         *reinterpret_cast<float4*>(ablk(tri(I, M)) + r * BLD + (jb & 15)) =
@@ -243,10 +245,13 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                     for (int c4 = 0; c4 < 4; ++c4) {
                         const int c8 = 4 * h2 + c4;
                         float x[8];
+                        const float4 e0 = *reinterpret_cast<const float4*>(sEi + 8 * c8);
+                        const float4 e1 = *reinterpret_cast<const float4*>(sEi + 8 * c8 + 4);
+                        const float evs[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             const int jj = 8 * c8 + u;
-                            const float d = pw ? expf(gi - sGam[jj]) : ei * sEi[jj];
+                            const float d = pw ? expf(gi - sGam[jj]) : ei * evs[u];
                             x[u] = (jj <= i && i < c) ? d * raw[8 * c4 + u] : 0.f;
                         }
                         uint4 q4;
@@ -370,8 +375,11 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         PTRACE(3);
         // TU = T diag(beta) and TW = -T diag(beta e) as swizzled bf16 tiles over the dead A
         // blocks: TU leaves by a bulk copy, TW is the B operand of W'^T = K^T TW^T
+        // item it -> row r = it % 64 (consecutive lanes take consecutive rows of one block:
+        // conflict-free reads with the block row stride, and the swizzled stores spread over
+        // all banks), 8-column chunk c8 = it / 64 (warp-uniform: broadcast gate loads)
         for (int it = tid; it < CH * 8; it += PT) {
-            const int r = it >> 3, c8 = it & 7;
+            const int r = it & 63, c8 = it >> 6;
             float4 t0v = make_float4(0.f, 0.f, 0.f, 0.f), t1v = t0v;
             if ((c8 >> 1) <= (r >> 4)) {
                 const float* tp = tblk(tri(r >> 4, c8 >> 1)) + (r & 15) * BLD + (c8 & 1) * 8;
@@ -379,12 +387,18 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 t1v = *reinterpret_cast<const float4*>(tp + 4);
             }
             const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+            const float4 b0 = *reinterpret_cast<const float4*>(sBeta + 8 * c8);
+            const float4 b1 = *reinterpret_cast<const float4*>(sBeta + 8 * c8 + 4);
+            const float4 be0 = *reinterpret_cast<const float4*>(sBe + 8 * c8);
+            const float4 be1 = *reinterpret_cast<const float4*>(sBe + 8 * c8 + 4);
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float bev[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
             float xu[8], xw[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int cc = 8 * c8 + u;
-                xu[u] = cc <= r ? tv[u] * sBeta[cc] : 0.f;
-                xw[u] = cc <= r ? -tv[u] * sBe[cc] : 0.f;
+                xu[u] = cc <= r ? tv[u] * bv[u] : 0.f;
+                xw[u] = cc <= r ? -tv[u] * bev[u] : 0.f;
             }
             uint4 a, b;
             a.x = pack_bf16(xu[0], xu[1]);
@@ -419,7 +433,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         if (want_t) {
 #pragma unroll
             for (int u4 = 0; u4 < 4; ++u4) {
-                const int it = tid + PT * u4, r = it >> 3, c8 = it & 7;
+                const int it = tid + PT * u4, r = it & 63, c8 = it >> 6;  // as the staging above
 #pragma unroll
                 for (int u = 0; u < 8; ++u) tkeep[8 * u4 + u] = 0.f;
                 if ((c8 >> 1) <= (r >> 4)) {
@@ -440,7 +454,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         if (want_t) {
 #pragma unroll
             for (int u4 = 0; u4 < 4; ++u4) {
-                const int it = tid + PT * u4, r = it >> 3, c8 = it & 7;
+                const int it = tid + PT * u4, r = it & 63, c8 = it >> 6;
                 uint4 q4;
                 q4.x = pack_bf16(tkeep[8 * u4 + 0], tkeep[8 * u4 + 1]);
                 q4.y = pack_bf16(tkeep[8 * u4 + 2], tkeep[8 * u4 + 3]);
