@@ -130,10 +130,15 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def make_step(inp, dev, backward, save_states=False):
+def make_step(inp, dev, backward, save_states=False, d=None, stream=None):
+    """One step on device inputs (copied from inp, or the given dict d), with its own outputs
+    and workspace; every library call is enqueued on ``stream`` (None = current stream)."""
     from chunked_prefill_gb300 import gdn
-    d = {n: (None if getattr(inp, n) is None else getattr(inp, n).to(dev).contiguous())
-         for n in ("q", "k", "v", "g", "beta", "h0", "dO", "dht")}
+    if d is None:
+        d = {n: (None if getattr(inp, n) is None else getattr(inp, n).to(dev).contiguous())
+             for n in ("q", "k", "v", "g", "beta", "h0", "dO", "dht")}
+    else:
+        d = {n: d.get(n) for n in ("q", "k", "v", "g", "beta", "h0", "dO", "dht")}
     cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
     cu_host = inp.cu_seqlens
     o = torch.empty_like(d["v"])
@@ -159,19 +164,20 @@ def make_step(inp, dev, backward, save_states=False):
             gdn.gdn_chunk_fwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale,
                                     h0=d["h0"], cu_seqlens=cu, cu_seqlens_host=cu_host,
                                     want_g_cum=False, want_A=False, workspace=ws_b, o=o, ht=ht,
-                                    h=hbuf)
+                                    h=hbuf, stream=stream)
             gdn.gdn_chunk_bwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, hbuf,
                                     ws_b, d["dO"], dht=d["dht"], cu_seqlens=cu,
-                                    cu_seqlens_host=cu_host, out=bufs)
+                                    cu_seqlens_host=cu_host, out=bufs, stream=stream)
         return step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs
 
     def step():
         gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, h0=d["h0"],
-                          cu_seqlens=cu, cu_seqlens_host=cu_host, o=o, ht=ht, workspace=ws_f)
+                          cu_seqlens=cu, cu_seqlens_host=cu_host, o=o, ht=ht, workspace=ws_f,
+                          stream=stream)
         if backward:
             gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, d["dO"],
                               h0=d["h0"], dht=d["dht"], cu_seqlens=cu, cu_seqlens_host=cu_host,
-                              workspace=ws_b, out=bufs)
+                              workspace=ws_b, out=bufs, stream=stream)
     return step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs
 
 
@@ -189,55 +195,56 @@ def time_steps(step, K, flush):
 
 
 def e2e_run(inp, dev, K, W, backward, save_states=False):
-    """The same step through the public API with HOST buffers: pinned host inputs copied in,
-    the call, the result copied out, all inside the timed region."""
-    from chunked_prefill_gb300 import gdn
+    """The same step through the public API with HOST buffers: every step copies its inputs
+    from pinned host memory, runs the call and copies its results back to pinned host memory,
+    all inside the timed region.  Steps are pipelined the way a host-fed loop would run them:
+    host-to-device copies on one stream, the calls on a second, device-to-host copies on a
+    third, two device buffer sets alternating between steps, with events ordering each
+    buffer's reuse; the clock runs from the first copy in to the last copy out."""
     names = ["q", "k", "v", "g", "beta", "h0"] + (["dO", "dht"] if backward else [])
     host = {n: getattr(inp, n).pin_memory() for n in names if getattr(inp, n) is not None}
-    devb = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
-    step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs = make_step(inp, dev, backward)
-    outs = [o, ht] if not backward else [o, ht] + [b for b in bufs if b is not None]
-    hbuf = None
-    if backward and save_states:
-        nchunks = gdn.gdn_chunk_layout(gdn.Problem(d["q"], d["v"], inp.scale, cu, cu_host))[1]
-        hbuf = torch.empty(nchunks, d["v"].shape[2], 128, 128, dtype=d["v"].dtype, device=dev)
-    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    NB = 2
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    sets = []
+    for _ in range(NB):
+        devb = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+        step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs = make_step(inp, dev, backward, save_states,
+                                                                  d=devb, stream=s_run)
+        outs = [o, ht] if not backward else [o, ht] + [x for x in bufs if x is not None]
+        host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+        ev = {k: torch.cuda.Event() for k in ("in", "run", "out")}
+        sets.append((devb, step, outs, host_out, ev))
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    d2h = sum(t.numel() * t.element_size() for t in sets[0][3])
 
-    def e2e_step():
-        for n, t in host.items():
-            devb[n].copy_(t, non_blocking=True)
-        if hbuf is not None:
-            gdn.gdn_chunk_fwd_saved(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"],
-                                    inp.scale, h0=devb.get("h0"), cu_seqlens=cu,
-                                    cu_seqlens_host=cu_host, want_g_cum=False, want_A=False,
-                                    workspace=ws_b, o=o, ht=ht, h=hbuf)
-            gdn.gdn_chunk_bwd_saved(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"],
-                                    inp.scale, hbuf, ws_b, devb["dO"], dht=devb.get("dht"),
-                                    cu_seqlens=cu, cu_seqlens_host=cu_host, out=bufs)
+    def run(i):
+        devb, step, outs, host_out, ev = sets[i % NB]
+        if i >= NB:
+            s_in.wait_event(ev["run"])     # the call of step i - NB has read these inputs
+            s_run.wait_event(ev["out"])    # and its results have left
+        with torch.cuda.stream(s_in):
+            for n, t in host.items():
+                devb[n].copy_(t, non_blocking=True)
+        ev["in"].record(s_in)
+        s_run.wait_event(ev["in"])
+        step()
+        ev["run"].record(s_run)
+        s_out.wait_event(ev["run"])
+        with torch.cuda.stream(s_out):
             for src, dst in zip(outs, host_out):
                 dst.copy_(src, non_blocking=True)
-            return
-        gdn.gdn_chunk_fwd(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"], inp.scale,
-                          h0=devb.get("h0"), cu_seqlens=cu, cu_seqlens_host=cu_host, o=o, ht=ht,
-                          workspace=ws_f)
-        if backward:
-            gdn.gdn_chunk_bwd(devb["q"], devb["k"], devb["v"], devb["g"], devb["beta"], inp.scale,
-                              devb["dO"], h0=devb.get("h0"), dht=devb.get("dht"), cu_seqlens=cu,
-                              cu_seqlens_host=cu_host, workspace=ws_b, out=bufs)
-        for src, dst in zip(outs, host_out):
-            dst.copy_(src, non_blocking=True)
+        ev["out"].record(s_out)
 
-    for _ in range(W):
-        e2e_step()
-    torch.cuda.synchronize()
+    for i in range(W):
+        run(i)
+    torch.cuda.synchronize(dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(K):
-        e2e_step()
-    b.record()
-    torch.cuda.synchronize()
+    a.record(s_in)
+    for i in range(K):
+        run(i)
+    s_out.wait_event(sets[(K - 1) % NB][4]["out"])
+    b.record(s_out)
+    torch.cuda.synchronize(dev)
     return a.elapsed_time(b) / K, h2d, d2h
 
 
@@ -569,7 +576,9 @@ def main():
         e2e_ms, h2d, d2h = e2e_run(inp, dev, args.steps, args.warmup, w.backward, save)
         e2e_ms = max_over_ranks(e2e_ms, world)
         line["e2e"] = {"value": world * tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                       "mode": "pinned host buffers; copies in, calls and copies out on three "
+                               "streams, two device buffer sets alternating between steps"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, toks, dt, thr, n = oracle_sample(inp, 10.0, w.backward)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
