@@ -265,13 +265,8 @@ void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Proble
     P.scale = p->scale;
 }
 
-// bf16 runs on the tcgen05 kernels; GDN_FWD_PATH=mma selects the mma.sync kernels instead
-// (kept for comparison benchmarks), and the fp32 test mode always uses the CUDA-core kernels.
-bool use_tensor_cores(int dtype) {
-    if (dtype != GDN_BF16) return false;
-    const char* env = getenv("GDN_FWD_PATH");
-    return !(env && strcmp(env, "mma") == 0);
-}
+// bf16 runs on the tcgen05 kernels; the fp32 test mode on the CUDA-core kernels.
+bool use_tensor_cores(int dtype) { return dtype == GDN_BF16; }
 
 gdn_status check_ptrs(std::initializer_list<const void*> required,
                       std::initializer_list<const void*> optional) {

@@ -695,7 +695,9 @@ static cudaError_t launch_fwd_t(const Problem& P, bool hist, cudaStream_t st) {
 }
 
 cudaError_t launch_fwd(const Problem& P, int dtype, bool hist, cudaStream_t st) {
-    if (dtype == 0) return launch_fwd_t<__nv_bfloat16, 64>(P, hist, st);
+    // bf16 problems run on the tensor-core kernels (launch_fwd_tc); this path is the fp32
+    // test mode
+    if (dtype != 1) return cudaErrorInvalidValue;
     return launch_fwd_t<float, 32>(P, hist, st);
 }
 
