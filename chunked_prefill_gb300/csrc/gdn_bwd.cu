@@ -490,28 +490,56 @@ __device__ __forceinline__ float col_sum8(float v) {
 }
 
 template <typename Op, int C, int NTL>
-__global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
+__global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t items) {
     using S = LocSmem<Op, C>;
     constexpr int LDK = S::LDK, LDC = S::LDC, LDF = S::LDF;
     extern __shared__ __align__(128) char smem[];
     const Problem& P = B.f;
-    const int gch = blockIdx.x, j = blockIdx.y;
-    // chunk -> (sequence, local chunk) by binary search over chunk_off
-    int lo = 0, hi = P.N - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (P.plan.chunk_off[mid] <= gch) lo = mid;
-        else hi = mid - 1;
+    // One CTA per SM walks the (chunk, v-head) items item = chunk Hv + v-head with a stride of
+    // the grid.  bf16: while an item's later phases run, the tiles of the CTA's next item
+    // that land in regions those phases no longer read (P, W', dh, h, V, Q) are requested
+    // asynchronously, so that only K, T and TU are waited for at the next item's start.
+    struct Item {
+        int gch, j, s, ch, c, qh;
+        int64_t t0, t1, tc;
+    };
+    auto locate = [&](int64_t item, Item& x) -> bool {
+        x.gch = int(item / P.Hv);
+        x.j = int(item % P.Hv);
+        x.qh = x.j / (P.Hv / P.Hqk);
+        if (x.gch >= P.plan.chunk_off[P.N]) return false;
+        int lo = 0, hi = P.N - 1;  // chunk -> (sequence, local chunk) by binary search
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.plan.chunk_off[mid] <= x.gch) lo = mid;
+            else hi = mid - 1;
+        }
+        x.s = lo;
+        x.ch = x.gch - P.plan.chunk_off[x.s];
+        seq_range(P, x.s, x.t0, x.t1);
+        x.tc = x.t0 + int64_t(x.ch) * C;
+        if (x.tc >= x.t1) return false;
+        x.c = int((x.t1 - x.tc) < int64_t(C) ? (x.t1 - x.tc) : int64_t(C));
+        return true;
+    };
+    bool pre = false;  // this item's P, W', dh, h, V, Q were requested during the previous one
+#pragma unroll 1
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    Item cur, nxt;
+    if (!locate(item, cur)) {
+        cp_async_wait_all();  // nothing may still land in the tiles
+        __syncthreads();
+        pre = false;
+        continue;
     }
-    const int s = lo;
-    if (gch >= P.plan.chunk_off[P.N]) return;
-    const int ch = gch - P.plan.chunk_off[s];
-    int64_t t0, t1;
-    seq_range(P, s, t0, t1);
-    const int64_t tc = t0 + int64_t(ch) * C;
-    if (tc >= t1) return;
-    const int c = int((t1 - tc) < int64_t(C) ? (t1 - tc) : int64_t(C));
-
+    const bool has_next = S::BF && item + gridDim.x < items && locate(item + gridDim.x, nxt);
+    const int gch = cur.gch, j = cur.j, s = cur.s, ch = cur.ch;
+    const int64_t t0 = cur.t0, t1 = cur.t1, tc = cur.tc;
+    (void)s;
+    (void)ch;
+    (void)t0;
+    (void)t1;
+    const int c = cur.c;
     Op* tK = reinterpret_cast<Op*>(smem + S::oK);
     Op* tQ = reinterpret_cast<Op*>(smem + S::oQ);
     Op* tDW = tQ;
@@ -561,39 +589,63 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
     const int r0 = m0 + gq, r1 = m0 + gq + 8;
 
     LTRACE(0);
+    // asynchronous tile requests of an item (bf16): K, Q, V rows (past the sequence end zero),
+    // the tiles of its chunk record (unswizzled), its entering state h and gradient dh
+    auto req_rows = [&](const Item& x, Op* dst, const Op* base, int64_t stride) {
+        for (int idx = tid; idx < C * 16; idx += NTL) {
+            const int r = idx >> 4, cv = idx & 15;
+            const bool ok = r < x.c;
+            cp_async16(dst + r * LDK + cv * 8, base + (ok ? r : 0) * stride + cv * 8, ok);
+        }
+    };
+    auto kq_of = [&](const Item& x, const void* t) {
+        return reinterpret_cast<const Op*>(t) + x.qh * KD + x.tc * qk_stride;
+    };
+    auto v_of = [&](const Item& x) { return reinterpret_cast<const Op*>(P.v) + x.j * VD + x.tc * v_stride; };
+    auto rec_of = [&](const Item& x) {
+        return static_cast<const unsigned char*>(P.prep) + (int64_t(x.gch) * Hv + x.j) * P.prep_stride;
+    };
+    auto req_w = [&](const Item& x) {
+        const unsigned char* rec = rec_of(x);
+        for (int q = tid; q < 1024; q += NTL) {
+            const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
+            cp_async16(tW + r * LDK + blk * 64 + cc * 8, rec + PREP_W + q * 16, true);
+        }
+    };
+    auto req_tile = [&](const Item& x, Op* dst, int off) {
+        const unsigned char* rec = rec_of(x);
+        for (int q = tid; q < 512; q += NTL) {
+            const int r = q >> 3, cc = (q & 7) ^ (r & 7);
+            cp_async16(dst + r * LDC + cc * 8, rec + off + q * 16, true);
+        }
+    };
+    auto req_state = [&](const Op* src, Op* dst) {
+        for (int idx = tid; idx < KD * 16; idx += NTL) {
+            const int r = idx >> 4, cv = idx & 15;
+            cp_async16(dst + r * LDK + cv * 8, src + r * VD + cv * 8, true);
+        }
+    };
+    auto hist_of = [&](const void* base, const Item& x) {
+        return reinterpret_cast<const Op*>(base) + (int64_t(x.gch) * Hv + x.j) * KVN;
+    };
+
     // ---- phase 1: tiles, gates, K K^T, Q K^T, A, P, T
     if (S::BF) {
         // bf16: every tile the first phases read is requested at once (asynchronous copies):
-        // K, Q, V (rows past the sequence end zero), the chunk record (W' -> its tile, P, T,
-        // TU -> the dQk tile, free until phase 3), the entering state h and the gradient dh
-        const Op* kg = reinterpret_cast<const Op*>(P.k) + qh * KD + tc * qk_stride;
-        const Op* qg = reinterpret_cast<const Op*>(P.q) + qh * KD + tc * qk_stride;
-        const Op* vg = reinterpret_cast<const Op*>(P.v) + j * VD + tc * v_stride;
-        for (int idx = tid; idx < C * 16; idx += NTL) {
-            const int r = idx >> 4, cv = idx & 15;
-            const bool ok = r < c;
-            const int rr = ok ? r : 0;
-            cp_async16(tK + r * LDK + cv * 8, kg + rr * qk_stride + cv * 8, ok);
-            cp_async16(tQ + r * LDK + cv * 8, qg + rr * qk_stride + cv * 8, ok);
-            cp_async16(tV + r * LDK + cv * 8, vg + rr * v_stride + cv * 8, ok);
+        // K, Q, V, the chunk record (W' -> its tile, P, T, TU -> the dQk tile, free until
+        // phase 3), the entering state h and the gradient dh -- all but K, T and TU already
+        // requested during the previous item when there was one
+        if (!pre) {
+            req_rows(cur, tQ, kq_of(cur, P.q), qk_stride);
+            req_rows(cur, tV, v_of(cur), v_stride);
+            req_w(cur);
+            req_tile(cur, oP, PREP_P);
+            req_state(hsrc, const_cast<Op*>(sH));
+            req_state(dhsrc, const_cast<Op*>(sDH));
         }
-        const unsigned char* rec = static_cast<const unsigned char*>(P.prep) + (int64_t(gch) * Hv + j) * P.prep_stride;
-        for (int q = tid; q < 1024 + 3 * 512; q += NTL) {
-            if (q < 1024) {
-                const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
-                cp_async16(tW + r * LDK + blk * 64 + cc * 8, rec + PREP_W + q * 16, true);
-            } else {
-                const int t3 = (q - 1024) >> 9, q2 = (q - 1024) & 511, r = q2 >> 3, cc = (q2 & 7) ^ (r & 7);
-                Op* dst = t3 == 0 ? oP : (t3 == 1 ? oT : oX1);
-                const int off = t3 == 0 ? PREP_P : (t3 == 1 ? PREP_T : PREP_TU);
-                cp_async16(dst + r * LDC + cc * 8, rec + off + q2 * 16, true);
-            }
-        }
-        for (int idx = tid; idx < KD * 16; idx += NTL) {
-            const int r = idx >> 4, cv = idx & 15;
-            cp_async16(const_cast<Op*>(sH) + r * LDK + cv * 8, hsrc + r * VD + cv * 8, true);
-            cp_async16(const_cast<Op*>(sDH) + r * LDK + cv * 8, dhsrc + r * VD + cv * 8, true);
-        }
+        req_rows(cur, tK, kq_of(cur, P.k), qk_stride);
+        req_tile(cur, oT, PREP_T);
+        req_tile(cur, oX1, PREP_TU);
         cp_async_commit();
     } else {
         load_rows<Op, C>(tK, LDK, reinterpret_cast<const Op*>(P.k) + qh * KD + tc * qk_stride, qk_stride, c);
@@ -787,6 +839,10 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
         sDg[i] += v;
     }
     __syncthreads();
+    if (has_next) {  // P is no longer read: the next item's P
+        req_tile(nxt, oP, PREP_P);
+        cp_async_commit();
+    }
 
     LTRACE(3);
     // ---- phase 4: dQ = scale diag(e) dO h^T + dQk K; e_i <dOs_i, (Q h)_i>; <dh, h>
@@ -848,6 +904,10 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
         sRed[8] = hd;
     }
     __syncthreads();
+    if (has_next) {  // dO is no longer read: the next item's W' into its tile
+        req_w(nxt);
+        cp_async_commit();
+    }
 
     LTRACE(4);
     // ---- phase 5: dK = dQk^T Q + diag(kd) (V' dh^T) (+ later terms); r_i
@@ -889,6 +949,10 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
         sDg[C - 1] += rsum + sE[C - 1] * sRed[8];
     }
     __syncthreads();
+    if (has_next) {  // dh is no longer read: the next item's dh
+        req_state(hist_of(B.dhist, nxt), const_cast<Op*>(sDH));
+        cp_async_commit();
+    }
 
     LTRACE(5);
     // ---- phase 6: dW = -dV' h^T -> tile (reuses the Q tile)
@@ -905,6 +969,10 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
         }
     }
     __syncthreads();
+    if (has_next) {  // h is no longer read: the next item's h
+        req_state(hist_of(P.hist, nxt), const_cast<Op*>(sH));
+        cp_async_commit();
+    }
 
     LTRACE(6);
     // ---- phase 7: dT = (dW K^T) diag(beta e) + (dV' V^T) diag(beta) -> fA (fp32) -> oX2
@@ -973,6 +1041,11 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
         sDg[i] += sBeta[i] * sE[i] * tw;
     }
     __syncthreads();
+    if (has_next) {  // V and dW (the Q tile) are no longer read: the next item's V and Q
+        req_rows(nxt, tV, v_of(nxt), v_stride);
+        req_rows(nxt, tQ, kq_of(nxt, P.q), qk_stride);
+        cp_async_commit();
+    }
 
     LTRACE(8);
     // ---- phase 9: Z = dT T^T; dA = strictly-lower(-T^T Z); dB = diag(beta) dA * Dm
@@ -1004,8 +1077,10 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
                 const float dav = (rr > cj) ? -da[n][e] : 0.f;
                 const float db = fDB[rr * LDF + cj];
                 aa[e] = dav * sBeta[rr] * db;                 // dA * A
-                // dB = beta_i dA_ij Dm_ij (dav is zero on and above the diagonal)
-                fT[rr * LDF + cj] = (rr > cj) ? sBeta[rr] * dav * expf(sGam[rr] - sGam[cj]) : 0.f;
+                // dB = beta_i dA_ij Dm_ij (dav is zero on and above the diagonal), in place of
+                // the Dm * Bm entry just read (the dh tile region may already hold the next
+                // item's dh)
+                fDB[rr * LDF + cj] = (rr > cj) ? sBeta[rr] * dav * expf(sGam[rr] - sGam[cj]) : 0.f;
                 if (e < 2) rs0 += dav * db; else rs1 += dav * db;
             }
             ra0 += aa[0] + aa[1];
@@ -1046,7 +1121,7 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
     // (dB + dB^T) as an MMA operand
     for (int idx = tid; idx < C * C; idx += NTL) {
         const int i = idx / C, jj = idx % C;
-        oX2[i * LDC + jj] = from_f<Op>(fT[i * LDF + jj] + fT[jj * LDF + i]);
+        oX2[i * LDC + jj] = from_f<Op>(fDB[i * LDF + jj] + fDB[jj * LDF + i]);
     }
     __syncthreads();
 
@@ -1094,6 +1169,9 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B) {
                 B.dbeta[(tc + r) * Hv + j] = sDb[r];
             }
         }
+    }
+    pre = has_next;
+    __syncthreads();  // the next item re-initialises the gate and partial-sum arrays
     }
 }
 
@@ -1166,7 +1244,9 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
     timing_end(st);
     if (P.total_chunks > 0) {
         timing_begin("bwd_local", st);
-        k_bwd_local<Op, C, NTL><<<dim3(P.total_chunks, P.Hv), NTL, LS::bytes, st>>>(B);
+        const int64_t items = int64_t(P.total_chunks) * P.Hv;
+        const int grid = int(std::min<int64_t>(items, sm_count()));  // one CTA per SM, persistent
+        k_bwd_local<Op, C, NTL><<<grid, NTL, LS::bytes, st>>>(B, items);
         timing_end(st);
     }
     if (B.dqp) {
