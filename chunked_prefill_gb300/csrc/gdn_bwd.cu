@@ -1211,8 +1211,10 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
     e = cudaFuncSetAttribute(k_bwd_phase_c<Op, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SS::bytes));
     if (e != cudaSuccess) return e;
     constexpr int NTL = NT;
-    e = cudaFuncSetAttribute(k_bwd_local<Op, C, NTL>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(LS::bytes));
-    if (e != cudaSuccess) return e;
+    if constexpr (sizeof(Op) != 2) {
+        e = cudaFuncSetAttribute(k_bwd_local<Op, C, NTL>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(LS::bytes));
+        if (e != cudaSuccess) return e;
+    }
     const int fix_smem = (KD * 129 + KD * 8) * 4;
     e = cudaFuncSetAttribute(k_bwd_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, fix_smem);
     if (e != cudaSuccess) return e;
@@ -1244,9 +1246,14 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
     timing_end(st);
     if (P.total_chunks > 0) {
         timing_begin("bwd_local", st);
-        const int64_t items = int64_t(P.total_chunks) * P.Hv;
-        const int grid = int(std::min<int64_t>(items, sm_count()));  // one CTA per SM, persistent
-        k_bwd_local<Op, C, NTL><<<grid, NTL, LS::bytes, st>>>(B, items);
+        if constexpr (TC) {
+            e = launch_bwd_local_tc(B, T_total, st);
+            if (e != cudaSuccess) return e;
+        } else {
+            const int64_t items = int64_t(P.total_chunks) * P.Hv;
+            const int grid = int(std::min<int64_t>(items, sm_count()));  // one CTA per SM, persistent
+            k_bwd_local<Op, C, NTL><<<grid, NTL, LS::bytes, st>>>(B, items);
+        }
         timing_end(st);
     }
     if (B.dqp) {

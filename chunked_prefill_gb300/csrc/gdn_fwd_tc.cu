@@ -1374,7 +1374,9 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_bwd_c(BwdProblem B, const __grid_
     tc_bwd_scan<true>(B, maps.f, &maps.dO, sm, j, t0, t1, cb, ce, x0, x_out, P.plan.chunk_off[s]);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* p = nullptr;
@@ -1387,7 +1389,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [T_total, H, 128] bf16 viewed as (d, head, token); box 64 x 1 x 64, 128-byte swizzle
 bool make_map(CUtensorMap* m, const void* base, int H, int64_t T_total) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -1400,7 +1401,18 @@ bool make_map(CUtensorMap* m, const void* base, int H, int64_t T_total) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
+bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, cuuint64_t(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {cuuint64_t(128 * 2)};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 
 #ifdef GDN_TRACE
 extern "C" int gdn_debug_trace(unsigned long long* out) {

@@ -32,6 +32,12 @@ void launch_bwd_fixup_tc(const BwdProblem& B, cudaStream_t st);
 struct TcMaps {
     CUtensorMap k, q, v;
 };
+// [T_total, H, 128] bf16 viewed as (d, head, token), box 64 x 1 x 64 (one 64-column block of
+// a 64-token tile), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int H, int64_t T_total);
+// [rows, 128] bf16 (rows of 256 bytes), box 64 x 128 (one 64-column block of a 128-row
+// tile), 128-byte swizzle.
+bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows);
 // Chunk-parallel preparation of the tensor-core path into P.prep: per (chunk, v-head) one
 // record of P.prep_stride bytes holding W' = -T diag(beta e) K (bf16 64 x 128, two
 // 128-byte-swizzled 64-column blocks), TU = T diag(beta) and P (bf16 64 x 64, swizzled), and
@@ -46,6 +52,11 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
 // Tensor-core reverse dh scan of the backward (bf16; needs the forward's chunk records):
 // which = 0 first context-parallel phase, 1 the rerun storing dh per chunk.
 cudaError_t launch_bwd_scan_tc(const BwdProblem& B, int which, int64_t T_total, cudaStream_t st);
+
+// Tensor-core local gradients of the backward (bf16): one persistent CTA per SM over the
+// (chunk, v-head) items; needs the chunk records (with T), the states per chunk in B.f.hist and
+// the gradients per chunk in B.dhist.
+cudaError_t launch_bwd_local_tc(const BwdProblem& B, int64_t T_total, cudaStream_t st);
 
 // Backward: reverse dh scan (with the same context-parallel segments as the forward) and
 // the chunk-parallel local gradients; expects the forward recompute (states per chunk in
