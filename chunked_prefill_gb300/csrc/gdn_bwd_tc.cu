@@ -87,10 +87,18 @@ constexpr int F_PAR = 1728;  // [4][64]  row sums of dA * A (by column group)
 constexpr int F_PAC = 1984;  // [2][64]  column sums of dA * A
 constexpr int F_PRS = 2112;  // [4][64]  row sums of dA * (Dm * Bm)
 constexpr int F_RED = 2368;  // [16]     <dh, h> by warp
-constexpr int F_END = 2384;
+constexpr int F_EI = 2384;   // [64]     exp(-gamma)
+constexpr int F_PW = 2448;   // (int)    1: exp(gamma_i - gamma_j) formed directly (extreme decay)
+constexpr int F_END = 2452;
 constexpr uint32_t L_BAR = L_SM + F_END * 4;
+// copies landed (B_*); products done (M_*: M_1 dO^T P, M_10 dh^T K^T, M_2 h dO^T, M_11 K K^T,
+// committed by whichever thread issued them)
 enum LocBar { B_K = 0, B_Q, B_V, B_DO, B_W, B_TU, B_P, B_T, B_H, B_DH, NLD,
-              M_0 = NLD, M_1, M_2, M_3, M_4, M_5, M_6, M_7, M_8, M_9, M_DRAIN, NBAR };
+              M_0 = NLD, M_1, M_2, M_3, M_4, M_5, M_6, M_7, M_8, M_9, M_10, M_11, M_DRAIN, NBAR };
+// The thread that requests every copy and issues every product: lane 0 of warp 2, which has no
+// share in the 64-row epilogues, so that the next item's first products (issued there) cost
+// no epilogue time.
+constexpr int ISS = 64;
 constexpr uint32_t L_SLOT = L_BAR + NBAR * 8;  // TMEM base address, error word
 constexpr uint32_t L_END = L_SLOT + 16;
 constexpr uint32_t LOC_SMEM = L_END + 1024;    // + alignment slack
@@ -227,6 +235,8 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
     float* sKd = sF + F_KD;
     float* sBeta = sF + F_BETA;
     float* sBe = sF + F_BE;
+    float* sEi = sF + F_EI;
+    int* sPw = reinterpret_cast<int*>(sF + F_PW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L_BAR);
     uint32_t* slot = reinterpret_cast<uint32_t*>(sm + L_SLOT);
     int* errflag = reinterpret_cast<int*>(sm + L_SLOT + 4);
@@ -238,10 +248,9 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
     const float sc = P.scale;
     const int64_t qk_stride = int64_t(Hqk) * KD, v_stride = int64_t(Hv) * VD;
     const uint32_t base = smem_addr(sm);
-    const uint32_t aK = base + L_K, aQ = base + L_Q, aV = base + L_V, aDO = base + L_DO, aW = base + L_W,
-                   aTU = base + L_TU, aP = base + L_P, aT = base + L_T, aDT = base + L_DT,
-                   aQK = base + L_QK, aDV = base + L_DV, aH = base + L_H, aDH = base + L_DH,
-                   aSTG = base + L_STG;
+    const uint32_t aV = base + L_V, aDO = base + L_DO, aW = base + L_W, aTU = base + L_TU, aP = base + L_P,
+                   aT = base + L_T, aDT = base + L_DT, aQK = base + L_QK, aDV = base + L_DV, aH = base + L_H,
+                   aDH = base + L_DH, aSTG = base + L_STG;
 
     if (tid == 0) {
         for (int b = 0; b < NBAR; ++b) mbar_init(&bars[b], 1);
@@ -274,7 +283,19 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         return true;
     };
 
-    // ---- copies (thread 0 only); ldn counts the phases requested on each load barrier
+    // Tensor-memory slots of an item: an odd item swaps {s0, s1} with {s6, s7}, so that the next
+    // item's first products can go to the slots this item no longer uses while its last product
+    // and the dK epilogue still hold s0, s1 (or s6, s7) and s5.  K and Q trade shared-memory
+    // regions the same way (K of an even item in the K region), so that the next item's K can
+    // land while the last product still reads this item's K.
+    auto slot_v = [](uint32_t par) { return par ? SL6 : SL0; };
+    auto slot_a = [](uint32_t par) { return par ? SL7 : SL1; };
+    auto slot_u = [](uint32_t par) { return par ? SL0 : SL6; };
+    auto slot_z = [](uint32_t par) { return par ? SL1 : SL7; };
+    auto kreg_of = [](uint32_t par) { return par ? L_Q : L_K; };
+    auto qreg_of = [](uint32_t par) { return par ? L_K : L_Q; };
+
+    // ---- copies and products (thread ISS only); ldn counts the phases requested on each load barrier
     int ldn[NLD];
 #pragma unroll
     for (int b = 0; b < NLD; ++b) ldn[b] = 0;
@@ -285,29 +306,72 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         mbar_expect_tx(&bars[b], 16384);
         tma_load_3d(sm + off, m, &bars[b], 0, head, int(tcx));
         tma_load_3d(sm + off + 8192, m, &bars[b], 64, head, int(tcx));
+        ++ldn[b];
     };
     auto req_rec = [&](int b, uint32_t off, const Item& x, int roff, uint32_t bytes) {
         mbar_expect_tx(&bars[b], bytes);
         bulk_load(sm + off, rec_of(x) + roff, bytes, &bars[b]);
+        ++ldn[b];
     };
     auto req_state = [&](int b, uint32_t off, const CUtensorMap* m, const Item& x) {
         const int row = (x.gch * Hv + x.j) * 128;
         mbar_expect_tx(&bars[b], 32768);
         tma_load_2d(sm + off, m, &bars[b], 0, row);
         tma_load_2d(sm + off + 16384, m, &bars[b], 64, row);
+        ++ldn[b];
     };
-    auto req_K = [&](const Item& x) { req_rows(B_K, L_K, &maps.k, x.qh, x.tc); ++ldn[B_K]; };
-    auto req_Q = [&](const Item& x) { req_rows(B_Q, L_Q, &maps.q, x.qh, x.tc); ++ldn[B_Q]; };
-    auto req_V = [&](const Item& x) { req_rows(B_V, L_V, &maps.v, x.j, x.tc); ++ldn[B_V]; };
-    auto req_DO = [&](const Item& x) { req_rows(B_DO, L_DO, &maps.dO, x.j, x.tc); ++ldn[B_DO]; };
-    auto req_W = [&](const Item& x) { req_rec(B_W, L_W, x, PREP_W, 16384); ++ldn[B_W]; };
-    auto req_TU = [&](const Item& x) { req_rec(B_TU, L_TU, x, PREP_TU, 8192); ++ldn[B_TU]; };
-    auto req_P = [&](const Item& x) { req_rec(B_P, L_P, x, PREP_P, 8192); ++ldn[B_P]; };
-    auto req_T = [&](const Item& x) { req_rec(B_T, L_T, x, PREP_T, 8192); ++ldn[B_T]; };
-    auto req_H = [&](const Item& x) { req_state(B_H, L_H, &maps.h, x); ++ldn[B_H]; };
-    auto req_DH = [&](const Item& x) { req_state(B_DH, L_DH, &maps.dh, x); ++ldn[B_DH]; };
+    auto req_K = [&](const Item& x, uint32_t off) { req_rows(B_K, off, &maps.k, x.qh, x.tc); };
+    auto req_Q = [&](const Item& x, uint32_t off) { req_rows(B_Q, off, &maps.q, x.qh, x.tc); };
+    auto req_V = [&](const Item& x) { req_rows(B_V, L_V, &maps.v, x.j, x.tc); };
+    auto req_DO = [&](const Item& x) { req_rows(B_DO, L_DO, &maps.dO, x.j, x.tc); };
+    auto req_W = [&](const Item& x) { req_rec(B_W, L_W, x, PREP_W, 16384); };
+    auto req_TU = [&](const Item& x) { req_rec(B_TU, L_TU, x, PREP_TU, 8192); };
+    auto req_P = [&](const Item& x) { req_rec(B_P, L_P, x, PREP_P, 8192); };
+    auto req_T = [&](const Item& x) { req_rec(B_T, L_T, x, PREP_T, 8192); };
+    auto req_H = [&](const Item& x) { req_state(B_H, L_H, &maps.h, x); };
+    auto req_DH = [&](const Item& x) { req_state(B_DH, L_DH, &maps.dh, x); };
+    // the first products of an item in two groups: V'^T, dO^T P, h dO^T (need V, TU, W', h, dO,
+    // P) and dh^T K^T, K K^T (need dh, K)
+    auto issue_A = [&](uint32_t xpar) {
+        const uint32_t s_v = slot_v(xpar), s_a = slot_a(xpar);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) mma_bf16(tm + s_v, dM_(aV, 8192, s), dK_(aTU, 64, s), ID_MK, s > 0);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mma_bf16(tm + s_v, dM_(aH, 16384, s), dK_(aW, 64, s), ID_MK, 1u);
+        commit(&bars[M_0]);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) mma_bf16(tm + s_a, dM_(aDO, 8192, s), dM_(aP, 8192, s), ID_MM, s > 0);
+        commit(&bars[M_1]);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mma_bf16(tm + SL3, dK_(aH, 128, s), dK_(aDO, 64, s), ID_KK, s > 0);
+        commit(&bars[M_2]);
+    };
+    auto issue_B = [&](uint32_t xpar) {
+        const uint32_t xK = base + kreg_of(xpar);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mma_bf16(tm + SL2, dM_(aDH, 16384, s), dK_(xK, 64, s), ID_MK, s > 0);
+        commit(&bars[M_10]);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mma_bf16(tm + SL4, dK_(xK, 64, s), dK_(xK, 64, s), ID_KK, s > 0);
+        commit(&bars[M_11]);
+    };
+    // (issuer) copies of the next item landed within limit_ns (polling; no error when not)
+    auto landed = [&](uint32_t npar, bool group_a, uint64_t limit_ns) -> bool {
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            const bool in = group_a ? (mbar_test(&bars[B_V], npar) && mbar_test(&bars[B_TU], npar) &&
+                                       mbar_test(&bars[B_W], npar) && mbar_test(&bars[B_H], npar) &&
+                                       mbar_test(&bars[B_DO], npar) && mbar_test(&bars[B_P], npar))
+                                    : (mbar_test(&bars[B_DH], npar) && mbar_test(&bars[B_K], npar));
+            if (in) return true;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    };
 
-    bool pre = false;    // the current item's tiles were requested during the previous one
+    bool pre = false;             // (issuer) the current item's tiles were requested during the previous one
+    bool eA = false, eB = false;  // (issuer) its first product groups were issued during the previous one
+    float ngv[2] = {0.f, 0.f}, nbv[2] = {0.f, 0.f};  // (warp 0) the next item's g, beta
+    bool have_ng = false;
     bool failed = false;
     uint32_t n = 0;      // items done (parity of every barrier phase)
 #pragma unroll 1
@@ -315,16 +379,22 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         Item cur, nxt;
         if (!locate(item, cur)) {
             pre = false;
+            eA = eB = false;
+            have_ng = false;
             continue;
         }
         const bool has_next = item + gridDim.x < items && locate(item + gridDim.x, nxt);
         const uint32_t par = n & 1;
         TTRACE(0);
+        const uint32_t sv = slot_v(par), sa = slot_a(par), su = slot_u(par), sz = slot_z(par);
+        const uint32_t kreg = kreg_of(par), qreg = qreg_of(par);
+        const uint32_t aK = base + kreg, aQ = base + qreg;
         const int j = cur.j, qh = cur.qh, c = cur.c;
         const int64_t tc = cur.tc;
         bool ok = true;
-        if (tid == 0 && !pre) {
-            req_K(cur);
+        bool nA = false, nB = false;  // (issuer) the next item's groups issued during this one
+        if (tid == ISS && !pre) {
+            req_K(cur, kreg);
             req_V(cur);
             req_W(cur);
             req_TU(cur);
@@ -332,7 +402,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             req_DO(cur);
             req_P(cur);
             req_DH(cur);
-            req_Q(cur);
+            req_Q(cur, qreg);
             req_T(cur);
         }
 
@@ -343,8 +413,8 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             for (int u = 0; u < 2; ++u) {
                 const int r = 2 * lane + u;
                 const bool in = r < c;
-                gv[u] = in ? P.g[(tc + r) * Hv + j] : 0.f;
-                bv[u] = in ? P.beta[(tc + r) * Hv + j] : 0.f;
+                gv[u] = have_ng ? ngv[u] : (in ? P.g[(tc + r) * Hv + j] : 0.f);
+                bv[u] = have_ng ? nbv[u] : (in ? P.beta[(tc + r) * Hv + j] : 0.f);
             }
             const float run0 = gv[0], run1 = gv[0] + gv[1];
             float tot = run1;
@@ -365,7 +435,9 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 sKd[r] = expf(last - gm[u]);
                 sBeta[r] = bv[u];
                 sBe[r] = bv[u] * e;
+                sEi[r] = expf(-gm[u]);
             }
+            if (lane == 0) *sPw = (last < -80.f || !(last == last)) ? 1 : 0;
         }
         // a chunk cut by the sequence end: the rows past it belong to the next sequence (or
         // are the fill past the tensor end); zero them in K, Q, V, dO
@@ -388,37 +460,30 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(1);
 
-        // ---- first products (every input tile)
-        if (tid == 0) {
+        // ---- first products (those the previous item did not issue)
+        if (tid == ISS) {
             fence_after_sync();
-            ok = twait(bars, B_V, par, errflag) && twait(bars, B_TU, par, errflag) &&
-                 twait(bars, B_W, par, errflag) && twait(bars, B_H, par, errflag);
-            if (ok) {
-                // V'^T = V^T TU^T + h^T W'^T
-#pragma unroll
-                for (int s = 0; s < 4; ++s) mma_bf16(tm + SL0, dM_(aV, 8192, s), dK_(aTU, 64, s), ID_MK, s > 0);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) mma_bf16(tm + SL0, dM_(aH, 16384, s), dK_(aW, 64, s), ID_MK, 1u);
+            if (!eA) {
+                ok = twait(bars, B_V, par, errflag) && twait(bars, B_TU, par, errflag) &&
+                     twait(bars, B_W, par, errflag) && twait(bars, B_H, par, errflag) &&
+                     twait(bars, B_DO, par, errflag) && twait(bars, B_P, par, errflag);
+                if (ok) {
+                    issue_A(par);
+                } else {
+                    commit(&bars[M_0]);
+                    commit(&bars[M_1]);
+                    commit(&bars[M_2]);
+                }
             }
-            commit(&bars[M_0]);
-            ok = ok && twait(bars, B_DO, par, errflag) && twait(bars, B_P, par, errflag) &&
-                 twait(bars, B_DH, par, errflag) && twait(bars, B_K, par, errflag);
-            if (ok) {
-                // dO^T P, dh^T K^T
-#pragma unroll
-                for (int s = 0; s < 4; ++s) mma_bf16(tm + SL1, dM_(aDO, 8192, s), dM_(aP, 8192, s), ID_MM, s > 0);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) mma_bf16(tm + SL2, dM_(aDH, 16384, s), dK_(aK, 64, s), ID_MK, s > 0);
+            if (!eB) {
+                ok = ok && twait(bars, B_DH, par, errflag) && twait(bars, B_K, par, errflag);
+                if (ok) {
+                    issue_B(par);
+                } else {
+                    commit(&bars[M_10]);
+                    commit(&bars[M_11]);
+                }
             }
-            commit(&bars[M_1]);
-            if (ok) {
-                // (dO h^T)^T = h dO^T, K K^T (lanes 0-63)
-#pragma unroll
-                for (int s = 0; s < 8; ++s) mma_bf16(tm + SL3, dK_(aH, 128, s), dK_(aDO, 64, s), ID_KK, s > 0);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) mma_bf16(tm + SL4, dK_(aK, 64, s), dK_(aK, 64, s), ID_KK, s > 0);
-            }
-            commit(&bars[M_2]);
         }
         __syncwarp();
 
@@ -444,7 +509,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_after_sync();
         {
             float x[16];
-            tmem_ld16(tm + lb + SL0 + c16, x);
+            tmem_ld16(tm + lb + sv + c16, x);
             tmem_ld_wait();
             st_row16(aW, 32 * q4 + lane, c16, x);
         }
@@ -452,11 +517,11 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(3);
-        if (tid == 0) {
+        if (tid == ISS) {
             fence_after_sync();
             // dP = dO V'^T (lanes 0-63), (V' dh^T)^T = dh V'^T
 #pragma unroll
-            for (int s = 0; s < 8; ++s) mma_bf16(tm + SL0, dK_(aDO, 64, s), dM_(aW, 16384, s), ID_KM, s > 0);
+            for (int s = 0; s < 8; ++s) mma_bf16(tm + sv, dK_(aDO, 64, s), dM_(aW, 16384, s), ID_KM, s > 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s) mma_bf16(tm + SL5, dK_(aDH, 128, s), dM_(aW, 16384, s), ID_KM, s > 0);
             commit(&bars[M_3]);
@@ -464,12 +529,12 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         __syncwarp();
 
         // dV'^T = scale dO^T P + dh^T K^T diag(kd) -> bf16 tile
-        ok = lwait(bars, M_1, par, errflag) && ok;
+        ok = lwait(bars, M_1, par, errflag) && lwait(bars, M_10, par, errflag) && ok;
         TTRACE(4);
         fence_after_sync();
         {
             float a[16], b[16];
-            tmem_ld16(tm + lb + SL1 + c16, a);
+            tmem_ld16(tm + lb + sa + c16, a);
             tmem_ld16(tm + lb + SL2 + c16, b);
             tmem_ld_wait();
 #pragma unroll
@@ -486,17 +551,17 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(5);
-        if (tid == 0) {
+        if (tid == ISS) {
             fence_after_sync();
             ok = twait(bars, B_T, par, errflag);
             if (ok) {
                 // dW^T = -(h dV'^T), dV' V^T (lanes 0-63), dYU^T = dV'^T T
 #pragma unroll
-                for (int s = 0; s < 8; ++s) mma_bf16(tm + SL1, dK_(aH, 128, s), dM_(aDV, 16384, s), ID_KM, s > 0);
+                for (int s = 0; s < 8; ++s) mma_bf16(tm + sa, dK_(aH, 128, s), dM_(aDV, 16384, s), ID_KM, s > 0);
 #pragma unroll
                 for (int s = 0; s < 8; ++s) mma_bf16(tm + SL2, dM_(aDV, 16384, s), dK_(aV, 64, s), ID_MK, s > 0);
 #pragma unroll
-                for (int s = 0; s < 4; ++s) mma_bf16(tm + SL6, dK_(aDV, 128, s), dM_(aT, 8192, s), ID_KM, s > 0);
+                for (int s = 0; s < 4; ++s) mma_bf16(tm + su, dK_(aDV, 128, s), dM_(aT, 8192, s), ID_KM, s > 0);
             }
             commit(&bars[M_4]);
         }
@@ -511,10 +576,11 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (q4 < 2) {
             const int i = 32 * q4 + lane;
             float x[16], pr[16];
-            tmem_ld16(tm + lb + SL0 + c16, x);
+            tmem_ld16(tm + lb + sv + c16, x);
             ld_row16(aP, i, c16, pr);
             tmem_ld_wait();
-            const float gi = sGam[i];
+            const float gi = sGam[i], ei = sE[i];
+            const bool pw = *sPw != 0;
             float rs = 0.f;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
@@ -524,7 +590,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 const float pp = v * pr[jj];
                 rs += pp;
                 pr[jj] = pp;
-                x[jj] = on ? v * expf(gi - sGam[jx]) : 0.f;
+                x[jj] = on ? v * (pw ? expf(gi - sGam[jx]) : ei * sEi[jx]) : 0.f;
             }
             sF[F_PPR + 64 * cg + i] = rs;
             const float cs = lane_colsum16(pr);
@@ -545,15 +611,15 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(7);
-        if (tid == 0) {
+        if (tid == ISS) {
             fence_after_sync();
             // (dQk K)^T = K^T dQk^T, (dQk^T Q)^T = Q^T dQk
 #pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tm + SL7, dM_(aK, 8192, s), dK_(aQK, 64, s), ID_MK, s > 0);
+            for (int s = 0; s < 4; ++s) mma_bf16(tm + sz, dM_(aK, 8192, s), dK_(aQK, 64, s), ID_MK, s > 0);
             ok = twait(bars, B_Q, par, errflag);
             if (ok) {
 #pragma unroll
-                for (int s = 0; s < 4; ++s) mma_bf16(tm + SL0, dM_(aQ, 8192, s), dM_(aQK, 8192, s), ID_MM, s > 0);
+                for (int s = 0; s < 4; ++s) mma_bf16(tm + sv, dM_(aQ, 8192, s), dM_(aQK, 8192, s), ID_MM, s > 0);
             }
             commit(&bars[M_5]);
             if (has_next) {  // W' (now V'^T), TU, P and dh are no longer read
@@ -571,8 +637,8 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_after_sync();
         {
             float x[16], y[16];
-            tmem_ld16(tm + lb + SL1 + c16, x);
-            tmem_ld16(tm + lb + SL6 + c16, y);
+            tmem_ld16(tm + lb + sa + c16, x);
+            tmem_ld16(tm + lb + su + c16, y);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = -x[i];
@@ -592,13 +658,13 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(9);
-        if (tid == 0) {
+        if (tid == ISS) {
             fence_after_sync();
             // dW K^T (lanes 0-63), dYW^T = dW^T T
 #pragma unroll
-            for (int s = 0; s < 8; ++s) mma_bf16(tm + SL6, dM_(aDO, 16384, s), dK_(aK, 64, s), ID_MK, s > 0);
+            for (int s = 0; s < 8; ++s) mma_bf16(tm + su, dM_(aDO, 16384, s), dK_(aK, 64, s), ID_MK, s > 0);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tm + SL1, dK_(aDO, 128, s), dM_(aT, 8192, s), ID_KM, s > 0);
+            for (int s = 0; s < 4; ++s) mma_bf16(tm + sa, dK_(aDO, 128, s), dM_(aT, 8192, s), ID_KM, s > 0);
             commit(&bars[M_6]);
             if (has_next) {  // h and V are no longer read
                 req_H(nxt);
@@ -608,13 +674,14 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         __syncwarp();
 
         // dQ = scale diag(e) dO h^T + dQk K; <Q_i, (dO h^T)_i>
-        ok = lwait(bars, M_5, par, errflag) && lwait(bars, B_Q, par, errflag) && ok;
+        ok = lwait(bars, M_5, par, errflag) && lwait(bars, M_2, par, errflag) &&
+             lwait(bars, B_Q, par, errflag) && ok;
         TTRACE(10);
         fence_after_sync();
         {
             float a[16], b[16];
             tmem_ld16(tm + lb + SL3 + c16, a);
-            tmem_ld16(tm + lb + SL7 + c16, b);
+            tmem_ld16(tm + lb + sz + c16, b);
             tmem_ld_wait();
             const int k = 32 * q4 + lane;
             if (B.dqp) {
@@ -643,10 +710,11 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         ok = lwait(bars, M_6, par, errflag) && ok;
         TTRACE(11);
         fence_after_sync();
+        if (tid == ISS && ok && has_next) req_DO(nxt);  // the dW products are done: next dO
         if (q4 < 2) {
             const int i = 32 * q4 + lane;
             float d1[16], d2[16];
-            tmem_ld16(tm + lb + SL6 + c16, d1);
+            tmem_ld16(tm + lb + su + c16, d1);
             tmem_ld16(tm + lb + SL2 + c16, d2);
             tmem_ld_wait();
 #pragma unroll
@@ -663,7 +731,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         {
             const int k = 32 * q4 + lane;
             float z[16];
-            tmem_ld16(tm + lb + SL1 + c16, z);
+            tmem_ld16(tm + lb + sa + c16, z);
             tmem_ld_wait();
 #pragma unroll
             for (int ii = 0; ii < 16; ++ii) z[ii] *= ld_el(aK, c16 + ii, k);
@@ -674,16 +742,13 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(12);
-        if (tid == 0) {
+        if (tid == ISS) {
             fence_after_sync();
             // Z = dT T^T (lanes 0-63)
 #pragma unroll
             for (int s = 0; s < 4; ++s) mma_bf16(tm + SL3, dK_(aDT, 64, s), dK_(aT, 64, s), ID_KK, s > 0);
             commit(&bars[M_7]);
-            if (has_next) {  // dO (now dW^T) and Q are no longer read
-                req_DO(nxt);
-                req_Q(nxt);
-            }
+            if (has_next) req_K(nxt, qreg);  // Q is no longer read: next K into its region
         }
         __syncwarp();
 
@@ -701,33 +766,40 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(14);
-        if (tid == 0) {
+        if (tid == ISS) {
             fence_after_sync();
             // T^T Z (lanes 0-63)
 #pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tm + SL7, dM_(aT, 8192, s), dM_(aQK, 8192, s), ID_MM, s > 0);
+            for (int s = 0; s < 4; ++s) mma_bf16(tm + SL2, dM_(aT, 8192, s), dM_(aQK, 8192, s), ID_MM, s > 0);
             commit(&bars[M_8]);
+            // the next item's first group while the 64-row epilogues run (its warp has no share in
+            // them): slots s6/s7 (or s0/s1) and s3 are free
+            if (has_next && nxt.c == LCH && landed(par ^ 1u, true, 1500)) {
+                issue_A(par ^ 1u);
+                nA = true;
+            }
         }
         __syncwarp();
 
         // dA = strictly-lower(-T^T Z), its dgamma / dbeta terms with A = diag(beta) (Dm * Bm),
         // dB = diag(beta) (dA * Dm) -> fp32 staging -> dB + dB^T as a bf16 tile (dT region)
-        ok = lwait(bars, M_8, par, errflag) && ok;
+        ok = lwait(bars, M_8, par, errflag) && lwait(bars, M_11, par, errflag) && ok;
         TTRACE(15);
         fence_after_sync();
         if (q4 < 2) {
             const int i = 32 * q4 + lane;
             float da[16], bm[16];
-            tmem_ld16(tm + lb + SL7 + c16, da);
+            tmem_ld16(tm + lb + SL2 + c16, da);
             tmem_ld16(tm + lb + SL4 + c16, bm);
             tmem_ld_wait();
-            const float gi = sGam[i], bi = sBeta[i];
+            const float gi = sGam[i], bi = sBeta[i], ei = sE[i];
+            const bool pw = *sPw != 0;
             float rs = 0.f, ra = 0.f;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int jx = c16 + jj;
                 const bool strict = i > jx;
-                const float D = strict ? expf(gi - sGam[jx]) : 0.f;
+                const float D = strict ? (pw ? expf(gi - sGam[jx]) : ei * sEi[jx]) : 0.f;
                 const float dav = strict ? -da[jj] : 0.f;
                 const float fdb = D * bm[jj];
                 rs += dav * fdb;
@@ -747,10 +819,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                        make_uint4(__float_as_uint(da[4 * u]), __float_as_uint(da[4 * u + 1]),
                                   __float_as_uint(da[4 * u + 2]), __float_as_uint(da[4 * u + 3])));
             }
-        }
-        __syncthreads();
-        if (q4 < 2) {
-            const int i = 32 * q4 + lane;
+            named_sync(2, LT / 2);  // the warps of lane quarters 0 and 1
             float s2[16];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -773,13 +842,18 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(16);
-        if (tid == 0) {
+        if (tid == ISS) {
             fence_after_sync();
             // ((dB + dB^T) K)^T = K^T (dB + dB^T) onto (dQk^T Q)^T
 #pragma unroll
-            for (int s = 0; s < 4; ++s) mma_bf16(tm + SL0, dM_(aK, 8192, s), dM_(aDT, 8192, s), ID_MM, 1u);
+            for (int s = 0; s < 4; ++s) mma_bf16(tm + sv, dM_(aK, 8192, s), dM_(aDT, 8192, s), ID_MM, 1u);
             commit(&bars[M_9]);
             if (has_next) req_T(nxt);  // T is no longer read
+            // the next item's second group (s2 and s4 were read by the dA epilogue)
+            if (nA && landed(par ^ 1u, false, 0)) {
+                issue_B(par ^ 1u);
+                nB = true;
+            }
         }
         __syncwarp();
 
@@ -787,12 +861,23 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         ok = lwait(bars, M_9, par, errflag) && ok;
         TTRACE(17);
         fence_after_sync();
-        if (tid == 0 && ok && has_next) req_K(nxt);  // the last product has read K
+        if (tid == ISS && ok && has_next) req_Q(nxt, kreg);  // the last product has read K
+        have_ng = false;
+        if (w == 0 && has_next) {  // the next item's gates, in flight during the epilogue
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = 2 * lane + u;
+                const bool in = r < nxt.c;
+                ngv[u] = in ? P.g[(nxt.tc + r) * Hv + nxt.j] : 0.f;
+                nbv[u] = in ? P.beta[(nxt.tc + r) * Hv + nxt.j] : 0.f;
+            }
+            have_ng = true;
+        }
         {
             float x[16], y[16], z[16];
-            tmem_ld16(tm + lb + SL0 + c16, x);
+            tmem_ld16(tm + lb + sv + c16, x);
             tmem_ld16(tm + lb + SL5 + c16, y);
-            tmem_ld16(tm + lb + SL1 + c16, z);
+            tmem_ld16(tm + lb + sa + c16, z);
             tmem_ld_wait();
             const int k = 32 * q4 + lane;
 #pragma unroll
@@ -868,10 +953,12 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(18);
         pre = has_next;
+        eA = nA;
+        eB = nB;
         ++n;
     }
 
-    if (failed && tid == 0) {
+    if (failed && tid == ISS) {
         // let the copies in flight land and the products drain before the CTA leaves
 #pragma unroll
         for (int b = 0; b < NLD; ++b)
