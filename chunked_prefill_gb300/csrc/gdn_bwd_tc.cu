@@ -161,13 +161,20 @@ __device__ __forceinline__ void ld_row16(uint32_t tile, int r, int c0, float (&x
         x[8 * u + 7] = bf_hi(q.w);
     }
 }
-// element (r, c) of a [64][128] SW128 tile (two 64-column blocks)
-__device__ __forceinline__ float ld_el(uint32_t tile, int r, int c) {
-    const uint32_t a = tile + uint32_t(c >> 6) * 8192u + uint32_t(r) * 128u +
-                       (uint32_t(((c & 63) >> 3) ^ (r & 7)) << 4) + uint32_t(c & 7) * 2u;
-    unsigned short h;
-    asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(h) : "r"(a) : "memory");
-    return __uint_as_float(uint32_t(h) << 16);
+// rows c0 .. c0 + 15 (c0 a multiple of 16) of column col of a [64][128] SW128 tile: the
+// swizzled chunk of row c0 + ii depends on ii % 8 only, so eight bases serve the sixteen loads
+__device__ __forceinline__ void ld_col16(uint32_t tile, int c0, int col, float (&x)[16]) {
+    const uint32_t b0 = tile + uint32_t(col >> 6) * 8192u + uint32_t(c0) * 128u + uint32_t(col & 7) * 2u;
+    const uint32_t ck = uint32_t((col & 63) >> 3);
+    uint32_t bm[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) bm[m] = b0 + ((ck ^ uint32_t(m)) << 4);
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+        unsigned short h;
+        asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(h) : "r"(bm[ii & 7] + uint32_t(ii) * 128u) : "memory");
+        x[ii] = __uint_as_float(uint32_t(h) << 16);
+    }
 }
 
 // Column sums over the 32 lanes of the warp of 16 values per lane (butterfly transpose):
@@ -187,8 +194,8 @@ __device__ __forceinline__ float lane_colsum16(float (&v)[16]) {
     return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-// lane 0 waits (bounded, polling: these waits are on the item's critical path), the result is
-// broadcast to the warp
+// lane 0 waits (bounded, polling: a parked lane wakes too late for these waits, which are on
+// the item's critical path), the result is broadcast to the warp
 __device__ __forceinline__ bool lwait(uint64_t* bars, int b, uint32_t par, int* errflag) {
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
@@ -487,22 +494,6 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         }
         __syncwarp();
 
-        // <dh, h> over the two state tiles (identical swizzled layouts)
-        {
-            ok = lwait(bars, B_H, par, errflag) && lwait(bars, B_DH, par, errflag) && ok;
-            float hd = 0.f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t off = uint32_t(tid + LT * u) * 16u;
-                const uint4 a = lds128(aH + off), b = lds128(aDH + off);
-                hd += bf_lo(a.x) * bf_lo(b.x) + bf_hi(a.x) * bf_hi(b.x) + bf_lo(a.y) * bf_lo(b.y) +
-                      bf_hi(a.y) * bf_hi(b.y) + bf_lo(a.z) * bf_lo(b.z) + bf_hi(a.z) * bf_hi(b.z) +
-                      bf_lo(a.w) * bf_lo(b.w) + bf_hi(a.w) * bf_hi(b.w);
-            }
-#pragma unroll
-            for (int off = 16; off; off >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, off);
-            if (lane == 0) sF[F_RED + w] = hd;
-        }
         // V'^T -> bf16 tile (in the W' region)
         ok = lwait(bars, M_0, par, errflag) && ok;
         TTRACE(2);
@@ -602,10 +593,30 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             float y[16];
             tmem_ld16(tm + lb + SL5 + c16, y);
             tmem_ld_wait();
+            float kc[16];
+            ld_col16(aK, c16, k, kc);
 #pragma unroll
-            for (int ii = 0; ii < 16; ++ii) y[ii] *= ld_el(aK, c16 + ii, k);
+            for (int ii = 0; ii < 16; ++ii) y[ii] *= kc[ii];
             const float cs = lane_colsum16(y);
             if (!(lane & 1)) sF[F_PR + 64 * q4 + c16 + (lane >> 1)] = cs;
+        }
+        if (q4 >= 2) {
+            // <dh, h> over the two state tiles (identical swizzled layouts), by the warps without
+            // a share in the 64-row epilogue
+            const int t2 = 32 * ((w >> 2) * 2 + (q4 - 2)) + lane;  // 0 .. 255
+            ok = lwait(bars, B_H, par, errflag) && lwait(bars, B_DH, par, errflag) && ok;
+            float hd = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t off = uint32_t(t2 + 256 * u) * 16u;
+                const uint4 a = lds128(aH + off), b = lds128(aDH + off);
+                hd += bf_lo(a.x) * bf_lo(b.x) + bf_hi(a.x) * bf_hi(b.x) + bf_lo(a.y) * bf_lo(b.y) +
+                      bf_hi(a.y) * bf_hi(b.y) + bf_lo(a.z) * bf_lo(b.z) + bf_hi(a.z) * bf_hi(b.z) +
+                      bf_lo(a.w) * bf_lo(b.w) + bf_hi(a.w) * bf_hi(b.w);
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, off);
+            if (lane == 0) sF[F_RED + (t2 >> 5)] = hd;
         }
         fence_proxy_async_smem();
         fence_before_sync();
@@ -644,12 +655,14 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             for (int i = 0; i < 16; ++i) x[i] = -x[i];
             st_row16(aDO, 32 * q4 + lane, c16, x);
             const int v = 32 * q4 + lane;
-            __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(B.dv) + int64_t(j) * VD + v;
+            __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(B.dv) + int64_t(j) * VD + v + (tc + c16) * v_stride;
+            float vc[16];
+            ld_col16(aV, c16, v, vc);
 #pragma unroll
             for (int ii = 0; ii < 16; ++ii) {
                 const int cx = c16 + ii;
-                if (cx < c) dv[(tc + cx) * v_stride] = __float2bfloat16_rn(sBeta[cx] * y[ii]);
-                y[ii] *= ld_el(aV, cx, v);
+                if (cx < c) dv[ii * v_stride] = __float2bfloat16_rn(sBeta[cx] * y[ii]);
+                y[ii] *= vc[ii];
             }
             const float cs = lane_colsum16(y);
             if (!(lane & 1)) sF[F_PTU + 64 * q4 + c16 + (lane >> 1)] = cs;
@@ -699,8 +712,10 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                     if (cx < c) dq[(tc + cx) * qk_stride] = __float2bfloat16_rn(sc * sE[cx] * a[ii] + b[ii]);
                 }
             }
+            float qc[16];
+            ld_col16(aQ, c16, k, qc);
 #pragma unroll
-            for (int ii = 0; ii < 16; ++ii) a[ii] *= ld_el(aQ, c16 + ii, k);
+            for (int ii = 0; ii < 16; ++ii) a[ii] *= qc[ii];
             const float cs = lane_colsum16(a);
             if (!(lane & 1)) sF[F_PQ + 64 * q4 + c16 + (lane >> 1)] = cs;
         }
@@ -733,8 +748,10 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             float z[16];
             tmem_ld16(tm + lb + sa + c16, z);
             tmem_ld_wait();
+            float kc[16];
+            ld_col16(aK, c16, k, kc);
 #pragma unroll
-            for (int ii = 0; ii < 16; ++ii) z[ii] *= ld_el(aK, c16 + ii, k);
+            for (int ii = 0; ii < 16; ++ii) z[ii] *= kc[ii];
             const float cs = lane_colsum16(z);
             if (!(lane & 1)) sF[F_PTW + 64 * q4 + c16 + (lane >> 1)] = cs;
         }
@@ -837,6 +854,30 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                                  uint32_t(i & 3) * 4u);
             }
             st_row16(aDT, i, c16, s2);
+        } else if (w == 6 || w == 7) {
+            // every per-token term but those of dA, in place (thread i reads its own entries
+            // before writing them): F_PQ[i] dgamma so far, F_PQ[64 + i] dbeta so far,
+            // F_PQ[128 + i] r_i; F_RED[8] = <dh, h>
+            const int i = tid - 192;
+            float pq = 0.f, pr = 0.f, ptw = 0.f, ptu = 0.f, ppr = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                pq += sF[F_PQ + 64 * q + i];
+                pr += sF[F_PR + 64 * q + i];
+                ptw += sF[F_PTW + 64 * q + i];
+                ptu += sF[F_PTU + 64 * q + i];
+                ppr += sF[F_PPR + 64 * q + i];
+            }
+            const float ri = sKd[i] * pr;
+            sF[F_PQ + i] = ppr - (sF[F_PPC + i] + sF[F_PPC + 64 + i]) + sc * sE[i] * pq - ri + sBe[i] * ptw;
+            sF[F_PQ + 64 + i] = sE[i] * ptw + ptu;
+            sF[F_PQ + 128 + i] = ri;
+            if (i == 0) {
+                float hd = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) hd += sF[F_RED + q];
+                sF[F_RED + 8] = hd;
+            }
         }
         fence_proxy_async_smem();
         fence_before_sync();
@@ -908,29 +949,19 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int i = 2 * lane + u;
-                float pq = 0.f, pr = 0.f, ptw = 0.f, ptu = 0.f, ppr = 0.f, par4 = 0.f, prs = 0.f;
+                float par4 = 0.f, prs = 0.f;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    pq += sF[F_PQ + 64 * q + i];
-                    pr += sF[F_PR + 64 * q + i];
-                    ptw += sF[F_PTW + 64 * q + i];
-                    ptu += sF[F_PTU + 64 * q + i];
-                    ppr += sF[F_PPR + 64 * q + i];
                     par4 += sF[F_PAR + 64 * q + i];
                     prs += sF[F_PRS + 64 * q + i];
                 }
-                const float ri = sKd[i] * pr;
-                rr += ri;
-                dgv[u] = ppr - (sF[F_PPC + i] + sF[F_PPC + 64 + i]) + sc * sE[i] * pq - ri + sBe[i] * ptw +
-                         par4 - (sF[F_PAC + i] + sF[F_PAC + 64 + i]);
-                dbv[u] = sE[i] * ptw + ptu + prs;
+                rr += sF[F_PQ + 128 + i];
+                dgv[u] = sF[F_PQ + i] + par4 - (sF[F_PAC + i] + sF[F_PAC + 64 + i]);
+                dbv[u] = sF[F_PQ + 64 + i] + prs;
             }
 #pragma unroll
             for (int off = 16; off; off >>= 1) rr += __shfl_xor_sync(0xffffffffu, rr, off);
-            float hd = 0.f;
-#pragma unroll
-            for (int q = 0; q < LT / 32; ++q) hd += sF[F_RED + q];
-            if (lane == 31) dgv[1] += rr + sE[LCH - 1] * hd;
+            if (lane == 31) dgv[1] += rr + sE[LCH - 1] * sF[F_RED + 8];
             const float v1 = dgv[1], v0 = dgv[0] + dgv[1];
             float tot = v0;  // suffix scan over lanes (from the top)
 #pragma unroll
