@@ -45,12 +45,19 @@ namespace {
 using namespace tc;
 
 #ifdef GDN_TRACE
-__device__ unsigned long long g_tcl_trace[32];  // debug builds: SM clock at the steps of one item of CTA 0
+__device__ unsigned long long g_tcl_trace[48];  // debug builds: SM clock at the steps of one item of CTA 0
 #define TTRACE(e)                                                                                \
     do {                                                                                         \
-        if (blockIdx.x == 0 && threadIdx.x == 0 && n == 2) g_tcl_trace[e] = clock64();            \
+        if (blockIdx.x == 0 && threadIdx.x == 0 && n == 2 && (e) >= 0 && (e) < 20) g_tcl_trace[e] = clock64(); \
+    } while (0)
+#define ITRACE(e)                                                                                \
+    do {                                                                                         \
+        if (blockIdx.x == 0 && n == 2 && (e) >= 0 && (e) < 16) g_tcl_trace[20 + (e)] = clock64(); \
     } while (0)
 #else
+#define ITRACE(e) \
+    do {          \
+    } while (0)
 #define TTRACE(e) \
     do {          \
     } while (0)
@@ -380,6 +387,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
     float ngv[2] = {0.f, 0.f}, nbv[2] = {0.f, 0.f};  // (warp 0) the next item's g, beta
     bool have_ng = false;
     bool failed = false;
+    bool carry_ok = true;  // the previous item's last step (its failure is acted on at the next barrier)
     uint32_t n = 0;      // items done (parity of every barrier phase)
 #pragma unroll 1
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
@@ -464,11 +472,12 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 fence_proxy_async_smem();
             }
         }
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (__syncthreads_or(!ok || !carry_ok)) { failed = true; break; }
         TTRACE(1);
 
         // ---- first products (those the previous item did not issue)
         if (tid == ISS) {
+            ITRACE(0);
             fence_after_sync();
             if (!eA) {
                 ok = twait(bars, B_V, par, errflag) && twait(bars, B_TU, par, errflag) &&
@@ -491,6 +500,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                     commit(&bars[M_11]);
                 }
             }
+            ITRACE(1);
         }
         __syncwarp();
 
@@ -509,6 +519,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(3);
         if (tid == ISS) {
+            ITRACE(2);
             fence_after_sync();
             // dP = dO V'^T (lanes 0-63), (V' dh^T)^T = dh V'^T
 #pragma unroll
@@ -516,6 +527,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
 #pragma unroll
             for (int s = 0; s < 8; ++s) mma_bf16(tm + SL5, dK_(aDH, 128, s), dM_(aW, 16384, s), ID_KM, s > 0);
             commit(&bars[M_3]);
+            ITRACE(3);
         }
         __syncwarp();
 
@@ -543,6 +555,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(5);
         if (tid == ISS) {
+            ITRACE(4);
             fence_after_sync();
             ok = twait(bars, B_T, par, errflag);
             if (ok) {
@@ -555,6 +568,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 for (int s = 0; s < 4; ++s) mma_bf16(tm + su, dK_(aDV, 128, s), dM_(aT, 8192, s), ID_KM, s > 0);
             }
             commit(&bars[M_4]);
+            ITRACE(5);
         }
         __syncwarp();
 
@@ -571,7 +585,20 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             ld_row16(aP, i, c16, pr);
             tmem_ld_wait();
             const float gi = sGam[i], ei = sE[i];
-            const bool pw = *sPw != 0;
+            float dm[16];  // D_ij = exp(gamma_i - gamma_j)
+            if (*sPw) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) dm[jj] = expf(gi - sGam[c16 + jj]);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 4) {
+                    const float4 e4 = *reinterpret_cast<const float4*>(sEi + c16 + jj);
+                    dm[jj] = ei * e4.x;
+                    dm[jj + 1] = ei * e4.y;
+                    dm[jj + 2] = ei * e4.z;
+                    dm[jj + 3] = ei * e4.w;
+                }
+            }
             float rs = 0.f;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
@@ -581,7 +608,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 const float pp = v * pr[jj];
                 rs += pp;
                 pr[jj] = pp;
-                x[jj] = on ? v * (pw ? expf(gi - sGam[jx]) : ei * sEi[jx]) : 0.f;
+                x[jj] = on ? v * dm[jj] : 0.f;
             }
             sF[F_PPR + 64 * cg + i] = rs;
             const float cs = lane_colsum16(pr);
@@ -600,15 +627,15 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             const float cs = lane_colsum16(y);
             if (!(lane & 1)) sF[F_PR + 64 * q4 + c16 + (lane >> 1)] = cs;
         }
-        if (q4 >= 2) {
+        if (q4 >= 2 && w != ISS / 32) {
             // <dh, h> over the two state tiles (identical swizzled layouts), by the warps without
-            // a share in the 64-row epilogue
-            const int t2 = 32 * ((w >> 2) * 2 + (q4 - 2)) + lane;  // 0 .. 255
+            // a share in the 64-row epilogue other than the issuer's
+            const int t2 = 32 * ((w >> 2) * 2 + (q4 - 2) - 1) + lane;  // 0 .. 223
             ok = lwait(bars, B_H, par, errflag) && lwait(bars, B_DH, par, errflag) && ok;
             float hd = 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t off = uint32_t(t2 + 256 * u) * 16u;
+#pragma unroll 1
+            for (int u = t2; u < 2048; u += 224) {
+                const uint32_t off = uint32_t(u) * 16u;
                 const uint4 a = lds128(aH + off), b = lds128(aDH + off);
                 hd += bf_lo(a.x) * bf_lo(b.x) + bf_hi(a.x) * bf_hi(b.x) + bf_lo(a.y) * bf_lo(b.y) +
                       bf_hi(a.y) * bf_hi(b.y) + bf_lo(a.z) * bf_lo(b.z) + bf_hi(a.z) * bf_hi(b.z) +
@@ -616,13 +643,14 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             }
 #pragma unroll
             for (int off = 16; off; off >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, off);
-            if (lane == 0) sF[F_RED + (t2 >> 5)] = hd;
+            if (lane == 0) sF[F_RED + (t2 >> 5)] = hd;  // warps 0 .. 6 of this group
         }
         fence_proxy_async_smem();
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(7);
         if (tid == ISS) {
+            ITRACE(6);
             fence_after_sync();
             // (dQk K)^T = K^T dQk^T, (dQk^T Q)^T = Q^T dQk
 #pragma unroll
@@ -639,6 +667,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 req_P(nxt);
                 req_DH(nxt);
             }
+            ITRACE(7);
         }
         __syncwarp();
 
@@ -672,6 +701,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(9);
         if (tid == ISS) {
+            ITRACE(8);
             fence_after_sync();
             // dW K^T (lanes 0-63), dYW^T = dW^T T
 #pragma unroll
@@ -683,6 +713,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 req_H(nxt);
                 req_V(nxt);
             }
+            ITRACE(9);
         }
         __syncwarp();
 
@@ -760,12 +791,14 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(12);
         if (tid == ISS) {
+            ITRACE(10);
             fence_after_sync();
             // Z = dT T^T (lanes 0-63)
 #pragma unroll
             for (int s = 0; s < 4; ++s) mma_bf16(tm + SL3, dK_(aDT, 64, s), dK_(aT, 64, s), ID_KK, s > 0);
             commit(&bars[M_7]);
             if (has_next) req_K(nxt, qreg);  // Q is no longer read: next K into its region
+            ITRACE(11);
         }
         __syncwarp();
 
@@ -784,6 +817,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(14);
         if (tid == ISS) {
+            ITRACE(12);
             fence_after_sync();
             // T^T Z (lanes 0-63)
 #pragma unroll
@@ -795,6 +829,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 issue_A(par ^ 1u);
                 nA = true;
             }
+            ITRACE(13);
         }
         __syncwarp();
 
@@ -810,13 +845,26 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             tmem_ld16(tm + lb + SL4 + c16, bm);
             tmem_ld_wait();
             const float gi = sGam[i], bi = sBeta[i], ei = sE[i];
-            const bool pw = *sPw != 0;
+            float dm[16];  // D_ij = exp(gamma_i - gamma_j)
+            if (*sPw) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) dm[jj] = expf(gi - sGam[c16 + jj]);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 4) {
+                    const float4 e4 = *reinterpret_cast<const float4*>(sEi + c16 + jj);
+                    dm[jj] = ei * e4.x;
+                    dm[jj + 1] = ei * e4.y;
+                    dm[jj + 2] = ei * e4.z;
+                    dm[jj + 3] = ei * e4.w;
+                }
+            }
             float rs = 0.f, ra = 0.f;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int jx = c16 + jj;
                 const bool strict = i > jx;
-                const float D = strict ? (pw ? expf(gi - sGam[jx]) : ei * sEi[jx]) : 0.f;
+                const float D = strict ? dm[jj] : 0.f;
                 const float dav = strict ? -da[jj] : 0.f;
                 const float fdb = D * bm[jj];
                 rs += dav * fdb;
@@ -875,7 +923,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             if (i == 0) {
                 float hd = 0.f;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) hd += sF[F_RED + q];
+                for (int q = 0; q < 7; ++q) hd += sF[F_RED + q];
                 sF[F_RED + 8] = hd;
             }
         }
@@ -884,17 +932,14 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(16);
         if (tid == ISS) {
+            ITRACE(14);
             fence_after_sync();
             // ((dB + dB^T) K)^T = K^T (dB + dB^T) onto (dQk^T Q)^T
 #pragma unroll
             for (int s = 0; s < 4; ++s) mma_bf16(tm + sv, dM_(aK, 8192, s), dM_(aDT, 8192, s), ID_MM, 1u);
             commit(&bars[M_9]);
             if (has_next) req_T(nxt);  // T is no longer read
-            // the next item's second group (s2 and s4 were read by the dA epilogue)
-            if (nA && landed(par ^ 1u, false, 0)) {
-                issue_B(par ^ 1u);
-                nB = true;
-            }
+            ITRACE(15);
         }
         __syncwarp();
 
@@ -980,8 +1025,21 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 }
             }
         }
+        // end of the item: the issuer's warp only signals its arrival (its dK share is done) and
+        // issues the next item's second group (s2 and s4 were read by the dA epilogue) while
+        // the others finish; the next item's first barrier takes it in again
         fence_before_sync();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (w == ISS / 32) {
+            named_arrive(3, LT);
+            if (tid == ISS && nA && landed(par ^ 1u, false, 0)) {
+                issue_B(par ^ 1u);
+                nB = true;
+            }
+            __syncwarp();
+        } else {
+            named_sync(3, LT);
+        }
+        carry_ok = ok;
         TTRACE(18);
         pre = has_next;
         eA = nA;
@@ -989,6 +1047,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         ++n;
     }
 
+    if (!failed && __syncthreads_or(!carry_ok)) failed = true;
     if (failed && tid == ISS) {
         // let the copies in flight land and the products drain before the CTA leaves
 #pragma unroll

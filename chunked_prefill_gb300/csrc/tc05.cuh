@@ -359,6 +359,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
+// arrive on a named barrier without waiting for the others
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
 // named barrier that also ANDs a predicate over the participating threads
 __device__ __forceinline__ bool named_and(int id, int nthreads, bool v) {
     uint32_t r;
