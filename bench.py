@@ -343,7 +343,8 @@ def oracle_sample_fixed(inp, n, backward):
 
 # DRAM bytes (read + write) of one launch, from the ncu capture summarised in profiles/
 # (fwd_prep_t32k_hqk2_hv8.md); None where no capture of the current kernel exists.
-NCU_TRAFFIC = {("fwd_t32k_hqk2_hv8", "fwd_prep"): 36.740096e6 + 73.815040e6}
+NCU_TRAFFIC = {("fwd_t32k_hqk2_hv8", "fwd_prep"): 36.740096e6 + 73.815040e6,
+               ("fwdbwd_t32k_hqk16_hv16", "bwd_local"): 1413.688e6 + 382.684416e6}
 
 
 def kernel_bytes(name, tokens, lens, w):
