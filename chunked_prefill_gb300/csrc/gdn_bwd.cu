@@ -448,19 +448,17 @@ __global__ void __launch_bounds__(256) k_bwd_fixup(BwdProblem B) {
 // =====================================================================================
 template <typename Op, int C>
 struct LocSmem {
-    static constexpr bool BF = sizeof(Op) == 2;
     static constexpr int LDK = KD + OpTraits<Op>::PAD, LDC = C + OpTraits<Op>::PAD, LDF = C + 1;
     static constexpr size_t TILE = size_t(C) * LDK * sizeof(Op);
-    static constexpr size_t ST = size_t(KD) * LDK * sizeof(Op);
     static constexpr size_t CT = size_t(C) * LDC * sizeof(Op);
     static constexpr size_t FT = size_t(C) * LDF * 4;
     // c x 128 tiles
     static constexpr size_t oK = 0, oQ = oK + TILE /* later dW */, oV = oQ + TILE,
                             oW = oV + TILE /* W', later dO */, oVP = oW + TILE, oDV = oVP + TILE;
-    // state tiles (bf16 only; the fp32 test mode reads h, dh from global memory)
-    static constexpr size_t oH = oDV + TILE;                 // TW, TU before h arrives
-    static constexpr size_t oDH = oH + (BF ? ST : 2 * CT);   // fp32 A, T before dh arrives
-    static constexpr size_t oFDB = oDH + (BF ? ST : 2 * FT);
+    // TW, TU staging; fp32 A, T (the states h, dh are read from global memory)
+    static constexpr size_t oH = oDV + TILE;
+    static constexpr size_t oDH = oH + 2 * CT;
+    static constexpr size_t oFDB = oDH + 2 * FT;
     static constexpr size_t oOP = oFDB + FT, oOT = oOP + CT, oO1 = oOT + CT, oO2 = oO1 + CT;
     static constexpr size_t oTmp = oO1;                      // inverse scratch (phase 1 only)
     static constexpr size_t oGam = oO2 + CT, oE = oGam + C * 4, oKd = oE + C * 4,
@@ -472,7 +470,6 @@ struct LocSmem {
     static constexpr size_t bytes = oRed + 64;
     static_assert(CT >= 3 * 16 * 17 * 4, "inverse scratch alias");
     static_assert(bytes <= 232448, "shared memory budget");
-    static_assert((BF ? ST : 2 * CT) >= 2 * CT && (BF ? ST : 2 * FT) >= 2 * FT, "aliases");
 };
 
 // sum of v over the four lanes that share a fragment row (t = lane & 3)
@@ -496,9 +493,7 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
     extern __shared__ __align__(128) char smem[];
     const Problem& P = B.f;
     // One CTA per SM walks the (chunk, v-head) items item = chunk Hv + v-head with a stride of
-    // the grid.  bf16: while an item's later phases run, the tiles of the CTA's next item
-    // that land in regions those phases no longer read (P, W', dh, h, V, Q) are requested
-    // asynchronously, so that only K, T and TU are waited for at the next item's start.
+    // the grid (fp32 test mode; bf16 runs the tensor-core kernel of gdn_bwd_tc.cu).
     struct Item {
         int gch, j, s, ch, c, qh;
         int64_t t0, t1, tc;
@@ -522,17 +517,10 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
         x.c = int((x.t1 - x.tc) < int64_t(C) ? (x.t1 - x.tc) : int64_t(C));
         return true;
     };
-    bool pre = false;  // this item's P, W', dh, h, V, Q were requested during the previous one
 #pragma unroll 1
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
-    Item cur, nxt;
-    if (!locate(item, cur)) {
-        cp_async_wait_all();  // nothing may still land in the tiles
-        __syncthreads();
-        pre = false;
-        continue;
-    }
-    const bool has_next = S::BF && item + gridDim.x < items && locate(item + gridDim.x, nxt);
+    Item cur;
+    if (!locate(item, cur)) continue;
     const int gch = cur.gch, j = cur.j, s = cur.s, ch = cur.ch;
     const int64_t t0 = cur.t0, t1 = cur.t1, tc = cur.tc;
     (void)s;
@@ -576,10 +564,10 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
     const int64_t qk_stride = int64_t(Hqk) * KD, v_stride = int64_t(Hv) * VD;
     const Op* hsrc = reinterpret_cast<const Op*>(P.hist) + (int64_t(gch) * Hv + j) * KVN;
     const Op* dhsrc = reinterpret_cast<const Op*>(B.dhist) + (int64_t(gch) * Hv + j) * KVN;
-    // state operands: shared copies (bf16) or the global tensors directly (fp32 test mode)
-    const Op* sH = S::BF ? reinterpret_cast<const Op*>(smem + S::oH) : hsrc;
-    const Op* sDH = S::BF ? reinterpret_cast<const Op*>(smem + S::oDH) : dhsrc;
-    constexpr int LDS = S::BF ? LDK : VD;
+    // state operands: the global tensors directly
+    const Op* sH = hsrc;
+    const Op* sDH = dhsrc;
+    constexpr int LDS = VD;
 
     constexpr int RB = C / 16, WPR = (NTL / 32) / RB, COLS = 128 / WPR, NTC = COLS / 8;
     constexpr int CCOLS = C / WPR, NTS = CCOLS / 8;
@@ -589,65 +577,8 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
     const int r0 = m0 + gq, r1 = m0 + gq + 8;
 
     LTRACE(0);
-    // asynchronous tile requests of an item (bf16): K, Q, V rows (past the sequence end zero),
-    // the tiles of its chunk record (unswizzled), its entering state h and gradient dh
-    auto req_rows = [&](const Item& x, Op* dst, const Op* base, int64_t stride) {
-        for (int idx = tid; idx < C * 16; idx += NTL) {
-            const int r = idx >> 4, cv = idx & 15;
-            const bool ok = r < x.c;
-            cp_async16(dst + r * LDK + cv * 8, base + (ok ? r : 0) * stride + cv * 8, ok);
-        }
-    };
-    auto kq_of = [&](const Item& x, const void* t) {
-        return reinterpret_cast<const Op*>(t) + x.qh * KD + x.tc * qk_stride;
-    };
-    auto v_of = [&](const Item& x) { return reinterpret_cast<const Op*>(P.v) + x.j * VD + x.tc * v_stride; };
-    auto rec_of = [&](const Item& x) {
-        return static_cast<const unsigned char*>(P.prep) + (int64_t(x.gch) * Hv + x.j) * P.prep_stride;
-    };
-    auto req_w = [&](const Item& x) {
-        const unsigned char* rec = rec_of(x);
-        for (int q = tid; q < 1024; q += NTL) {
-            const int blk = q >> 9, r = (q >> 3) & 63, cc = (q & 7) ^ (r & 7);
-            cp_async16(tW + r * LDK + blk * 64 + cc * 8, rec + PREP_W + q * 16, true);
-        }
-    };
-    auto req_tile = [&](const Item& x, Op* dst, int off) {
-        const unsigned char* rec = rec_of(x);
-        for (int q = tid; q < 512; q += NTL) {
-            const int r = q >> 3, cc = (q & 7) ^ (r & 7);
-            cp_async16(dst + r * LDC + cc * 8, rec + off + q * 16, true);
-        }
-    };
-    auto req_state = [&](const Op* src, Op* dst) {
-        for (int idx = tid; idx < KD * 16; idx += NTL) {
-            const int r = idx >> 4, cv = idx & 15;
-            cp_async16(dst + r * LDK + cv * 8, src + r * VD + cv * 8, true);
-        }
-    };
-    auto hist_of = [&](const void* base, const Item& x) {
-        return reinterpret_cast<const Op*>(base) + (int64_t(x.gch) * Hv + x.j) * KVN;
-    };
-
     // ---- phase 1: tiles, gates, K K^T, Q K^T, A, P, T
-    if (S::BF) {
-        // bf16: every tile the first phases read is requested at once (asynchronous copies):
-        // K, Q, V, the chunk record (W' -> its tile, P, T, TU -> the dQk tile, free until
-        // phase 3), the entering state h and the gradient dh -- all but K, T and TU already
-        // requested during the previous item when there was one
-        if (!pre) {
-            req_rows(cur, tQ, kq_of(cur, P.q), qk_stride);
-            req_rows(cur, tV, v_of(cur), v_stride);
-            req_w(cur);
-            req_tile(cur, oP, PREP_P);
-            req_state(hsrc, const_cast<Op*>(sH));
-            req_state(dhsrc, const_cast<Op*>(sDH));
-        }
-        req_rows(cur, tK, kq_of(cur, P.k), qk_stride);
-        req_tile(cur, oT, PREP_T);
-        req_tile(cur, oX1, PREP_TU);
-        cp_async_commit();
-    } else {
+    {
         load_rows<Op, C>(tK, LDK, reinterpret_cast<const Op*>(P.k) + qh * KD + tc * qk_stride, qk_stride, c);
         load_rows<Op, C>(tQ, LDK, reinterpret_cast<const Op*>(P.q) + qh * KD + tc * qk_stride, qk_stride, c);
         load_rows<Op, C>(tV, LDK, reinterpret_cast<const Op*>(P.v) + j * VD + tc * v_stride, v_stride, c);
@@ -662,33 +593,7 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
     __syncthreads();
     if (w == 0) gates_warp0<C>(sGam, sE, sKd);
     float acc[NTC][4];
-    if (S::BF) {
-        // bf16: P, T, TU and W' = -T diag(beta e) K came from the forward's chunk records
-        // (unswizzled by the copies above); only the decayed K K^T (for the dbeta and dgamma
-        // terms) and U = TU V are recomputed
-        cp_async_wait_all();
-        __syncthreads();
-        {
-            float a1[NTS][4];
-            zero_acc(a1);
-            warp_mma<NTS, false, true>(a1, tK, LDK, tK, LDK, m0, s0, KD);
-#pragma unroll
-            for (int n = 0; n < NTS; ++n) {
-                const int cc = s0 + 8 * n + 2 * tq;
-                fDB[r0 * LDF + cc] = a1[n][0];
-                fDB[r0 * LDF + cc + 1] = a1[n][1];
-                fDB[r1 * LDF + cc] = a1[n][2];
-                fDB[r1 * LDF + cc + 1] = a1[n][3];
-            }
-        }
-        __syncthreads();
-        for (int idx = tid; idx < C * C; idx += NTL) {
-            const int i = idx / C, jj = idx % C;
-            fDB[i * LDF + jj] = (i > jj) ? expf(sGam[i] - sGam[jj]) * fDB[i * LDF + jj] : 0.f;  // Dm * Bm
-        }
-        zero_acc(acc);
-        warp_mma<NTC, false, false>(acc, oX1, LDC, tV, LDK, m0, n0, C);
-    } else {
+    {
     {
         float a1[NTS][4], a2[NTS][4];
         zero_acc(a1);
@@ -757,16 +662,7 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
 
     LTRACE(2);
     // ---- phase 3: dO, dh; dV' = scale P^T dO + diag(kd) K dh
-    if (S::BF) {  // dh arrived with the first copies; dO lands while K dh is formed
-        const Op* dg = reinterpret_cast<const Op*>(B.dO) + j * VD + tc * v_stride;
-        for (int idx = tid; idx < C * 16; idx += NTL) {
-            const int r = idx >> 4, cv = idx & 15;
-            const bool ok = r < c;
-            cp_async16(tDO + r * LDK + cv * 8, dg + (ok ? r : 0) * v_stride + cv * 8, ok);
-        }
-        cp_async_commit();
-        cp_async_wait_all();
-    } else {
+    {
         load_rows<Op, C>(tDO, LDK, reinterpret_cast<const Op*>(B.dO) + j * VD + tc * v_stride, v_stride, c);
     }
     __syncthreads();
@@ -839,10 +735,6 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
         sDg[i] += v;
     }
     __syncthreads();
-    if (has_next) {  // P is no longer read: the next item's P
-        req_tile(nxt, oP, PREP_P);
-        cp_async_commit();
-    }
 
     LTRACE(3);
     // ---- phase 4: dQ = scale diag(e) dO h^T + dQk K; e_i <dOs_i, (Q h)_i>; <dh, h>
@@ -904,10 +796,6 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
         sRed[8] = hd;
     }
     __syncthreads();
-    if (has_next) {  // dO is no longer read: the next item's W' into its tile
-        req_w(nxt);
-        cp_async_commit();
-    }
 
     LTRACE(4);
     // ---- phase 5: dK = dQk^T Q + diag(kd) (V' dh^T) (+ later terms); r_i
@@ -949,10 +837,6 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
         sDg[C - 1] += rsum + sE[C - 1] * sRed[8];
     }
     __syncthreads();
-    if (has_next) {  // dh is no longer read: the next item's dh
-        req_state(hist_of(B.dhist, nxt), const_cast<Op*>(sDH));
-        cp_async_commit();
-    }
 
     LTRACE(5);
     // ---- phase 6: dW = -dV' h^T -> tile (reuses the Q tile)
@@ -969,10 +853,6 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
         }
     }
     __syncthreads();
-    if (has_next) {  // h is no longer read: the next item's h
-        req_state(hist_of(P.hist, nxt), const_cast<Op*>(sH));
-        cp_async_commit();
-    }
 
     LTRACE(6);
     // ---- phase 7: dT = (dW K^T) diag(beta e) + (dV' V^T) diag(beta) -> fA (fp32) -> oX2
@@ -1041,11 +921,6 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
         sDg[i] += sBeta[i] * sE[i] * tw;
     }
     __syncthreads();
-    if (has_next) {  // V and dW (the Q tile) are no longer read: the next item's V and Q
-        req_rows(nxt, tV, v_of(nxt), v_stride);
-        req_rows(nxt, tQ, kq_of(nxt, P.q), qk_stride);
-        cp_async_commit();
-    }
 
     LTRACE(8);
     // ---- phase 9: Z = dT T^T; dA = strictly-lower(-T^T Z); dB = diag(beta) dA * Dm
@@ -1078,8 +953,7 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
                 const float db = fDB[rr * LDF + cj];
                 aa[e] = dav * sBeta[rr] * db;                 // dA * A
                 // dB = beta_i dA_ij Dm_ij (dav is zero on and above the diagonal), in place of
-                // the Dm * Bm entry just read (the dh tile region may already hold the next
-                // item's dh)
+                // the Dm * Bm entry just read
                 fDB[rr * LDF + cj] = (rr > cj) ? sBeta[rr] * dav * expf(sGam[rr] - sGam[cj]) : 0.f;
                 if (e < 2) rs0 += dav * db; else rs1 += dav * db;
             }
@@ -1170,7 +1044,6 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
             }
         }
     }
-    pre = has_next;
     __syncthreads();  // the next item re-initialises the gate and partial-sum arrays
     }
 }
@@ -1202,27 +1075,28 @@ __global__ void k_bwd_reduce(BwdProblem B, int64_t T_total) {
 
 template <typename Op, int C>
 cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
+    // bf16: the tensor-core reverse scan and local-gradient kernels; fp32 test mode: the
+    // CUDA-core kernels of this file
     const Problem& P = B.f;
     using SS = ScanSmem<Op, C>;
     using LS = LocSmem<Op, C>;
+    constexpr bool TC = sizeof(Op) == 2;
     cudaError_t e;
-    e = cudaFuncSetAttribute(k_bwd_phase_a<Op, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SS::bytes));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_bwd_phase_c<Op, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SS::bytes));
-    if (e != cudaSuccess) return e;
-    constexpr int NTL = NT;
-    if constexpr (sizeof(Op) != 2) {
-        e = cudaFuncSetAttribute(k_bwd_local<Op, C, NTL>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(LS::bytes));
-        if (e != cudaSuccess) return e;
-    }
     const int fix_smem = (KD * 129 + KD * 8) * 4;
     e = cudaFuncSetAttribute(k_bwd_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, fix_smem);
     if (e != cudaSuccess) return e;
-    constexpr bool TC = sizeof(Op) == 2;  // bf16: tensor-core reverse scan
+    if constexpr (!TC) {
+        e = cudaFuncSetAttribute(k_bwd_phase_a<Op, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SS::bytes));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_bwd_phase_c<Op, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SS::bytes));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_bwd_local<Op, C, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(LS::bytes));
+        if (e != cudaSuccess) return e;
+    }
     const int64_t T_total = P.cu ? P.T : int64_t(P.N) * P.T;
     if (P.cp != CP_NONE) {
         timing_begin("bwd_phase_a", st);
-        if (TC) {
+        if constexpr (TC) {
             e = launch_bwd_scan_tc(B, 0, T_total, st);
             if (e != cudaSuccess) return e;
         } else {
@@ -1237,7 +1111,7 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
         timing_end(st);
     }
     timing_begin("bwd_dh_scan", st);
-    if (TC) {
+    if constexpr (TC) {
         e = launch_bwd_scan_tc(B, 1, T_total, st);
         if (e != cudaSuccess) return e;
     } else {
@@ -1252,7 +1126,7 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
         } else {
             const int64_t items = int64_t(P.total_chunks) * P.Hv;
             const int grid = int(std::min<int64_t>(items, sm_count()));  // one CTA per SM, persistent
-            k_bwd_local<Op, C, NTL><<<grid, NTL, LS::bytes, st>>>(B, items);
+            k_bwd_local<Op, C, NT><<<grid, NT, LS::bytes, st>>>(B, items);
         }
         timing_end(st);
     }
