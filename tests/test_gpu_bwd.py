@@ -123,3 +123,23 @@ def test_context_parallel_many_heads(Hqk, Hv):
     """Enough (sequence, v-head) chains that the fix-up runs 2, 4 or 8 column groups per CTA."""
     inp = make_inputs(1, 64 * 12 + 5, Hqk, Hv, seed=46 + Hv, h0_std=0.1, backward=True)
     check(inp, BF16_TOL, cp_mode=2, cp_segment_chunks=2)
+
+
+@pytest.mark.parametrize("cp_mode", [None, 1])
+def test_extreme_decay(cp_mode):
+    """Chunk decays past exp(-80): the local-gradient kernel forms exp(gamma_i - gamma_j)
+    directly instead of as exp(gamma_i) exp(-gamma_j)."""
+    inp = make_inputs(1, 300, 1, 2, seed=47, h0_std=0.1, gate_scale=8.0, backward=True)
+    kw = {} if cp_mode is None else {"cp_mode": cp_mode}
+    check(inp, BF16_TOL, **kw)
+
+
+def test_varlen_many_short_sequences():
+    """Forty sequences of 1-199 tokens, q/k heads shared by two v-heads: several (chunk,
+    v-head) items per CTA of the persistent local-gradient kernel, many of them cut by a
+    sequence end (the next item's tiles and first products are requested and issued during
+    the current one, except for a cut chunk, whose rows past the end are zeroed first)."""
+    lens = [int(x) for x in np.random.RandomState(48).randint(1, 200, size=40)]
+    inp = make_inputs(1, sum(lens), 4, 8, seed=48, h0_std=0.1, lengths=lens, backward=True)
+    check(inp, BF16_TOL)
+    check(inp, BF16_TOL, cp_mode=2, cp_segment_chunks=1)
