@@ -1076,8 +1076,12 @@ extern "C" int gdn_debug_tcl_trace(unsigned long long* out) {
 cudaError_t launch_bwd_local_tc(const BwdProblem& B, int64_t T_total, cudaStream_t st) {
     const Problem& P = B.f;
     if (P.total_chunks <= 0) return cudaSuccess;
+    // the chunk records must carry T, and the states of every chunk must be there
+    if (P.prep_stride < PREP_BWD_BYTES || !P.prep || !P.hist || !B.dhist) return cudaErrorInvalidValue;
     LocMaps maps;
     const int64_t rows = int64_t(P.total_chunks) * P.Hv * KD;
+    // the per-chunk state rows are addressed by 32-bit TMA coordinates
+    if (rows > int64_t(0x7fffffff) - KD) return cudaErrorNotSupported;
     if (!make_map(&maps.k, P.k, P.Hqk, T_total) || !make_map(&maps.q, P.q, P.Hqk, T_total) ||
         !make_map(&maps.v, P.v, P.Hv, T_total) || !make_map(&maps.dO, B.dO, P.Hv, T_total) ||
         !make_rows_map(&maps.h, P.hist, rows) || !make_rows_map(&maps.dh, B.dhist, rows))
