@@ -9,17 +9,18 @@
 // product with N = 64:
 //
 //   * products with a 128-wide side (key dk or value v) are formed TRANSPOSED, that side on the
-//     128 tensor-memory lanes and the chunk's 64 tokens on the columns (slot: 64 columns):
-//       s0  V'^T = V^T TU^T + h^T W'^T                  s1  dO^T P       s2  dh^T K^T
-//           (dV'^T = scale s1 + s2 diag(kd))
+//     128 tensor-memory lanes and the chunk's 64 tokens on the columns (slots of 64 columns;
+//     v, a, u, z name s0, s1, s6, s7 on even items and s6, s7, s0, s1 on odd ones):
+//       v   V'^T = V^T TU^T + h^T W'^T                   a   dO^T P        s2  dh^T K^T
+//           (dV'^T = scale a + s2 diag(kd))
 //       s3  (dO h^T)^T = h dO^T                          s5  (V' dh^T)^T = dh V'^T
-//       s1  dW^T = -(h dV'^T)                            s6  dYU^T = dV'^T T
-//       s7  (dQk K)^T = K^T dQk^T                        s0  (dQk^T Q)^T = Q^T dQk, later
-//       s1  dYW^T = dW^T T                                   + ((dB + dB^T) K)^T
+//       a   dW^T = -(h dV'^T)                            u   dYU^T = dV'^T T
+//       z   (dQk K)^T = K^T dQk^T                        v   (dQk^T Q)^T = Q^T dQk, later
+//       a   dYW^T = dW^T T                                   + ((dB + dB^T) K)^T
 //   * the 64 x 64 products use lanes 0-63 of a 128-row product (the A rows past 64 read the
 //     neighbouring tile; those lanes are never read):
-//       s4  K K^T      s0  dP = dO V'^T      s6 / s2  dW K^T, dV' V^T      s3  Z = dT T^T
-//       s7  T^T Z
+//       s4  K K^T     v  dP = dO V'^T     u / s2  dW K^T, dV' V^T     s3  Z = dT T^T
+//       s2  T^T Z
 //
 // Intermediate operands return to shared memory as bf16 128-byte-swizzled tiles with one
 // tensor-memory lane per tile row (V'^T, dV'^T, dW^T: 128 rows of 64 tokens; dQk, dT, Z,
@@ -28,10 +29,16 @@
 // transposes across the 32 lanes of a warp, then a fixed-order sum over the four lane
 // quarters (deterministic).
 //
+// 16 warps share every epilogue step (warp w: lanes 32 (w % 4) .. + 31, 16 of the 64
+// columns); the 64-row steps fall to the warps of lane quarters 0 and 1, and the others take
+// the <dh, h> sum and the per-token pre-sums meanwhile.  One thread, lane 0 of warp 2 (no share
+// in the 64-row steps), requests every copy and issues every product: a tcgen05.mma issue
+// waits for the tensor pipe, so the issuing warp loses the execution time of what it issues.
 // While an item's later products run, the next item's tiles are requested into the regions
-// the remaining products no longer read, so that only K is fetched after the last product.
-// Every wait on an mbarrier is bounded; on a timeout the CTA records an error word, lets its
-// copies and products drain (again bounded) and leaves.
+// the remaining products no longer read (K and Q alternate between two regions so that the
+// next K lands while the last product still reads this K), and its first products are issued
+// into the slots this item no longer uses.  Every wait on an mbarrier is bounded; on a timeout
+// the CTA records an error word, lets its copies and products drain (again bounded) and leaves.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
