@@ -168,38 +168,65 @@ __device__ __forceinline__ void init_state_half(uint32_t tm, uint32_t lb, int ha
     tmem_st_wait();
 }
 
-// One half (64 key columns) of the per-chunk state hand-off: read the fp32 state, write its
-// bf16 copy (the A operand of the V' and Q h products), store it for the backward when asked
-// (the recompute kind always, the output kind when P.hist is set),
-// and decay the fp32 state by exp(gamma_C) before the chunk's update accumulates onto it.
-template <int KIND, bool WIDE = true>
-__device__ __forceinline__ void convert_state_half(const Problem& P, uint32_t tm, uint32_t lb,
-                                                   uint32_t xb, int half, int v, float eC,
-                                                   int64_t chunk, int j, uint32_t xf = T_XF) {
-    // WIDE: both 32-column loads in flight before the wait (64 registers); otherwise in turn
-    constexpr int W = WIDE ? 64 : 32;
+// The same hand-off in two parts, so that the chain's next products can start after the
+// first: (1) read the fp32 state of one half and write its bf16 copy (all the next products
+// read); (2) after the hand-off has been signalled, store the state for the backward when
+// asked and decay the fp32 state by exp(gamma_C) in place -- the state update accumulates onto
+// it only after the V' conversion, whose store wait and arrival follow.  Part 1 leaves the 64
+// values in x for part 2.
+__device__ __forceinline__ void state_bf16_half(uint32_t tm, uint32_t lb, uint32_t xb, int half,
+                                                uint32_t xf, float (&x)[64]) {
+    const int c0 = 64 * half;
+    tmem_ld32(tm + lb + xf + c0, x);
+    tmem_ld32(tm + lb + xf + c0 + 32, x + 32);
+    tmem_ld_wait();
+    float pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
+    tmem_st16(tm + lb + xb + c0 / 2, pk);
+    tmem_st16(tm + lb + xb + c0 / 2 + 16, pk + 16);
+    tmem_st_wait();
+}
+template <int KIND>
+__device__ __forceinline__ void state_decay_half(const Problem& P, uint32_t tm, uint32_t lb, int half,
+                                                 int v, float eC, int64_t chunk, int j, uint32_t xf,
+                                                 float (&x)[64]) {
+    const int c0 = 64 * half;
+    if (KIND == TK_HIST || (KIND == TK_OUT && P.hist)) {
+        __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(P.hist) + (chunk * P.Hv + j) * (KD * VD);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 64; ++i) x[i] *= eC;
+    tmem_st32(tm + lb + xf + c0, x);
+    tmem_st32(tm + lb + xf + c0 + 32, x + 32);
+}
+
+// The two parts for a warp that hands off all 128 columns (too many to keep in registers
+// between the parts: the second reads the fp32 state again), 32 columns at a time.
+__device__ __forceinline__ void state_bf16_all(uint32_t tm, uint32_t lb, uint32_t xb, uint32_t xf) {
 #pragma unroll 1
-    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += W) {
-        float x[W];
+    for (int c0 = 0; c0 < KD; c0 += 32) {
+        float x[32], pk[16];
         tmem_ld32(tm + lb + xf + c0, x);
-        if (WIDE) tmem_ld32(tm + lb + xf + c0 + 32, x + (W - 32));
         tmem_ld_wait();
-        if (KIND == TK_HIST || (KIND == TK_OUT && P.hist)) {
-            __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(P.hist) + (chunk * P.Hv + j) * (KD * VD);
 #pragma unroll
-            for (int i = 0; i < W; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
-        }
-        float pk[W / 2];
-#pragma unroll
-        for (int i = 0; i < W / 2; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
+        for (int i = 0; i < 16; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
         tmem_st16(tm + lb + xb + c0 / 2, pk);
-        if (WIDE) tmem_st16(tm + lb + xb + c0 / 2 + 16, pk + (W / 2 - 16));
-#pragma unroll
-        for (int i = 0; i < W; ++i) x[i] *= eC;
-        tmem_st32(tm + lb + xf + c0, x);
-        if (WIDE) tmem_st32(tm + lb + xf + c0 + 32, x + (W - 32));
     }
     tmem_st_wait();
+}
+__device__ __forceinline__ void state_decay_all(uint32_t tm, uint32_t lb, uint32_t xf, float eC) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < KD; c0 += 32) {
+        float x[32];
+        tmem_ld32(tm + lb + xf + c0, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] *= eC;
+        tmem_st32(tm + lb + xf + c0, x);
+    }
 }
 
 template <int KIND>
@@ -491,10 +518,14 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 fence_after_sync();
             }
             if (v == 0 && !hf) TRACE(k, 17);
-            convert_state_half<KIND>(P, tm, lb, T_XB, hf, v, gb.eC, hist_base + cb + k, j);
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_EX]);
+            {
+                float xs[64];
+                state_bf16_half(tm, lb, T_XB, hf, T_XF, xs);
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_EX]);
+                state_decay_half<KIND>(P, tm, lb, hf, v, gb.eC, hist_base + cb + k, j, T_XF, xs);
+            }
             if (v == 0 && !hf) TRACE(k, 18);
             // V' of tokens [32 hf, 32 hf + 32): fp32 -> bf16 V'^T and bf16 diag(kd) V'^T, both
             // inside the 32 columns just read (no other warp touches them)
@@ -844,14 +875,19 @@ __device__ void tc_scan_pair(const Problem& P, const TcMaps& maps, unsigned char
                 fence_after_sync();
             }
             if (isS) {
-                convert_state_half<TK_STATE>(P, tm, lb, xb, hf, v, gb.eC, 0, j, xf);
+                float xs[64];
+                state_bf16_half(tm, lb, xb, hf, xf, xs);
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[bEX]);
+                state_decay_half<TK_STATE>(P, tm, lb, hf, v, gb.eC, 0, j, xf, xs);
             } else {
-                convert_state_half<TK_TRANS, false>(P, tm, lb, xb, 0, v, gb.eC, 0, j, xf);
-                convert_state_half<TK_TRANS, false>(P, tm, lb, xb, 1, v, gb.eC, 0, j, xf);
+                state_bf16_all(tm, lb, xb, xf);
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[bEX]);
+                state_decay_all(tm, lb, xf, gb.eC);
             }
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[bEX]);
             if (!warp_wait(bars, b3, k & 1, errflag)) { ok = false; break; }
             fence_after_sync();
             // diag(kd) V' in bf16 over the fp32 V' of the same tokens (S: one half of them)
@@ -1027,7 +1063,7 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
                             unsigned char* sm, int j, int64_t t0, int64_t t1, int cb, int ce,
                             const float* x0, float* x_out, int64_t gbase) {
     enum RB { R_FULL0 = 0, R_FULL1, R_EMPTY0, R_EMPTY1, R_GATE0, R_GFREE0 = R_GATE0 + NGATE,
-              R_MMA3 = R_GFREE0 + NGATE, R_MMA5, R_EX, R_EV, R_DOE0, R_DOE1, R_DRAIN, R_COUNT };
+              R_MMA3 = R_GFREE0 + NGATE, R_MMA5, R_EX, R_EV, R_DOE0, R_DOE1, R_DRAIN, R_DEC, R_COUNT };
     static_assert(R_COUNT * 8 + 8 <= 512, "barrier area");
     const Problem& P = B.f;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -1056,6 +1092,7 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
         mbar_init(&bars[R_DOE0], 4);
         mbar_init(&bars[R_DOE1], 4);
         mbar_init(&bars[R_DRAIN], 1);
+        mbar_init(&bars[R_DEC], 8);
         *errflag = 0;
         mbar_fence_init();
     }
@@ -1136,6 +1173,8 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
                 }
                 commit(&bars[R_MMA3]);
                 if (!wait_bar(bars, R_DOE0 + st, (k >> 1) & 1, errflag)) { ok = false; break; }
+                // the state warps have decayed the fp32 state (after the hand-off arrival)
+                if (!wait_bar(bars, R_DEC, k & 1, errflag)) { ok = false; break; }
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
@@ -1248,31 +1287,31 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
                 if (!warp_wait(bars, R_MMA5, (k - 1) & 1, errflag)) { ok = false; break; }
                 fence_after_sync();
             }
-            // hand-off: (store dh of the state leaving the chunk,) bf16 copy, decay by e_C
-#pragma unroll 1
-            for (int q = 0; q < 2; ++q) {
-                const int c0 = 64 * hf + 32 * q;
-                float x[32];
-                tmem_ld32(tm + lb + T_XF + c0, x);
-                tmem_ld_wait();
+            // hand-off: bf16 copy (what the chain's next product reads), signalled at once; then
+            // (the store of dh of the state leaving the chunk and) the decay by e_C, signalled
+            // separately for the products that accumulate onto the state
+            {
+                float xs[64];
+                state_bf16_half(tm, lb, T_XB, hf, T_XF, xs);
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[R_EX]);
+                const int c0 = 64 * hf;
                 if (HIST) {
                     __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(B.dhist) +
                                         ((gbase + chunk_of(k)) * P.Hv + j) * (KD * VD);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
+                    for (int i = 0; i < 64; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(xs[i]);
                 }
-                float pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
-                tmem_st16(tm + lb + T_XB + c0 / 2, pk);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] *= gb.eC;
-                tmem_st32(tm + lb + T_XF + c0, x);
+                for (int i = 0; i < 64; ++i) xs[i] *= gb.eC;
+                tmem_st32(tm + lb + T_XF + c0, xs);
+                tmem_st32(tm + lb + T_XF + c0 + 32, xs + 32);
+                tmem_st_wait();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[R_DEC]);
             }
-            tmem_st_wait();
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[R_EX]);
             // dV'^T of tokens [32 hf, 32 hf + 32) = scale D_a + kd D_b, packed bf16 in place
             if (!warp_wait(bars, R_MMA3, k & 1, errflag)) { ok = false; break; }
             fence_after_sync();
