@@ -291,6 +291,27 @@ extern "C" {
 
 const char* gdn_last_error(void) { return g_err; }
 
+gdn_status gdn_device_status(const void* workspace, void* stream) {
+    if (!workspace || !aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace missing or not 16-byte aligned");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+    if (word != 0)
+        return fail(GDN_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%08x)", unsigned(word));
+    return GDN_OK;
+}
+
+gdn_status gdn_debug_wait_timeout(void* workspace, int32_t limit_us, void* stream) {
+    if (!workspace || !aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace missing or not 16-byte aligned");
+    if (limit_us < 1 || limit_us > 1000000) return fail(GDN_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
+    const cudaError_t e = gdn::launch_debug_wait(static_cast<int*>(workspace), limit_us,
+                                                 static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "debug wait launch: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
 gdn_status gdn_chunk_fwd_workspace_size(const gdn_problem* p, size_t* bytes) {
     gdn_status st = validate_problem(p);
     if (st != GDN_OK) return st;

@@ -623,8 +623,9 @@ static void launch_fixup_cg(int N, int Hv, const int* seg_off, const float* mats
 
 // Work decomposition on the device from the device cu_seqlens (same rule as the host).
 __global__ void k_plan(const int* cu, int N, int T, int C, int L, int total_segs, int2* seg,
-                       int* seg_off, int* chunk_off) {
+                       int* seg_off, int* chunk_off, int* err) {
     tc::pdl_launch_dependents();
+    if (err && threadIdx.x == 0) *err = 0;  // the call's error word starts clear
     for (int i = threadIdx.x; i < total_segs; i += blockDim.x) seg[i] = make_int2(-1, -1);
     __syncthreads();
     if (threadIdx.x != 0) return;
@@ -644,10 +645,26 @@ __global__ void k_plan(const int* cu, int N, int T, int C, int L, int total_segs
     chunk_off[N] = acc_c;
 }
 
+// One thread waits (bounded) on an mbarrier that nothing completes; on giving up it sets its
+// bit in the error word.  No other memory is touched.
+__global__ void k_debug_wait(int* err, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::mbar_fence_init();
+        if (!tc::mbar_wait(&bar, 0, limit_ns)) atomicOr(err, 1 << 25);
+    }
+}
+
+cudaError_t launch_debug_wait(int* err, int limit_us, cudaStream_t st) {
+    k_debug_wait<<<1, 32, 0, st>>>(err, 1000ull * unsigned(limit_us));
+    return cudaGetLastError();
+}
+
 void launch_plan(const Problem& P, int C, cudaStream_t st) {
     timing_begin("fwd_plan", st);
     k_plan<<<1, 256, 0, st>>>(P.cu, P.N, P.T, C, P.L, P.total_segs, P.plan.seg, P.plan.seg_off,
-                              P.plan.chunk_off);
+                              P.plan.chunk_off, P.err);
     timing_end(st);
 }
 

@@ -95,6 +95,9 @@ size_t prologue_bwd_workspace(int Hv);
 cudaError_t launch_prologue_fwd(const PrologueArgs& A, cudaStream_t st);
 cudaError_t launch_prologue_bwd(const PrologueArgs& A, cudaStream_t st);
 
+// Test hook of the device failure report: a bounded wait that gives up after limit_us.
+cudaError_t launch_debug_wait(int* err, int limit_us, cudaStream_t st);
+
 // Per-kernel event timing hooks (no-ops unless gdn_timing_enable(1)).
 void timing_begin(const char* name, cudaStream_t st);
 void timing_end(cudaStream_t st);

@@ -19,7 +19,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
 
-GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA = range(5)
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = range(6)
 GDN_BF16, GDN_FP32 = 0, 1
 CP_AUTO, CP_OFF, CP_EXACT, CP_WARMUP = 0, 1, 2, 3
 _STATUS = {1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE",
@@ -77,6 +77,10 @@ def lib():
                   "gdn_chunk_bwd_saved", "gdn_prologue_fwd", "gdn_prologue_bwd_workspace_size",
                   "gdn_prologue_bwd"):
             getattr(L, f).restype = ctypes.c_int
+        L.gdn_device_status.argtypes = [vp, vp]
+        L.gdn_device_status.restype = ctypes.c_int
+        L.gdn_debug_wait_timeout.argtypes = [vp, ctypes.c_int32, vp]
+        L.gdn_debug_wait_timeout.restype = ctypes.c_int
         L.gdn_last_error.restype = ctypes.c_char_p
         L.gdn_timing_enable.argtypes = [ctypes.c_int32]
         L.gdn_timing_enable.restype = ctypes.c_int
@@ -90,6 +94,18 @@ def lib():
 def _check(rc: int):
     if rc != GDN_OK:
         raise GdnError(rc, lib().gdn_last_error().decode())
+
+
+def gdn_device_status(workspace, stream=None) -> int:
+    """Wait for the stream and read the error word of a call's workspace: GDN_OK, or
+    GDN_ERR_TIMEOUT when a device-side wait of that call gave up (see include/gdn.h)."""
+    return lib().gdn_device_status(_ptr(workspace), _stream(stream))
+
+
+def gdn_debug_wait_timeout(workspace, limit_us: int, stream=None):
+    """Test hook: a kernel whose bounded wait runs out after limit_us, setting its bit in the
+    error word of `workspace`."""
+    _check(lib().gdn_debug_wait_timeout(_ptr(workspace), int(limit_us), _stream(stream)))
 
 
 def gdn_timing_enable(on: bool = True):

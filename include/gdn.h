@@ -46,7 +46,8 @@ typedef enum {
     GDN_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment or cu_seqlens */
     GDN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. K != 128) */
     GDN_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the *_workspace_size */
-    GDN_ERR_CUDA = 4           /* a CUDA launch or attribute call failed */
+    GDN_ERR_CUDA = 4,          /* a CUDA launch or attribute call failed */
+    GDN_ERR_TIMEOUT = 5        /* a device-side wait gave up (gdn_device_status) */
 } gdn_status;
 
 typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
@@ -236,6 +237,27 @@ gdn_status gdn_timing_collect(gdn_kernel_time* out, int32_t max_entries, int32_t
 gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* p, const void* q, const void* k,
                                  const void* v, const float* g, const float* beta,
                                  const float* h0, void* o, float* ht, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Device-side failure report.  Every wait of the tensor-core kernels on an mbarrier (a TMA
+ * copy landing, a tensor-core product completing, a warp role handing over) is bounded: after
+ * 2 s of wall time it gives up, sets a bit in the call's error word -- the first 4 bytes of
+ * its workspace, cleared by the first kernel of every gdn_chunk_fwd, gdn_chunk_bwd,
+ * gdn_chunk_fwd_saved and gdn_chunk_bwd_saved call -- and the kernel winds down (issued copies
+ * and products drained, tensor memory released) instead of hanging; the outputs of that call
+ * are then not valid.
+ *
+ * gdn_device_status waits for `stream` (this call does synchronise), reads the error word of
+ * `workspace` (the workspace of the call(s) just enqueued on that stream) and returns GDN_OK,
+ * or GDN_ERR_TIMEOUT with the word's bits in gdn_last_error().  workspace: device pointer, at
+ * least 4 bytes, 16-byte aligned.
+ * ------------------------------------------------------------------------------------ */
+gdn_status gdn_device_status(const void* workspace, void* stream);
+
+/* Test hook of the failure report: one block waits on an mbarrier that no thread ever
+ * completes, gives up after limit_us microseconds (1 .. 1000000) and sets its bit in the error
+ * word of `workspace` (only those 4 bytes are touched).  Asynchronous on `stream`. */
+gdn_status gdn_debug_wait_timeout(void* workspace, int32_t limit_us, void* stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* gdn_last_error(void);

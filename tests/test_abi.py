@@ -112,3 +112,13 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         gdn.lib()
+
+
+def test_device_status_rejects_bad_arguments(L):
+    """The failure-report entry points validate on the host and launch nothing."""
+    lib = L.lib()
+    assert lib.gdn_device_status(None, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_device_status(ctypes.c_void_p(0x1008), None) == L.GDN_ERR_INVALID_ARG  # misaligned
+    assert lib.gdn_debug_wait_timeout(None, 1000, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_debug_wait_timeout(ctypes.c_void_p(0x1000), 0, None) == L.GDN_ERR_INVALID_ARG
+    assert lib.gdn_debug_wait_timeout(ctypes.c_void_p(0x1000), 2000000, None) == L.GDN_ERR_INVALID_ARG
