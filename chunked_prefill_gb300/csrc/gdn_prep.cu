@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         }
         __syncthreads();
         // ... then the off-diagonal blocks on TF32 tiles, by halves: with T_AA, T_BB the inverses
-        // of the two 32 x 32 diagonal halves, T_BA = -T_BB (A_BA T_AA).  Three rounds of at most
+        // of the two 32 x 32 diagonal halves, T_BA = -T_BB (A_BA T_AA).  Three passes of at most
         // two 16 x 16 products per warp; scratch blocks S0..S3 in sTmp.
         {
             auto mm = [&](float (&acc)[2][4], const float* Am, const float* Bm) {  // acc += Am Bm
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
             };
-            // round 1: T10 = -T11 (A10 T00), T32 = -T33 (A32 T22); Y21 = A21 T11, Y31 = A31 T11
+            // pass 1: T10 = -T11 (A10 T00), T32 = -T33 (A32 T22); Y21 = A21 T11, Y31 = A31 T11
             zero();
             if (w == 0 || w == 1) {
                 const int lo = 2 * w;  // 0 or 2
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 put(slot(w), acc, 1.f);
             }
             __syncthreads();
-            // round 2: Y20 = A20 T00 + A21 T10 (S0), Y30 = A30 T00 + A31 T10 (S1);
+            // pass 2: Y20 = A20 T00 + A21 T10 (S0), Y30 = A30 T00 + A31 T10 (S1);
             // T21 = -T22 Y21, T31 = -(T32 Y21 + T33 Y31)
             zero();
             if (w == 0 || w == 1) {
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 put(tblk(tri(3, 1)), acc, -1.f);
             }
             __syncthreads();
-            // round 3: T20 = -T22 Y20, T30 = -(T32 Y20 + T33 Y30)
+            // pass 3: T20 = -T22 Y20, T30 = -(T32 Y20 + T33 Y30)
             if (w == 0) {
                 zero();
                 mm(acc, tblk(tri(2, 2)), slot(0));
