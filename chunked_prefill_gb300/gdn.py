@@ -314,6 +314,36 @@ def gdn_chunk_bwd_saved(q, k, v, g, beta, scale, h, ctx, dO, dht=None, cu_seqlen
     return dq, dk, dv, dg, db, dh0
 
 
+def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
+                               output_final_state=True, cu_seqlens=None, stream=None):
+    """Low-level forward under the FlashQLA name (usage page, "low-level API"): returns
+    (g_cum, A, o, h, final_state) -- the in-chunk cumulative gate, every token's row of its
+    chunk's (I + A)^-1, the output, the state entering every chunk and the final state (None
+    unless output_final_state).  The chunk records that chunk_gated_delta_rule_bwd reads back
+    stay attached to h (attribute gdn_ctx), so h must be passed to it unchanged."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    g_cum, A, o, h, ht, ctx = gdn_chunk_fwd_saved(q, k, v, g, beta, scale, h0=initial_state,
+                                                  output_final_state=output_final_state,
+                                                  cu_seqlens=cu_seqlens, stream=stream)
+    h.gdn_ctx = ctx
+    return g_cum, A, o, h, ht
+
+
+def chunk_gated_delta_rule_bwd(q, k, v, g, beta, h, do, dht=None, scale=None,
+                               cu_seqlens=None, stream=None):
+    """Low-level backward from chunk_gated_delta_rule_fwd's h (same q, k, v, g, beta, scale and
+    cu_seqlens): returns (dq, dk, dv, dg, dbeta, dh0).  g and beta are the forward's inputs,
+    not its cumulative gate."""
+    ctx = getattr(h, "gdn_ctx", None)
+    if ctx is None:
+        raise ValueError("h must be the state tensor returned by chunk_gated_delta_rule_fwd")
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    return gdn_chunk_bwd_saved(q, k, v, g, beta, scale, h, ctx, do, dht=dht,
+                               cu_seqlens=cu_seqlens, stream=stream)
+
+
 def _prologue_problem(q_raw, a):
     if q_raw.dim() != 4 or a.dim() != 3 or a.shape[:2] != q_raw.shape[:2]:
         raise ValueError("q_raw must be [B,T,Hqk,K] and a [B,T,Hv]")

@@ -120,3 +120,28 @@ def test_autograd_with_saved_states_matches_recompute():
         grads.append([xs[n].grad.float().cpu().numpy() for n in ("q", "k", "v", "g", "beta", "h0")])
     for a, b in zip(*grads):
         assert np.array_equal(a, b)
+
+
+def test_low_level_names_match_the_saved_pair():
+    """chunk_gated_delta_rule_fwd / _bwd (the usage page's low-level names, varlen form) give
+    the saved pair's results bit for bit, and those are checked against the oracle above."""
+    from chunked_prefill_gb300 import gdn
+    lens = [70, 0, 129]
+    inp = make_inputs(1, sum(lens), 2, 4, seed=65, h0_std=0.1, lengths=lens, backward=True)
+    d, (g_cum, A, o, h, ht, ws) = saved_fwd(inp)
+    ref_b = gdn.gdn_chunk_bwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, h, ws,
+                                    d["dO"], dht=d["dht"], cu_seqlens=d["cu"])
+    got_f = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                           scale=inp.scale, initial_state=d["h0"],
+                                           output_final_state=True, cu_seqlens=d["cu"])
+    got_b = gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], got_f[3],
+                                           d["dO"], dht=d["dht"], scale=inp.scale,
+                                           cu_seqlens=d["cu"])
+    torch.cuda.synchronize()
+    for a, b in zip(got_f, (g_cum, A, o, h, ht)):
+        assert torch.equal(a, b)
+    for name, a, b in zip(NAMES, got_b, ref_b):
+        assert torch.equal(a, b), name
+    with pytest.raises(ValueError):
+        gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h.clone(),
+                                       d["dO"], scale=inp.scale, cu_seqlens=d["cu"])
