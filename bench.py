@@ -582,9 +582,16 @@ def main():
                                "streams, two device buffer sets alternating between steps"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, toks, dt, thr, n = oracle_sample(inp, 10.0, w.backward)
+        reps = 1
+        if n >= max(lens):  # the whole workload fits the budget: repeat it up to ~10 s
+            while dt < 10.0 and reps < 50:
+                _, tk, d, thr, _ = oracle_sample_fixed(inp, n, w.backward)
+                toks, dt, reps = toks + tk, dt + d, reps + 1
+            tps = toks / dt
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": f"first {n} tokens of each of {len(lens)} sequence(s), "
-                                          f"all {w.Hv} v-heads ({toks} tokens, {dt:.1f} s)"}
+                                          f"all {w.Hv} v-heads, {reps} call(s) ({toks} tokens, "
+                                          f"{dt:.1f} s)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
