@@ -14,6 +14,10 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libgdn.so")
 BUILD = os.path.join(ROOT, "_build")
+# checked variant (-DGDN_CHECK): every output store tests its index against the tensor's
+# extent and records ERR_BOUNDS instead of writing out of range; for tests, not for timing
+LIB_CHECK = os.path.join(HERE, "libgdn_check.so")
+BUILD_CHECK = os.path.join(ROOT, "_build_check")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,22 +35,24 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale(objs) -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
     deps.append(os.path.join(ROOT, "include", "gdn.h"))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False,
+          checked: bool = False) -> str:
+    lib, bdir = (LIB_CHECK, BUILD_CHECK) if checked else (LIB, BUILD)
+    os.makedirs(bdir, exist_ok=True)
     srcs = sources()
-    objs = [os.path.join(BUILD, os.path.basename(s) + ".o") for s in srcs]
-    if not force and not _stale(objs):
-        return LIB
-    extra = ["-Xptxas", "-v"] if ptxas_v else []
+    objs = [os.path.join(bdir, os.path.basename(s) + ".o") for s in srcs]
+    if not force and not _stale(lib):
+        return lib
+    extra = (["-Xptxas", "-v"] if ptxas_v else []) + (["-DGDN_CHECK"] if checked else [])
 
     def compile_one(so):
         src, obj = so
@@ -63,14 +69,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
     if ptxas_v:
         for s, log in zip(srcs, logs):
             print(f"== {os.path.basename(s)}\n{log}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv,
+                checked="--checked" in sys.argv))

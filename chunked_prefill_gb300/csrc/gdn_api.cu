@@ -298,6 +298,9 @@ gdn_status gdn_device_status(const void* workspace, void* stream) {
     cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, cs);
     if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+    if (word & int(0x80000000u))  // ERR_BOUNDS: set by checked builds only
+        return fail(GDN_ERR_BOUNDS, "a checked build skipped an out-of-range store (error word 0x%08x)",
+                    unsigned(word));
     if (word != 0)
         return fail(GDN_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%08x)", unsigned(word));
     return GDN_OK;

@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
     const int Hv = P.Hv, Hqk = P.Hqk, G = Hv / Hqk;
     const float sc = P.scale;
     const int64_t qk_stride = int64_t(Hqk) * KD, v_stride = int64_t(Hv) * VD;
+    const int64_t T_all = P.cu ? int64_t(P.T) : int64_t(P.N) * P.T;  // tokens (store extents)
     const uint32_t base = smem_addr(sm);
     const uint32_t aV = base + L_V, aDO = base + L_DO, aW = base + L_W, aTU = base + L_TU, aP = base + L_P,
                    aT = base + L_T, aDT = base + L_DT, aQK = base + L_QK, aDV = base + L_DV, aH = base + L_H,
@@ -697,7 +698,8 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
 #pragma unroll
             for (int ii = 0; ii < 16; ++ii) {
                 const int cx = c16 + ii;
-                if (cx < c) dv[ii * v_stride] = __float2bfloat16_rn(sBeta[cx] * y[ii]);
+                if (cx < c && in_range(int64_t(j) * VD + v + (tc + cx) * v_stride, T_all * v_stride, P.err))
+                    dv[ii * v_stride] = __float2bfloat16_rn(sBeta[cx] * y[ii]);
                 y[ii] *= vc[ii];
             }
             const float cs = lane_colsum16(y);
@@ -740,14 +742,16 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
                     const int cx = c16 + ii;
-                    if (cx < c) dq[(tc + cx) * Hv * KD] = sc * sE[cx] * a[ii] + b[ii];
+                    if (cx < c && in_range(int64_t(j) * KD + k + (tc + cx) * Hv * KD, T_all * Hv * KD, P.err))
+                        dq[(tc + cx) * Hv * KD] = sc * sE[cx] * a[ii] + b[ii];
                 }
             } else {
                 __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(B.dq) + int64_t(qh) * KD + k;
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
                     const int cx = c16 + ii;
-                    if (cx < c) dq[(tc + cx) * qk_stride] = __float2bfloat16_rn(sc * sE[cx] * a[ii] + b[ii]);
+                    if (cx < c && in_range(int64_t(qh) * KD + k + (tc + cx) * qk_stride, T_all * qk_stride, P.err))
+                        dq[(tc + cx) * qk_stride] = __float2bfloat16_rn(sc * sE[cx] * a[ii] + b[ii]);
                 }
             }
             float qc[16];
@@ -983,14 +987,16 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
                     const int cx = c16 + ii;
-                    if (cx < c) dk[(tc + cx) * Hv * KD] = x[ii];
+                    if (cx < c && in_range(int64_t(j) * KD + k + (tc + cx) * Hv * KD, T_all * Hv * KD, P.err))
+                        dk[(tc + cx) * Hv * KD] = x[ii];
                 }
             } else {
                 __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(B.dk) + int64_t(qh) * KD + k;
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
                     const int cx = c16 + ii;
-                    if (cx < c) dk[(tc + cx) * qk_stride] = __float2bfloat16_rn(x[ii]);
+                    if (cx < c && in_range(int64_t(qh) * KD + k + (tc + cx) * qk_stride, T_all * qk_stride, P.err))
+                        dk[(tc + cx) * qk_stride] = __float2bfloat16_rn(x[ii]);
                 }
             }
         }
@@ -1026,7 +1032,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int r = 2 * lane + u;
-                if (r < c) {
+                if (r < c && in_range((tc + r) * Hv + j, T_all * Hv, P.err)) {
                     B.dg[(tc + r) * Hv + j] = vals[u];
                     B.dbeta[(tc + r) * Hv + j] = dbv[u];
                 }

@@ -11,6 +11,20 @@ namespace gdn {
 constexpr int KD = 128;  // key dim
 constexpr int VD = 128;  // value dim
 
+// Checked builds (compiled with -DGDN_CHECK): an output store first tests its element index
+// against the extent of the tensor it writes; an index outside [0, n) sets ERR_BOUNDS in the
+// call's error word and the store is skipped.  Release builds compile the test away.
+constexpr int ERR_BOUNDS = int(0x80000000u);
+#ifdef GDN_CHECK
+__device__ __forceinline__ bool in_range(int64_t i, int64_t n, int* err) {
+    if (i >= 0 && i < n) return true;
+    if (err) atomicOr(err, ERR_BOUNDS);
+    return false;
+}
+#else
+__device__ __forceinline__ bool in_range(int64_t, int64_t, int*) { return true; }
+#endif
+
 template <typename Op> struct OpTraits;
 template <> struct OpTraits<__nv_bfloat16> {
     static constexpr int PAD = 8;  // 16 bytes: ldmatrix rows land on distinct banks

@@ -642,9 +642,11 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             const int c = gb.c;
             __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(P.o) + (tc * P.Hv + j) * VD;
             const int64_t rs = int64_t(P.Hv) * VD;
+            const int64_t o_n = (P.cu ? int64_t(P.T) : int64_t(P.N) * P.T) * rs;
             for (int idx = v; idx < c * 16; idx += 128) {
                 const int r = idx >> 4, cv = idx & 15;
-                *reinterpret_cast<uint4*>(ob + r * rs + cv * 8) = lds128(so + (r * LDO + cv * 8) * 2);
+                if (in_range((tc * P.Hv + j) * VD + r * rs + cv * 8 + 7, o_n, P.err))
+                    *reinterpret_cast<uint4*>(ob + r * rs + cv * 8) = lds128(so + (r * LDO + cv * 8) * 2);
             }
             named_sync(2, 128);
             if (lane == 0) mbar_arrive(&bars[B_GFREE0 + gs]);  // done with this chunk's gates

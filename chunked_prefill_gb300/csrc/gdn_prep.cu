@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     const int gq = lane >> 2, tq = lane & 3;
     const uint32_t kq = smem_addr(smem + S::oKQ);
     int* err = P.err;
+    const int64_t T_all = P.cu ? int64_t(P.T) : int64_t(P.N) * P.T;  // tokens (store extents)
     const bool store_t = P.prep_stride >= PREP_BWD_BYTES;  // T in the record (backward)
     const bool want_t = store_t || P.a_out != nullptr;
 
@@ -202,7 +203,8 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 sEi[r] = expf(-gm[u]);
                 sBeta[r] = bv[u];
                 sBe[r] = bv[u] * e;
-                if (P.gam_out && r < c) P.gam_out[(tc + r) * P.Hv + j] = gm[u];
+                if (P.gam_out && r < c && in_range((tc + r) * P.Hv + j, T_all * P.Hv, err))
+                    P.gam_out[(tc + r) * P.Hv + j] = gm[u];
             }
             if (lane == 0) *sFlag = (last < -80.f || !(last == last)) ? 1 : 0;
         }
@@ -461,7 +463,8 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 q4.z = pack_bf16(tkeep[8 * u4 + 4], tkeep[8 * u4 + 5]);
                 q4.w = pack_bf16(tkeep[8 * u4 + 6], tkeep[8 * u4 + 7]);
                 if (store_t) *reinterpret_cast<uint4*>(smem + S::oT + r * 128 + ((c8 ^ (r & 7)) << 4)) = q4;
-                if (P.a_out && r < c)  // token tc + r: its row of T, 64 bf16 columns
+                if (P.a_out && r < c &&  // token tc + r: its row of T, 64 bf16 columns
+                    in_range(((tc + r) * P.Hv + j) * CH + 8 * c8 + 7, T_all * P.Hv * CH, err))
                     *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.a_out) +
                                               ((tc + r) * P.Hv + j) * CH + 8 * c8) = q4;
             }

@@ -17,9 +17,12 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgdn.so")
+# GDN_LIB selects another in-tree build of the same library (the checked variant
+# libgdn_check.so in the bounds tests); the default is the release build
+LIB_PATH = os.environ.get("GDN_LIB") or os.path.join(_HERE, "libgdn.so")
 
-GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = range(6)
+(GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_TIMEOUT,
+ GDN_ERR_BOUNDS) = range(7)
 GDN_BF16, GDN_FP32 = 0, 1
 CP_AUTO, CP_OFF, CP_EXACT, CP_WARMUP = 0, 1, 2, 3
 _STATUS = {1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE",
@@ -97,8 +100,9 @@ def _check(rc: int):
 
 
 def gdn_device_status(workspace, stream=None) -> int:
-    """Wait for the stream and read the error word of a call's workspace: GDN_OK, or
-    GDN_ERR_TIMEOUT when a device-side wait of that call gave up (see include/gdn.h)."""
+    """Wait for the stream and read the error word of a call's workspace: GDN_OK,
+    GDN_ERR_BOUNDS when a checked build skipped an out-of-range store, or GDN_ERR_TIMEOUT
+    when a device-side wait of that call gave up (see include/gdn.h)."""
     return lib().gdn_device_status(_ptr(workspace), _stream(stream))
 
 

@@ -47,7 +47,8 @@ typedef enum {
     GDN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. K != 128) */
     GDN_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the *_workspace_size */
     GDN_ERR_CUDA = 4,          /* a CUDA launch or attribute call failed */
-    GDN_ERR_TIMEOUT = 5        /* a device-side wait gave up (gdn_device_status) */
+    GDN_ERR_TIMEOUT = 5,       /* a device-side wait gave up (gdn_device_status) */
+    GDN_ERR_BOUNDS = 6         /* checked build: a store index fell outside its tensor (gdn_device_status) */
 } gdn_status;
 
 typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
@@ -251,6 +252,12 @@ gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* p, const void* q, const void
  * `workspace` (the workspace of the call(s) just enqueued on that stream) and returns GDN_OK,
  * or GDN_ERR_TIMEOUT with the word's bits in gdn_last_error().  workspace: device pointer, at
  * least 4 bytes, 16-byte aligned.
+ *
+ * Checked builds of this library (compiled with -DGDN_CHECK; libgdn_check.so, for tests)
+ * also test the element index of every output store of the bf16 path (o, dq, dk, dv, dg,
+ * dbeta, gamma and the rows of T) against the tensor's extent; a store outside it is skipped
+ * and sets bit 31 of the error word, and gdn_device_status then returns GDN_ERR_BOUNDS.
+ * Release builds do not test and never set that bit.
  * ------------------------------------------------------------------------------------ */
 gdn_status gdn_device_status(const void* workspace, void* stream);
 
