@@ -122,3 +122,13 @@ def test_device_status_rejects_bad_arguments(L):
     assert lib.gdn_debug_wait_timeout(None, 1000, None) == L.GDN_ERR_INVALID_ARG
     assert lib.gdn_debug_wait_timeout(ctypes.c_void_p(0x1000), 0, None) == L.GDN_ERR_INVALID_ARG
     assert lib.gdn_debug_wait_timeout(ctypes.c_void_p(0x1000), 2000000, None) == L.GDN_ERR_INVALID_ARG
+
+
+def test_status_codes_match_the_header(L):
+    """Every GDN_* status value the header's enum declares has the same value in the binding."""
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    codes = dict((n, int(v)) for n, v in re.findall(r"\b(GDN_(?:OK|ERR_\w+))\s*=\s*(\d+)", src))
+    assert {"GDN_OK", "GDN_ERR_TIMEOUT", "GDN_ERR_BOUNDS"} <= set(codes)
+    for name, value in codes.items():
+        assert getattr(L, name) == value, name
