@@ -2,9 +2,11 @@
 """Benchmark of the chunked gated delta rule on one or more GB300 GPUs.
 
 One step = one full pass of the hot path over one synthetic batch: gdn_chunk_fwd for the
-forward workloads (planner, context-parallel phase A + fix-up when used, output stage),
-gdn_chunk_fwd + gdn_chunk_bwd for the training-step workload.  Prints ONE JSON line on
-rank 0.
+forward workloads, gdn_chunk_fwd + gdn_chunk_bwd for the training-step workload.  Prints ONE
+JSON line on rank 0; for the default forward workload (1 x 32768 tokens, 2 / 8 heads) the
+line also carries the training step at 1 x 32768 tokens, 16 / 16 heads ("fwdbwd"), the
+metric's other half.  "roofline" is the whole step's: the method's compulsory bytes (each
+input read once, each output written once) over the step time, with each kernel's share.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -130,9 +132,11 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def make_step(inp, dev, backward, save_states=False, d=None, stream=None):
+def make_step(inp, dev, backward, save_states=False, d=None, stream=None, fwd_kw=None):
     """One step on device inputs (copied from inp, or the given dict d), with its own outputs
-    and workspace; every library call is enqueued on ``stream`` (None = current stream)."""
+    and workspace; every library call is enqueued on ``stream`` (None = current stream).
+    fwd_kw: extra problem fields of the forward (context-parallel mode, warm-up chunks)."""
+    fwd_kw = dict(fwd_kw or {})
     from chunked_prefill_gb300 import gdn
     if d is None:
         d = {n: (None if getattr(inp, n) is None else getattr(inp, n).to(dev).contiguous())
@@ -142,7 +146,7 @@ def make_step(inp, dev, backward, save_states=False, d=None, stream=None):
     cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
     cu_host = inp.cu_seqlens
     o = torch.empty_like(d["v"])
-    prob = gdn.Problem(d["q"], d["v"], inp.scale, cu, cu_host)
+    prob = gdn.Problem(d["q"], d["v"], inp.scale, cu, cu_host, **fwd_kw)
     ht = torch.empty(prob.num_seqs, d["v"].shape[2], 128, 128, device=dev)
     ws_f = torch.empty(max(gdn.gdn_chunk_fwd_workspace_size(prob), 16), dtype=torch.uint8, device=dev)
     bufs = None
@@ -173,7 +177,7 @@ def make_step(inp, dev, backward, save_states=False, d=None, stream=None):
     def step():
         gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, h0=d["h0"],
                           cu_seqlens=cu, cu_seqlens_host=cu_host, o=o, ht=ht, workspace=ws_f,
-                          stream=stream)
+                          stream=stream, **fwd_kw)
         if backward:
             gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, d["dO"],
                               h0=d["h0"], dht=d["dht"], cu_seqlens=cu, cu_seqlens_host=cu_host,
@@ -341,35 +345,51 @@ def oracle_sample_fixed(inp, n, backward):
     return new_cu[-1] / dt, new_cu[-1], dt, orc.max_threads(), n
 
 
-# DRAM bytes (read + write) of one launch, from the ncu capture summarised in profiles/
-# (fwd_prep_t32k_hqk2_hv8.md); None where no capture of the current kernel exists.
-NCU_TRAFFIC = {("fwd_t32k_hqk2_hv8", "fwd_prep"): 36.740096e6 + 73.815040e6,
-               ("fwdbwd_t32k_hqk16_hv16", "bwd_local"): 1413.688e6 + 382.684416e6}
+# DRAM bytes (read + write) of one whole step, from an ncu capture of the step's kernels,
+# keyed by workload and by the set of kernels the step launches: a key that no longer
+# matches the kernels this build launches gives no figure (null), so a capture of an older
+# kernel set is never reported against a newer one.
+NCU_STEP_TRAFFIC = {}
 
 
-def kernel_bytes(name, tokens, lens, w):
-    """Algorithmic HBM bytes of one launch of a kernel: the tensors its step of the method
-    must read or write once (bf16 activations, fp32 gates and states; for the chunk-local
-    preparation also the 32 KB per (chunk, v-head) record it hands to the scan)."""
+def method_bytes(tokens, lens, w):
+    """Compulsory HBM bytes of the method per tensor (bf16 activations, fp32 gates and
+    states): what the step must read or write once, whatever the kernels in between."""
     nseq = len(lens)
-    qk = tokens * w.Hqk * 128 * 2
-    vv = tokens * w.Hv * 128 * 2
-    gb = tokens * w.Hv * 4 * 2
     st = nseq * w.Hv * 128 * 128 * 4
-    h0 = st if w.h0_std > 0 else 0
-    chunks = sum((int(n) + 63) // 64 for n in lens)
-    rec = chunks * w.Hv * 32768
-    table = {
-        "fwd_prep": (2 * qk + gb + rec, "q,k,g,beta read; W',TU,P records written"),
-        "fwd_phase_c": (2 * qk + 2 * vv + gb + h0 + st, "q,k,v,g,beta,h0 read; o,ht written"),
-        "fwd_phase_a": (qk + vv + gb + h0, "k,v,g,beta,h0 read"),
-        "fwd_recompute_states": (qk + vv + gb + h0, "k,v,g,beta,h0 read"),
-        "bwd_phase_a": (2 * qk + vv + gb + st, "q,k,dO,g,beta,dht read"),
-        "bwd_dh_scan": (2 * qk + vv + gb + 2 * st, "q,k,dO,g,beta,dht read; dh0 written"),
-        "bwd_local": (2 * qk + 2 * vv + gb + 2 * qk + vv + gb,
-                      "q,k,v,dO,g,beta read; dq,dk,dv,dg,dbeta written"),
-    }
-    return table.get(name, (0.0, "not counted"))
+    return {"q": tokens * w.Hqk * 128 * 2, "k": tokens * w.Hqk * 128 * 2,
+            "v": tokens * w.Hv * 128 * 2, "g": tokens * w.Hv * 4, "beta": tokens * w.Hv * 4,
+            "h0": st if w.h0_std > 0 else 0, "o": tokens * w.Hv * 128 * 2, "ht": st,
+            "dO": tokens * w.Hv * 128 * 2, "dht": st, "dq": tokens * w.Hqk * 128 * 2,
+            "dk": tokens * w.Hqk * 128 * 2, "dv": tokens * w.Hv * 128 * 2,
+            "dg": tokens * w.Hv * 4, "dbeta": tokens * w.Hv * 4, "dh0": st}
+
+
+# the method tensors each kernel reads or writes (intermediate records and partial states
+# handed between this library's own kernels are not method bytes and are not counted)
+KERNEL_TENSORS = {
+    "fwd_prep": ("q", "k", "g", "beta"),
+    "fwd_pass1": ("q", "k", "v", "g", "beta", "h0", "o", "ht"),
+    "fwd_phase_c": ("q", "k", "v", "g", "beta", "h0", "o", "ht"),
+    "fwd_phase_a": ("k", "v", "g", "beta", "h0"),
+    "fwd_recompute_states": ("k", "v", "g", "beta", "h0"),
+    "bwd_phase_a": ("q", "k", "dO", "g", "beta", "dht"),
+    "bwd_dh_scan": ("q", "k", "dO", "g", "beta", "dht", "dh0"),
+    "bwd_local": ("q", "k", "v", "dO", "g", "beta", "dq", "dk", "dv", "dg", "dbeta"),
+}
+
+
+def kernel_bytes(name, mb):
+    names = KERNEL_TENSORS.get(name)
+    if not names:
+        return 0.0, "no method tensors"
+    return float(sum(mb[n] for n in names)), ",".join(names)
+
+
+def step_tensors(backward):
+    f = ("q", "k", "v", "g", "beta", "h0", "o", "ht")
+    b = ("dO", "dht", "dq", "dk", "dv", "dg", "dbeta", "dh0")
+    return f + b if backward else f
 
 
 def config_of(name):
@@ -483,6 +503,11 @@ def main():
     ap.add_argument("--prologue", action="store_true",
                     help="fused prologue forward / reverse: one JSON line per leg and shape "
                          "(an auxiliary report, not the benchmark line)")
+    ap.add_argument("--no-fwdbwd", action="store_true",
+                    help="forward workloads: skip the fwd+bwd training-step sub-record")
+    ap.add_argument("--warmup-report", action="store_true",
+                    help="opt-in warm-up mode vs the exact mode: step time and error against "
+                         "the oracle (an auxiliary report, not the benchmark line)")
     ap.add_argument("--sweep", action="store_true",
                     help="head / length sweep of the forward: one JSON line per point "
                          "(an auxiliary report, not the benchmark line)")
@@ -495,92 +520,57 @@ def main():
     if args.prologue:
         prologue_bench(args, local)
         return
+    if args.warmup_report:
+        warmup_report(args, local)
+        return
 
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
 
-    from chunked_prefill_gb300 import build, gdn
+    from chunked_prefill_gb300 import build
     build.build()
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
-    inp = workload_inputs(args.workload)
-    lens = lengths_of(inp)
-    tokens = sum(lens)
-    save = args.save_states and w.backward
-    step, d, o, ht, cu, cu_host, ws_f, ws_b, bufs = make_step(inp, dev, w.backward, save)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
     if args.profile:
         args.no_e2e = args.no_cpu_baseline = True
-    with ClockSampler(local if not args.profile else None) as clk:
-        # keep the GPU busy (untimed) while nvidia-smi starts, so the sampled clocks are
-        # those under load and its start-up does not overlap the timed steps
-        t_busy = time.time() + (0.0 if args.profile else 1.0)
-        while time.time() < t_busy:
-            step()
-            torch.cuda.synchronize()
-        ms_total = time_steps(step, args.steps, flush)
-    # per-kernel split from a second, instrumented pass (the event records between kernels
-    # would otherwise sit inside the headline's timed region)
-    gdn.gdn_timing_enable(True)
-    time_steps(step, args.steps, flush)
-    gdn.gdn_timing_enable(False)
-    kt = gdn.gdn_timing_collect()
-    torch.cuda.synchronize()
-    barrier(world)
-    ms_total = max_over_ranks(ms_total, world)
-    ms_per_step = ms_total / args.steps
-    value = world * tokens / (ms_per_step / 1000.0)
-
-    pk, pk_kind = peaks()
-    fl = rl.fwd_flops(lens, w.Hqk, w.Hv) + (rl.bwd_flops(lens, w.Hqk, w.Hv) if w.backward else 0)
-    by = rl.fwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
-    if w.backward:
-        by += rl.bwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
-    t_roof = max(fl / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
-
-    # dominant kernel and its roofline
-    launches = sum(v[0] for v in kt.values())
-    dom = max(kt.items(), key=lambda kv: kv[1][1]) if kt else ("none", (1, float("nan")))
-    dom_name, (dom_n, dom_ms) = dom
-    dom_avg_s = dom_ms / max(dom_n, 1) / 1000.0
-    alg, unit_note = kernel_bytes(dom_name, tokens, lens, w)
-    achieved = alg / dom_avg_s / 1e9
-    roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-            "traffic": NCU_TRAFFIC.get((args.workload, dom_name)),
-            "peak_kind": pk_kind, "algorithmic_bytes_per_launch": alg, "bytes_counted": unit_note,
-            "avg_launch_ms": dom_avg_s * 1000.0,
-            "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items()}}
-
+    res = measure(args.workload, args, dev, world, local, clocks=not args.profile,
+                  save=args.save_states)
+    w = WORKLOADS[args.workload]
+    tokens = res["tokens"]
+    value = world * tokens / (res["ms_per_step"] / 1000.0)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / (tokens / (PUBLISHED_MS[args.workload] / 1000.0))
                         if args.workload in PUBLISHED_MS and world == 1 else None),
+        "vs_baseline_note": ("ratio to the FlashQLA pages' H200 forward latency for this "
+                             "shape (another machine: context, not the target)"
+                             if args.workload in PUBLISHED_MS else None),
         "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_of(args.workload), **({"save_states": True} if save else {})),
-        "roofline": roof,
-        "step_roofline": {"flops": fl, "bytes": by, "roofline_ms": t_roof * 1000.0,
-                          "frac": t_roof * 1000.0 / ms_per_step, "peak_kind": pk_kind},
-        "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "config": dict(config_of(args.workload),
+                       **({"save_states": True} if args.save_states and w.backward else {})),
+        "roofline": res["roofline"],
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
     }
-    if not args.no_e2e:
-        e2e_ms, h2d, d2h = e2e_run(inp, dev, args.steps, args.warmup, w.backward, save)
-        e2e_ms = max_over_ranks(e2e_ms, world)
-        line["e2e"] = {"value": world * tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                       "mode": "pinned host buffers; copies in, calls and copies out on three "
-                               "streams, two device buffer sets alternating between steps"}
+    if "e2e" in res:
+        line["e2e"] = res["e2e"]
+    # the metric's other half: the fwd+bwd training step at T = 32768 (16 / 16 heads), as a
+    # sub-record of the same line
+    if not w.backward and not args.no_fwdbwd and not args.profile:
+        sub = measure(FWDBWD_WORKLOAD, args, dev, world, local, clocks=True, save=False)
+        line["fwdbwd"] = {
+            "workload": FWDBWD_WORKLOAD, "config": config_of(FWDBWD_WORKLOAD),
+            "ms_per_step": sub["ms_per_step"],
+            "value": world * sub["tokens"] / (sub["ms_per_step"] / 1000.0), "unit": "tokens/s",
+            "roofline": sub["roofline"], "gpu_launches": sub["launches"], "clocks": sub["clocks"],
+        }
+        if "e2e" in sub:
+            line["fwdbwd"]["e2e"] = sub["e2e"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp = workload_inputs(args.workload)
+        lens = lengths_of(inp)
         tps, toks, dt, thr, n = oracle_sample(inp, 10.0, w.backward)
         reps = 1
         if n >= max(lens):  # the whole workload fits the budget: repeat it up to ~10 s
@@ -597,6 +587,123 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+FWDBWD_WORKLOAD = "fwdbwd_t32k_hqk16_hv16"
+
+
+def measure(name, args, dev, world, local, clocks=True, save=False, fwd_kw=None):
+    """Warm-up, then K timed steps (L2 flushed between them, CUDA events, max over ranks),
+    a second instrumented pass for the per-kernel split, the step roofline and (unless
+    disabled) the end-to-end leg of one workload."""
+    from chunked_prefill_gb300 import gdn
+    w = WORKLOADS[name]
+    inp = workload_inputs(name)
+    lens = lengths_of(inp)
+    tokens = sum(lens)
+    save = save and w.backward
+    step = make_step(inp, dev, w.backward, save, fwd_kw=fwd_kw)[0]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local if clocks else None) as clk:
+        # keep the GPU busy (untimed) while nvidia-smi starts, so the sampled clocks are
+        # those under load and its start-up does not overlap the timed steps
+        t_busy = time.time() + (1.0 if clocks else 0.0)
+        while time.time() < t_busy:
+            step()
+            torch.cuda.synchronize()
+        ms_total = time_steps(step, args.steps, flush)
+    # per-kernel split from a second, instrumented pass (the event records between kernels
+    # would otherwise sit inside the headline's timed region)
+    gdn.gdn_timing_enable(True)
+    time_steps(step, args.steps, flush)
+    gdn.gdn_timing_enable(False)
+    kt = gdn.gdn_timing_collect()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_per_step = ms_total / args.steps
+
+    pk, pk_kind = peaks()
+    fl = rl.fwd_flops(lens, w.Hqk, w.Hv) + (rl.bwd_flops(lens, w.Hqk, w.Hv) if w.backward else 0)
+    by = rl.fwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
+    if w.backward:
+        by += rl.bwd_bytes(tokens, len(lens), w.Hqk, w.Hv, h0=w.h0_std > 0)
+    t_tc = fl / (pk["bf16_tflops"] * 1e12)
+    t_hbm = by / (pk["hbm_gbs"] * 1e9)
+    mb = method_bytes(tokens, lens, w)
+    kernels = {}
+    for k, (n, ms) in kt.items():
+        kb, names = kernel_bytes(k, mb)
+        avg_s = ms / max(n, 1) / 1000.0
+        kernels[k] = {"launches_per_step": n / args.steps, "ms_per_step": ms / args.steps,
+                      "share": ms / max(sum(v[1] for v in kt.values()), 1e-30),
+                      "method_bytes_per_launch": kb, "method_tensors": names,
+                      "achieved_gbs": kb / avg_s / 1e9 if kb else None,
+                      "frac": kb / avg_s / 1e9 / pk["hbm_gbs"] if kb else None}
+    dom = max(kt.items(), key=lambda kv: kv[1][1])[0] if kt else None
+    achieved = by / (ms_per_step / 1000.0) / 1e9
+    key = (name, tuple(sorted(kt)))
+    roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor", "scope": "whole step",
+            "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "peak_kind": pk_kind,
+            "traffic": NCU_STEP_TRAFFIC.get(key),
+            "algorithmic_bytes_per_step": by,
+            "bytes_counted": "+".join(step_tensors(w.backward)) + " (each read or written once)",
+            "algorithmic_flops_per_step": fl,
+            "roofline_ms": max(t_tc, t_hbm) * 1000.0,
+            "dominant_kernel": dom, "kernels": kernels}
+    res = {"tokens": tokens, "ms_per_step": ms_per_step, "roofline": roof,
+           "launches": sum(v[0] for v in kt.values()),  # this library's kernels in K steps
+           "clocks": clk.summary() if clocks else None}
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_run(inp, dev, args.steps, args.warmup, w.backward, save)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        res["e2e"] = {"value": world * tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                      "mode": "pinned host buffers; copies in, calls and copies out on three "
+                              "streams, two device buffer sets alternating between steps"}
+    del inp, step, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def warmup_report(args, local):
+    """The opt-in warm-up mode against the exact mode on one workload: step time, and the
+    error of o and of the final state against the fp64 oracle, for warm-up windows of 6 and
+    8 chunks (one JSON line per mode)."""
+    import numpy as np
+    from chunked_prefill_gb300 import build, gdn
+    from oracle import oracle as orc
+    build.build()
+    dev = torch.device("cuda", local)
+    inp = workload_inputs(args.workload)
+    w = WORKLOADS[args.workload]
+    ro, rht = orc.fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.scale, h0=inp.h0,
+                      cu_seqlens=None if inp.cu_seqlens is None else inp.cu_seqlens.numpy())
+    args.no_e2e = True
+    modes = [("exact", dict(cp_mode=gdn.CP_AUTO))]
+    modes += [(f"warmup{wc}", dict(cp_mode=gdn.CP_WARMUP, warmup_chunks=wc)) for wc in (6, 8)]
+    for label, kw in modes:
+        res = measure(args.workload, args, dev, 1, local, clocks=False, fwd_kw=kw)
+        step, d, o, ht = make_step(inp, dev, False, fwd_kw=kw)[:4]
+        step()
+        torch.cuda.synchronize()
+        oo, hh = o.float().cpu().numpy(), ht.cpu().numpy()
+        rel = lambda a, b: float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
+        print(json.dumps({"warmup_report": True, "workload": args.workload, "mode": label,
+                          "cp": kw, "ms_per_step": res["ms_per_step"],
+                          "tokens_per_s": res["tokens"] / (res["ms_per_step"] / 1000.0),
+                          "o_rel_err": rel(oo, ro), "ht_rel_err": rel(hh, rht),
+                          "kernels_ms_per_step": {k: v["ms_per_step"] for k, v in
+                                                  res["roofline"]["kernels"].items()}}),
+              flush=True)
+        del step, d, o, ht
+        torch.cuda.empty_cache()
 
 
 if __name__ == "__main__":

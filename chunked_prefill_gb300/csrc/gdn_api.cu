@@ -72,7 +72,8 @@ gdn_status validate_problem(const gdn_problem* p) {
         return fail(GDN_ERR_INVALID_ARG, "Hv (%d) must be a multiple of Hqk (%d)", p->Hv, p->Hqk);
     if (p->dtype != GDN_BF16 && p->dtype != GDN_FP32)
         return fail(GDN_ERR_INVALID_ARG, "dtype must be GDN_BF16 or GDN_FP32");
-    if (!isfinite(p->scale)) return fail(GDN_ERR_INVALID_ARG, "scale must be finite");
+    if (!isfinite(p->scale) || !(p->scale > 0.f))
+        return fail(GDN_ERR_INVALID_ARG, "scale must be finite and > 0 (got %g)", double(p->scale));
     if (p->T < 0 || p->B < 0) return fail(GDN_ERR_INVALID_ARG, "B and T must be >= 0");
     if (p->cp_mode < GDN_CP_AUTO || p->cp_mode > GDN_CP_WARMUP)
         return fail(GDN_ERR_INVALID_ARG, "unknown cp_mode %d", p->cp_mode);

@@ -56,7 +56,10 @@ typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
 /* Intra-GPU context parallelism over chunk ranges (FlashQLA pages, "AutoCP" section: when
  * batch * heads leaves SMs idle, each sequence's chunks are split into segments). */
 typedef enum {
-    GDN_CP_AUTO = 0,    /* planner picks segment length L = lambda * sqrt(chunks); exact */
+    GDN_CP_AUTO = 0,    /* exact; the planner picks the segment length L: by default the L
+                           that minimises a cost model of the launches on this GPU (waves of
+                           one CTA per SM, chunk steps, fix-up steps); with cp_lambda > 0 the
+                           pages' rule L = cp_lambda * sqrt(chunks) instead */
     GDN_CP_OFF = 1,     /* one segment per sequence: a plain serial chunk scan */
     GDN_CP_EXACT = 2,   /* segments of cp_segment_chunks chunks; transition fix-up, exact */
     GDN_CP_WARMUP = 3   /* opt-in approximation: each segment starts warmup_chunks chunks
@@ -72,7 +75,8 @@ typedef struct gdn_problem {
     int32_t K;                        /* key dim (128) */
     int32_t V;                        /* value dim (128) */
     int32_t dtype;                    /* gdn_dtype of q, k, v, o, dO, dq, dk, dv */
-    float scale;                      /* output scale (> 0); usually K^-0.5 */
+    float scale;                      /* output scale, finite and > 0 (GDN_ERR_INVALID_ARG
+                                         otherwise); usually K^-0.5 */
     const int32_t* cu_seqlens;        /* device [num_seqs+1] or NULL (then B sequences of T) */
     const int32_t* cu_seqlens_host;   /* HOST copy with the same contents; required iff
                                          cu_seqlens != NULL (sizes the launch grids) */
@@ -80,7 +84,7 @@ typedef struct gdn_problem {
     int32_t cp_mode;                  /* gdn_cp_mode */
     int32_t cp_segment_chunks;        /* EXACT / WARMUP: chunks per segment (0 = auto) */
     int32_t warmup_chunks;            /* WARMUP: warm-up chunks (0 = 8) */
-    float cp_lambda;                  /* AUTO: lambda in L = lambda sqrt(N) (0 = default) */
+    float cp_lambda;                  /* AUTO: lambda in L = lambda sqrt(N) (0 = cost model) */
 } gdn_problem;
 
 /* Bytes of device workspace gdn_chunk_fwd needs for *p (written to *bytes). */
@@ -228,16 +232,28 @@ gdn_status gdn_timing_collect(gdn_kernel_time* out, int32_t max_entries, int32_t
  * cudaFree, no allocating library routine.
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream capture.  All calls
- * share the one array and it keeps the last call's contents (every byte a call reads is
- * written earlier by the same call), so calls whose GPU work overlaps -- on different
- * streams, or from different threads -- race on it and must be serialised by the caller.
+ * with that device current); make that first call before any stream capture.  The lookup is
+ * repeated when the device's context has changed since (e.g. after cudaDeviceReset, which
+ * may load the array at another address), so such a call, too, belongs outside a capture.
+ * All calls share the one array and it keeps the last call's contents (every byte a call
+ * reads is written earlier by the same call), so calls whose GPU work overlaps -- on
+ * different streams, or from different threads -- race on it and must be serialised by the
+ * caller.
+ *
+ * gdn_noalloc_device_status is gdn_device_status for these calls: it waits for `stream` and
+ * reads the error word that the calls keep at the start of the array (their device-side
+ * failure report, see below).  gdn_noalloc_debug_wait_timeout is gdn_debug_wait_timeout on
+ * that word (a test hook).
  * ------------------------------------------------------------------------------------ */
 #define GDN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
 gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* p, const void* q, const void* k,
                                  const void* v, const float* g, const float* beta,
                                  const float* h0, void* o, float* ht, void* stream);
+
+gdn_status gdn_noalloc_device_status(void* stream);
+
+gdn_status gdn_noalloc_debug_wait_timeout(int32_t limit_us, void* stream);
 
 /* ------------------------------------------------------------------------------------
  * Device-side failure report.  Every wait of the tensor-core kernels on an mbarrier (a TMA

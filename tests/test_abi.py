@@ -60,6 +60,8 @@ def fwd_status(L, p, ptrs=None, ws_bytes=1 << 30):
     (dict(T=-1), 1),
     (dict(cp_mode=9), 1),
     (dict(scale=float("nan")), 1),
+    (dict(scale=0.0), 1),           # the scale must be > 0
+    (dict(scale=-0.5), 1),
 ])
 def test_rejects_bad_problems(L, kw, code):
     rc, msg = fwd_status(L, problem(L, **kw))
@@ -122,6 +124,8 @@ def test_device_status_rejects_bad_arguments(L):
     assert lib.gdn_debug_wait_timeout(None, 1000, None) == L.GDN_ERR_INVALID_ARG
     assert lib.gdn_debug_wait_timeout(ctypes.c_void_p(0x1000), 0, None) == L.GDN_ERR_INVALID_ARG
     assert lib.gdn_debug_wait_timeout(ctypes.c_void_p(0x1000), 2000000, None) == L.GDN_ERR_INVALID_ARG
+    lib.gdn_noalloc_debug_wait_timeout.argtypes = [ctypes.c_int32, ctypes.c_void_p]
+    assert lib.gdn_noalloc_debug_wait_timeout(0, None) == L.GDN_ERR_INVALID_ARG
 
 
 def test_status_codes_match_the_header(L):
