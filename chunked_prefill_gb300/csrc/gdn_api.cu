@@ -54,7 +54,8 @@ struct HostPlan {
     int64_t prep_stride = 0;  // bytes per (chunk, v-head) preparation record
     // workspace layout (bytes)
     size_t off_err = 0, off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0,
-           off_mbuf = 0, off_mbuf_t = 0, off_prep = 0, off_end = 0;
+           off_mbuf = 0, off_mbuf_t = 0, off_logb = 0, off_dec = 0, off_prep = 0, off_end = 0;
+    bool full_cp = false;   // every transition computed and every segment rerun
     // backward only
     size_t off_hist = 0, off_dhist = 0, off_dhb = 0, off_dqp = 0, off_dkp = 0;
 };
@@ -75,7 +76,7 @@ gdn_status validate_problem(const gdn_problem* p) {
     if (!isfinite(p->scale) || !(p->scale > 0.f))
         return fail(GDN_ERR_INVALID_ARG, "scale must be finite and > 0 (got %g)", double(p->scale));
     if (p->T < 0 || p->B < 0) return fail(GDN_ERR_INVALID_ARG, "B and T must be >= 0");
-    if (p->cp_mode < GDN_CP_AUTO || p->cp_mode > GDN_CP_WARMUP)
+    if (p->cp_mode < GDN_CP_AUTO || p->cp_mode > GDN_CP_EXACT_FULL)
         return fail(GDN_ERR_INVALID_ARG, "unknown cp_mode %d", p->cp_mode);
     if (p->cp_segment_chunks < 0 || p->warmup_chunks < 0 || !(p->cp_lambda >= 0.f))
         return fail(GDN_ERR_INVALID_ARG, "cp_segment_chunks, warmup_chunks, cp_lambda must be >= 0");
@@ -179,6 +180,7 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
             L = autoL;
             break;
         case GDN_CP_EXACT:
+        case GDN_CP_EXACT_FULL:
         case GDN_CP_WARMUP:
             L = p->cp_segment_chunks > 0 ? p->cp_segment_chunks : autoL;
             break;
@@ -199,6 +201,9 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
     if (max_nseg > 1)
         h.cp = (p->cp_mode == GDN_CP_WARMUP && !backward) ? gdn::CP_WARMUP : gdn::CP_EXACT;
     h.warmup = p->warmup_chunks > 0 ? p->warmup_chunks : 8;
+    // exact mode with decay bounds on the bf16 path; every transition and rerun otherwise
+    h.full_cp = p->cp_mode == GDN_CP_EXACT_FULL || p->dtype != GDN_BF16;
+    const bool bounded = h.cp == gdn::CP_EXACT && !h.full_cp;
 
     size_t off = 0;
     h.off_err = off;
@@ -216,6 +221,10 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
     h.off_mbuf_t = off;  // the backward's reverse fix-up reads the transitions untransposed
     if (h.cp == gdn::CP_EXACT && backward && p->dtype == GDN_BF16) off += KVB * size_t(total_segs) * p->Hv;
     off = align_up(off, 256);
+    h.off_logb = off;  // per (chunk, v-head) transition log-bound, per (segment, v-head) decision
+    if (bounded) off = align_up(off + sizeof(float) * size_t(h.total_chunks) * p->Hv, 256);
+    h.off_dec = off;
+    if (bounded) off = align_up(off + sizeof(int) * size_t(total_segs) * p->Hv, 256);
     h.off_prep = off;  // W', TU, P (and T) tiles of every (chunk, v-head): tensor-core path only
     h.prep_stride = backward ? gdn::PREP_BWD_BYTES : gdn::PREP_FWD_BYTES;
     if (p->dtype == GDN_BF16) off = align_up(off + size_t(h.prep_stride) * h.total_chunks * p->Hv, 256);
@@ -263,6 +272,10 @@ void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Proble
     P.L = h.L;
     P.warmup = h.warmup;
     P.cp = h.cp;
+    P.full_cp = h.full_cp ? 1 : 0;
+    const bool bounded = h.cp == gdn::CP_EXACT && !h.full_cp;
+    P.logb = bounded ? reinterpret_cast<float*>(ws + h.off_logb) : nullptr;
+    P.dec = bounded ? reinterpret_cast<int*>(ws + h.off_dec) : nullptr;
     P.scale = p->scale;
 }
 

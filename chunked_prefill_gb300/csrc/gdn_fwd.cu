@@ -481,9 +481,12 @@ constexpr int fix_smem(int CG) { return FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 +
 // column group over its slice, and the slices are summed through shared memory.  Few chains
 // take CG = 1 (short steps, many CTAs per chain); many chains take a wider CG so that all
 // chains run in one wave and each transition tile is read by fewer CTAs.
+// dec (null = every step composes): the decay-bounded exact mode's per-(segment, v-head)
+// flag; a step whose segment has dec >= 0 has a negligible transition, so its result is S
+// itself (already in xbuf) and the step neither loads its transition nor computes.
 template <bool REV, int CG>
 __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float* mats, float* xbuf,
-                                                 int Hv, int* err) {
+                                                 int Hv, int* err, const int* dec) {
     constexpr int W = 8 * CG, KS = 8 / CG, MS = KD / KS;
     tc::pdl_launch_dependents();
     tc::pdl_wait();
@@ -506,6 +509,22 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
     auto hp = [&](int g, int c) {
         return reinterpret_cast<float4*>(xbuf + (int64_t(g) * Hv + j) * KV + orow * VD + cb + 8 * c + oc);
     };
+    // the first step at or after q whose transition is not negligible (last: none)
+    auto next_active = [&](int q) {
+        if (!dec) return q;
+        while (q < last && dec[int64_t(g0 + seg_of(q)) * Hv + j] >= 0) ++q;
+        return q;
+    };
+    // the first composing step, found by all threads at once (one flag load each)
+    __shared__ int s_first;
+    if (t == 0) s_first = dec ? last : 0;
+    __syncthreads();
+    if (dec)
+        for (int q = t; q < last; q += FIX_T)
+            if (dec[int64_t(g0 + seg_of(q)) * Hv + j] < 0) atomicMin(&s_first, q);
+    __syncthreads();
+    const int q0 = s_first;
+    if (q0 >= last) return;  // every result is its S, already in place
     if (t == 0) {
         for (int b = 0; b < FIX_NB; ++b) tc::mbar_init(&bar[b], 1);
         tc::mbar_fence_init();
@@ -513,23 +532,26 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
     __syncthreads();
     if (t == 0) {
         tc::mbar_expect_tx(&bar[0], KD * KD * 4);
-        tc::bulk_load(Ms, mt(0), KD * KD * 4, &bar[0]);
+        tc::bulk_load(Ms, mt(q0), KD * KD * 4, &bar[0]);
     }
     float4 snext[CG];
 #pragma unroll
     for (int c = 0; c < CG; ++c) {
-        *reinterpret_cast<float4*>(&xs[orow * W + 8 * c + oc]) = *hp(xin(0), c);
-        snext[c] = *hp(xout(0), c);
+        *reinterpret_cast<float4*>(&xs[orow * W + 8 * c + oc]) = *hp(xin(q0), c);
+        snext[c] = *hp(xout(q0), c);
     }
     bool ok = true;
-    for (int q = 0; q < last; ++q) {
-        const int b = q & 1;
-        if (t == 0 && q + 1 < last) {  // into the buffer step q-1 used
+    int uses[FIX_NB] = {0, 0};  // completed loads per buffer (mbarrier phase parity)
+    int b = 0;
+    for (int q = q0; q < last;) {
+        const int qn = next_active(q + 1);
+        if (t == 0 && qn < last) {  // into the other buffer (its last step is done with it)
             tc::mbar_expect_tx(&bar[b ^ 1], KD * KD * 4);
-            tc::bulk_load(Ms + (b ^ 1) * KD * KD, mt(q + 1), KD * KD * 4, &bar[b ^ 1]);
+            tc::bulk_load(Ms + (b ^ 1) * KD * KD, mt(qn), KD * KD * 4, &bar[b ^ 1]);
         }
         FTRACE(q + 1, 0);
-        ok = ok && tc::mbar_wait(&bar[b], (q >> 1) & 1);
+        ok = ok && tc::mbar_wait(&bar[b], uses[b] & 1);
+        ++uses[b];
         FTRACE(q + 1, 1);
         __syncthreads();  // also orders the previous step's xs update
         FTRACE(q + 1, 2);
@@ -537,7 +559,7 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
 #pragma unroll
         for (int c = 0; c < CG; ++c) {
             sj[c] = snext[c];
-            if (q + 1 < last) snext[c] = *hp(xout(q + 1), c);
+            if (qn < last) snext[c] = *hp(xout(qn), c);
         }
         const float* M = Ms + b * KD * KD;
         // acc[r][p]: row r, columns (2p, 2p + 1) as a packed pair (one packed FMA per pair)
@@ -586,10 +608,16 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
                     o.z += p.z;
                     o.w += p.w;
                 }
-                *reinterpret_cast<float4*>(&xs[orow * W + 8 * c + oc]) = o;
                 *hp(xout(q), c) = o;
+                // x entering the next composing step: this result when it follows at once,
+                // else the S that the negligible steps in between left in place (the last
+                // of them is the entering slot of step qn)
+                *reinterpret_cast<float4*>(&xs[orow * W + 8 * c + oc]) =
+                    (qn == q + 1 || qn >= last) ? o : *hp(xin(qn), c);
             }
         }
+        q = qn;
+        b ^= 1;
     }
     if (!ok && t == 0 && err) atomicOr(err, 1 << 30);
 }
@@ -605,13 +633,13 @@ int fixup_groups(int chains) {
 
 template <bool REV>
 static void launch_fixup_cg(int N, int Hv, const int* seg_off, const float* mats, float* xbuf,
-                            int* err, bool pdl, cudaStream_t st) {
+                            int* err, bool pdl, cudaStream_t st, const int* dec) {
     auto run = [&](auto kern, int cg) {
         const int smem = fix_smem(cg);
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         const dim3 grid(N, Hv, VD / (8 * cg));
-        if (pdl) launch_pdl(kern, grid, dim3(FIX_T), smem, st, seg_off, mats, xbuf, Hv, err);
-        else kern<<<grid, FIX_T, smem, st>>>(seg_off, mats, xbuf, Hv, err);
+        if (pdl) launch_pdl(kern, grid, dim3(FIX_T), smem, st, seg_off, mats, xbuf, Hv, err, dec);
+        else kern<<<grid, FIX_T, smem, st>>>(seg_off, mats, xbuf, Hv, err, dec);
     };
     switch (fixup_groups(N * Hv)) {
         case 1: run(k_fixup<REV, 1>, 1); break;
@@ -670,13 +698,13 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
-    launch_fixup_cg<false>(P.N, P.Hv, P.plan.seg_off, P.mbuf, P.hin, P.err, true, st);
+    launch_fixup_cg<false>(P.N, P.Hv, P.plan.seg_off, P.mbuf, P.hin, P.err, true, st, P.dec);
     timing_end(st);
 }
 
 void launch_bwd_fixup_tc(const BwdProblem& B, cudaStream_t st) {
     const Problem& P = B.f;
-    launch_fixup_cg<true>(P.N, P.Hv, P.plan.seg_off, P.mbuf_t, B.dhb, P.err, false, st);
+    launch_fixup_cg<true>(P.N, P.Hv, P.plan.seg_off, P.mbuf_t, B.dhb, P.err, false, st, P.dec);
 }
 
 template <typename Op, int C>

@@ -229,10 +229,16 @@ __device__ __forceinline__ void state_decay_all(uint32_t tm, uint32_t lb, uint32
     }
 }
 
+// x_out_t (TK_TRANS only, or null): the transition also untransposed.  dec_out (or null): the
+// gate warp sums the chunks' transition log-bounds (P.logb): with P_c the sum over chunks
+// [0, c), chunk c's entering state depends on the scan's own entering state above the
+// negligible level unless P_c < LOG_NEGLIGIBLE, and so does the final state unless P_n is;
+// it writes -1 when P_n is not below it, else 1 + the last c with P_c not below it (a bound
+// above 1 -- beta |k|^2 > 2 -- can raise the sum again, so this is not the first crossing).
 template <int KIND>
 __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm, int j,
                         int64_t t0, int64_t t1, int cb, int ce, const float* x0, float* x_out,
-                        int64_t hist_base) {
+                        int64_t hist_base, float* x_out_t = nullptr, int* dec_out = nullptr) {
     constexpr bool OUT = KIND == TK_OUT;
     constexpr bool NEEDU = KIND != TK_TRANS;
     constexpr int NDD = OUT ? 128 : 64;  // columns of a DD buffer the MMAs write
@@ -415,6 +421,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         __syncwarp();
     } else if (w == 2) {
         // ------------------------------------------------------------ gates
+        float lb_run = 0.f;  // sum of the chunks' transition log-bounds so far (dec_out)
+        int need = 0;        // 1 + the last chunk whose entering state is not yet decoupled
         for (int k = 0; k < n; ++k) {
             const int gs = k & (NGATE - 1);
             const int64_t tc = t0 + int64_t(cb + k) * CH;
@@ -424,6 +432,10 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             for (int u = 0; u < 2; ++u) {  // issue the global loads before waiting for a buffer
                 const int r = 2 * lane + u;
                 gv[u] = r < c ? P.g[(tc + r) * P.Hv + j] : 0.f;
+            }
+            if (dec_out) {
+                if (!(lb_run < LOG_NEGLIGIBLE)) need = k + 1;  // (NaN counts as not negligible)
+                lb_run += P.logb[(hist_base + cb + k) * P.Hv + j];
             }
             TRACE(k, 21);
             if (k >= NGATE && !warp_wait<true>(bars, B_GFREE0 + gs, ((k - NGATE) >> 2) & 1, errflag)) break;
@@ -454,6 +466,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             if (lane == 0) mbar_arrive(&bars[B_GATE0 + gs]);
             TRACE(k, 23);
         }
+        if (dec_out && lane == 0) *dec_out = (lb_run < LOG_NEGLIGIBLE) ? need : -1;
     } else if (w == 3 && OUT) {
         // ------------------------------------------------------------ output MMA issuer
         // D4b = (P V')^T once V' of chunk k is converted and the output warps have read D4b
@@ -581,6 +594,10 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                         for (int i = 0; i < 16; i += 4)
                             *reinterpret_cast<float4*>(x_out + v * VD + c0 + i) =
                                 make_float4(xv[i], xv[i + 1], xv[i + 2], xv[i + 3]);
+                        if (x_out_t) {  // and untransposed, for the backward's reverse fix-up
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) x_out_t[(c0 + i) * VD + v] = xv[i];
+                        }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) x_out[(c0 + i) * VD + v] = xv[i];
@@ -994,6 +1011,18 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
     seq_range(P, s, t0, t1);
     const int nt = int((t1 - t0 + CH - 1) / CH);
     const float* h0 = P.h0 ? P.h0 + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    if (P.cp == CP_EXACT && !P.full_cp) {
+        // decay-bounded exact mode: only the transitions that are not negligible, of the
+        // segments between the first and the last (the first output pass has stored every
+        // segment's state from zero, S, where the fix-up reads it)
+        if (lj < 1 || lj >= nseg - 1) return;
+        if (P.dec[int64_t(gseg) * P.Hv + j] >= 0) return;
+        const int cb = lj * P.L, ce = min(cb + P.L, nt);
+        float* mout = P.mbuf + (int64_t(gseg) * P.Hv + j) * KVN;
+        float* mout_t = P.mbuf_t ? P.mbuf_t + (int64_t(gseg) * P.Hv + j) * KVN : nullptr;
+        tc_scan<TK_TRANS>(P, maps, sm, j, t0, t1, cb, ce, nullptr, mout, P.plan.chunk_off[s], mout_t);
+        return;
+    }
     if (P.cp == CP_EXACT) {
         if (lj >= nseg - 1) return;
         const int cb = lj * P.L, ce = min(cb + P.L, nt);
@@ -1022,8 +1051,18 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
     }
 }
 
+// Output stage (KIND = TK_OUT) or the backward's recompute of the state entering every chunk
+// (TK_HIST), one CTA per (segment, v-head).  mode 0: every segment from its entering state
+// (h0, or the fix-up's), the last one's final state to ht.  Decay-bounded exact mode: mode 1,
+// the first pass, runs every segment from h0 (the first) or from zero (the others), storing
+// each one's final state S in the entering slot of the next (the last one's in ht) and its
+// decision (P.dec); mode 2, the correction, reruns from the true entering state only the
+// leading chunks of a segment whose outputs depend on it above the negligible level (the
+// whole segment, and then also ht, when its transition is not negligible), overwriting what
+// the first pass wrote for them.
 template <int KIND>
-__global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_constant__ TcMaps maps,
+                                                      int mode) {
     CTRACE(1, 0);
     pdl_launch_dependents();
     pdl_wait();
@@ -1038,9 +1077,28 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_c
     seq_range(P, s, t0, t1);
     const int nt = int((t1 - t0 + CH - 1) / CH);
     const int cb = lj * P.L, ce = min(cb + P.L, nt);
-    const float* x0 = (lj == 0) ? (P.h0 ? P.h0 + (int64_t(s) * P.Hv + j) * KVN : nullptr)
-                                : P.hin + (int64_t(gseg) * P.Hv + j) * KVN;
-    float* x_out = (lj == nseg - 1 && P.ht) ? P.ht + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    const int64_t sjh = int64_t(gseg) * P.Hv + j;
+    const bool last = lj == nseg - 1;
+    const float* h0 = P.h0 ? P.h0 + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    float* ht = P.ht ? P.ht + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    if (mode == 1) {
+        const float* x0 = lj == 0 ? h0 : nullptr;
+        float* x_out = last ? ht : P.hin + (sjh + P.Hv) * KVN;
+        if (ce <= cb) { copy_state(x0, x_out, false); return; }  // only an empty sequence
+        tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce, x0, x_out, P.plan.chunk_off[s], nullptr,
+                      lj >= 1 ? P.dec + sjh : nullptr);
+        return;
+    }
+    if (mode == 2) {
+        if (lj == 0 || ce <= cb) return;
+        const int d = P.dec[sjh];
+        const int n = d < 0 ? ce - cb : min(d, ce - cb);
+        float* x_out = (last && d < 0) ? ht : nullptr;
+        tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, cb + n, P.hin + sjh * KVN, x_out, P.plan.chunk_off[s]);
+        return;
+    }
+    const float* x0 = (lj == 0) ? h0 : P.hin + sjh * KVN;
+    float* x_out = last ? ht : nullptr;
     if (ce <= cb) { copy_state(x0, x_out, false); return; }
     tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce, x0, x_out, P.plan.chunk_off[s]);
     CTRACE(1, 3);
@@ -1478,22 +1536,39 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
     if (e != cudaSuccess) return e;
     launch_plan(P, CH, st);
     launch_prep(P, maps, st);
+    const dim3 grid(P.total_segs, P.Hv);
+    auto out_pass = [&](const char* name, int mode) {
+        timing_begin(name, st);
+        const cudaError_t r =
+            hist ? launch_pdl(k_tc_phase_c<TK_HIST>, grid, dim3(TCT), SMEM_BYTES, st, P, maps, mode)
+                 : launch_pdl(k_tc_phase_c<TK_OUT>, grid, dim3(TCT), SMEM_BYTES, st, P, maps, mode);
+        timing_end(st);
+        return r;
+    };
+    if (P.cp == CP_EXACT && !P.full_cp) {
+        // decay-bounded exact context parallelism: first pass from zero (outputs, segment
+        // states, decisions), the transitions and the fix-up only where not negligible, then
+        // the correction of the leading chunks of every segment past the first
+        e = out_pass(hist ? "fwd_recompute_pass1" : "fwd_pass1", 1);
+        if (e != cudaSuccess) return e;
+        timing_begin("fwd_transitions", st);
+        e = launch_pdl(k_tc_phase_a, grid, dim3(TCT), SMEM_BYTES, st, P, maps);
+        timing_end(st);
+        if (e != cudaSuccess) return e;
+        launch_fixup(P, st);
+        e = out_pass(hist ? "fwd_recompute_correction" : "fwd_correction", 2);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     if (P.cp != CP_NONE) {
-        dim3 ga(P.total_segs, P.Hv);
         timing_begin("fwd_phase_a", st);
-        e = launch_pdl(k_tc_phase_a, ga, dim3(TCT), SMEM_BYTES, st, P, maps);
+        e = launch_pdl(k_tc_phase_a, grid, dim3(TCT), SMEM_BYTES, st, P, maps);
         if (e != cudaSuccess) return e;
         timing_end(st);
         if (P.cp == CP_EXACT) launch_fixup(P, st);
     }
-    dim3 gc(P.total_segs, P.Hv);
-    timing_begin(hist ? "fwd_recompute_states" : "fwd_phase_c", st);
-    if (hist)
-        e = launch_pdl(k_tc_phase_c<TK_HIST>, gc, dim3(TCT), SMEM_BYTES, st, P, maps);
-    else
-        e = launch_pdl(k_tc_phase_c<TK_OUT>, gc, dim3(TCT), SMEM_BYTES, st, P, maps);
+    e = out_pass(hist ? "fwd_recompute_states" : "fwd_phase_c", 0);
     if (e != cudaSuccess) return e;
-    timing_end(st);
     return cudaGetLastError();
 }
 

@@ -11,6 +11,10 @@ namespace gdn {
 
 enum CpKind { CP_NONE = 0, CP_EXACT = 1, CP_WARMUP = 2 };
 
+// A transition whose 2-norm is bounded by exp(LOG_NEGLIGIBLE) = 2^-126 (the smallest normal
+// fp32 number) contributes less than 2^-126 ||h|| to any state it maps h into: it is dropped.
+constexpr float LOG_NEGLIGIBLE = -87.33654475f;
+
 struct PlanDev {
     int2* seg;          // [total_segs] (sequence, local segment index)
     int* seg_off;       // [N+1]
@@ -44,6 +48,15 @@ struct Problem {
     int L;              // chunks per segment
     int warmup;         // warm-up chunks (CP_WARMUP)
     int cp;             // CpKind
+    // Exact context parallelism with decay bounds (bf16 path, CP_EXACT unless full_cp):
+    // logb[chunk][v-head] = log of a bound on the 2-norm of the chunk's state transition
+    // (written by the preparation), dec[segment][v-head] = the number of leading chunks of a
+    // segment whose outputs depend on its entering state above the negligible level, or -1
+    // when even the whole segment's transition is not negligible (written by the first
+    // output pass; read by the transition, fix-up and correction launches)
+    float* logb;        // [total_chunks, Hv] or null
+    int* dec;           // [total_segs, Hv] or null
+    int full_cp;        // 1: every transition computed and every segment rerun (no bound)
     float scale;
     int* err;           // device error word (bounded waits that timed out), or null
 };

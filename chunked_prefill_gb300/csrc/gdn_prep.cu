@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     float* sBeta = reinterpret_cast<float*>(smem + S::oBeta);
     float* sBe = reinterpret_cast<float*>(smem + S::oBe);
     int* sFlag = reinterpret_cast<int*>(smem + S::oFlag);
+    float* sPart = reinterpret_cast<float*>(smem + S::oFlag + 8);  // two partial sums
     float* sGin = reinterpret_cast<float*>(smem + S::oGin);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);  // load, [K;Q]K^T, W'
     uint32_t* slot = reinterpret_cast<uint32_t*>(smem + S::oSlot);
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     }
     fence_after_sync();
 
+    float kn = 0.f;  // threads of warps 0-1: |k_i|^2 of their row of KK^T (from the first head)
 #pragma unroll 1
     for (int hh = 0; hh < nh; ++hh) {
         const int j = j0 + hh;
@@ -224,6 +226,10 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 float raw[32];
                 tmem_ld32(tm + (uint32_t(32 * w) << 16) + 32 * h2, raw);
                 tmem_ld_wait();
+                if (!qrows && hh == 0 && h2 == (w & 1)) {  // the diagonal: |k_i|^2, once
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) kn = (u == lane) ? raw[u] : kn;
+                }
                 if (!qrows) {
                     const int I = i >> 4, r = i & 15;
 #pragma unroll
@@ -266,9 +272,25 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 }
             }
             if (qrows) fence_proxy_async_smem();
+            if (!qrows && P.logb) {
+                // log of a bound on the 2-norm of this chunk's state transition: per token
+                // exp(g) (I - beta k k^T), whose norm is exp(g) max(1, |1 - beta |k|^2|); the
+                // 1e-3 |beta |k|^2| term covers the rounding of |k|^2.  Row i's term, summed
+                // over the warp, then over the two warps below
+                float term = 0.f;
+                if (i < c) {
+                    const float t = bi * kn;
+                    const float a = fabsf(1.f - t) + 1e-3f * fabsf(t);
+                    term = sGin[(hh * 2) * CH + i] + logf(fmaxf(1.f, a));
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) term += __shfl_xor_sync(0xffffffffu, term, off);
+                if (lane == 0) sPart[w] = term;
+            }
         }
         __syncthreads();
         PTRACE(2);
+        if (tid == 32 && P.logb) P.logb[int64_t(gch) * P.Hv + j] = sPart[0] + sPart[1];
         if (tid == 0) {
             bulk_store(rec + PREP_P, smem + S::oT, 8192);
             bulk_commit();

@@ -24,7 +24,7 @@ LIB_PATH = os.environ.get("GDN_LIB") or os.path.join(_HERE, "libgdn.so")
 (GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_TIMEOUT,
  GDN_ERR_BOUNDS) = range(7)
 GDN_BF16, GDN_FP32 = 0, 1
-CP_AUTO, CP_OFF, CP_EXACT, CP_WARMUP = 0, 1, 2, 3
+CP_AUTO, CP_OFF, CP_EXACT, CP_WARMUP, CP_EXACT_FULL = 0, 1, 2, 3, 4
 _STATUS = {1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE",
            4: "GDN_ERR_CUDA"}
 

@@ -62,10 +62,23 @@ typedef enum {
                            pages' rule L = cp_lambda * sqrt(chunks) instead */
     GDN_CP_OFF = 1,     /* one segment per sequence: a plain serial chunk scan */
     GDN_CP_EXACT = 2,   /* segments of cp_segment_chunks chunks; transition fix-up, exact */
-    GDN_CP_WARMUP = 3   /* opt-in approximation: each segment starts warmup_chunks chunks
+    GDN_CP_WARMUP = 3,  /* opt-in approximation: each segment starts warmup_chunks chunks
                            early from a zero state instead of the exact fix-up (FlashQLA
                            pages, "warm-up" paragraph: 6-8 chunks); NOT exact */
+    GDN_CP_EXACT_FULL = 4 /* as GDN_CP_EXACT, with every segment's transition computed and
+                           composed and every segment rerun from its entering state */
 } gdn_cp_mode;
+
+/* How the exact modes (AUTO, EXACT) skip work without changing the result.  Every chunk's
+ * state transition X -> prod_t exp(g_t) (I - beta_t k_t k_t^T) X has 2-norm at most
+ * B = exp(sum_t g_t) prod_t max(1, |1 - beta_t |k_t|^2|), computed per (chunk, v-head) from
+ * the inputs (bf16 path).  Where the product of these bounds over a prefix of a segment falls
+ * below 2^-126, the smallest normal fp32 number, whatever enters the segment changes the states
+ * past that prefix by less than 2^-126 times its norm: the segment's transition is then not
+ * computed (the fix-up takes the segment's state from zero as its result) and only the
+ * prefix's outputs are recomputed from the true entering state.  Elsewhere the transition is
+ * computed, composed and the whole segment rerun, as in GDN_CP_EXACT_FULL.  The fp32 test mode
+ * always works as GDN_CP_EXACT_FULL. */
 
 typedef struct gdn_problem {
     int32_t B;                        /* batch; must be 1 when cu_seqlens is given */
@@ -82,7 +95,8 @@ typedef struct gdn_problem {
                                          cu_seqlens != NULL (sizes the launch grids) */
     int32_t num_seqs;                 /* N_seq when varlen */
     int32_t cp_mode;                  /* gdn_cp_mode */
-    int32_t cp_segment_chunks;        /* EXACT / WARMUP: chunks per segment (0 = auto) */
+    int32_t cp_segment_chunks;        /* EXACT, EXACT_FULL, WARMUP: chunks per segment
+                                         (0 = auto) */
     int32_t warmup_chunks;            /* WARMUP: warm-up chunks (0 = 8) */
     float cp_lambda;                  /* AUTO: lambda in L = lambda sqrt(N) (0 = cost model) */
 } gdn_problem;

@@ -91,6 +91,54 @@ def test_warmup_mode_matches_its_own_definition_fp32():
     assert rel_err(o, eo) > 1e-3
 
 
+def _mixed_decay(inp, lo, hi):
+    """No decay (g = 0) on tokens [lo, hi) of v-head 0, mild decay elsewhere on it, the
+    default gates on the other v-heads: segments inside [lo, hi) keep their entering state
+    (their transitions are computed and composed), the others forget it."""
+    inp.g[:, :, 0].mul_(0.05)
+    inp.g[:, lo:hi, 0] = 0.0
+    return inp
+
+
+@pytest.mark.parametrize("seg", [1, 2, 3, 4, 7])
+def test_context_parallel_decay_bounded_mixed(seg):
+    """Exact mode with decay bounds against the oracle and against the mode that computes
+    every transition and reruns every segment (GDN_CP_EXACT_FULL), on gates that make some
+    segments' transitions negligible and others not."""
+    inp = _mixed_decay(make_inputs(1, 64 * 40 + 17, 1, 3, seed=31, h0_std=0.1), 64 * 9, 64 * 27)
+    ro, rht = oracle_fwd(inp)
+    o_b, ht_b = gpu_fwd(inp, cp_mode=2, cp_segment_chunks=seg)
+    o_f, ht_f = gpu_fwd(inp, cp_mode=4, cp_segment_chunks=seg)
+    for o, ht in ((o_b, ht_b), (o_f, ht_f)):
+        assert rel_err(o, ro) <= BF16_TOL and rel_err(ht, rht) <= BF16_TOL
+    # both are the exact result: they differ by rounding only
+    assert rel_err(o_b, o_f) <= BF16_TOL and rel_err(ht_b, ht_f) <= BF16_TOL
+
+
+def test_context_parallel_decay_bounded_large_keys():
+    """Keys longer than 1 (beta |k|^2 up to ~2.9): some tokens' transitions expand, the
+    chunks' log-bounds turn positive and the running sum is no longer monotone."""
+    inp = make_inputs(1, 64 * 30 + 9, 2, 4, seed=32, h0_std=0.1)
+    inp.k = (inp.k.float() * 1.7).to(inp.k.dtype)
+    inp.g.mul_(0.3)
+    for seg in (2, 5):
+        check(inp, BF16_TOL, cp_mode=2, cp_segment_chunks=seg)
+
+
+def test_context_parallel_decay_bounded_varlen_and_backward():
+    """Varlen with empty, one-chunk and long sequences, mixed decay, through the forward and
+    the backward (whose recompute and reverse fix-up use the same decisions)."""
+    from tests.gpu_util import gpu_bwd, oracle_bwd
+    lens = [0, 700, 64, 1500, 3, 900]
+    inp = make_inputs(1, sum(lens), 1, 2, seed=33, h0_std=0.1, lengths=lens, backward=True)
+    inp = _mixed_decay(inp, 800, 2000)
+    check(inp, BF16_TOL, cp_mode=2, cp_segment_chunks=3)
+    got = gpu_bwd(inp, cp_mode=2, cp_segment_chunks=3)
+    ref = oracle_bwd(inp)
+    for name, a, r in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), got, ref):
+        assert rel_err(a.reshape(r.shape), r) <= BF16_TOL, name
+
+
 def _warmup_bounds(inp, chunk, seg_chunks, warmup):
     """Contraction bound of the warm-up mode's error (one sequence, every v-head): segment
     j >= 1 starts its scan `warmup` chunks early from zero, so its state at the segment start

@@ -162,3 +162,26 @@ def test_lowlevel_T_inverts_the_chunk_matrix_by_loops():
             Tc = A[c0:c0 + c, j, :c]
             np.testing.assert_allclose(Lc @ Tc, np.eye(c), atol=1e-12)
             assert np.all(A[c0:c0 + c, j, c:] == 0)
+
+
+def test_transition_norm_bound_used_by_the_exact_mode():
+    """The decay-bounded exact mode drops a segment's transition when the product of the
+    per-token bounds exp(g_t) max(1, |1 - beta_t |k_t|^2|) falls below 2^-126.  That product
+    bounds the 2-norm of the token transitions' product X -> (I - beta k k^T) exp(g) X in any
+    order of factors: checked on random chains, with keys of length up to 1.8 (so that some
+    factors expand) and with the factors composed in the recurrence's order."""
+    rng = np.random.default_rng(7)
+    for trial in range(40):
+        n = int(rng.integers(1, 40))
+        d = 8
+        k = rng.standard_normal((n, d))
+        k *= (rng.uniform(0.2, 1.8, n) / np.linalg.norm(k, axis=1))[:, None]
+        beta = rng.uniform(0.0, 1.0, n)
+        g = -rng.exponential(0.3, n) * (trial % 3)  # some chains without decay
+        phi = np.eye(d)
+        log_bound = 0.0
+        for t in range(n):
+            step = np.exp(g[t]) * (np.eye(d) - beta[t] * np.outer(k[t], k[t]))
+            phi = step @ phi
+            log_bound += g[t] + np.log(max(1.0, abs(1.0 - beta[t] * k[t] @ k[t])))
+        assert np.linalg.norm(phi, 2) <= np.exp(log_bound) * (1 + 1e-12)
