@@ -54,7 +54,8 @@ struct HostPlan {
     int64_t prep_stride = 0;  // bytes per (chunk, v-head) preparation record
     // workspace layout (bytes)
     size_t off_err = 0, off_seg = 0, off_segoff = 0, off_chunkoff = 0, off_hin = 0,
-           off_mbuf = 0, off_mbuf_t = 0, off_logb = 0, off_dec = 0, off_prep = 0, off_end = 0;
+           off_mbuf = 0, off_mbuf_t = 0, off_logb = 0, off_dec = 0, off_rerun = 0, off_prep = 0,
+           off_end = 0;
     bool full_cp = false;   // every transition computed and every segment rerun
     // backward only
     size_t off_hist = 0, off_dhist = 0, off_dhb = 0, off_dqp = 0, off_dkp = 0;
@@ -225,6 +226,8 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
     if (bounded) off = align_up(off + sizeof(float) * size_t(h.total_chunks) * p->Hv, 256);
     h.off_dec = off;
     if (bounded) off = align_up(off + sizeof(int) * size_t(total_segs) * p->Hv, 256);
+    h.off_rerun = off;
+    if (bounded) off = align_up(off + sizeof(int) * size_t(total_segs) * p->Hv, 256);
     h.off_prep = off;  // W', TU, P (and T) tiles of every (chunk, v-head): tensor-core path only
     h.prep_stride = backward ? gdn::PREP_BWD_BYTES : gdn::PREP_FWD_BYTES;
     if (p->dtype == GDN_BF16) off = align_up(off + size_t(h.prep_stride) * h.total_chunks * p->Hv, 256);
@@ -276,6 +279,7 @@ void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Proble
     const bool bounded = h.cp == gdn::CP_EXACT && !h.full_cp;
     P.logb = bounded ? reinterpret_cast<float*>(ws + h.off_logb) : nullptr;
     P.dec = bounded ? reinterpret_cast<int*>(ws + h.off_dec) : nullptr;
+    P.rerun = bounded ? reinterpret_cast<int*>(ws + h.off_rerun) : nullptr;
     P.scale = p->scale;
 }
 

@@ -79,6 +79,19 @@ struct alignas(16) Gate {
     float kd[CH];    // exp(gamma_C - gamma)
     float eC;
     int c;           // valid rows
+    int store;       // store this chunk's outputs (and entering state, when asked)
+    int pad;
+};
+
+// First pass of the decay-bounded exact mode (see k_tc_phase_c): which chunks' results this
+// CTA stores and where its decisions go.
+struct ScanRule {
+    int n_own;       // chunks of the own segment (the scan may run on into the next one)
+    int e_own;       // leading chunks of the own segment that the previous CTA stores (0: none)
+    int lj;          // segment index within the sequence
+    int* dec;        // -1: the own segment's transition is not negligible, else 0
+    int* rerun;      // 1: some output of the own segment is left to the correction pass
+    float* x_mid;    // the state at the end of the own segment, when the scan runs on (or null)
 };
 static_assert(sizeof(Gate) <= GATE_BYTES && sizeof(Gate) % 16 == 0, "gate buffer");
 
@@ -190,9 +203,9 @@ __device__ __forceinline__ void state_bf16_half(uint32_t tm, uint32_t lb, uint32
 template <int KIND>
 __device__ __forceinline__ void state_decay_half(const Problem& P, uint32_t tm, uint32_t lb, int half,
                                                  int v, float eC, int64_t chunk, int j, uint32_t xf,
-                                                 float (&x)[64]) {
+                                                 float (&x)[64], bool store = true) {
     const int c0 = 64 * half;
-    if (KIND == TK_HIST || (KIND == TK_OUT && P.hist)) {
+    if ((KIND == TK_HIST || (KIND == TK_OUT && P.hist)) && store) {
         __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(P.hist) + (chunk * P.Hv + j) * (KD * VD);
 #pragma unroll
         for (int i = 0; i < 64; ++i) hp[(c0 + i) * VD + v] = __float2bfloat16_rn(x[i]);
@@ -229,16 +242,17 @@ __device__ __forceinline__ void state_decay_all(uint32_t tm, uint32_t lb, uint32
     }
 }
 
-// x_out_t (TK_TRANS only, or null): the transition also untransposed.  dec_out (or null): the
-// gate warp sums the chunks' transition log-bounds (P.logb): with P_c the sum over chunks
-// [0, c), chunk c's entering state depends on the scan's own entering state above the
-// negligible level unless P_c < LOG_NEGLIGIBLE, and so does the final state unless P_n is;
-// it writes -1 when P_n is not below it, else 1 + the last c with P_c not below it (a bound
-// above 1 -- beta |k|^2 > 2 -- can raise the sum again, so this is not the first crossing).
+// x_out_t (TK_TRANS only, or null): the transition also untransposed.  rule (or null: store
+// everything): the gate warp sums the own chunks' transition log-bounds (P.logb); with P_c the
+// sum over chunks [0, c), chunk c's entering state depends on the scan's entering state by less
+// than 2^-126 of its norm when P_c < LOG_NEGLIGIBLE.  An own chunk's results are stored when
+// the previous CTA does not store them (c >= e_own) and P_c is below it (a chunk at or past
+// e_own that fails is left to the correction: rerun); the chunks past the own segment are
+// stored when the scan reached them from a true state (the first segment, or P_n below it).
 template <int KIND>
 __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm, int j,
                         int64_t t0, int64_t t1, int cb, int ce, const float* x0, float* x_out,
-                        int64_t hist_base, float* x_out_t = nullptr, int* dec_out = nullptr) {
+                        int64_t hist_base, float* x_out_t = nullptr, const ScanRule* rule = nullptr) {
     constexpr bool OUT = KIND == TK_OUT;
     constexpr bool NEEDU = KIND != TK_TRANS;
     constexpr int NDD = OUT ? 128 : 64;  // columns of a DD buffer the MMAs write
@@ -421,8 +435,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         __syncwarp();
     } else if (w == 2) {
         // ------------------------------------------------------------ gates
-        float lb_run = 0.f;  // sum of the chunks' transition log-bounds so far (dec_out)
-        int need = 0;        // 1 + the last chunk whose entering state is not yet decoupled
+        float lb_run = 0.f;  // sum of the own chunks' transition log-bounds so far (rule)
+        bool bad = rule && rule->lj >= 1 && rule->e_own == 0, ext_ok = true, nm = false;
         for (int k = 0; k < n; ++k) {
             const int gs = k & (NGATE - 1);
             const int64_t tc = t0 + int64_t(cb + k) * CH;
@@ -433,9 +447,26 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 const int r = 2 * lane + u;
                 gv[u] = r < c ? P.g[(tc + r) * P.Hv + j] : 0.f;
             }
-            if (dec_out) {
-                if (!(lb_run < LOG_NEGLIGIBLE)) need = k + 1;  // (NaN counts as not negligible)
-                lb_run += P.logb[(hist_base + cb + k) * P.Hv + j];
+            int store = 1;
+            if (rule) {
+                if (k < rule->n_own) {
+                    if (rule->lj >= 1) {
+                        const float lb = P.logb[(hist_base + cb + k) * P.Hv + j];
+                        if (rule->e_own == 0 || k < rule->e_own) {
+                            store = 0;
+                        } else {
+                            store = lb_run < LOG_NEGLIGIBLE ? 1 : 0;  // (NaN: not negligible)
+                            if (!store) bad = true;
+                        }
+                        lb_run += lb;
+                        if (k == rule->n_own - 1) {
+                            nm = !(lb_run < LOG_NEGLIGIBLE);
+                            ext_ok = !nm;
+                        }
+                    }
+                } else {
+                    store = ext_ok ? 1 : 0;
+                }
             }
             TRACE(k, 21);
             if (k >= NGATE && !warp_wait<true>(bars, B_GFREE0 + gs, ((k - NGATE) >> 2) & 1, errflag)) break;
@@ -461,12 +492,16 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             if (lane == 0) {
                 gb.eC = expf(last);
                 gb.c = c;
+                gb.store = store;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_GATE0 + gs]);
             TRACE(k, 23);
         }
-        if (dec_out && lane == 0) *dec_out = (lb_run < LOG_NEGLIGIBLE) ? need : -1;
+        if (rule && rule->lj >= 1 && lane == 0) {
+            *rule->dec = nm ? -1 : 0;
+            *rule->rerun = bad ? 1 : 0;
+        }
     } else if (w == 3 && OUT) {
         // ------------------------------------------------------------ output MMA issuer
         // D4b = (P V')^T once V' of chunk k is converted and the output warps have read D4b
@@ -537,7 +572,12 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_EX]);
-                state_decay_half<KIND>(P, tm, lb, hf, v, gb.eC, hist_base + cb + k, j, T_XF, xs);
+                if (rule && rule->x_mid && k == rule->n_own) {  // the state at the end of the own segment
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) rule->x_mid[(64 * hf + i) * VD + v] = xs[i];
+                }
+                state_decay_half<KIND>(P, tm, lb, hf, v, gb.eC, hist_base + cb + k, j, T_XF, xs,
+                                       gb.store != 0);
             }
             if (v == 0 && !hf) TRACE(k, 18);
             // V' of tokens [32 hf, 32 hf + 32): fp32 -> bf16 V'^T and bf16 diag(kd) V'^T, both
@@ -660,7 +700,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(P.o) + (tc * P.Hv + j) * VD;
             const int64_t rs = int64_t(P.Hv) * VD;
             const int64_t o_n = (P.cu ? int64_t(P.T) : int64_t(P.N) * P.T) * rs;
-            for (int idx = v; idx < c * 16; idx += 128) {
+            for (int idx = v; idx < (gb.store ? c * 16 : 0); idx += 128) {
                 const int r = idx >> 4, cv = idx & 15;
                 if (in_range((tc * P.Hv + j) * VD + r * rs + cv * 8 + 7, o_n, P.err))
                     *reinterpret_cast<uint4*>(ob + r * rs + cv * 8) = lds128(so + (r * LDO + cv * 8) * 2);
@@ -1051,15 +1091,49 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
     }
 }
 
+// g-only extension length of a segment starting at chunk cs with n chunks: the smallest e in
+// [1, min(n, EXT_MAX)] whose first e chunks' gate sum is below LOG_NEGLIGIBLE, else 0.  Since
+// beta |k|^2 terms only raise a chunk's log-bound above its gate sum, chunks before e are
+// certainly not decoupled from the segment's entering state.  Every warp computes it with the
+// same code and summation order, so the CTA of segment lj (looking ahead) and that of lj + 1
+// (looking at itself) agree bit for bit.
+constexpr int EXT_MAX = 4;
+__device__ int ext_len(const Problem& P, int64_t t0, int64_t t1, int cs, int n, int j) {
+    const int lane = threadIdx.x & 31;
+    const int m = min(n, EXT_MAX);
+    float gv[EXT_MAX][2];
+#pragma unroll
+    for (int e = 0; e < EXT_MAX; ++e)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t t = t0 + int64_t(cs + e) * CH + 2 * lane + u;
+            gv[e][u] = (e < m && t < t1) ? P.g[t * P.Hv + j] : 0.f;
+        }
+    float run = 0.f;
+#pragma unroll
+    for (int e = 0; e < EXT_MAX; ++e) {
+        if (e >= m) break;
+        float v = gv[e][0] + gv[e][1];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        run += v;
+        if (run < LOG_NEGLIGIBLE) return e + 1;
+    }
+    return 0;
+}
+
 // Output stage (KIND = TK_OUT) or the backward's recompute of the state entering every chunk
 // (TK_HIST), one CTA per (segment, v-head).  mode 0: every segment from its entering state
 // (h0, or the fix-up's), the last one's final state to ht.  Decay-bounded exact mode: mode 1,
-// the first pass, runs every segment from h0 (the first) or from zero (the others), storing
-// each one's final state S in the entering slot of the next (the last one's in ht) and its
-// decision (P.dec); mode 2, the correction, reruns from the true entering state only the
-// leading chunks of a segment whose outputs depend on it above the negligible level (the
-// whole segment, and then also ht, when its transition is not negligible), overwriting what
-// the first pass wrote for them.
+// the first pass, runs every segment from h0 (the first) or from zero (the others) and stores
+// only the results that provably do not depend on that start (ScanRule); the leading chunks of
+// segment lj + 1 that the bound does not reach are scanned by the CTA of segment lj right after
+// its own, from its own final state -- the true entering state of lj + 1 when lj's transition
+// is negligible (or lj is the first).  Each segment's state from zero, S, goes to the entering
+// slot of the next (the last one's to ht), with the decisions (P.dec, P.rerun).  mode 2, the
+// correction, reruns from its true entering state every segment with an unwritten result: one
+// flagged by its own CTA, one that follows a segment whose transition is not negligible, and
+// a last segment whose own transition is not negligible (its final state).
 template <int KIND>
 __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_constant__ TcMaps maps,
                                                       int mode) {
@@ -1083,18 +1157,25 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_c
     float* ht = P.ht ? P.ht + (int64_t(s) * P.Hv + j) * KVN : nullptr;
     if (mode == 1) {
         const float* x0 = lj == 0 ? h0 : nullptr;
-        float* x_out = last ? ht : P.hin + (sjh + P.Hv) * KVN;
-        if (ce <= cb) { copy_state(x0, x_out, false); return; }  // only an empty sequence
-        tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce, x0, x_out, P.plan.chunk_off[s], nullptr,
-                      lj >= 1 ? P.dec + sjh : nullptr);
+        float* x_seg = last ? ht : P.hin + (sjh + P.Hv) * KVN;
+        if (ce <= cb) { copy_state(x0, x_seg, false); return; }  // only an empty sequence
+        ScanRule rule;
+        rule.n_own = ce - cb;
+        rule.e_own = lj >= 1 ? ext_len(P, t0, t1, cb, ce - cb, j) : 0;
+        rule.lj = lj;
+        rule.dec = P.dec + sjh;
+        rule.rerun = P.rerun + sjh;
+        const int e_next = last ? 0 : ext_len(P, t0, t1, ce, min(P.L, nt - ce), j);
+        rule.x_mid = e_next > 0 ? x_seg : nullptr;
+        tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce + e_next, x0, e_next > 0 ? nullptr : x_seg,
+                      P.plan.chunk_off[s], nullptr, &rule);
         return;
     }
     if (mode == 2) {
         if (lj == 0 || ce <= cb) return;
-        const int d = P.dec[sjh];
-        const int n = d < 0 ? ce - cb : min(d, ce - cb);
-        float* x_out = (last && d < 0) ? ht : nullptr;
-        tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, cb + n, P.hin + sjh * KVN, x_out, P.plan.chunk_off[s]);
+        if (!(P.rerun[sjh] != 0 || (lj >= 2 && P.dec[sjh - P.Hv] < 0) || (last && P.dec[sjh] < 0))) return;
+        tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce, P.hin + sjh * KVN, last ? ht : nullptr,
+                      P.plan.chunk_off[s]);
         return;
     }
     const float* x0 = (lj == 0) ? h0 : P.hin + sjh * KVN;

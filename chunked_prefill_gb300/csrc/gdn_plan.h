@@ -50,12 +50,13 @@ struct Problem {
     int cp;             // CpKind
     // Exact context parallelism with decay bounds (bf16 path, CP_EXACT unless full_cp):
     // logb[chunk][v-head] = log of a bound on the 2-norm of the chunk's state transition
-    // (written by the preparation), dec[segment][v-head] = the number of leading chunks of a
-    // segment whose outputs depend on its entering state above the negligible level, or -1
-    // when even the whole segment's transition is not negligible (written by the first
-    // output pass; read by the transition, fix-up and correction launches)
+    // (written by the preparation), dec[segment][v-head] = -1 when the segment's transition is
+    // not negligible, else 0 (written by the first output pass; read by the transition, fix-up
+    // and correction launches)
     float* logb;        // [total_chunks, Hv] or null
     int* dec;           // [total_segs, Hv] or null
+    int* rerun;         // [total_segs, Hv] or null: some result of the segment is left to the
+                        // correction pass
     int full_cp;        // 1: every transition computed and every segment rerun (no bound)
     float scale;
     int* err;           // device error word (bounded waits that timed out), or null
