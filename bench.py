@@ -373,7 +373,9 @@ KERNEL_TENSORS = {
     "fwd_phase_c": ("q", "k", "v", "g", "beta", "h0", "o", "ht"),
     "fwd_phase_a": ("k", "v", "g", "beta", "h0"),
     "fwd_recompute_states": ("k", "v", "g", "beta", "h0"),
+    "fwd_recompute_pass1": ("k", "v", "g", "beta", "h0"),
     "bwd_phase_a": ("q", "k", "dO", "g", "beta", "dht"),
+    "bwd_dh_pass1": ("q", "k", "dO", "g", "beta", "dht", "dh0"),
     "bwd_dh_scan": ("q", "k", "dO", "g", "beta", "dht", "dh0"),
     "bwd_local": ("q", "k", "v", "dO", "g", "beta", "dq", "dk", "dv", "dg", "dbeta"),
 }

@@ -58,7 +58,7 @@ struct HostPlan {
            off_end = 0;
     bool full_cp = false;   // every transition computed and every segment rerun
     // backward only
-    size_t off_hist = 0, off_dhist = 0, off_dhb = 0, off_dqp = 0, off_dkp = 0;
+    size_t off_hist = 0, off_dhist = 0, off_dhb = 0, off_rrerun = 0, off_dqp = 0, off_dkp = 0;
 };
 
 constexpr size_t KVB = size_t(128) * 128 * 4;
@@ -240,6 +240,8 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
         off = align_up(off + per_chunk * size_t(h.total_chunks), 256);
         h.off_dhb = off;
         if (h.cp != gdn::CP_NONE) off = align_up(off + KVB * size_t(total_segs) * p->Hv, 256);
+        h.off_rrerun = off;
+        if (bounded) off = align_up(off + sizeof(int) * size_t(total_segs) * p->Hv, 256);
         h.off_dqp = off;
         if (p->Hv != p->Hqk) {
             const size_t part = size_t(h.total_tokens) * p->Hv * 128 * 4;
@@ -440,6 +442,7 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, con
     B.dbeta = dbeta;
     B.dhist = ws + h.off_dhist;
     B.dhb = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_dhb) : nullptr;
+    B.rrerun = P.dec ? reinterpret_cast<int*>(ws + h.off_rrerun) : nullptr;
     B.dqp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dqp) : nullptr;
     B.dkp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dkp) : nullptr;
     // recompute the state entering every chunk, then the reverse scan and local gradients
@@ -549,6 +552,7 @@ gdn_status gdn_chunk_bwd_saved(const gdn_problem* p, const void* q, const void* 
     B.dbeta = dbeta;
     B.dhist = ws + h.off_dhist;
     B.dhb = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_dhb) : nullptr;
+    B.rrerun = P.dec ? reinterpret_cast<int*>(ws + h.off_rrerun) : nullptr;
     B.dqp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dqp) : nullptr;
     B.dkp = p->Hv != p->Hqk ? reinterpret_cast<float*>(ws + h.off_dkp) : nullptr;
     // the states, chunk records and segment transitions come from gdn_chunk_fwd_saved: only

@@ -1094,7 +1094,22 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     const int64_t T_total = P.cu ? P.T : int64_t(P.N) * P.T;
-    if (P.cp != CP_NONE) {
+    if (TC && P.dec && B.rrerun) {
+        // decay-bounded exact mode (the forward's decisions in P.dec): first pass from the
+        // segments' right ends, the reverse fix-up only where a transition is not negligible,
+        // the correction of the segments left with unwritten gradients
+        timing_begin("bwd_dh_pass1", st);
+        e = launch_bwd_scan_tc(B, 2, T_total, st);
+        if (e != cudaSuccess) return e;
+        timing_end(st);
+        timing_begin("bwd_fixup", st);
+        launch_bwd_fixup_tc(B, st);
+        timing_end(st);
+        timing_begin("bwd_dh_correction", st);
+        e = launch_bwd_scan_tc(B, 3, T_total, st);
+        if (e != cudaSuccess) return e;
+        timing_end(st);
+    } else if (P.cp != CP_NONE) {
         timing_begin("bwd_phase_a", st);
         if constexpr (TC) {
             e = launch_bwd_scan_tc(B, 0, T_total, st);
@@ -1110,14 +1125,16 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
             k_bwd_fixup<<<dim3(P.N, P.Hv, VD / 8), 256, fix_smem, st>>>(B);
         timing_end(st);
     }
-    timing_begin("bwd_dh_scan", st);
-    if constexpr (TC) {
-        e = launch_bwd_scan_tc(B, 1, T_total, st);
-        if (e != cudaSuccess) return e;
-    } else {
-        k_bwd_phase_c<Op, C><<<dim3(P.total_segs, P.Hv), NT, SS::bytes, st>>>(B);
+    if (!(TC && P.dec && B.rrerun)) {
+        timing_begin("bwd_dh_scan", st);
+        if constexpr (TC) {
+            e = launch_bwd_scan_tc(B, 1, T_total, st);
+            if (e != cudaSuccess) return e;
+        } else {
+            k_bwd_phase_c<Op, C><<<dim3(P.total_segs, P.Hv), NT, SS::bytes, st>>>(B);
+        }
+        timing_end(st);
     }
-    timing_end(st);
     if (P.total_chunks > 0) {
         timing_begin("bwd_local", st);
         if constexpr (TC) {

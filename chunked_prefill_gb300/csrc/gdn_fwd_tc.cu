@@ -88,8 +88,11 @@ struct alignas(16) Gate {
 struct ScanRule {
     int n_own;       // chunks of the own segment (the scan may run on into the next one)
     int e_own;       // leading chunks of the own segment that the previous CTA stores (0: none)
-    int lj;          // segment index within the sequence
-    int* dec;        // -1: the own segment's transition is not negligible, else 0
+    int lj;          // segment index within the sequence (reverse scan: 0 for every segment but
+                     // the last, whose scan starts from the true gradient)
+    int* dec;        // -1: the own segment's transition is not negligible, else 0 (or null)
+    int ext_ok;      // reverse scan: the own segment's transition is negligible (the forward's
+                     // decision), so the scan past it starts from a true state
     int* rerun;      // 1: some output of the own segment is left to the correction pass
     float* x_mid;    // the state at the end of the own segment, when the scan runs on (or null)
 };
@@ -450,19 +453,19 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             int store = 1;
             if (rule) {
                 if (k < rule->n_own) {
+                    const float lb = P.logb[(hist_base + cb + k) * P.Hv + j];
                     if (rule->lj >= 1) {
-                        const float lb = P.logb[(hist_base + cb + k) * P.Hv + j];
                         if (rule->e_own == 0 || k < rule->e_own) {
                             store = 0;
                         } else {
                             store = lb_run < LOG_NEGLIGIBLE ? 1 : 0;  // (NaN: not negligible)
                             if (!store) bad = true;
                         }
-                        lb_run += lb;
-                        if (k == rule->n_own - 1) {
-                            nm = !(lb_run < LOG_NEGLIGIBLE);
-                            ext_ok = !nm;
-                        }
+                    }
+                    lb_run += lb;
+                    if (k == rule->n_own - 1) {
+                        nm = !(lb_run < LOG_NEGLIGIBLE);
+                        ext_ok = rule->lj == 0 || !nm;
                     }
                 } else {
                     store = ext_ok ? 1 : 0;
@@ -498,8 +501,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             if (lane == 0) mbar_arrive(&bars[B_GATE0 + gs]);
             TRACE(k, 23);
         }
-        if (rule && rule->lj >= 1 && lane == 0) {
-            *rule->dec = nm ? -1 : 0;
+        if (rule && lane == 0) {  // (the first segment's dec serves the backward's reverse scan)
+            if (rule->dec) *rule->dec = nm ? -1 : 0;
             *rule->rerun = bad ? 1 : 0;
         }
     } else if (w == 3 && OUT) {
@@ -1199,10 +1202,17 @@ constexpr uint32_t R_K = 0, R_Q = 32768, R_DO = 65536, R_DOE = 98304, R_W = 1310
 static_assert(R_P + 2 * 8192 <= S_GATE, "backward scan stages fit below the gate buffers");
 constexpr uint32_t T_DB = 192, T_DA = 256;
 
+// rule (or null: store everything): the first pass of the decay-bounded exact mode, in
+// reverse.  The own segment is the first rule->n_own chunks of the scan (from its right end);
+// the gate warp sums their transition log-bounds in scan order, and the gradient leaving a
+// chunk is stored when the next segment's CTA does not store it (k >= e_own) and the sum over
+// the chunks scanned before it is below LOG_NEGLIGIBLE (else the segment is left to the
+// correction: rerun); the chunks past the own segment are stored when rule->ext_ok.
 template <bool HIST>
 __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUtensorMap* mdo,
                             unsigned char* sm, int j, int64_t t0, int64_t t1, int cb, int ce,
-                            const float* x0, float* x_out, int64_t gbase) {
+                            const float* x0, float* x_out, int64_t gbase,
+                            const ScanRule* rule = nullptr) {
     enum RB { R_FULL0 = 0, R_FULL1, R_EMPTY0, R_EMPTY1, R_GATE0, R_GFREE0 = R_GATE0 + NGATE,
               R_MMA3 = R_GFREE0 + NGATE, R_MMA5, R_EX, R_EV, R_DOE0, R_DOE1, R_DRAIN, R_DEC, R_COUNT };
     static_assert(R_COUNT * 8 + 8 <= 512, "barrier area");
@@ -1340,6 +1350,8 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
         __syncwarp();
     } else if (w == 2) {
         // ------------------------------------------------------------ gates
+        float lb_run = 0.f;
+        bool bad = rule && rule->lj >= 1 && rule->e_own == 0;
         for (int k = 0; k < n; ++k) {
             const int gs = k & (NGATE - 1);
             const int64_t tc = t0 + int64_t(chunk_of(k)) * CH;
@@ -1349,6 +1361,23 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
             for (int u = 0; u < 2; ++u) {
                 const int r = 2 * lane + u;
                 gv[u] = r < c ? P.g[(tc + r) * P.Hv + j] : 0.f;
+            }
+            int store = 1;
+            if (rule) {
+                if (k < rule->n_own) {
+                    const float lb = P.logb[(gbase + chunk_of(k)) * P.Hv + j];
+                    if (rule->lj >= 1) {
+                        if (rule->e_own == 0 || k < rule->e_own) {
+                            store = 0;
+                        } else {
+                            store = lb_run < LOG_NEGLIGIBLE ? 1 : 0;  // (NaN: not negligible)
+                            if (!store) bad = true;
+                        }
+                    }
+                    lb_run += lb;
+                } else {
+                    store = rule->ext_ok;
+                }
             }
             if (k >= NGATE && !warp_wait<true>(bars, R_GFREE0 + gs, ((k - NGATE) >> 2) & 1, errflag)) break;
             Gate& gb = gates[gs];
@@ -1372,10 +1401,12 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
             if (lane == 0) {
                 gb.eC = expf(last);
                 gb.c = c;
+                gb.store = store;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[R_GATE0 + gs]);
         }
+        if (rule && lane == 0) *rule->rerun = bad ? 1 : 0;
     } else if (w >= 12) {
         // ------------------------------------------------------------ dOe = scale e_i dO_i (i < c)
         const int v = tid - 384;
@@ -1438,7 +1469,11 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[R_EX]);
                 const int c0 = 64 * hf;
-                if (HIST) {
+                if (rule && rule->x_mid && k == rule->n_own) {  // the own segment's left end
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) rule->x_mid[(c0 + i) * VD + v] = xs[i];
+                }
+                if (HIST && gb.store) {
                     __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(B.dhist) +
                                         ((gbase + chunk_of(k)) * P.Hv + j) * (KD * VD);
 #pragma unroll
@@ -1533,9 +1568,46 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_bwd_a(BwdProblem B, const __grid_
     tc_bwd_scan<false>(B, maps.f, &maps.dO, sm, j, t0, t1, cb, ce, x0, out, P.plan.chunk_off[s]);
 }
 
-// rerun of every segment from its true right-end gradient, storing dh for every chunk; the
-// first segment's result is dh0
-__global__ void __launch_bounds__(TCT, 1) k_tc_bwd_c(BwdProblem B, const __grid_constant__ BwdMaps maps) {
+// g-only extension length of the reverse scan into the segment ending at chunk ce (n chunks):
+// the smallest e in [1, min(n, EXT_MAX)] whose last e chunks' gate sum is below
+// LOG_NEGLIGIBLE, else 0 (the mirror image of ext_len, with the same guarantees).
+__device__ int ext_len_rev(const Problem& P, int64_t t0, int64_t t1, int ce, int n, int j) {
+    const int lane = threadIdx.x & 31;
+    const int m = min(n, EXT_MAX);
+    float gv[EXT_MAX][2];
+#pragma unroll
+    for (int e = 0; e < EXT_MAX; ++e)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t t = t0 + int64_t(ce - 1 - e) * CH + 2 * lane + u;
+            gv[e][u] = (e < m && t < t1) ? P.g[t * P.Hv + j] : 0.f;
+        }
+    float run = 0.f;
+#pragma unroll
+    for (int e = 0; e < EXT_MAX; ++e) {
+        if (e >= m) break;
+        float v = gv[e][0] + gv[e][1];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        run += v;
+        if (run < LOG_NEGLIGIBLE) return e + 1;
+    }
+    return 0;
+}
+
+// The reverse dh scan storing dh for every chunk; the first segment's result is dh0.  mode 0:
+// every segment from its true right-end gradient (dht, or the fix-up's).  Decay-bounded exact
+// mode (the mirror image of k_tc_phase_c's): mode 1, the first pass, runs every segment from
+// its right end from zero (the last from dht), stores the gradients that provably do not
+// depend on that start and scans on into the trailing chunks of the previous segment that the
+// bound does not reach -- from a true gradient when its own transition is negligible (the
+// forward's P.dec) or it is the last; each segment's left-end gradient goes to its slot of
+// B.dhb (the first one's to dh0).  mode 2 reruns from its true right-end gradient every
+// segment with an unwritten result: flagged by its own CTA, preceding a segment (not the last)
+// whose transition is not negligible, or the first segment when its own transition is not
+// negligible (dh0).
+__global__ void __launch_bounds__(TCT, 1) k_tc_bwd_c(BwdProblem B, const __grid_constant__ BwdMaps maps,
+                                                    int mode) {
     unsigned char* sm = aligned_smem();
     const Problem& P = B.f;
     const int gseg = blockIdx.x, j = blockIdx.y;
@@ -1547,9 +1619,38 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_bwd_c(BwdProblem B, const __grid_
     seq_range(P, s, t0, t1);
     const int nt = int((t1 - t0 + CH - 1) / CH);
     const int cb = lj * P.L, ce = min(cb + P.L, nt);
-    const float* x0 = (lj == nseg - 1) ? (B.dht ? B.dht + (int64_t(s) * P.Hv + j) * KVN : nullptr)
-                                       : B.dhb + (int64_t(gseg + 1) * P.Hv + j) * KVN;
-    float* x_out = (lj == 0 && B.dh0) ? B.dh0 + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    const int64_t sjh = int64_t(gseg) * P.Hv + j;
+    const bool last = lj == nseg - 1;
+    const float* dht = B.dht ? B.dht + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    float* dh0 = B.dh0 ? B.dh0 + (int64_t(s) * P.Hv + j) * KVN : nullptr;
+    if (mode == 1) {
+        const float* x0 = last ? dht : nullptr;
+        float* x_seg = lj == 0 ? dh0 : B.dhb + sjh * KVN;
+        if (ce <= cb) { copy_state(x0, x_seg, false); return; }  // only an empty sequence
+        ScanRule rule;
+        rule.n_own = ce - cb;
+        rule.e_own = last ? 0 : ext_len_rev(P, t0, t1, ce, ce - cb, j);
+        rule.lj = last ? 0 : 1;
+        rule.dec = nullptr;
+        rule.rerun = B.rrerun + sjh;
+        rule.ext_ok = (last || P.dec[sjh] >= 0) ? 1 : 0;
+        const int e_prev = lj >= 1 ? ext_len_rev(P, t0, t1, cb, P.L, j) : 0;  // the previous segment is full
+        rule.x_mid = e_prev > 0 ? x_seg : nullptr;
+        tc_bwd_scan<true>(B, maps.f, &maps.dO, sm, j, t0, t1, cb - e_prev, ce, x0,
+                          e_prev > 0 ? nullptr : x_seg, P.plan.chunk_off[s], &rule);
+        return;
+    }
+    if (mode == 2) {
+        if (last || ce <= cb) return;
+        const bool next_inner = lj + 1 <= nseg - 2;  // the next segment is not the last
+        if (!(B.rrerun[sjh] != 0 || (next_inner && P.dec[sjh + P.Hv] < 0) || (lj == 0 && P.dec[sjh] < 0)))
+            return;
+        tc_bwd_scan<true>(B, maps.f, &maps.dO, sm, j, t0, t1, cb, ce, B.dhb + (sjh + P.Hv) * KVN,
+                          lj == 0 ? dh0 : nullptr, P.plan.chunk_off[s]);
+        return;
+    }
+    const float* x0 = last ? dht : B.dhb + (sjh + P.Hv) * KVN;
+    float* x_out = (lj == 0) ? dh0 : nullptr;
     if (ce <= cb) { copy_state(x0, x_out, false); return; }
     tc_bwd_scan<true>(B, maps.f, &maps.dO, sm, j, t0, t1, cb, ce, x0, x_out, P.plan.chunk_off[s]);
 }
@@ -1653,18 +1754,25 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
     return cudaGetLastError();
 }
 
-// The two reverse-scan launches of the backward (bf16): first phase, then (after the caller's
-// fix-up) the rerun that stores dh per chunk.  `which` = 0 first phase, 1 rerun.
+// The reverse-scan launches of the backward (bf16): `which` = 0 first phase, 1 the rerun that
+// stores dh per chunk (after the caller's fix-up); decay-bounded exact mode: 2 first pass,
+// 3 correction.
 cudaError_t launch_bwd_scan_tc(const BwdProblem& B, int which, int64_t T_total, cudaStream_t st) {
     const Problem& P = B.f;
     BwdMaps maps;
     if (!make_map(&maps.f.k, P.k, P.Hqk, T_total) || !make_map(&maps.f.q, P.q, P.Hqk, T_total) ||
         !make_map(&maps.f.v, P.v, P.Hv, T_total) || !make_map(&maps.dO, B.dO, P.Hv, T_total))
         return cudaErrorInvalidValue;
-    auto kern = which == 0 ? k_tc_bwd_a : k_tc_bwd_c;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    kern<<<dim3(P.total_segs, P.Hv), TCT, SMEM_BYTES, st>>>(B, maps);
+    cudaError_t e;
+    if (which == 0) {
+        e = cudaFuncSetAttribute(k_tc_bwd_a, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        k_tc_bwd_a<<<dim3(P.total_segs, P.Hv), TCT, SMEM_BYTES, st>>>(B, maps);
+    } else {
+        e = cudaFuncSetAttribute(k_tc_bwd_c, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        k_tc_bwd_c<<<dim3(P.total_segs, P.Hv), TCT, SMEM_BYTES, st>>>(B, maps, which - 1);
+    }
     return cudaGetLastError();
 }
 

@@ -76,6 +76,8 @@ struct BwdProblem {
     float* dbeta;       // [T, Hv]
     void* dhist;        // [total_chunks, Hv, K, V] gradient w.r.t. the state leaving each chunk
     float* dhb;         // [total_segs, Hv, K, V] gradient entering each segment from the right
+    int* rrerun;        // [total_segs, Hv] decay-bounded reverse scan: some gradient of the
+                        // segment is left to the correction pass (or null)
     float* dqp;         // [T, Hv, K] per-v-head partial dq (G > 1) or null
     float* dkp;         // [T, Hv, K] per-v-head partial dk (G > 1) or null
 };
