@@ -349,7 +349,13 @@ def oracle_sample_fixed(inp, n, backward):
 # keyed by workload and by the set of kernels the step launches: a key that no longer
 # matches the kernels this build launches gives no figure (null), so a capture of an older
 # kernel set is never reported against a newer one.
-NCU_STEP_TRAFFIC = {}
+NCU_STEP_TRAFFIC = {
+    # 1 x 32768 tokens, 2 / 8 heads: k_prep 110.8 MB + first output pass 298.7 MB (section
+    # captures of this kernel set); the plan and the three gated launches (transitions, fix-up,
+    # correction: they read a few flags here) are not captured
+    ("fwd_t32k_hqk2_hv8", ("fwd_correction", "fwd_fixup", "fwd_pass1", "fwd_plan", "fwd_prep",
+                           "fwd_transitions")): 409.5e6,
+}
 
 
 def method_bytes(tokens, lens, w):
@@ -570,6 +576,18 @@ def main():
         }
         if "e2e" in sub:
             line["fwdbwd"]["e2e"] = sub["e2e"]
+        # the same training step with the low-level saved pair: the forward keeps the state
+        # entering every chunk (and its chunk records) and the backward reads them instead of
+        # recomputing the forward (more memory, less work)
+        sv = measure(FWDBWD_WORKLOAD, args, dev, world, local, clocks=True, save=True)
+        line["fwdbwd_saved_states"] = {
+            "ms_per_step": sv["ms_per_step"],
+            "value": world * sv["tokens"] / (sv["ms_per_step"] / 1000.0), "unit": "tokens/s",
+            "roofline_frac": sv["roofline"]["frac"], "gpu_launches": sv["launches"],
+            "kernels_ms_per_step": {k: v["ms_per_step"] for k, v in sv["roofline"]["kernels"].items()},
+            "clocks": sv["clocks"]}
+        if "e2e" in sv:
+            line["fwdbwd_saved_states"]["e2e"] = sv["e2e"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp = workload_inputs(args.workload)
         lens = lengths_of(inp)
