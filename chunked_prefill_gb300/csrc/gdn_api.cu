@@ -8,12 +8,29 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
+#include <set>
+#include <tuple>
 #include <vector>
 
 #include "../../include/gdn.h"
 #include "gdn_internal.h"
 
 namespace gdn {
+cudaError_t smem_attr_once(const void* kern, int bytes) {
+    static std::mutex mu;
+    static std::set<std::tuple<const void*, int, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const auto key = std::make_tuple(kern, dev, bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -105,8 +122,23 @@ gdn_status validate_problem(const gdn_problem* p) {
 // phase runs a segment's state and transition in one CTA) times the chunks a CTA scans, plus
 // the serial fix-up steps.  The step costs are measured ratios on GB300 (a first-phase chunk
 // step ~1.0 of an output chunk step; a fix-up step as below).
-double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int warmup) {
+double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int warmup, bool bounded) {
     constexpr double tC = 1.0, tA = 1.0;
+    if (bounded) {
+        // exact mode with decay bounds, costed for decaying gates: one pass of L chunks plus
+        // the ~2 chunks each segment scans into the next, and the three extra launches
+        // (transitions, fix-up, correction: ~3 us each, returning at once) when segmented
+        long segs = 0;
+        int maxn = 0;
+        for (int s = 0; s < N; ++s) {
+            const int ns = std::max(1, (nts[s] + L - 1) / L);
+            segs += ns;
+            maxn = std::max(maxn, ns);
+        }
+        const long cw = (segs * Hv + sms - 1) / sms;
+        const int Lc = std::min(L, *std::max_element(nts, nts + N));
+        return maxn > 1 ? double(cw) * (Lc + 2) * tC + 4.0 : double(cw) * Lc * tC;
+    }
     long segs = 0, actas = 0;
     int maxn = 0;
     for (int s = 0; s < N; ++s) {
@@ -164,9 +196,10 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
             }
             const int sms = sm_count();
             const bool exact = p->cp_mode != GDN_CP_WARMUP;
+            const bool bounded_cost = exact && p->cp_mode != GDN_CP_EXACT_FULL && p->dtype == GDN_BF16;
             double best = 1e300;
             for (int cand = nt_max; cand >= 1; --cand) {  // ties go to longer segments
-                const double c = cp_cost(cand, nts.data(), h.N, p->Hv, sms, exact, warm);
+                const double c = cp_cost(cand, nts.data(), h.N, p->Hv, sms, exact, warm, bounded_cost);
                 if (c < best - 1e-9) {
                     best = c;
                     autoL = cand;

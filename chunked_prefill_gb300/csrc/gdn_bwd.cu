@@ -1083,7 +1083,7 @@ cudaError_t launch_bwd_t(const BwdProblem& B, cudaStream_t st) {
     constexpr bool TC = sizeof(Op) == 2;
     cudaError_t e;
     const int fix_smem = (KD * 129 + KD * 8) * 4;
-    e = cudaFuncSetAttribute(k_bwd_fixup, cudaFuncAttributeMaxDynamicSharedMemorySize, fix_smem);
+    e = smem_attr(k_bwd_fixup, fix_smem);
     if (e != cudaSuccess) return e;
     if constexpr (!TC) {
         e = cudaFuncSetAttribute(k_bwd_phase_a<Op, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SS::bytes));

@@ -1099,7 +1099,7 @@ cudaError_t launch_bwd_local_tc(const BwdProblem& B, int64_t T_total, cudaStream
         !make_map(&maps.v, P.v, P.Hv, T_total) || !make_map(&maps.dO, B.dO, P.Hv, T_total) ||
         !make_rows_map(&maps.h, P.hist, rows) || !make_rows_map(&maps.dh, B.dhist, rows))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_tc_bwd_local, cudaFuncAttributeMaxDynamicSharedMemorySize, int(LOC_SMEM));
+    cudaError_t e = smem_attr(k_tc_bwd_local, int(LOC_SMEM));
     if (e != cudaSuccess) return e;
     const int64_t items = int64_t(P.total_chunks) * P.Hv;
     const int grid = int(items < int64_t(sm_count()) ? items : int64_t(sm_count()));  // persistent

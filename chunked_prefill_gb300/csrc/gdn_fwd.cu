@@ -636,7 +636,7 @@ static void launch_fixup_cg(int N, int Hv, const int* seg_off, const float* mats
                             int* err, bool pdl, cudaStream_t st, const int* dec) {
     auto run = [&](auto kern, int cg) {
         const int smem = fix_smem(cg);
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        smem_attr(kern, smem);
         const dim3 grid(N, Hv, VD / (8 * cg));
         if (pdl) launch_pdl(kern, grid, dim3(FIX_T), smem, st, seg_off, mats, xbuf, Hv, err, dec);
         else kern<<<grid, FIX_T, smem, st>>>(seg_off, mats, xbuf, Hv, err, dec);

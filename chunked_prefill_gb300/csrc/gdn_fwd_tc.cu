@@ -1710,11 +1710,11 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
         !make_map(&maps.v, P.v, P.Hv, T_total))
         return cudaErrorInvalidValue;
     cudaError_t e;
-    e = cudaFuncSetAttribute(k_tc_phase_a, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = smem_attr(k_tc_phase_a, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_tc_phase_c<TK_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = smem_attr(k_tc_phase_c<TK_OUT>, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_tc_phase_c<TK_HIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = smem_attr(k_tc_phase_c<TK_HIST>, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     launch_plan(P, CH, st);
     launch_prep(P, maps, st);
@@ -1765,11 +1765,11 @@ cudaError_t launch_bwd_scan_tc(const BwdProblem& B, int which, int64_t T_total, 
         return cudaErrorInvalidValue;
     cudaError_t e;
     if (which == 0) {
-        e = cudaFuncSetAttribute(k_tc_bwd_a, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        e = smem_attr(k_tc_bwd_a, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         k_tc_bwd_a<<<dim3(P.total_segs, P.Hv), TCT, SMEM_BYTES, st>>>(B, maps);
     } else {
-        e = cudaFuncSetAttribute(k_tc_bwd_c, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        e = smem_attr(k_tc_bwd_c, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         k_tc_bwd_c<<<dim3(P.total_segs, P.Hv), TCT, SMEM_BYTES, st>>>(B, maps, which - 1);
     }

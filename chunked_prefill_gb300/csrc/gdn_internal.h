@@ -98,6 +98,14 @@ cudaError_t launch_prologue_bwd(const PrologueArgs& A, cudaStream_t st);
 // Test hook of the device failure report: a bounded wait that gives up after limit_us.
 cudaError_t launch_debug_wait(int* err, int limit_us, cudaStream_t st);
 
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device): the attribute
+// persists, and setting it again on every call costs host time the small problems feel.
+cudaError_t smem_attr_once(const void* kern, int bytes);
+template <typename... KArgs>
+cudaError_t smem_attr(void (*kern)(KArgs...), int bytes) {
+    return smem_attr_once(reinterpret_cast<const void*>(kern), bytes);
+}
+
 // Per-kernel event timing hooks (no-ops unless gdn_timing_enable(1)).
 void timing_begin(const char* name, cudaStream_t st);
 void timing_end(cudaStream_t st);

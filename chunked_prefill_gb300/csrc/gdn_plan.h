@@ -58,6 +58,7 @@ struct Problem {
     int* rerun;         // [total_segs, Hv] or null: some result of the segment is left to the
                         // correction pass
     int full_cp;        // 1: every transition computed and every segment rerun (no bound)
+    int prep_heads;     // v-heads per preparation CTA (set by the preparation's launcher)
     float scale;
     int* err;           // device error word (bounded waits that timed out), or null
 };

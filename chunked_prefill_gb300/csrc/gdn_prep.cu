@@ -13,6 +13,8 @@
 // backward's dO^T P must not see them).
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "tc05.cuh"
@@ -100,9 +102,10 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     const int gch = blockIdx.x;
     if (gch >= P.plan.chunk_off[P.N]) return;
     const int G = P.Hv / P.Hqk;
-    const int nsl = (G + S::GMAX - 1) / S::GMAX;          // slices of a q/k group
-    const int qh = blockIdx.y / nsl, j0 = qh * G + (blockIdx.y % nsl) * S::GMAX;
-    const int nh = min(S::GMAX, qh * G + G - j0);         // v-heads of this CTA
+    const int hpc = P.prep_heads;                         // v-heads per CTA (<= GMAX)
+    const int nsl = (G + hpc - 1) / hpc;                  // slices of a q/k group
+    const int qh = blockIdx.y / nsl, j0 = qh * G + (blockIdx.y % nsl) * hpc;
+    const int nh = min(hpc, qh * G + G - j0);             // v-heads of this CTA
     int lo = 0, hi = P.N - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -533,10 +536,16 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
 
 void launch_prep(const Problem& P, const TcMaps& maps, cudaStream_t st) {
     if (P.total_chunks <= 0) return;
-    cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PrepSmem::bytes));
-    const int G = P.Hv / P.Hqk, nsl = (G + PrepSmem::GMAX - 1) / PrepSmem::GMAX;
+    smem_attr(k_prep, int(PrepSmem::bytes));
+    // a CTA prepares the v-heads of (a slice of) one q/k group in turn, sharing K, Q and
+    // [K;Q] K^T; a launch too small to fill the SMs several times over gives each CTA one
+    // v-head instead, so that the heads run side by side
+    const int G = P.Hv / P.Hqk;
+    Problem Q = P;
+    Q.prep_heads = int64_t(P.total_chunks) * P.Hqk >= 2 * int64_t(sm_count()) ? std::min(G, PrepSmem::GMAX) : 1;
+    const int nsl = (G + Q.prep_heads - 1) / Q.prep_heads;
     timing_begin("fwd_prep", st);
-    launch_pdl(k_prep, dim3(P.total_chunks, P.Hqk * nsl), dim3(PT), PrepSmem::bytes, st, P, maps);
+    launch_pdl(k_prep, dim3(P.total_chunks, P.Hqk * nsl), dim3(PT), PrepSmem::bytes, st, Q, maps);
     timing_end(st);
 }
 
