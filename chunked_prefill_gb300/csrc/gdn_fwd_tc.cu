@@ -8,21 +8,20 @@
 //   * the state is kept TRANSPOSED in tensor memory, Xt[v][dk] = h[dk][v] (fp32 master,
 //     128 columns) plus a bf16 copy (64 columns) that is the A operand of the V' and Q h
 //     products straight from TMEM;
-//   * K, Q, V chunk tiles arrive by TMA (128-byte swizzle) and the chunk-local TW, TU, P
+//   * K, Q, V chunk tiles arrive by TMA (128-byte swizzle) and the chunk-local W', TU, P
 //     tiles of the preparation kernel by bulk copies, into a 2-stage ring;
 //   * per chunk of 64 tokens (i, j tokens; dk key dim; v value dim):
-//       D2  = K^T TW^T   = W'^T          (dk x i)      -> shared-memory tile (B operand)
 //       D3  = V^T TU^T + Xt W'^T = V'^T  (v x i)       -> bf16 V'^T and diag(kd) V'^T in TMEM
 //       D4a = Xt Q^T     = (Q h)^T       (v x i)
 //       D4b = V'^T P^T   = (P V')^T      (v x i)       -> O = scale (e * D4a + D4b)
 //       Xt  = e^{gamma_C} Xt + (diag(kd) V')^T K       (v x dk)
 //
-// Warp roles (16 warps): 0 TMA producer; 1 state-chain MMA issuer (W', U, V', state update);
-// 2 gates (cumsum of g and its exponentials); 3 output MMA issuer (D4a, D4b); 4-11 state
-// warps, one warpgroup per half of the key columns (state hand-off, V' conversion; the second
-// also moves W'^T to shared memory); 12-15 output warps.  The two issuers run independently:
-// the state chain never queues behind the output products.  Every wait on an mbarrier is
-// bounded; on a timeout the kernel records an error word and winds down.
+// Warp roles (16 warps): 0 TMA producer; 1 state-chain MMA issuer (V' with D4a, state update;
+// U too without an output side); 2 gates (cumsum of g and its exponentials); 3 output MMA
+// issuer (U, D4b); 4-11 state warps, one warpgroup per half of the key columns (state
+// hand-off, V' conversion); 12-15 output warps.  The two issuers run independently: the state
+// chain never queues behind the output products.  Every wait on an mbarrier is bounded; on a
+// timeout the kernel records an error word and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,8 +40,9 @@ constexpr int CH = 64;    // chunk
 // tensor-memory columns: Xt (fp32 state, transposed), its bf16 copy, two chunk buffers DD
 // (by chunk parity) and D4b.  A DD buffer holds [V'^T | (Q h)^T] (64 + 64 columns): U^T is
 // written first (the (Q h)^T half is zero: the output warps clear it after reading it), then
-// one MMA over [W'; Q] adds Xt W'^T and Xt Q^T.  D4b = (P V')^T; the output warps combine
-// O = scale (e (Q h) + P V').
+// one MMA over [W'; Q] adds Xt W'^T and Xt Q^T (as two products of N = 64, V' first, the
+// whole scan ran slower: more tensor-pipe instructions per chunk).  D4b = (P V')^T; the
+// output warps combine O = scale (e (Q h) + P V').
 constexpr uint32_t T_XF = 0, T_XB = 128, T_D4B = 448;
 __device__ __forceinline__ uint32_t t_dd(int k) { return (k & 1) ? 320u : 192u; }
 // converted V' in a DD buffer: tokens [0,32) at columns [0,16) (V'^T) and [16,32)
@@ -100,7 +100,7 @@ static_assert(sizeof(Gate) <= GATE_BYTES && sizeof(Gate) % 16 == 0, "gate buffer
 
 enum Bar { B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GFREE0,
            B_GFREE1, B_GFREE2, B_GFREE3, B_MMA3, B_MMA5, B_MMA4_0, B_MMA4_1, B_DRAIN, B_EX, B_EV0,
-           B_EV1, B_EPI0, B_EPI1, B_M5C0, B_M5C1, B_FULLP0, B_EMPTYP0 = B_FULLP0 + NP,
+           B_EV1, B_EPI0, B_EPI1, B_M5C0, B_M5C1, B_U0, B_U1, B_FULLP0, B_EMPTYP0 = B_FULLP0 + NP,
            B_COUNT = B_EMPTYP0 + NP };
 
 static_assert(B_COUNT * 8 + 8 <= 512, "barrier area");
@@ -258,7 +258,6 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                         int64_t hist_base, float* x_out_t = nullptr, const ScanRule* rule = nullptr) {
     constexpr bool OUT = KIND == TK_OUT;
     constexpr bool NEEDU = KIND != TK_TRANS;
-    constexpr int NDD = OUT ? 128 : 64;  // columns of a DD buffer the MMAs write
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + B_COUNT * 8);
@@ -292,6 +291,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         mbar_init(&bars[B_EPI1], 4);
         mbar_init(&bars[B_M5C0], 1);  // per chunk parity: the state update has completed
         mbar_init(&bars[B_M5C1], 1);
+        mbar_init(&bars[B_U0], 1);
+        mbar_init(&bars[B_U1], 1);
         *errflag = 0;
         mbar_fence_init();
     }
@@ -318,7 +319,6 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         __syncthreads();
         fence_after_sync();
     }
-
     if (w == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -357,28 +357,27 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         __syncwarp();
     } else if (w == 1) {
         // ------------------------------------------------------------ state-chain MMA issuer
-        // per chunk k: [V'|Qh] (one MMA over [W'; Q]), the state update, then U of k+1 --
-        // only the reuse of a DD buffer two chunks later waits for the output side.
+        // per chunk k: [V'|Q h], then the state update.  With an output side (OUT) its MMA
+        // issuer forms U of each chunk, else U of k+1 follows here.  Lane 0 alone runs the
+        // loop: issued from warp-uniform code (elect.sync) the MMAs leave the tensor pipe
+        // sooner, but the whole scan runs slower (the state warps that share this warp's SMSP
+        // lose issue slots).
         if (lane == 0) {
             constexpr uint32_t IDU = make_idesc(128, 64, 1, 0);
-            constexpr uint32_t IDV = make_idesc(128, NDD, 0, 0);
+            constexpr uint32_t IDV = make_idesc(128, OUT ? 128 : 64, 0, 0);
             constexpr uint32_t ID5 = make_idesc(128, 128, 0, 1);
             const uint32_t k0a = smem_addr(sm + S_K), wq0 = smem_addr(sm + S_WQ);
             const uint32_t v0a = smem_addr(sm + S_V), tu0 = smem_addr(sm + S_TU);
-            const uint64_t dK[2] = {mdesc(k0a, 8192), mdesc(k0a + S_K_STRIDE, 8192)};
-            const uint64_t dWQ[2] = {kdesc(wq0), kdesc(wq0 + S_WQ_STRIDE)};
-            const uint64_t dV[2] = {mdesc(v0a, 8192), mdesc(v0a + S_V_STRIDE, 8192)};
-            const uint64_t dTU[2] = {kdesc(tu0), kdesc(tu0 + S_TU_STRIDE)};
             // U^T = V^T TU^T for chunk k into the V' half of its DD buffer
             auto issue_u = [&](int k) {
                 const int st = k & 1;
+                const uint64_t dV = mdesc(v0a + st * S_V_STRIDE, 8192), dTU = kdesc(tu0 + st * S_TU_STRIDE);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_bf16(tm + t_dd(k), (st ? dV[1] : dV[0]) + (s * 2048 >> 4),
-                             (st ? dTU[1] : dTU[0]) + (s * 32 >> 4), IDU, s > 0);
+                    mma_bf16(tm + t_dd(k), dV + (s * 2048 >> 4), dTU + (s * 32 >> 4), IDU, s > 0);
             };
             bool ok = true;
-            if (NEEDU) {
+            if (NEEDU && !OUT) {
                 ok = wait_bar(bars, B_FULL0, 0, errflag);
                 if (ok) {
                     fence_after_sync();
@@ -388,19 +387,26 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             for (int k = 0; ok && k < n; ++k) {
                 const int st = k & 1;
                 const uint32_t dd = tm + t_dd(k);
+                const uint64_t dWQ = kdesc(wq0 + st * S_WQ_STRIDE), dK = mdesc(k0a + st * S_K_STRIDE, 8192);
                 TRACE(k, 0);
                 if ((!NEEDU && !wait_bar(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) ||
+                    (OUT && !wait_bar(bars, B_U0 + st, (k >> 1) & 1, errflag)) ||
                     !wait_bar(bars, B_EX, k & 1, errflag)) {
                     ok = false;
                     break;
                 }
                 TRACE(k, 1);
                 fence_after_sync();
+                // [V'^T | (Q h)^T] in one product over [W'; Q]; the (Q h)^T half of this DD
+                // buffer last held chunk k-2's, read (and cleared) by its output warps
+                if (OUT && k >= 2 && !wait_bar(bars, B_EPI0 + (k & 1), ((k - 2) >> 1) & 1, errflag)) {
+                    ok = false;
+                    break;
+                }
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                    mma_bf16_ta(dd, tm + T_XB + 8 * s, (st ? dWQ[1] : dWQ[0]) + (off >> 4), IDV,
-                                (NEEDU || s > 0) ? 1u : 0u);
+                    mma_bf16_ta(dd, tm + T_XB + 8 * s, dWQ + (off >> 4), IDV, (NEEDU || s > 0) ? 1u : 0u);
                 }
                 commit(&bars[B_MMA3]);
                 TRACE(k, 2);
@@ -409,20 +415,13 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_bf16_ta(tm + T_XF, dd + (OUT ? kd_col(s) : p_col(s)), (st ? dK[1] : dK[0]) + (s * 2048 >> 4),
-                                ID5, 1u);
+                    mma_bf16_ta(tm + T_XF, dd + (OUT ? kd_col(s) : p_col(s)), dK + (s * 2048 >> 4), ID5, 1u);
                 commit(&bars[B_MMA5]);
                 if (OUT) commit(&bars[B_M5C0 + (k & 1)]);
                 commit(&bars[B_EMPTY0 + st]);  // last reader of this stage on this issuer
                 TRACE(k, 5);
-                if (NEEDU && k + 1 < n) {
+                if (NEEDU && !OUT && k + 1 < n) {
                     if (!wait_bar(bars, B_FULL0 + ((k + 1) & 1), ((k + 1) >> 1) & 1, errflag)) {
-                        ok = false;
-                        break;
-                    }
-                    // DD[(k+1) & 1] last held chunk k-1, read by its output warps
-                    if (OUT && k >= 1 &&
-                        !wait_bar(bars, B_EPI0 + ((k - 1) & 1), ((k - 1) >> 1) & 1, errflag)) {
                         ok = false;
                         break;
                     }
@@ -508,7 +507,8 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     } else if (w == 3 && OUT) {
         // ------------------------------------------------------------ output MMA issuer
         // D4b = (P V')^T once V' of chunk k is converted and the output warps have read D4b
-        // of chunk k-1.
+        // of chunk k-1; U of chunk k+1 before that, right after the last reader of its buffer
+        // (the P V' product of chunk k-1, issued here), so the state chain never waits on it.
         if (lane == 0) {
             constexpr uint32_t ID4 = make_idesc(128, 64, 0, 0);
             const uint32_t p0 = smem_addr(sm + S_P);
@@ -519,10 +519,27 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 mbar_expect_tx(&bars[B_FULLP0 + b], 8192);
                 bulk_load(sm + S_P + b * S_P_STRIDE, rec + PREP_P, 8192, &bars[B_FULLP0 + b]);
             };
+            constexpr uint32_t IDU = make_idesc(128, 64, 1, 0);
+            const uint32_t v0a = smem_addr(sm + S_V), tu0 = smem_addr(sm + S_TU);
+            // U^T = V^T TU^T of chunk q into the V' half of its DD buffer, whose last reader
+            // (the P V' product of chunk q-2) was issued here before
+            auto issue_u = [&](int q) {
+                const int st = q & 1;
+                const uint64_t dV = mdesc(v0a + st * S_V_STRIDE, 8192), dTU = kdesc(tu0 + st * S_TU_STRIDE);
+                if (!wait_bar(bars, B_FULL0 + st, (q >> 1) & 1, errflag)) return false;
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tm + t_dd(q), dV + (s * 2048 >> 4), dTU + (s * 32 >> 4), IDU, s > 0);
+                commit(&bars[B_U0 + st]);
+                return true;
+            };
             int issued = 0, used = 0;
             for (; issued < NP - 1 && issued < n; ++issued) load_p(issued);
-            for (int k = 0; k < n; ++k) {
+            bool uok = n > 0 ? issue_u(0) : true;
+            for (int k = 0; uok && k < n; ++k) {
                 const int b = k % NP;
+                if (k + 1 < n && !issue_u(k + 1)) break;
                 if (!wait_bar(bars, B_FULLP0 + b, (k / NP) & 1, errflag)) break;
                 used = k + 1;
                 if (k >= 1 && !wait_bar(bars, B_EPI0 + ((k - 1) & 1), ((k - 1) >> 1) & 1, errflag)) break;
@@ -575,9 +592,17 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_EX]);
-                if (rule && rule->x_mid && k == rule->n_own) {  // the state at the end of the own segment
+                if (rule && rule->x_mid && k == rule->n_own) {
+                    // the state at the end of the own segment (read again from TMEM in a rolled
+                    // loop: once per scan, so the loop body's code stays small)
+#pragma unroll 1
+                    for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 16) {
+                        float xv[16];
+                        tmem_ld16(tm + lb + T_XF + c0, xv);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) rule->x_mid[(64 * hf + i) * VD + v] = xs[i];
+                        for (int i = 0; i < 16; ++i) rule->x_mid[(c0 + i) * VD + v] = xv[i];
+                    }
                 }
                 state_decay_half<KIND>(P, tm, lb, hf, v, gb.eC, hist_base + cb + k, j, T_XF, xs,
                                        gb.store != 0);
@@ -665,37 +690,38 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             const float sc = P.scale;
             const uint32_t dqa = tm + lb + t_dd(k) + 64;
             const uint32_t ge = smem_addr(&gb.e[0]);
+            // a rolled loop over four 16-column groups: this role's code stays small (the 16
+            // warps' roles share each SMSP's instruction cache)
+            float z16[16];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float qa[32], pb[32];
-                tmem_ld32(dqa + 32 * half, qa);
-                tmem_ld32(tm + lb + T_D4B + 32 * half, pb);
+            for (int i = 0; i < 16; ++i) z16[i] = 0.f;
+#pragma unroll 1
+            for (int g4 = 0; g4 < 4; ++g4) {
+                float qa[16], pb[16];
+                tmem_ld16(dqa + 16 * g4, qa);
+                tmem_ld16(tm + lb + T_D4B + 16 * g4, pb);
                 tmem_ld_wait();
-                {  // clear the output columns for the chunk that reuses this buffer
-                    float z[32];
+                tmem_st16(dqa + 16 * g4, z16);  // clear for the chunk that reuses this buffer
+                float ev[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) z[i] = 0.f;
-                    tmem_st32(dqa + 32 * half, z);
+                for (int i = 0; i < 4; ++i) {
+                    const float4 e4 = lds128f(ge + 4 * (16 * g4 + 4 * i));
+                    ev[4 * i] = e4.x;
+                    ev[4 * i + 1] = e4.y;
+                    ev[4 * i + 2] = e4.z;
+                    ev[4 * i + 3] = e4.w;
                 }
-                if (half == 1) {
-                    tmem_st_wait();
-                    fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[B_EPI0 + (k & 1)]);
-                    if (v == 0) TRACE(k, 28);
-                }
+                const uint32_t sb = so + ((16 * g4) * LDO + v) * 2;
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const float4 e4 = lds128f(ge + 4 * (32 * half + 4 * q4));
-                    const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int qq = 4 * q4 + u;
-                        sts16(so + ((32 * half + qq) * LDO + v) * 2,
-                              __bfloat16_as_ushort(__float2bfloat16_rn(sc * fmaf(ev[u], qa[qq], pb[qq]))));
-                    }
-                }
+                for (int u = 0; u < 16; ++u)
+                    sts16(sb + u * LDO * 2,
+                          __bfloat16_as_ushort(__float2bfloat16_rn(sc * fmaf(ev[u], qa[u], pb[u]))));
             }
+            tmem_st_wait();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_EPI0 + (k & 1)]);
+            if (v == 0) TRACE(k, 28);
             named_sync(2, 128);
             // rows of O leave as 16-byte vectors (only the rows of this sequence)
             const int64_t tc = t0 + int64_t(cb + k) * CH;
@@ -1140,10 +1166,10 @@ __device__ int ext_len(const Problem& P, int64_t t0, int64_t t1, int cs, int n, 
 template <int KIND>
 __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_constant__ TcMaps maps,
                                                       int mode) {
-    CTRACE(1, 0);
+    if (mode != 2) CTRACE(1, 0);
     pdl_launch_dependents();
     pdl_wait();
-    CTRACE(1, 1);
+    if (mode != 2) CTRACE(1, 1);
     unsigned char* sm = aligned_smem();
     const int gseg = blockIdx.x, j = blockIdx.y;
     const int2 sj = P.plan.seg[gseg];
@@ -1172,6 +1198,7 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_c
         rule.x_mid = e_next > 0 ? x_seg : nullptr;
         tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce + e_next, x0, e_next > 0 ? nullptr : x_seg,
                       P.plan.chunk_off[s], nullptr, &rule);
+        CTRACE(1, 3);
         return;
     }
     if (mode == 2) {
