@@ -7,7 +7,8 @@
 //     T  = (I + A)^-1                                (fp32: substitution + TF32 block products)
 //     TU = T diag(beta),  W' = -T diag(beta e) K     (W' = -W of the pages' WY form; tcgen05)
 // K and Q arrive by TMA; W', TU and P leave by bulk copies from shared-memory tiles already in
-// the 128-byte-swizzled layout the scan's tensor-core operands use.  Rows past the end of a
+// the 128-byte-swizzled layout the scan's tensor-core operands use (T, for the backward, by
+// 16-byte stores of the same image).  Rows past the end of a
 // sequence hold whatever tokens follow (finite); beta = g = 0 there makes T's rows and the
 // columns of TU and W' for them exactly zero, and P's rows for them are written as zeros (the
 // backward's dO^T P must not see them).
@@ -45,7 +46,13 @@ __device__ unsigned long long g_prep_trace[8 * 9];  // debug builds: SM clock at
     } while (0)
 #endif
 
-constexpr int PT = 128;  // threads
+// 8 warps: warp w reads TMEM lanes [32 (w % 4), +32); the row-per-thread phases (A and P,
+// W' staging) split a row's 64 columns between warps w and w + 4, the item loops (gates in,
+// TU / TW staging) spread over all 256 threads, and the inverse runs on warps 0-3.  At 64
+// registers per thread four CTAs (32 warps) fit an SM, as four CTAs of 4 warps did: each CTA's
+// row phases take half the time.
+constexpr int PT = 256;  // threads
+constexpr int TU4 = 64 * 8 / PT;  // (row, 8-column chunk) items per thread of the TU / TW staging
 constexpr int CH = 64;
 
 // The 64 x 64 lower-triangular A and T are kept as their ten nonzero 16 x 16 blocks (row
@@ -216,45 +223,48 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         __syncthreads();  // gates visible; the previous head's staging has been read
         PTRACE(1);
 
-        // A (rows of KK) and P (rows of QK): thread = one row of the stacked product, in two
-        // halves of 32 columns
+        // A (rows of KK) and P (rows of QK): thread = one row of the stacked product, warp w
+        // its half w / 4 of the 64 columns
         {
             const bool pw = *sFlag != 0;
-            const bool qrows = w >= 2;
-            const int i = 32 * (w & 1) + lane;
+            const int wq = w & 3;
+            const bool qrows = wq >= 2;
+            const int i = 32 * (wq & 1) + lane;
             const float gi = sGam[i], ei = sE[i], bi = sBeta[i];
             unsigned char* pt = smem + S::oT;  // P staging (bf16, swizzled rows)
 #pragma unroll 1
-            for (int h2 = 0; h2 < 2; ++h2) {
-                float raw[32];
-                tmem_ld32(tm + (uint32_t(32 * w) << 16) + 32 * h2, raw);
+            for (int q16 = 0; q16 < 2; ++q16) {  // 16 columns at a time (register budget)
+                const int c0 = 32 * (w >> 2) + 16 * q16;
+                float raw[16];
+                tmem_ld16(tm + (uint32_t(32 * wq) << 16) + c0, raw);
                 tmem_ld_wait();
-                if (!qrows && hh == 0 && h2 == (w & 1)) {  // the diagonal: |k_i|^2, once
+                if (!qrows && hh == 0 && (c0 >> 4) == (i >> 4)) {  // the diagonal: |k_i|^2, once
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) kn = (u == lane) ? raw[u] : kn;
+                    for (int u = 0; u < 16; ++u) kn = (u == (i & 15)) ? raw[u] : kn;
                 }
                 if (!qrows) {
-                    const int I = i >> 4, r = i & 15;
+                    const int I = i >> 4, r = i & 15, M = c0 >> 4;
+                    if (M <= I) {  // blocks above the diagonal are not stored
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const int jb = 32 * h2 + 4 * j4, M = jb >> 4;
-                        if (M > I) continue;  // above the diagonal blocks: not stored
-                        float x[4];
-                        const float4 ev = *reinterpret_cast<const float4*>(sEi + jb);
-                        const float evs[4] = {ev.x, ev.y, ev.z, ev.w};
+                        for (int j4 = 0; j4 < 4; ++j4) {
+                            const int jb = c0 + 4 * j4;
+                            float x[4];
+                            const float4 ev = *reinterpret_cast<const float4*>(sEi + jb);
+                            const float evs[4] = {ev.x, ev.y, ev.z, ev.w};
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int jj = jb + u;
-                            const float d = pw ? expf(gi - sGam[jj]) : ei * evs[u];
-                            x[u] = jj < i ? bi * d * raw[4 * j4 + u] : 0.f;
+                            for (int u = 0; u < 4; ++u) {
+                                const int jj = jb + u;
+                                const float d = pw ? expf(gi - sGam[jj]) : ei * evs[u];
+                                x[u] = jj < i ? bi * d * raw[4 * j4 + u] : 0.f;
+                            }
+                            *reinterpret_cast<float4*>(ablk(tri(I, M)) + r * BLD + (jb & 15)) =
+                                make_float4(x[0], x[1], x[2], x[3]);
                         }
-                        *reinterpret_cast<float4*>(ablk(tri(I, M)) + r * BLD + (jb & 15)) =
-                            make_float4(x[0], x[1], x[2], x[3]);
                     }
                 } else {
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int c8 = 4 * h2 + c4;
+                    for (int c4 = 0; c4 < 2; ++c4) {
+                        const int c8 = (c0 >> 3) + c4;
                         float x[8];
                         const float4 e0 = *reinterpret_cast<const float4*>(sEi + 8 * c8);
                         const float4 e1 = *reinterpret_cast<const float4*>(sEi + 8 * c8 + 4);
@@ -275,11 +285,11 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 }
             }
             if (qrows) fence_proxy_async_smem();
-            if (!qrows && P.logb) {
+            if (!qrows && P.logb && (w >> 2) == (wq & 1)) {  // warps 0 and 5 hold |k_i|^2
                 // log of a bound on the 2-norm of this chunk's state transition: per token
                 // exp(g) (I - beta k k^T), whose norm is exp(g) max(1, |1 - beta |k|^2|); the
                 // 1e-3 |beta |k|^2| term covers the rounding of |k|^2.  Row i's term, summed
-                // over the warp, then over the two warps below
+                // over the warp, then over the two warps (rows 0-31, 32-63) below
                 float term = 0.f;
                 if (i < c) {
                     const float t = bi * kn;
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) term += __shfl_xor_sync(0xffffffffu, term, off);
-                if (lane == 0) sPart[w] = term;
+                if (lane == 0) sPart[wq & 1] = term;
             }
         }
         __syncthreads();
@@ -301,8 +311,8 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         }
         __syncthreads();
 
-        // T = (I + A)^-1: diagonal blocks by substitution (warp q, lane = column) ...
-        if (lane < 16) {
+        // T = (I + A)^-1: diagonal blocks by substitution (warp q < 4, lane = column) ...
+        if (w < 4 && lane < 16) {
             const int col = lane;
             const float* ab = ablk(tri(w, w));
             float* tb = tblk(tri(w, w));
@@ -364,7 +374,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 zero();
                 mm(acc, tblk(tri(lo + 1, lo + 1)), slot(w));
                 put(tblk(tri(lo + 1, lo)), acc, -1.f);
-            } else {
+            } else if (w < 4) {
                 mm(acc, ablk(tri(w, 1)), tblk(tri(1, 1)));
                 put(slot(w), acc, 1.f);
             }
@@ -380,7 +390,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
             } else if (w == 2) {
                 mm(acc, tblk(tri(2, 2)), slot(2));
                 put(tblk(tri(2, 1)), acc, -1.f);
-            } else {
+            } else if (w == 3) {
                 mm(acc, tblk(tri(3, 2)), slot(2));
                 mm(acc, tblk(tri(3, 3)), slot(3));
                 put(tblk(tri(3, 1)), acc, -1.f);
@@ -455,19 +465,30 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
             for (int st = 0; st < 4; ++st) mma_bf16(tm + 64, da + (st * 2048 >> 4), db + (st * 32 >> 4), ID2, st > 0);
             commit(&bars[2]);
         }
-        // T itself for the backward: held in registers, then staged in bf16 over the T region
-        float tkeep[32];
+        // T itself for the backward (the record's swizzled bf16 image) and for the low-level
+        // output: 16-byte stores straight from the fp32 blocks while the W' product runs
         if (want_t) {
 #pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4) {
+            for (int u4 = 0; u4 < TU4; ++u4) {
                 const int it = tid + PT * u4, r = it & 63, c8 = it >> 6;  // as the staging above
+                float t8[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) tkeep[8 * u4 + u] = 0.f;
+                for (int u = 0; u < 8; ++u) t8[u] = 0.f;
                 if ((c8 >> 1) <= (r >> 4)) {
                     const float* tp = tblk(tri(r >> 4, c8 >> 1)) + (r & 15) * BLD + (c8 & 1) * 8;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) tkeep[8 * u4 + u] = (8 * c8 + u <= r) ? tp[u] : 0.f;
+                    for (int u = 0; u < 8; ++u) t8[u] = (8 * c8 + u <= r) ? tp[u] : 0.f;
                 }
+                uint4 q4;
+                q4.x = pack_bf16(t8[0], t8[1]);
+                q4.y = pack_bf16(t8[2], t8[3]);
+                q4.z = pack_bf16(t8[4], t8[5]);
+                q4.w = pack_bf16(t8[6], t8[7]);
+                if (store_t) *reinterpret_cast<uint4*>(rec + PREP_T + r * 128 + ((c8 ^ (r & 7)) << 4)) = q4;
+                if (P.a_out && r < c &&  // token tc + r: its row of T, 64 bf16 columns
+                    in_range(((tc + r) * P.Hv + j) * CH + 8 * c8 + 7, T_all * P.Hv * CH, err))
+                    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.a_out) +
+                                              ((tc + r) * P.Hv + j) * CH + 8 * c8) = q4;
             }
         }
         {
@@ -478,36 +499,22 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         __syncthreads();
         PTRACE(5);
         fence_after_sync();
-        if (want_t) {
-#pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4) {
-                const int it = tid + PT * u4, r = it & 63, c8 = it >> 6;
-                uint4 q4;
-                q4.x = pack_bf16(tkeep[8 * u4 + 0], tkeep[8 * u4 + 1]);
-                q4.y = pack_bf16(tkeep[8 * u4 + 2], tkeep[8 * u4 + 3]);
-                q4.z = pack_bf16(tkeep[8 * u4 + 4], tkeep[8 * u4 + 5]);
-                q4.w = pack_bf16(tkeep[8 * u4 + 6], tkeep[8 * u4 + 7]);
-                if (store_t) *reinterpret_cast<uint4*>(smem + S::oT + r * 128 + ((c8 ^ (r & 7)) << 4)) = q4;
-                if (P.a_out && r < c &&  // token tc + r: its row of T, 64 bf16 columns
-                    in_range(((tc + r) * P.Hv + j) * CH + 8 * c8 + 7, T_all * P.Hv * CH, err))
-                    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.a_out) +
-                                              ((tc + r) * P.Hv + j) * CH + 8 * c8) = q4;
-            }
-        }
         {
-            // thread = key row dk; W' row i, column dk goes to its K-major staging block
-            // (columns 0-63 over the TU staging, 64-127 over the consumed TW tile)
-            const int dk = tid;
+            // thread = key row dk, warp w its half w / 4 of the 64 tokens; W' row i, column dk
+            // goes to its K-major staging block (columns 0-63 over the TU staging, 64-127 over
+            // the consumed TW tile)
+            const int dk = tid & 127;
             const uint32_t base = smem_addr(smem + ((dk >> 6) ? S::oQ1 : S::oQ0)) + (dk & 7) * 2;
             const int cch = (dk & 63) >> 3;
 #pragma unroll 1
-            for (int h2 = 0; h2 < 2; ++h2) {
-                float d[32];
-                tmem_ld32(tm + (uint32_t(32 * w) << 16) + 64 + 32 * h2, d);
+            for (int q16 = 0; q16 < 2; ++q16) {
+                const int i0 = 32 * (w >> 2) + 16 * q16;
+                float d[16];
+                tmem_ld16(tm + (uint32_t(32 * (w & 3)) << 16) + 64 + i0, d);
                 tmem_ld_wait();
 #pragma unroll
-                for (int ii = 0; ii < 32; ++ii) {
-                    const int i = 32 * h2 + ii;
+                for (int ii = 0; ii < 16; ++ii) {
+                    const int i = i0 + ii;
                     sts16(base + i * 128 + ((cch ^ (i & 7)) << 4), __bfloat16_as_ushort(__float2bfloat16_rn(d[ii])));
                 }
             }
@@ -518,7 +525,6 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         if (tid == 0) {
             bulk_store(rec + PREP_W, smem + S::oQ0, 8192);
             bulk_store(rec + PREP_W + 8192, smem + S::oQ1, 8192);
-            if (store_t) bulk_store(rec + PREP_T, smem + S::oT, 8192);
             bulk_commit();
             PTRACE(6);
             bulk_wait_read0();  // the next head (or the CTA's exit) may reuse the staging tiles
