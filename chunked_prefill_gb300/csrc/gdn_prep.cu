@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     float* sE = reinterpret_cast<float*>(smem + S::oE);
     float* sEi = reinterpret_cast<float*>(smem + S::oEi);
     float* sBeta = reinterpret_cast<float*>(smem + S::oBeta);
-    float* sBe = reinterpret_cast<float*>(smem + S::oBe);
+    float* sNbe = reinterpret_cast<float*>(smem + S::oBe);  // -beta e
     int* sFlag = reinterpret_cast<int*>(smem + S::oFlag);
     float* sPart = reinterpret_cast<float*>(smem + S::oFlag + 8);  // two partial sums
     float* sGin = reinterpret_cast<float*>(smem + S::oGin);
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                 sE[r] = e;
                 sEi[r] = expf(-gm[u]);
                 sBeta[r] = bv[u];
-                sBe[r] = bv[u] * e;
+                sNbe[r] = -(bv[u] * e);
                 if (P.gam_out && r < c && in_range((tc + r) * P.Hv + j, T_all * P.Hv, err))
                     P.gam_out[(tc + r) * P.Hv + j] = gm[u];
             }
@@ -242,6 +242,10 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
 #pragma unroll
                     for (int u = 0; u < 16; ++u) kn = (u == (i & 15)) ? raw[u] : kn;
                 }
+                // with rc the row's factor (beta_i e_i for A, e_i for P), element j is
+                // rc e^{-gamma_j} raw_j: two packed products per pair of columns; at extreme
+                // decay (pw) e^{gamma_i - gamma_j} is formed directly instead
+                const uint64_t rc2 = dup2(qrows ? ei : bi * ei);
                 if (!qrows) {
                     const int I = i >> 4, r = i & 15, M = c0 >> 4;
                     if (M <= I) {  // blocks above the diagonal are not stored
@@ -249,14 +253,17 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                         for (int j4 = 0; j4 < 4; ++j4) {
                             const int jb = c0 + 4 * j4;
                             float x[4];
-                            const float4 ev = *reinterpret_cast<const float4*>(sEi + jb);
-                            const float evs[4] = {ev.x, ev.y, ev.z, ev.w};
+                            if (pw) {
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int jj = jb + u;
-                                const float d = pw ? expf(gi - sGam[jj]) : ei * evs[u];
-                                x[u] = jj < i ? bi * d * raw[4 * j4 + u] : 0.f;
+                                for (int u = 0; u < 4; ++u)
+                                    x[u] = bi * expf(gi - sGam[jb + u]) * raw[4 * j4 + u];
+                            } else {
+                                const ulonglong2 ev = *reinterpret_cast<const ulonglong2*>(sEi + jb);
+                                unpk2(fmul2(fmul2(rc2, ev.x), pk2(raw[4 * j4], raw[4 * j4 + 1])), x[0], x[1]);
+                                unpk2(fmul2(fmul2(rc2, ev.y), pk2(raw[4 * j4 + 2], raw[4 * j4 + 3])), x[2], x[3]);
                             }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) x[u] = jb + u < i ? x[u] : 0.f;
                             *reinterpret_cast<float4*>(ablk(tri(I, M)) + r * BLD + (jb & 15)) =
                                 make_float4(x[0], x[1], x[2], x[3]);
                         }
@@ -266,15 +273,20 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                     for (int c4 = 0; c4 < 2; ++c4) {
                         const int c8 = (c0 >> 3) + c4;
                         float x[8];
-                        const float4 e0 = *reinterpret_cast<const float4*>(sEi + 8 * c8);
-                        const float4 e1 = *reinterpret_cast<const float4*>(sEi + 8 * c8 + 4);
-                        const float evs[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+                        if (pw) {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int jj = 8 * c8 + u;
-                            const float d = pw ? expf(gi - sGam[jj]) : ei * evs[u];
-                            x[u] = (jj <= i && i < c) ? d * raw[8 * c4 + u] : 0.f;
+                            for (int u = 0; u < 8; ++u) x[u] = expf(gi - sGam[8 * c8 + u]) * raw[8 * c4 + u];
+                        } else {
+                            const ulonglong2 e0 = *reinterpret_cast<const ulonglong2*>(sEi + 8 * c8);
+                            const ulonglong2 e1 = *reinterpret_cast<const ulonglong2*>(sEi + 8 * c8 + 4);
+                            const uint64_t evs[4] = {e0.x, e0.y, e1.x, e1.y};
+#pragma unroll
+                            for (int u2 = 0; u2 < 4; ++u2)
+                                unpk2(fmul2(fmul2(rc2, evs[u2]), pk2(raw[8 * c4 + 2 * u2], raw[8 * c4 + 2 * u2 + 1])),
+                                      x[2 * u2], x[2 * u2 + 1]);
                         }
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) x[u] = (8 * c8 + u <= i && i < c) ? x[u] : 0.f;
                         uint4 q4;
                         q4.x = pack_bf16(x[0], x[1]);
                         q4.y = pack_bf16(x[2], x[3]);
@@ -417,26 +429,28 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         // all banks), 8-column chunk c8 = it / 64 (warp-uniform: broadcast gate loads)
         for (int it = tid; it < CH * 8; it += PT) {
             const int r = it & 63, c8 = it >> 6;
-            float4 t0v = make_float4(0.f, 0.f, 0.f, 0.f), t1v = t0v;
+            // T is exactly zero above its diagonal (the substitution writes those zeros and the
+            // blocks above it are not read), so the products need no mask: two packed products
+            // per pair of columns
+            ulonglong2 t0 = make_ulonglong2(0ull, 0ull), t1 = t0;
             if ((c8 >> 1) <= (r >> 4)) {
                 const float* tp = tblk(tri(r >> 4, c8 >> 1)) + (r & 15) * BLD + (c8 & 1) * 8;
-                t0v = *reinterpret_cast<const float4*>(tp);
-                t1v = *reinterpret_cast<const float4*>(tp + 4);
+                t0 = *reinterpret_cast<const ulonglong2*>(tp);
+                t1 = *reinterpret_cast<const ulonglong2*>(tp + 4);
             }
-            const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
-            const float4 b0 = *reinterpret_cast<const float4*>(sBeta + 8 * c8);
-            const float4 b1 = *reinterpret_cast<const float4*>(sBeta + 8 * c8 + 4);
-            const float4 be0 = *reinterpret_cast<const float4*>(sBe + 8 * c8);
-            const float4 be1 = *reinterpret_cast<const float4*>(sBe + 8 * c8 + 4);
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-            const float bev[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
+            const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(sBeta + 8 * c8);
+            const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(sBeta + 8 * c8 + 4);
+            const ulonglong2 n0 = *reinterpret_cast<const ulonglong2*>(sNbe + 8 * c8);
+            const ulonglong2 n1 = *reinterpret_cast<const ulonglong2*>(sNbe + 8 * c8 + 4);
             float xu[8], xw[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int cc = 8 * c8 + u;
-                xu[u] = cc <= r ? tv[u] * bv[u] : 0.f;
-                xw[u] = cc <= r ? -tv[u] * bev[u] : 0.f;
-            }
+            unpk2(fmul2(t0.x, b0.x), xu[0], xu[1]);
+            unpk2(fmul2(t0.y, b0.y), xu[2], xu[3]);
+            unpk2(fmul2(t1.x, b1.x), xu[4], xu[5]);
+            unpk2(fmul2(t1.y, b1.y), xu[6], xu[7]);
+            unpk2(fmul2(t0.x, n0.x), xw[0], xw[1]);
+            unpk2(fmul2(t0.y, n0.y), xw[2], xw[3]);
+            unpk2(fmul2(t1.x, n1.x), xw[4], xw[5]);
+            unpk2(fmul2(t1.y, n1.y), xw[6], xw[7]);
             uint4 a, b;
             a.x = pack_bf16(xu[0], xu[1]);
             a.y = pack_bf16(xu[2], xu[3]);
