@@ -293,6 +293,14 @@ void fill_problem(const gdn_problem* p, const HostPlan& h, char* ws, gdn::Proble
     P.plan.seg = reinterpret_cast<int2*>(ws + h.off_seg);
     P.plan.seg_off = reinterpret_cast<int*>(ws + h.off_segoff);
     P.plan.chunk_off = reinterpret_cast<int*>(ws + h.off_chunkoff);
+    if (!p->cu_seqlens) {  // equal lengths: the decomposition in closed form
+        const int nt = (p->T + h.C - 1) / h.C;
+        P.plan.uni_nt = nt;
+        P.plan.uni_ns = std::max(1, (nt + h.L - 1) / h.L);
+        P.plan.uni_n = h.N;
+    } else {
+        P.plan.uni_nt = P.plan.uni_ns = P.plan.uni_n = 0;
+    }
     P.hin = h.cp != gdn::CP_NONE ? reinterpret_cast<float*>(ws + h.off_hin) : nullptr;
     P.mbuf = h.cp == gdn::CP_EXACT ? reinterpret_cast<float*>(ws + h.off_mbuf) : nullptr;
     P.mbuf_t = (h.cp == gdn::CP_EXACT && h.prep_stride == gdn::PREP_BWD_BYTES && p->dtype == GDN_BF16)

@@ -371,17 +371,17 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_phase_a(BwdProblem B) {
     extern __shared__ __align__(128) char smem[];
     const Problem& P = B.f;
     const int gseg = blockIdx.x, j = blockIdx.y;
-    const int2 sj = P.plan.seg[gseg];
+    const int2 sj = plan_seg(P.plan, gseg);
     const int s = sj.x, lj = sj.y;
     if (s < 0 || s >= P.N || lj == 0) return;
-    const int nseg = P.plan.seg_off[s + 1] - P.plan.seg_off[s];
+    const int nseg = plan_seg_off(P.plan, s + 1) - plan_seg_off(P.plan, s);
     int64_t t0, t1;
     seq_range(P, s, t0, t1);
     const int nt = int((t1 - t0 + C - 1) / C);
     const int cb = lj * P.L, ce = min(cb + P.L, nt);
     const float* x0 = (lj == nseg - 1 && B.dht) ? B.dht + (int64_t(s) * P.Hv + j) * KVN : nullptr;
     bwd_scan<Op, C, false>(B, smem, j, t0, t1, cb, ce, x0, B.dhb + (int64_t(gseg) * P.Hv + j) * KVN,
-                           P.plan.chunk_off[s]);
+                           plan_chunk_off(P.plan, s));
 }
 
 // Phase C: every segment from its true right-end gradient, storing dh for every chunk; the
@@ -391,10 +391,10 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_phase_c(BwdProblem B) {
     extern __shared__ __align__(128) char smem[];
     const Problem& P = B.f;
     const int gseg = blockIdx.x, j = blockIdx.y;
-    const int2 sj = P.plan.seg[gseg];
+    const int2 sj = plan_seg(P.plan, gseg);
     const int s = sj.x, lj = sj.y;
     if (s < 0 || s >= P.N) return;
-    const int nseg = P.plan.seg_off[s + 1] - P.plan.seg_off[s];
+    const int nseg = plan_seg_off(P.plan, s + 1) - plan_seg_off(P.plan, s);
     int64_t t0, t1;
     seq_range(P, s, t0, t1);
     const int nt = int((t1 - t0 + C - 1) / C);
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(NT, 1) k_bwd_phase_c(BwdProblem B) {
     const float* x0 = (lj == nseg - 1) ? (B.dht ? B.dht + (int64_t(s) * P.Hv + j) * KVN : nullptr)
                                        : B.dhb + (int64_t(gseg + 1) * P.Hv + j) * KVN;
     float* x_out = (lj == 0 && B.dh0) ? B.dh0 + (int64_t(s) * P.Hv + j) * KVN : nullptr;
-    bwd_scan<Op, C, true>(B, smem, j, t0, t1, cb, ce, x0, x_out, P.plan.chunk_off[s]);
+    bwd_scan<Op, C, true>(B, smem, j, t0, t1, cb, ce, x0, x_out, plan_chunk_off(P.plan, s));
 }
 
 // Reverse fix-up: dhb[g0+lj] = M_lj^T dhb[g0+lj+1] + dhb[g0+lj] for lj = nseg-2 .. 1.  The
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(256) k_bwd_fixup(BwdProblem B) {
     float* xs = fsm + KD * 129;      // 128 x 8
     const Problem& P = B.f;
     const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * 8;
-    const int g0 = P.plan.seg_off[s], nseg = P.plan.seg_off[s + 1] - g0;
+    const int g0 = plan_seg_off(P.plan, s), nseg = plan_seg_off(P.plan, s + 1) - g0;
     if (nseg <= 2) return;
     const int row = threadIdx.x & 127, c0 = (threadIdx.x >> 7) * 4;
     {
@@ -502,15 +502,15 @@ __global__ void __launch_bounds__(NTL, 1) k_bwd_local(BwdProblem B, int64_t item
         x.gch = int(item / P.Hv);
         x.j = int(item % P.Hv);
         x.qh = x.j / (P.Hv / P.Hqk);
-        if (x.gch >= P.plan.chunk_off[P.N]) return false;
+        if (x.gch >= plan_chunk_off(P.plan, P.N)) return false;
         int lo = 0, hi = P.N - 1;  // chunk -> (sequence, local chunk) by binary search
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (P.plan.chunk_off[mid] <= x.gch) lo = mid;
+            if (plan_chunk_off(P.plan, mid) <= x.gch) lo = mid;
             else hi = mid - 1;
         }
         x.s = lo;
-        x.ch = x.gch - P.plan.chunk_off[x.s];
+        x.ch = x.gch - plan_chunk_off(P.plan, x.s);
         seq_range(P, x.s, x.t0, x.t1);
         x.tc = x.t0 + int64_t(x.ch) * C;
         if (x.tc >= x.t1) return false;

@@ -290,16 +290,16 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         x.gch = gch;
         x.j = int(item % Hv);
         x.qh = x.j / G;
-        if (gch >= P.plan.chunk_off[P.N]) return false;
+        if (gch >= plan_chunk_off(P.plan, P.N)) return false;
         int lo = 0, hi = P.N - 1;  // chunk -> sequence by binary search
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (P.plan.chunk_off[mid] <= gch) lo = mid;
+            if (plan_chunk_off(P.plan, mid) <= gch) lo = mid;
             else hi = mid - 1;
         }
         int64_t t0, t1;
         seq_bounds(P, lo, t0, t1);
-        x.tc = t0 + int64_t(gch - P.plan.chunk_off[lo]) * LCH;
+        x.tc = t0 + int64_t(gch - plan_chunk_off(P.plan, lo)) * LCH;
         if (x.tc >= t1) return false;
         x.c = int((t1 - x.tc) < int64_t(LCH) ? (t1 - x.tc) : int64_t(LCH));
         return true;

@@ -399,10 +399,10 @@ template <typename Op, int C>
 __global__ void __launch_bounds__(NTHREADS, 1) k_phase_a(Problem P) {
     extern __shared__ __align__(128) char smem[];
     const int gseg = blockIdx.x, j = blockIdx.y;
-    const int2 sj = P.plan.seg[gseg];
+    const int2 sj = plan_seg(P.plan, gseg);
     const int s = sj.x, lj = sj.y;
     if (s < 0 || s >= P.N) return;
-    const int nseg = P.plan.seg_off[s + 1] - P.plan.seg_off[s];
+    const int nseg = plan_seg_off(P.plan, s + 1) - plan_seg_off(P.plan, s);
     int64_t t0, t1;
     seq_bounds(P, s, t0, t1);
     const int nt = int((t1 - t0 + C - 1) / C);
@@ -432,10 +432,10 @@ template <typename Op, int C, int KIND>
 __global__ void __launch_bounds__(NTHREADS, 1) k_phase_c(Problem P) {
     extern __shared__ __align__(128) char smem[];
     const int gseg = blockIdx.x, j = blockIdx.y;
-    const int2 sj = P.plan.seg[gseg];
+    const int2 sj = plan_seg(P.plan, gseg);
     const int s = sj.x, lj = sj.y;
     if (s < 0 || s >= P.N) return;
-    const int nseg = P.plan.seg_off[s + 1] - P.plan.seg_off[s];
+    const int nseg = plan_seg_off(P.plan, s + 1) - plan_seg_off(P.plan, s);
     int64_t t0, t1;
     seq_bounds(P, s, t0, t1);
     const int nt = int((t1 - t0 + C - 1) / C);
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_phase_c(Problem P) {
     const float* x0 = (lj == 0) ? (P.h0 ? P.h0 + (int64_t(s) * P.Hv + j) * KV : nullptr)
                                 : P.hin + (int64_t(gseg) * P.Hv + j) * KV;
     float* x_out = (lj == nseg - 1 && P.ht) ? P.ht + (int64_t(s) * P.Hv + j) * KV : nullptr;
-    const int64_t hb = P.plan.chunk_off[s];
+    const int64_t hb = plan_chunk_off(P.plan, s);
     scan_chunks<Op, C, KIND>(P, smem, s, j, t0, t1, cb, ce, x0, x_out, hb);
 }
 
@@ -485,7 +485,7 @@ constexpr int fix_smem(int CG) { return FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 +
 // flag; a step whose segment has dec >= 0 has a negligible transition, so its result is S
 // itself (already in xbuf) and the step neither loads its transition nor computes.
 template <bool REV, int CG>
-__global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float* mats, float* xbuf,
+__global__ void __launch_bounds__(FIX_T) k_fixup(const PlanDev plan, const float* mats, float* xbuf,
                                                  int Hv, int* err, const int* dec) {
     constexpr int W = 8 * CG, KS = 8 / CG, MS = KD / KS;
     tc::pdl_launch_dependents();
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(FIX_T) k_fixup(const int* seg_off, const float
     float* xs = reinterpret_cast<float*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4);  // 128 x W
     uint64_t* bar = reinterpret_cast<uint64_t*>(fsm + FIX_NB * KD * KD * 4 + 8 * 32 * 32 * 4 + KD * W * 4);
     const int s = blockIdx.x, j = blockIdx.y, cb = blockIdx.z * W;
-    const int g0 = seg_off[s], nseg = seg_off[s + 1] - g0;
+    const int g0 = plan_seg_off(plan, s), nseg = plan_seg_off(plan, s + 1) - g0;
     if (nseg <= 2) return;
     const int last = nseg - 2;  // steps 1..last
     const int t = threadIdx.x, rg = t & 31, ks = (t >> 5) / CG, cg = (t >> 5) % CG;
@@ -632,14 +632,14 @@ int fixup_groups(int chains) {
 }
 
 template <bool REV>
-static void launch_fixup_cg(int N, int Hv, const int* seg_off, const float* mats, float* xbuf,
+static void launch_fixup_cg(int N, int Hv, const PlanDev& plan, const float* mats, float* xbuf,
                             int* err, bool pdl, cudaStream_t st, const int* dec) {
     auto run = [&](auto kern, int cg) {
         const int smem = fix_smem(cg);
         smem_attr(kern, smem);
         const dim3 grid(N, Hv, VD / (8 * cg));
-        if (pdl) launch_pdl(kern, grid, dim3(FIX_T), smem, st, seg_off, mats, xbuf, Hv, err, dec);
-        else kern<<<grid, FIX_T, smem, st>>>(seg_off, mats, xbuf, Hv, err, dec);
+        if (pdl) launch_pdl(kern, grid, dim3(FIX_T), smem, st, plan, mats, xbuf, Hv, err, dec);
+        else kern<<<grid, FIX_T, smem, st>>>(plan, mats, xbuf, Hv, err, dec);
     };
     switch (fixup_groups(N * Hv)) {
         case 1: run(k_fixup<REV, 1>, 1); break;
@@ -698,13 +698,13 @@ void launch_plan(const Problem& P, int C, cudaStream_t st) {
 
 void launch_fixup(const Problem& P, cudaStream_t st) {
     timing_begin("fwd_fixup", st);
-    launch_fixup_cg<false>(P.N, P.Hv, P.plan.seg_off, P.mbuf, P.hin, P.err, true, st, P.dec);
+    launch_fixup_cg<false>(P.N, P.Hv, P.plan, P.mbuf, P.hin, P.err, true, st, P.dec);
     timing_end(st);
 }
 
 void launch_bwd_fixup_tc(const BwdProblem& B, cudaStream_t st) {
     const Problem& P = B.f;
-    launch_fixup_cg<true>(P.N, P.Hv, P.plan.seg_off, P.mbuf_t, B.dhb, P.err, false, st, P.dec);
+    launch_fixup_cg<true>(P.N, P.Hv, P.plan, P.mbuf_t, B.dhb, P.err, false, st, P.dec);
 }
 
 template <typename Op, int C>

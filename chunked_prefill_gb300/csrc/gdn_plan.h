@@ -15,11 +15,32 @@ enum CpKind { CP_NONE = 0, CP_EXACT = 1, CP_WARMUP = 2 };
 // fp32 number) contributes less than 2^-126 ||h|| to any state it maps h into: it is dropped.
 constexpr float LOG_NEGLIGIBLE = -87.33654475f;
 
+// Work decomposition: the segments of the sequences and the first chunk of each sequence.  A
+// batch of equal-length sequences (no cu_seqlens) has it in closed form (uni_ns > 0: every
+// sequence has uni_ns segments and uni_nt chunks) and no kernel writes or reads the arrays;
+// packed sequences read the arrays the planner kernel writes from the device cu_seqlens.
 struct PlanDev {
     int2* seg;          // [total_segs] (sequence, local segment index)
     int* seg_off;       // [N+1]
     int* chunk_off;     // [N+1]
+    int uni_ns;         // > 0: segments per sequence of an equal-length batch
+    int uni_nt;         //      chunks per sequence
+    int uni_n;          //      sequences
 };
+// (sequence, local segment) of global segment g, or (-1, -1) past the last
+__device__ __forceinline__ int2 plan_seg(const PlanDev& p, int g) {
+    if (p.uni_ns > 0)
+        return g < p.uni_n * p.uni_ns ? make_int2(g / p.uni_ns, g % p.uni_ns) : make_int2(-1, -1);
+    return p.seg[g];
+}
+// first global segment of sequence s (s = N: the number of segments)
+__device__ __forceinline__ int plan_seg_off(const PlanDev& p, int s) {
+    return p.uni_ns > 0 ? s * p.uni_ns : p.seg_off[s];
+}
+// first global chunk of sequence s (s = N: the number of chunks)
+__device__ __forceinline__ int plan_chunk_off(const PlanDev& p, int s) {
+    return p.uni_ns > 0 ? s * p.uni_nt : p.chunk_off[s];
+}
 
 struct Problem {
     // tensors

@@ -106,8 +106,13 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
 
     pdl_launch_dependents();
     pdl_wait();
+#ifndef GDN_CHECK
+    // no planner kernel ran before this one (equal-length batch): the call's error word starts
+    // clear here (a kernel of this call reports into it only after a bounded wait of seconds)
+    if (P.plan.uni_ns > 0 && P.err && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *P.err = 0;
+#endif
     const int gch = blockIdx.x;
-    if (gch >= P.plan.chunk_off[P.N]) return;
+    if (gch >= plan_chunk_off(P.plan, P.N)) return;
     const int G = P.Hv / P.Hqk;
     const int hpc = P.prep_heads;                         // v-heads per CTA (<= GMAX)
     const int nsl = (G + hpc - 1) / hpc;                  // slices of a q/k group
@@ -116,11 +121,11 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
     int lo = 0, hi = P.N - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (P.plan.chunk_off[mid] <= gch) lo = mid;
+        if (plan_chunk_off(P.plan, mid) <= gch) lo = mid;
         else hi = mid - 1;
     }
     const int s = lo;
-    const int ch = gch - P.plan.chunk_off[s];
+    const int ch = gch - plan_chunk_off(P.plan, s);
     int64_t t0, t1;
     if (P.cu) {
         t0 = P.cu[s];
