@@ -16,9 +16,9 @@
 //       D4b = V'^T P^T   = (P V')^T      (v x i)       -> O = scale (e * D4a + D4b)
 //       Xt  = e^{gamma_C} Xt + (diag(kd) V')^T K       (v x dk)
 //
-// Warp roles (16 warps): 0 TMA producer; 1 state-chain MMA issuer (V' with D4a, state update;
-// U too without an output side); 2 gates (cumsum of g and its exponentials); 3 output MMA
-// issuer (U, D4b); 4-11 state warps, one warpgroup per half of the key columns (state
+// Warp roles (16 warps): 0 TMA producer; 1 state-chain MMA issuer (V' with D4a, state
+// update); 2 gates (cumsum of g and its exponentials); 3 output MMA issuer (U, D4b), or U alone
+// without an output side; 4-11 state warps, one warpgroup per half of the key columns (state
 // hand-off, V' conversion); 12-15 output warps.  The two issuers run independently: the state
 // chain never queues behind the output products.  Every wait on an mbarrier is bounded; on a
 // timeout the kernel records an error word and winds down.
@@ -283,7 +283,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         mbar_init(&bars[B_MMA5], 1);
         mbar_init(&bars[B_MMA4_0], 1);
         mbar_init(&bars[B_MMA4_1], 1);
-        mbar_init(&bars[B_DRAIN], OUT ? 2 : 1);
+        mbar_init(&bars[B_DRAIN], NEEDU ? 2 : 1);  // the state-chain issuer and warp 3
         mbar_init(&bars[B_EX], 8);
         mbar_init(&bars[B_EV0], 8);
         mbar_init(&bars[B_EV1], 8);
@@ -357,40 +357,22 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         __syncwarp();
     } else if (w == 1) {
         // ------------------------------------------------------------ state-chain MMA issuer
-        // per chunk k: [V'|Q h], then the state update.  With an output side (OUT) its MMA
-        // issuer forms U of each chunk, else U of k+1 follows here.  Lane 0 alone runs the
-        // loop: issued from warp-uniform code (elect.sync) the MMAs leave the tensor pipe
-        // sooner, but the whole scan runs slower (the state warps that share this warp's SMSP
-        // lose issue slots).
+        // per chunk k: [V'|Q h] (V' alone without an output side), then the state update; U
+        // of each chunk comes from warp 3.  Lane 0 alone runs the loop: issued from
+        // warp-uniform code (elect.sync) the MMAs leave the tensor pipe sooner, but the whole
+        // scan runs slower (the state warps that share this warp's SMSP lose issue slots).
         if (lane == 0) {
-            constexpr uint32_t IDU = make_idesc(128, 64, 1, 0);
             constexpr uint32_t IDV = make_idesc(128, OUT ? 128 : 64, 0, 0);
             constexpr uint32_t ID5 = make_idesc(128, 128, 0, 1);
             const uint32_t k0a = smem_addr(sm + S_K), wq0 = smem_addr(sm + S_WQ);
-            const uint32_t v0a = smem_addr(sm + S_V), tu0 = smem_addr(sm + S_TU);
-            // U^T = V^T TU^T for chunk k into the V' half of its DD buffer
-            auto issue_u = [&](int k) {
-                const int st = k & 1;
-                const uint64_t dV = mdesc(v0a + st * S_V_STRIDE, 8192), dTU = kdesc(tu0 + st * S_TU_STRIDE);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tm + t_dd(k), dV + (s * 2048 >> 4), dTU + (s * 32 >> 4), IDU, s > 0);
-            };
             bool ok = true;
-            if (NEEDU && !OUT) {
-                ok = wait_bar(bars, B_FULL0, 0, errflag);
-                if (ok) {
-                    fence_after_sync();
-                    issue_u(0);
-                }
-            }
             for (int k = 0; ok && k < n; ++k) {
                 const int st = k & 1;
                 const uint32_t dd = tm + t_dd(k);
                 const uint64_t dWQ = kdesc(wq0 + st * S_WQ_STRIDE), dK = mdesc(k0a + st * S_K_STRIDE, 8192);
                 TRACE(k, 0);
                 if ((!NEEDU && !wait_bar(bars, B_FULL0 + st, (k >> 1) & 1, errflag)) ||
-                    (OUT && !wait_bar(bars, B_U0 + st, (k >> 1) & 1, errflag)) ||
+                    (NEEDU && !wait_bar(bars, B_U0 + st, (k >> 1) & 1, errflag)) ||
                     !wait_bar(bars, B_EX, k & 1, errflag)) {
                     ok = false;
                     break;
@@ -417,17 +399,9 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 for (int s = 0; s < 4; ++s)
                     mma_bf16_ta(tm + T_XF, dd + (OUT ? kd_col(s) : p_col(s)), dK + (s * 2048 >> 4), ID5, 1u);
                 commit(&bars[B_MMA5]);
-                if (OUT) commit(&bars[B_M5C0 + (k & 1)]);
+                if (NEEDU) commit(&bars[B_M5C0 + (k & 1)]);
                 commit(&bars[B_EMPTY0 + st]);  // last reader of this stage on this issuer
                 TRACE(k, 5);
-                if (NEEDU && !OUT && k + 1 < n) {
-                    if (!wait_bar(bars, B_FULL0 + ((k + 1) & 1), ((k + 1) >> 1) & 1, errflag)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_after_sync();
-                    issue_u(k + 1);
-                }
                 TRACE(k, 7);
             }
             // drain: every MMA issued here has completed before TMEM may be released
@@ -564,6 +538,27 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
                 }
             }
             for (int q = used; q < issued; ++q) mbar_wait(&bars[B_FULLP0 + q % NP], (q / NP) & 1);
+            commit(&bars[B_DRAIN]);
+        }
+        __syncwarp();
+    } else if (w == 3 && NEEDU) {
+        // ------------------------------------------------------------ U issuer (no output side)
+        // U of chunk k+1 once the state update of chunk k-1, the last reader of its buffer, has
+        // completed (and its tiles have landed), so the state chain never waits on it
+        if (lane == 0) {
+            constexpr uint32_t IDU = make_idesc(128, 64, 1, 0);
+            const uint32_t v0a = smem_addr(sm + S_V), tu0 = smem_addr(sm + S_TU);
+            for (int q = 0; q < n; ++q) {
+                const int st = q & 1;
+                if (q >= 2 && !wait_bar(bars, B_M5C0 + st, ((q - 2) >> 1) & 1, errflag)) break;
+                if (!wait_bar(bars, B_FULL0 + st, (q >> 1) & 1, errflag)) break;
+                fence_after_sync();
+                const uint64_t dV = mdesc(v0a + st * S_V_STRIDE, 8192), dTU = kdesc(tu0 + st * S_TU_STRIDE);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tm + t_dd(q), dV + (s * 2048 >> 4), dTU + (s * 32 >> 4), IDU, s > 0);
+                commit(&bars[B_U0 + st]);
+            }
             commit(&bars[B_DRAIN]);
         }
         __syncwarp();
