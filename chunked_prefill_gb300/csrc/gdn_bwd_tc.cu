@@ -229,7 +229,15 @@ __device__ __forceinline__ bool twait(uint64_t* bars, int b, uint32_t par, int* 
 
 struct LocMaps {
     CUtensorMap k, q, v, dO, h, dh;
+    CUtensorMap dv, dq, dk;  // outputs (dq, dk: bf16 ones only, G = 1)
 };
+
+// byte offset of element (row t, column col) of a [64][128] bf16 tile in the 128-byte-swizzled
+// image a TMA box of 64 columns uses (two 8 KB column blocks)
+__device__ __forceinline__ uint32_t out_tile_off(int t, int col) {
+    return uint32_t(col >> 6) * 8192u + uint32_t(t) * 128u + (uint32_t(((col & 63) >> 3) ^ (t & 7)) << 4) +
+           uint32_t(col & 7) * 2u;
+}
 
 __device__ __forceinline__ void seq_bounds(const Problem& P, int s, int64_t& t0, int64_t& t1) {
     if (P.cu) {
@@ -414,6 +422,11 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         const uint32_t aK = base + kreg, aQ = base + qreg;
         const int j = cur.j, qh = cur.qh, c = cur.c;
         const int64_t tc = cur.tc;
+        // a full chunk's dv (and with G = 1 its dq, dk) leave as tile stores of staged images:
+        // dv and dk through the dB staging region, dq through the dV' region (both free then);
+        // thread 0 issues each store after the barrier that follows its staging and waits for
+        // its reads before the barrier that precedes the region's next writer
+        const bool tile_out = c == LCH;
         bool ok = true;
         bool nA = false, nB = false;  // (issuer) the next item's groups issued during this one
         if (tid == ISS && !pre) {
@@ -522,6 +535,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             tmem_ld_wait();
             st_row16(aW, 32 * q4 + lane, c16, x);
         }
+        if (tid == 0) bulk_wait_read0();  // the previous item's dq and dk stores have read their images
         fence_proxy_async_smem();
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -692,15 +706,24 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             for (int i = 0; i < 16; ++i) x[i] = -x[i];
             st_row16(aDO, 32 * q4 + lane, c16, x);
             const int v = 32 * q4 + lane;
-            __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(B.dv) + int64_t(j) * VD + v + (tc + c16) * v_stride;
             float vc[16];
             ld_col16(aV, c16, v, vc);
+            if (tile_out) {  // staged for the tile store (the dB staging region is free here)
 #pragma unroll
-            for (int ii = 0; ii < 16; ++ii) {
-                const int cx = c16 + ii;
-                if (cx < c && in_range(int64_t(j) * VD + v + (tc + cx) * v_stride, T_all * v_stride, P.err))
-                    dv[ii * v_stride] = __float2bfloat16_rn(sBeta[cx] * y[ii]);
-                y[ii] *= vc[ii];
+                for (int ii = 0; ii < 16; ++ii) {
+                    sts16(aSTG + out_tile_off(c16 + ii, v),
+                          __bfloat16_as_ushort(__float2bfloat16_rn(sBeta[c16 + ii] * y[ii])));
+                    y[ii] *= vc[ii];
+                }
+            } else {
+                __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(B.dv) + int64_t(j) * VD + v + (tc + c16) * v_stride;
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii) {
+                    const int cx = c16 + ii;
+                    if (cx < c && in_range(int64_t(j) * VD + v + (tc + cx) * v_stride, T_all * v_stride, P.err))
+                        dv[ii * v_stride] = __float2bfloat16_rn(sBeta[cx] * y[ii]);
+                    y[ii] *= vc[ii];
+                }
             }
             const float cs = lane_colsum16(y);
             if (!(lane & 1)) sF[F_PTU + 64 * q4 + c16 + (lane >> 1)] = cs;
@@ -709,6 +732,11 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(9);
+        if (tid == 0 && tile_out) {
+            tma_store_3d(&maps.dv, sm + L_STG, 0, j, int(tc));
+            tma_store_3d(&maps.dv, sm + L_STG + 8192, 64, j, int(tc));
+            bulk_commit();
+        }
         if (tid == ISS) {
             ITRACE(8);
             fence_after_sync();
@@ -745,6 +773,12 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                     if (cx < c && in_range(int64_t(j) * KD + k + (tc + cx) * Hv * KD, T_all * Hv * KD, P.err))
                         dq[(tc + cx) * Hv * KD] = sc * sE[cx] * a[ii] + b[ii];
                 }
+            } else if (tile_out) {  // staged in the dV' region (its last products have completed)
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii)
+                    sts16(aDV + out_tile_off(c16 + ii, k),
+                          __bfloat16_as_ushort(__float2bfloat16_rn(sc * sE[c16 + ii] * a[ii] + b[ii])));
+                fence_proxy_async_smem();
             } else {
                 __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(B.dq) + int64_t(qh) * KD + k;
 #pragma unroll
@@ -801,6 +835,11 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(12);
+        if (tid == 0 && tile_out && !B.dqp) {
+            tma_store_3d(&maps.dq, sm + L_DV, 0, qh, int(tc));
+            tma_store_3d(&maps.dq, sm + L_DV + 8192, 64, qh, int(tc));
+            bulk_commit();
+        }
         if (tid == ISS) {
             ITRACE(10);
             fence_after_sync();
@@ -823,6 +862,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             tmem_ld_wait();
             st_row16(aQK, 32 * q4 + lane, c16, x);
         }
+        if (tid == 0) bulk_wait_read0();  // dv's tile store has read the staging region
         fence_proxy_async_smem();
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -990,6 +1030,11 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                     if (cx < c && in_range(int64_t(j) * KD + k + (tc + cx) * Hv * KD, T_all * Hv * KD, P.err))
                         dk[(tc + cx) * Hv * KD] = x[ii];
                 }
+            } else if (tile_out) {  // staged in the dB staging region (the dA step is done with it)
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii)
+                    sts16(aSTG + out_tile_off(c16 + ii, k), __bfloat16_as_ushort(__float2bfloat16_rn(x[ii])));
+                fence_proxy_async_smem();
             } else {
                 __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(B.dk) + int64_t(qh) * KD + k;
 #pragma unroll
@@ -1051,6 +1096,11 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             __syncwarp();
         } else {
             named_sync(3, LT);
+            if (tid == 0 && tile_out && !B.dkp) {
+                tma_store_3d(&maps.dk, sm + L_STG, 0, qh, int(tc));
+                tma_store_3d(&maps.dk, sm + L_STG + 8192, 64, qh, int(tc));
+                bulk_commit();
+            }
         }
         carry_ok = ok;
         TTRACE(18);
@@ -1060,6 +1110,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         ++n;
     }
 
+    if (tid == 0) bulk_wait0();  // the last tile stores have completed
     if (!failed && __syncthreads_or(!carry_ok)) failed = true;
     if (failed && tid == ISS) {
         // let the copies in flight land and the products drain before the CTA leaves
@@ -1097,7 +1148,9 @@ cudaError_t launch_bwd_local_tc(const BwdProblem& B, int64_t T_total, cudaStream
     if (rows > int64_t(0x7fffffff) - KD) return cudaErrorNotSupported;
     if (!make_map(&maps.k, P.k, P.Hqk, T_total) || !make_map(&maps.q, P.q, P.Hqk, T_total) ||
         !make_map(&maps.v, P.v, P.Hv, T_total) || !make_map(&maps.dO, B.dO, P.Hv, T_total) ||
-        !make_rows_map(&maps.h, P.hist, rows) || !make_rows_map(&maps.dh, B.dhist, rows))
+        !make_rows_map(&maps.h, P.hist, rows) || !make_rows_map(&maps.dh, B.dhist, rows) ||
+        !make_map(&maps.dv, B.dv, P.Hv, T_total) || (!B.dqp && !make_map(&maps.dq, B.dq, P.Hqk, T_total)) ||
+        (!B.dkp && !make_map(&maps.dk, B.dk, P.Hqk, T_total)))
         return cudaErrorInvalidValue;
     cudaError_t e = smem_attr(k_tc_bwd_local, int(LOC_SMEM));
     if (e != cudaSuccess) return e;

@@ -361,6 +361,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
         : "memory");
 }
 
+// Tiled bulk tensor store shared -> global of the box at (c0, c1, c2), in the issuing thread's
+// current bulk group (c0 x the element size a multiple of 16 bytes, no coordinate negative)
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned, size % 16 == 0)
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
