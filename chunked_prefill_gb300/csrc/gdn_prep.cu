@@ -6,9 +6,13 @@
 //     A  = diag(beta) (KK * Dm),  P = QK * D         (D_ij = exp(gamma_i - gamma_j), i >= j)
 //     T  = (I + A)^-1                                (fp32: substitution + TF32 block products)
 //     TU = T diag(beta),  W' = -T diag(beta e) K     (W' = -W of the pages' WY form; tcgen05)
-// K and Q arrive by TMA; W', TU and P leave by bulk copies from shared-memory tiles already in
-// the 128-byte-swizzled layout the scan's tensor-core operands use (T, for the backward, by
-// 16-byte stores of the same image).  Rows past the end of a
+// K and Q arrive by TMA; W' and TU leave by bulk copies from shared-memory tiles already in
+// the 128-byte-swizzled layout the scan's tensor-core operands use, P and T (for the backward)
+// by 16-byte stores of the same image from registers.  (P staged for a bulk copy instead cost
+// the inverse a wait for the copy's reads, and the backward's local-gradient kernel, which
+// reads the records later, ran 4 % slower when the backward's own preparation wrote P that
+// way; TU written by 16-byte stores instead made both the preparation and that kernel slower:
+// measured, cause not found.)  Rows past the end of a
 // sequence hold whatever tokens follow (finite); beta = g = 0 there makes T's rows and the
 // columns of TU and W' for them exactly zero, and P's rows for them are written as zeros (the
 // backward's dO^T P must not see them).
@@ -64,12 +68,12 @@ __device__ __forceinline__ int tri(int I, int M) { return I * (I + 1) / 2 + M; }
 // loaded and [K;Q] K^T formed once, then each v-head's gating, inverse and W' follow in turn.
 // Shared memory (from a 1024-aligned base), small enough for four CTAs per SM.  Once
 // [K;Q] K^T is in TMEM the two Q halves of the operand tile hold A's blocks (six, then four),
-// and after the inverse the TU staging tile and the TW operand tile; P is staged in the T
-// region before the inverse writes there; the whole [K;Q] tile finally stages W'.
+// and after the inverse the TU staging tile and the TW operand tile; the whole [K;Q] tile
+// finally stages W'.
 struct PrepSmem {
     static constexpr uint32_t oKQ = 0;                    // 2 x 16 KB: rows 0-63 K, 64-127 Q
     static constexpr uint32_t oQ0 = 8192, oQ1 = 24576;    // the Q halves
-    static constexpr uint32_t oT = 32768;                 // 10 blocks (12.5 KB), P staging first
+    static constexpr uint32_t oT = 32768;                 // T: 10 blocks (12.5 KB)
     static constexpr uint32_t oTmp = oT + 10 * BLKF * 4;  // 4 x 16 x 20 fp32
     static constexpr uint32_t oGam = oTmp + 4 * 16 * 20 * 4;
     static constexpr uint32_t oE = oGam + CH * 4, oEi = oE + CH * 4, oBeta = oEi + CH * 4,
@@ -79,7 +83,6 @@ struct PrepSmem {
     static constexpr uint32_t oGin = oSlot + 16;          // g, beta of those heads: [GMAX][2][64]
     static constexpr uint32_t bytes = oGin + GMAX * 2 * CH * 4 + 1024;  // + alignment slack
     static_assert(6 * BLKF * 4 <= 8192 && 4 * BLKF * 4 <= 8192, "A blocks fit the Q halves");
-    static_assert(10 * BLKF * 4 >= 8192, "P staging fits the T region");
 };
 
 __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant__ TcMaps maps) {
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
             const bool qrows = wq >= 2;
             const int i = 32 * (wq & 1) + lane;
             const float gi = sGam[i], ei = sE[i], bi = sBeta[i];
-            unsigned char* pt = smem + S::oT;  // P staging (bf16, swizzled rows)
+            unsigned char* pt = rec + PREP_P;  // P's record image (bf16, swizzled rows)
 #pragma unroll 1
             for (int q16 = 0; q16 < 2; ++q16) {  // 16 columns at a time (register budget)
                 const int c0 = 32 * (w >> 2) + 16 * q16;
@@ -301,7 +304,6 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
                     }
                 }
             }
-            if (qrows) fence_proxy_async_smem();
             if (!qrows && P.logb && (w >> 2) == (wq & 1)) {  // warps 0 and 5 hold |k_i|^2
                 // log of a bound on the 2-norm of this chunk's state transition: per token
                 // exp(g) (I - beta k k^T), whose norm is exp(g) max(1, |1 - beta |k|^2|); the
@@ -321,12 +323,6 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         __syncthreads();
         PTRACE(2);
         if (tid == 32 && P.logb) P.logb[int64_t(gch) * P.Hv + j] = sPart[0] + sPart[1];
-        if (tid == 0) {
-            bulk_store(rec + PREP_P, smem + S::oT, 8192);
-            bulk_commit();
-            bulk_wait_read0();  // the T region is free again
-        }
-        __syncthreads();
 
         // T = (I + A)^-1: diagonal blocks by substitution (warp q < 4, lane = column) ...
         if (w < 4 && lane < 16) {
