@@ -53,3 +53,17 @@ def gpu_bwd(inp, **kw):
                             cu_seqlens_host=inp.cu_seqlens, **kw)
     torch.cuda.synchronize()
     return [None if r is None else r.float().cpu().numpy() for r in res]
+
+
+def as_packed(inp):
+    """The same equal-length batch as varlen sequences packed along one row (cu_seqlens at
+    multiples of T): the library then reads the planner kernel's segmentation arrays instead
+    of the closed form it uses for an equal-length batch."""
+    import dataclasses
+    B, T = inp.q.shape[:2]
+    fields = {}
+    for name in ("q", "k", "v", "g", "beta", "dO"):
+        t = getattr(inp, name)
+        fields[name] = None if t is None else t.reshape(1, B * T, *t.shape[2:]).contiguous()
+    fields["cu_seqlens"] = torch.arange(0, B * T + 1, T, dtype=torch.int32)
+    return dataclasses.replace(inp, **fields)

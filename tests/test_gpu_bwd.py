@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from chunked_prefill_gb300.inputs import make_inputs, workload_inputs
-from tests.gpu_util import BF16_TOL, FP32_TOL, gpu_bwd, oracle_bwd, rel_err
+from tests.gpu_util import BF16_TOL, FP32_TOL, as_packed, gpu_bwd, oracle_bwd, rel_err
 
 pytestmark = pytest.mark.gpu
 NAMES = ["dq", "dk", "dv", "dg", "dbeta", "dh0"]
@@ -116,6 +116,25 @@ def test_full_size_training_step_sampled_heads():
     for name, a, r in zip(NAMES, got, ref):
         a = np.take(a, heads, axis=idx[name])
         assert rel_err(a, r) <= BF16_TOL, name
+
+
+@pytest.mark.parametrize("Hqk,Hv", [(2, 2), (2, 4)])
+@pytest.mark.parametrize("cp_kw", [dict(cp_mode=2, cp_segment_chunks=3), {}])
+def test_equal_length_batch_matches_packed(Hqk, Hv, cp_kw):
+    """The training step of an equal-length batch (closed-form segmentation, no planner kernel
+    in its forward recompute) against the same data packed with cu_seqlens (the planner's
+    arrays): bitwise-equal gradients.  With one v-head per q/k head the local-gradient kernel
+    writes full chunks' dq, dk, dv as tile stores and the cut last chunk by scalar stores."""
+    inp = make_inputs(3, 64 * 9 + 17, Hqk, Hv, seed=72 + Hv, h0_std=0.1, backward=True)
+    g1 = gpu_bwd(inp, **cp_kw)
+    g2 = gpu_bwd(as_packed(inp), **cp_kw)
+    for a, b in zip(g1, g2):
+        if a is not None:
+            assert np.array_equal(a.reshape(b.shape), b)
+    ref = oracle_bwd(inp)
+    for got, r in zip(g1, ref):
+        if got is not None and r is not None:
+            assert rel_err(got.reshape(r.shape), r) <= BF16_TOL
 
 
 @pytest.mark.parametrize("Hqk,Hv", [(2, 12), (4, 24), (4, 48)])

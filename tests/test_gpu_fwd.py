@@ -8,7 +8,7 @@ import torch
 
 from chunked_prefill_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 from oracle import chunked
-from tests.gpu_util import BF16_TOL, FP32_TOL, gpu_fwd, oracle_fwd, rel_err
+from tests.gpu_util import BF16_TOL, FP32_TOL, as_packed, gpu_fwd, oracle_fwd, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +46,22 @@ def test_odd_shapes(dtype, tol, B, T, Hqk, Hv, h0):
     inp = make_inputs(B, T, Hqk, Hv, seed=T * 7 + Hv, dtype=dtype, h0_std=0.1 if h0 else 0.0)
     check(inp, tol, cp_mode=1)
     check(inp, tol)  # planner's choice
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("cp_kw", [dict(cp_mode=2, cp_segment_chunks=3), dict(cp_mode=1), {}])
+def test_equal_length_batch_matches_packed(dtype, cp_kw):
+    """An equal-length batch (3 x 593 tokens: 10 chunks, the last cut) takes its segmentation
+    in closed form and launches no planner; packed along one row with cu_seqlens it reads the
+    planner's arrays.  Same kernels, same segments: bitwise-equal results."""
+    inp = make_inputs(3, 64 * 9 + 17, 2, 4, seed=71, dtype=dtype, h0_std=0.1)
+    o1, h1 = gpu_fwd(inp, **cp_kw)
+    o2, h2 = gpu_fwd(as_packed(inp), **cp_kw)
+    assert np.array_equal(o1.reshape(o2.shape), o2)
+    assert np.array_equal(h1, h2)
+    ro, rh = oracle_fwd(inp)
+    tol = BF16_TOL if dtype == torch.bfloat16 else FP32_TOL
+    assert rel_err(o1, ro) <= tol and rel_err(h1, rh) <= tol
 
 
 @pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, BF16_TOL), (torch.float32, FP32_TOL)])
