@@ -17,6 +17,7 @@ weak); value = tokens of all ranks / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -567,25 +568,26 @@ def main():
     # the metric's other half: the fwd+bwd training step at T = 32768 (16 / 16 heads), as a
     # sub-record of the same line
     if not w.backward and not args.no_fwdbwd and not args.profile:
-        sub = measure(FWDBWD_WORKLOAD, args, dev, world, local, clocks=True, save=False)
+        sub = sub_measure(FWDBWD_WORKLOAD, args, dev, world, local, save=False)
         line["fwdbwd"] = {
             "workload": FWDBWD_WORKLOAD, "config": config_of(FWDBWD_WORKLOAD),
             "ms_per_step": sub["ms_per_step"],
             "value": world * sub["tokens"] / (sub["ms_per_step"] / 1000.0), "unit": "tokens/s",
             "roofline": sub["roofline"], "gpu_launches": sub["launches"], "clocks": sub["clocks"],
+            "process": sub["process"],
         }
         if "e2e" in sub:
             line["fwdbwd"]["e2e"] = sub["e2e"]
         # the same training step with the low-level saved pair: the forward keeps the state
         # entering every chunk (and its chunk records) and the backward reads them instead of
         # recomputing the forward (more memory, less work)
-        sv = measure(FWDBWD_WORKLOAD, args, dev, world, local, clocks=True, save=True)
+        sv = sub_measure(FWDBWD_WORKLOAD, args, dev, world, local, save=True)
         line["fwdbwd_saved_states"] = {
             "ms_per_step": sv["ms_per_step"],
             "value": world * sv["tokens"] / (sv["ms_per_step"] / 1000.0), "unit": "tokens/s",
             "roofline_frac": sv["roofline"]["frac"], "gpu_launches": sv["launches"],
             "kernels_ms_per_step": {k: v["ms_per_step"] for k, v in sv["roofline"]["kernels"].items()},
-            "clocks": sv["clocks"]}
+            "clocks": sv["clocks"], "process": sv["process"]}
         if "e2e" in sv:
             line["fwdbwd_saved_states"]["e2e"] = sv["e2e"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -610,6 +612,35 @@ def main():
 
 
 FWDBWD_WORKLOAD = "fwdbwd_t32k_hqk16_hv16"
+
+
+def sub_measure(name, args, dev, world, local, save):
+    """A sub-record of the line, measured as if alone.  Where a workload's buffers land in
+    device memory depends on what the process allocated before, and the training step's local
+    gradients ran ~6 % slower (and the forward ~2 % faster) after another workload in the same
+    process; so on one GPU each sub-record runs in a fresh child process (the same bench.py,
+    its JSON line parsed back).  Several ranks measure it in-process, as the ranks must."""
+    if world > 1:
+        r = measure(name, args, dev, world, local, clocks=True, save=save)
+        r["process"] = "in-process (ranks)"
+        return r
+    gc.collect()
+    torch.cuda.empty_cache()
+    cmd = [sys.executable, os.path.abspath(__file__), "--workload", name, "--steps", str(args.steps),
+           "--warmup", str(args.warmup), "--no-cpu-baseline", "--no-fwdbwd"]
+    if save:
+        cmd.append("--save-states")
+    if args.no_e2e:
+        cmd.append("--no-e2e")
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES=os.environ.get("CUDA_VISIBLE_DEVICES", str(local)))
+    out = subprocess.run(cmd, env=env, capture_output=True, text=True, check=True).stdout
+    d = json.loads([l for l in out.splitlines() if l.startswith("{")][-1])
+    r = {"tokens": d["value"] * d["ms_per_step"] / 1000.0, "ms_per_step": d["ms_per_step"],
+         "roofline": d["roofline"], "launches": d["gpu_launches"], "clocks": d["clocks"],
+         "process": "fresh child process"}
+    if "e2e" in d:
+        r["e2e"] = d["e2e"]
+    return r
 
 
 def measure(name, args, dev, world, local, clocks=True, save=False, fwd_kw=None):
