@@ -208,6 +208,29 @@ __device__ __forceinline__ float lane_colsum16(float (&v)[16]) {
     return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
+// Paths that few items take, kept out of line so that the code every item runs stays compact
+// (the kernel's code is larger than an SM's instruction cache; instruction-fetch stalls were
+// the one stall that differed between otherwise identical runs).
+struct F16 {
+    float v[16];
+};
+// D_ij = exp(gamma_i - gamma_j) for the 16 columns from gam16, formed directly (a chunk whose
+// decay is too steep for the products of exponentials)
+__device__ __noinline__ F16 decay_row_direct(float gi, const float* gam16) {
+    F16 r;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) r.v[jj] = expf(gi - gam16[jj]);
+    return r;
+}
+// rows [0, n) of a 16-row column segment of a token-major bf16 gradient: element ii at
+// col[ii * stride] (index idx0 + ii * stride of lim), for a chunk cut by the sequence end
+__device__ __noinline__ void st_col_bf16(__nv_bfloat16* col, int64_t stride, F16 x, int n, int64_t idx0,
+                                         int64_t lim, int* err) {
+#pragma unroll 1
+    for (int ii = 0; ii < 16; ++ii)
+        if (ii < n && in_range(idx0 + ii * stride, lim, err)) col[ii * stride] = __float2bfloat16_rn(x.v[ii]);
+}
+
 // lane 0 waits (bounded, polling: a parked lane wakes too late for these waits, which are on
 // the item's critical path), the result is broadcast to the warp
 __device__ __forceinline__ bool lwait(uint64_t* bars, int b, uint32_t par, int* errflag) {
@@ -254,8 +277,12 @@ struct Item {
     int64_t tc;
 };
 
+// PART: several v-heads share a q/k head, so dq and dk go to the fp32 per-v-head partials
+// (B.dqp, B.dkp) that a later kernel reduces
+template <bool PART>
 __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __grid_constant__ LocMaps maps,
                                                         int64_t items) {
+    pdl_launch_dependents();
     unsigned char* sm = loc_smem();
     const Problem& P = B.f;
     float* sF = reinterpret_cast<float*>(sm + L_SM);
@@ -292,6 +319,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = *slot;
+    pdl_wait();  // (the set-up above reads nothing an earlier kernel writes)
 
     auto locate = [&](int64_t item, Item& x) -> bool {
         const int gch = int(item / Hv);
@@ -609,8 +637,9 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             const float gi = sGam[i], ei = sE[i];
             float dm[16];  // D_ij = exp(gamma_i - gamma_j)
             if (*sPw) {
+                const F16 r = decay_row_direct(gi, sGam + c16);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) dm[jj] = expf(gi - sGam[c16 + jj]);
+                for (int jj = 0; jj < 16; ++jj) dm[jj] = r.v[jj];
             } else {
 #pragma unroll
                 for (int jj = 0; jj < 16; jj += 4) {
@@ -716,14 +745,14 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                     y[ii] *= vc[ii];
                 }
             } else {
-                __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(B.dv) + int64_t(j) * VD + v + (tc + c16) * v_stride;
+                F16 o;
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
-                    const int cx = c16 + ii;
-                    if (cx < c && in_range(int64_t(j) * VD + v + (tc + cx) * v_stride, T_all * v_stride, P.err))
-                        dv[ii * v_stride] = __float2bfloat16_rn(sBeta[cx] * y[ii]);
+                    o.v[ii] = sBeta[c16 + ii] * y[ii];
                     y[ii] *= vc[ii];
                 }
+                st_col_bf16(reinterpret_cast<__nv_bfloat16*>(B.dv) + int64_t(j) * VD + v + (tc + c16) * v_stride,
+                            v_stride, o, c - c16, int64_t(j) * VD + v + (tc + c16) * v_stride, T_all * v_stride, P.err);
             }
             const float cs = lane_colsum16(y);
             if (!(lane & 1)) sF[F_PTU + 64 * q4 + c16 + (lane >> 1)] = cs;
@@ -765,7 +794,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             tmem_ld16(tm + lb + sz + c16, b);
             tmem_ld_wait();
             const int k = 32 * q4 + lane;
-            if (B.dqp) {
+            if (PART) {
                 float* dq = B.dqp + int64_t(j) * KD + k;
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
@@ -780,13 +809,12 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                           __bfloat16_as_ushort(__float2bfloat16_rn(sc * sE[c16 + ii] * a[ii] + b[ii])));
                 fence_proxy_async_smem();
             } else {
-                __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(B.dq) + int64_t(qh) * KD + k;
+                F16 o;
 #pragma unroll
-                for (int ii = 0; ii < 16; ++ii) {
-                    const int cx = c16 + ii;
-                    if (cx < c && in_range(int64_t(qh) * KD + k + (tc + cx) * qk_stride, T_all * qk_stride, P.err))
-                        dq[(tc + cx) * qk_stride] = __float2bfloat16_rn(sc * sE[cx] * a[ii] + b[ii]);
-                }
+                for (int ii = 0; ii < 16; ++ii) o.v[ii] = sc * sE[c16 + ii] * a[ii] + b[ii];
+                st_col_bf16(reinterpret_cast<__nv_bfloat16*>(B.dq) + int64_t(qh) * KD + k + (tc + c16) * qk_stride,
+                            qk_stride, o, c - c16, int64_t(qh) * KD + k + (tc + c16) * qk_stride, T_all * qk_stride,
+                            P.err);
             }
             float qc[16];
             ld_col16(aQ, c16, k, qc);
@@ -835,7 +863,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
         fence_before_sync();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         TTRACE(12);
-        if (tid == 0 && tile_out && !B.dqp) {
+        if (tid == 0 && tile_out && !PART) {
             tma_store_3d(&maps.dq, sm + L_DV, 0, qh, int(tc));
             tma_store_3d(&maps.dq, sm + L_DV + 8192, 64, qh, int(tc));
             bulk_commit();
@@ -898,8 +926,9 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             const float gi = sGam[i], bi = sBeta[i], ei = sE[i];
             float dm[16];  // D_ij = exp(gamma_i - gamma_j)
             if (*sPw) {
+                const F16 r = decay_row_direct(gi, sGam + c16);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) dm[jj] = expf(gi - sGam[c16 + jj]);
+                for (int jj = 0; jj < 16; ++jj) dm[jj] = r.v[jj];
             } else {
 #pragma unroll
                 for (int jj = 0; jj < 16; jj += 4) {
@@ -1022,7 +1051,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                 const int cx = c16 + ii;
                 x[ii] += sKd[cx] * y[ii] + sBe[cx] * z[ii];
             }
-            if (B.dkp) {
+            if (PART) {
                 float* dk = B.dkp + int64_t(j) * KD + k;
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
@@ -1036,13 +1065,12 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
                     sts16(aSTG + out_tile_off(c16 + ii, k), __bfloat16_as_ushort(__float2bfloat16_rn(x[ii])));
                 fence_proxy_async_smem();
             } else {
-                __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(B.dk) + int64_t(qh) * KD + k;
+                F16 o;
 #pragma unroll
-                for (int ii = 0; ii < 16; ++ii) {
-                    const int cx = c16 + ii;
-                    if (cx < c && in_range(int64_t(qh) * KD + k + (tc + cx) * qk_stride, T_all * qk_stride, P.err))
-                        dk[(tc + cx) * qk_stride] = __float2bfloat16_rn(x[ii]);
-                }
+                for (int ii = 0; ii < 16; ++ii) o.v[ii] = x[ii];
+                st_col_bf16(reinterpret_cast<__nv_bfloat16*>(B.dk) + int64_t(qh) * KD + k + (tc + c16) * qk_stride,
+                            qk_stride, o, c - c16, int64_t(qh) * KD + k + (tc + c16) * qk_stride, T_all * qk_stride,
+                            P.err);
             }
         }
         // per-token totals (warp 0, rows 2 lane and 2 lane + 1), then dg = reverse in-chunk
@@ -1096,7 +1124,7 @@ __global__ void __launch_bounds__(LT, 1) k_tc_bwd_local(BwdProblem B, const __gr
             __syncwarp();
         } else {
             named_sync(3, LT);
-            if (tid == 0 && tile_out && !B.dkp) {
+            if (tid == 0 && tile_out && !PART) {
                 tma_store_3d(&maps.dk, sm + L_STG, 0, qh, int(tc));
                 tma_store_3d(&maps.dk, sm + L_STG + 8192, 64, qh, int(tc));
                 bulk_commit();
@@ -1152,12 +1180,14 @@ cudaError_t launch_bwd_local_tc(const BwdProblem& B, int64_t T_total, cudaStream
         !make_map(&maps.dv, B.dv, P.Hv, T_total) || (!B.dqp && !make_map(&maps.dq, B.dq, P.Hqk, T_total)) ||
         (!B.dkp && !make_map(&maps.dk, B.dk, P.Hqk, T_total)))
         return cudaErrorInvalidValue;
-    cudaError_t e = smem_attr(k_tc_bwd_local, int(LOC_SMEM));
+    const bool part = B.dqp != nullptr;  // (B.dkp with it: both when Hv != Hqk)
+    if (part != (B.dkp != nullptr)) return cudaErrorInvalidValue;
+    cudaError_t e = part ? smem_attr(k_tc_bwd_local<true>, int(LOC_SMEM)) : smem_attr(k_tc_bwd_local<false>, int(LOC_SMEM));
     if (e != cudaSuccess) return e;
     const int64_t items = int64_t(P.total_chunks) * P.Hv;
     const int grid = int(items < int64_t(sm_count()) ? items : int64_t(sm_count()));  // persistent
-    k_tc_bwd_local<<<grid, LT, LOC_SMEM, st>>>(B, maps, items);
-    return cudaGetLastError();
+    return part ? launch_pdl(k_tc_bwd_local<true>, dim3(grid), dim3(LT), LOC_SMEM, st, B, maps, items)
+                : launch_pdl(k_tc_bwd_local<false>, dim3(grid), dim3(LT), LOC_SMEM, st, B, maps, items);
 }
 
 }  // namespace gdn

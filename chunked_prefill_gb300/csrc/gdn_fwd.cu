@@ -704,7 +704,7 @@ void launch_fixup(const Problem& P, cudaStream_t st) {
 
 void launch_bwd_fixup_tc(const BwdProblem& B, cudaStream_t st) {
     const Problem& P = B.f;
-    launch_fixup_cg<true>(P.N, P.Hv, P.plan, P.mbuf_t, B.dhb, P.err, false, st, P.dec);
+    launch_fixup_cg<true>(P.N, P.Hv, P.plan, P.mbuf_t, B.dhb, P.err, true, st, P.dec);
 }
 
 template <typename Op, int C>

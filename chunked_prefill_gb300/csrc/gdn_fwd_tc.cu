@@ -147,13 +147,13 @@ __device__ __forceinline__ uint64_t mdesc(uint32_t addr, uint32_t lbo) {  // MN-
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bars, int b, uint32_t parity, int* errflag) {
     if (mbar_wait_spin(&bars[b], parity)) return true;
-    atomicOr(errflag, 1 << b);
+    atomicOr(errflag, 1 << (b % 27));
     return false;
 }
 // a wait of a role that is not on the state chain: it backs off between tries
 __device__ __forceinline__ bool wait_bar_lazy(uint64_t* bars, int b, uint32_t parity, int* errflag) {
     if (mbar_wait_sleep(&bars[b], parity, 64)) return true;
-    atomicOr(errflag, 1 << b);
+    atomicOr(errflag, 1 << (b % 27));
     return false;
 }
 // warp-uniform wait: lane 0 waits, the result is broadcast, then the warp synchronises
@@ -252,20 +252,18 @@ __device__ __forceinline__ void state_decay_all(uint32_t tm, uint32_t lb, uint32
 // the previous CTA does not store them (c >= e_own) and P_c is below it (a chunk at or past
 // e_own that fails is left to the correction: rerun); the chunks past the own segment are
 // stored when the scan reached them from a true state (the first segment, or P_n below it).
+// The scan's barriers, its tensor memory and (with an output side) the zeroed (Q h)^T halves;
+// nothing here reads memory that an earlier kernel writes, so a kernel may run it before it
+// waits for its predecessor (then tc_scan is called with ready, or tc_scan_release frees the
+// tensor memory on a path that does not scan).
 template <int KIND>
-__device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm, int j,
-                        int64_t t0, int64_t t1, int cb, int ce, const float* x0, float* x_out,
-                        int64_t hist_base, float* x_out_t = nullptr, const ScanRule* rule = nullptr) {
+__device__ void tc_scan_setup(unsigned char* sm) {
     constexpr bool OUT = KIND == TK_OUT;
     constexpr bool NEEDU = KIND != TK_TRANS;
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, w = tid >> 5;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + B_COUNT * 8);
     int* errflag = reinterpret_cast<int*>(sm + S_BAR + B_COUNT * 8 + 4);
-    Gate* gates = reinterpret_cast<Gate*>(sm + S_GATE);
-    const int G = P.Hv / P.Hqk, qh = j / G;
-    const int n = ce - cb;
-
     if (tid == 0) {
         mbar_init(&bars[B_FULL0], 1);
         mbar_init(&bars[B_FULL1], 1);
@@ -300,7 +298,6 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    CTRACE(OUT || KIND == TK_HIST ? 1 : 0, 2);
     const uint32_t tm = *tmem_slot;
     if (OUT) {  // the (Q h)^T halves of both DD buffers start at zero
         if (w >= 12) {
@@ -319,6 +316,34 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
         __syncthreads();
         fence_after_sync();
     }
+}
+__device__ void tc_scan_release(unsigned char* sm) {
+    fence_before_sync();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) {
+        fence_after_sync();
+        tmem_dealloc(*reinterpret_cast<uint32_t*>(sm + S_BAR + B_COUNT * 8), 512);
+    }
+}
+
+template <int KIND>
+__device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm, int j,
+                        int64_t t0, int64_t t1, int cb, int ce, const float* x0, float* x_out,
+                        int64_t hist_base, float* x_out_t = nullptr, const ScanRule* rule = nullptr,
+                        bool ready = false) {
+    constexpr bool OUT = KIND == TK_OUT;
+    constexpr bool NEEDU = KIND != TK_TRANS;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + B_COUNT * 8);
+    int* errflag = reinterpret_cast<int*>(sm + S_BAR + B_COUNT * 8 + 4);
+    Gate* gates = reinterpret_cast<Gate*>(sm + S_GATE);
+    const int G = P.Hv / P.Hqk, qh = j / G;
+    const int n = ce - cb;
+
+    if (!ready) tc_scan_setup<KIND>(sm);
+    CTRACE(OUT || KIND == TK_HIST ? 1 : 0, 2);
+    const uint32_t tm = *tmem_slot;
     if (w == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -327,6 +352,7 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             for (int k = 0; k < n; ++k) {
                 const int st = k & 1;
                 if (k >= 2 && !wait_bar_lazy(bars, B_EMPTY0 + st, ((k - 2) >> 1) & 1, errflag)) break;
+                TRACE(k, 3);
                 const int tc = int(t0 + int64_t(cb + k) * CH);
                 uint64_t* full = &bars[B_FULL0 + st];
                 unsigned char* kt = sm + S_K + st * S_K_STRIDE;
@@ -500,7 +526,9 @@ __device__ void tc_scan(const Problem& P, const TcMaps& maps, unsigned char* sm,
             auto issue_u = [&](int q) {
                 const int st = q & 1;
                 const uint64_t dV = mdesc(v0a + st * S_V_STRIDE, 8192), dTU = kdesc(tu0 + st * S_TU_STRIDE);
+                TRACE(q, 8);
                 if (!wait_bar(bars, B_FULL0 + st, (q >> 1) & 1, errflag)) return false;
+                TRACE(q, 6);
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
@@ -1122,10 +1150,11 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
 // same code and summation order, so the CTA of segment lj (looking ahead) and that of lj + 1
 // (looking at itself) agree bit for bit.
 constexpr int EXT_MAX = 4;
-__device__ int ext_len(const Problem& P, int64_t t0, int64_t t1, int cs, int n, int j) {
+// (in two steps, so that a caller that needs two lengths issues all their loads at once)
+__device__ __forceinline__ void ext_load(const Problem& P, int64_t t0, int64_t t1, int cs, int n, int j,
+                                         float (&gv)[EXT_MAX][2]) {
     const int lane = threadIdx.x & 31;
     const int m = min(n, EXT_MAX);
-    float gv[EXT_MAX][2];
 #pragma unroll
     for (int e = 0; e < EXT_MAX; ++e)
 #pragma unroll
@@ -1133,6 +1162,9 @@ __device__ int ext_len(const Problem& P, int64_t t0, int64_t t1, int cs, int n, 
             const int64_t t = t0 + int64_t(cs + e) * CH + 2 * lane + u;
             gv[e][u] = (e < m && t < t1) ? P.g[t * P.Hv + j] : 0.f;
         }
+}
+__device__ __forceinline__ int ext_sum(const float (&gv)[EXT_MAX][2], int n) {
+    const int m = min(n, EXT_MAX);
     float run = 0.f;
 #pragma unroll
     for (int e = 0; e < EXT_MAX; ++e) {
@@ -1144,6 +1176,11 @@ __device__ int ext_len(const Problem& P, int64_t t0, int64_t t1, int cs, int n, 
         if (run < LOG_NEGLIGIBLE) return e + 1;
     }
     return 0;
+}
+__device__ int ext_len(const Problem& P, int64_t t0, int64_t t1, int cs, int n, int j) {
+    float gv[EXT_MAX][2];
+    ext_load(P, t0, t1, cs, n, j, gv);
+    return ext_sum(gv, n);
 }
 
 // Output stage (KIND = TK_OUT) or the backward's recompute of the state entering every chunk
@@ -1163,13 +1200,19 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_c
                                                       int mode) {
     if (mode != 2) CTRACE(1, 0);
     pdl_launch_dependents();
+    unsigned char* sm = aligned_smem();
+    // the passes that scan in every CTA set up while the previous kernel finishes
+    const bool pre = mode != 2;
+    if (pre) tc_scan_setup<KIND>(sm);
     pdl_wait();
     if (mode != 2) CTRACE(1, 1);
-    unsigned char* sm = aligned_smem();
     const int gseg = blockIdx.x, j = blockIdx.y;
     const int2 sj = plan_seg(P.plan, gseg);
     const int s = sj.x, lj = sj.y;
-    if (s < 0 || s >= P.N) return;
+    if (s < 0 || s >= P.N) {
+        if (pre) tc_scan_release(sm);
+        return;
+    }
     const int nseg = plan_seg_off(P.plan, s + 1) - plan_seg_off(P.plan, s);
     int64_t t0, t1;
     seq_range(P, s, t0, t1);
@@ -1182,17 +1225,26 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_c
     if (mode == 1) {
         const float* x0 = lj == 0 ? h0 : nullptr;
         float* x_seg = last ? ht : P.hin + (sjh + P.Hv) * KVN;
-        if (ce <= cb) { copy_state(x0, x_seg, false); return; }  // only an empty sequence
+        if (ce <= cb) {  // only an empty sequence
+            copy_state(x0, x_seg, false);
+            tc_scan_release(sm);
+            return;
+        }
+        // both extension lengths from one round of gate loads
+        const int n_own = lj >= 1 ? ce - cb : 0, n_next = last ? 0 : min(P.L, nt - ce);
+        float g_own[EXT_MAX][2], g_next[EXT_MAX][2];
+        ext_load(P, t0, t1, cb, n_own, j, g_own);
+        ext_load(P, t0, t1, ce, n_next, j, g_next);
         ScanRule rule;
         rule.n_own = ce - cb;
-        rule.e_own = lj >= 1 ? ext_len(P, t0, t1, cb, ce - cb, j) : 0;
+        rule.e_own = lj >= 1 ? ext_sum(g_own, n_own) : 0;
+        const int e_next = last ? 0 : ext_sum(g_next, n_next);
         rule.lj = lj;
         rule.dec = P.dec + sjh;
         rule.rerun = P.rerun + sjh;
-        const int e_next = last ? 0 : ext_len(P, t0, t1, ce, min(P.L, nt - ce), j);
         rule.x_mid = e_next > 0 ? x_seg : nullptr;
         tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce + e_next, x0, e_next > 0 ? nullptr : x_seg,
-                      plan_chunk_off(P.plan, s), nullptr, &rule);
+                      plan_chunk_off(P.plan, s), nullptr, &rule, true);
         CTRACE(1, 3);
         return;
     }
@@ -1205,8 +1257,12 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_c
     }
     const float* x0 = (lj == 0) ? h0 : P.hin + sjh * KVN;
     float* x_out = last ? ht : nullptr;
-    if (ce <= cb) { copy_state(x0, x_out, false); return; }
-    tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce, x0, x_out, plan_chunk_off(P.plan, s));
+    if (ce <= cb) {
+        copy_state(x0, x_out, false);
+        tc_scan_release(sm);
+        return;
+    }
+    tc_scan<KIND>(P, maps, sm, j, t0, t1, cb, ce, x0, x_out, plan_chunk_off(P.plan, s), nullptr, nullptr, true);
     CTRACE(1, 3);
 }
 
@@ -1230,25 +1286,17 @@ constexpr uint32_t T_DB = 192, T_DA = 256;
 // chunk is stored when the next segment's CTA does not store it (k >= e_own) and the sum over
 // the chunks scanned before it is below LOG_NEGLIGIBLE (else the segment is left to the
 // correction: rerun); the chunks past the own segment are stored when rule->ext_ok.
-template <bool HIST>
-__device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUtensorMap* mdo,
-                            unsigned char* sm, int j, int64_t t0, int64_t t1, int cb, int ce,
-                            const float* x0, float* x_out, int64_t gbase,
-                            const ScanRule* rule = nullptr) {
-    enum RB { R_FULL0 = 0, R_FULL1, R_EMPTY0, R_EMPTY1, R_GATE0, R_GFREE0 = R_GATE0 + NGATE,
-              R_MMA3 = R_GFREE0 + NGATE, R_MMA5, R_EX, R_EV, R_DOE0, R_DOE1, R_DRAIN, R_DEC, R_COUNT };
-    static_assert(R_COUNT * 8 + 8 <= 512, "barrier area");
-    const Problem& P = B.f;
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+enum RB { R_FULL0 = 0, R_FULL1, R_EMPTY0, R_EMPTY1, R_GATE0, R_GFREE0 = R_GATE0 + NGATE,
+          R_MMA3 = R_GFREE0 + NGATE, R_MMA5, R_EX, R_EV, R_DOE0, R_DOE1, R_DRAIN, R_DEC, R_COUNT };
+static_assert(R_COUNT * 8 + 8 <= 512, "barrier area");
+// The reverse scan's barriers and tensor memory (reads nothing an earlier kernel writes: may
+// run before the wait for it; tc_bwd_release frees the tensor memory on a path that does not
+// scan).
+__device__ void tc_bwd_setup(unsigned char* sm) {
+    const int tid = threadIdx.x, w = tid >> 5;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + R_COUNT * 8);
     int* errflag = reinterpret_cast<int*>(sm + S_BAR + R_COUNT * 8 + 4);
-    Gate* gates = reinterpret_cast<Gate*>(sm + S_GATE);
-    const int G = P.Hv / P.Hqk, qh = j / G;
-    const int n = ce - cb;
-    const float sc = P.scale;
-    auto chunk_of = [&](int k) { return ce - 1 - k; };  // reverse order
-
     if (tid == 0) {
         mbar_init(&bars[R_FULL0], 1);
         mbar_init(&bars[R_FULL1], 1);
@@ -1273,6 +1321,33 @@ __device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUten
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+}
+__device__ void tc_bwd_release(unsigned char* sm) {
+    fence_before_sync();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) {
+        fence_after_sync();
+        tmem_dealloc(*reinterpret_cast<uint32_t*>(sm + S_BAR + R_COUNT * 8), 512);
+    }
+}
+
+template <bool HIST>
+__device__ void tc_bwd_scan(const BwdProblem& B, const TcMaps& maps, const CUtensorMap* mdo,
+                            unsigned char* sm, int j, int64_t t0, int64_t t1, int cb, int ce,
+                            const float* x0, float* x_out, int64_t gbase,
+                            const ScanRule* rule = nullptr, bool ready = false) {
+    const Problem& P = B.f;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + R_COUNT * 8);
+    int* errflag = reinterpret_cast<int*>(sm + S_BAR + R_COUNT * 8 + 4);
+    Gate* gates = reinterpret_cast<Gate*>(sm + S_GATE);
+    const int G = P.Hv / P.Hqk, qh = j / G;
+    const int n = ce - cb;
+    const float sc = P.scale;
+    auto chunk_of = [&](int k) { return ce - 1 - k; };  // reverse order
+
+    if (!ready) tc_bwd_setup(sm);
     const uint32_t tm = *tmem_slot;
 
     if (w == 0) {
@@ -1593,10 +1668,11 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_bwd_a(BwdProblem B, const __grid_
 // g-only extension length of the reverse scan into the segment ending at chunk ce (n chunks):
 // the smallest e in [1, min(n, EXT_MAX)] whose last e chunks' gate sum is below
 // LOG_NEGLIGIBLE, else 0 (the mirror image of ext_len, with the same guarantees).
-__device__ int ext_len_rev(const Problem& P, int64_t t0, int64_t t1, int ce, int n, int j) {
+// (loads in ext_load_rev, the sum in ext_sum, as for ext_len)
+__device__ __forceinline__ void ext_load_rev(const Problem& P, int64_t t0, int64_t t1, int ce, int n, int j,
+                                             float (&gv)[EXT_MAX][2]) {
     const int lane = threadIdx.x & 31;
     const int m = min(n, EXT_MAX);
-    float gv[EXT_MAX][2];
 #pragma unroll
     for (int e = 0; e < EXT_MAX; ++e)
 #pragma unroll
@@ -1604,17 +1680,6 @@ __device__ int ext_len_rev(const Problem& P, int64_t t0, int64_t t1, int ce, int
             const int64_t t = t0 + int64_t(ce - 1 - e) * CH + 2 * lane + u;
             gv[e][u] = (e < m && t < t1) ? P.g[t * P.Hv + j] : 0.f;
         }
-    float run = 0.f;
-#pragma unroll
-    for (int e = 0; e < EXT_MAX; ++e) {
-        if (e >= m) break;
-        float v = gv[e][0] + gv[e][1];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        run += v;
-        if (run < LOG_NEGLIGIBLE) return e + 1;
-    }
-    return 0;
 }
 
 // The reverse dh scan storing dh for every chunk; the first segment's result is dh0.  mode 0:
@@ -1630,12 +1695,20 @@ __device__ int ext_len_rev(const Problem& P, int64_t t0, int64_t t1, int ce, int
 // negligible (dh0).
 __global__ void __launch_bounds__(TCT, 1) k_tc_bwd_c(BwdProblem B, const __grid_constant__ BwdMaps maps,
                                                     int mode) {
+    pdl_launch_dependents();
     unsigned char* sm = aligned_smem();
+    // the passes that scan in every CTA set up while the previous kernel finishes
+    const bool pre = mode != 2;
+    if (pre) tc_bwd_setup(sm);
+    pdl_wait();
     const Problem& P = B.f;
     const int gseg = blockIdx.x, j = blockIdx.y;
     const int2 sj = plan_seg(P.plan, gseg);
     const int s = sj.x, lj = sj.y;
-    if (s < 0 || s >= P.N) return;
+    if (s < 0 || s >= P.N) {
+        if (pre) tc_bwd_release(sm);
+        return;
+    }
     const int nseg = plan_seg_off(P.plan, s + 1) - plan_seg_off(P.plan, s);
     int64_t t0, t1;
     seq_range(P, s, t0, t1);
@@ -1648,18 +1721,27 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_bwd_c(BwdProblem B, const __grid_
     if (mode == 1) {
         const float* x0 = last ? dht : nullptr;
         float* x_seg = lj == 0 ? dh0 : B.dhb + sjh * KVN;
-        if (ce <= cb) { copy_state(x0, x_seg, false); return; }  // only an empty sequence
+        if (ce <= cb) {  // only an empty sequence
+            copy_state(x0, x_seg, false);
+            tc_bwd_release(sm);
+            return;
+        }
+        // both extension lengths from one round of gate loads (the previous segment is full)
+        const int n_own = last ? 0 : ce - cb, n_prev = lj >= 1 ? P.L : 0;
+        float g_own[EXT_MAX][2], g_prev[EXT_MAX][2];
+        ext_load_rev(P, t0, t1, ce, n_own, j, g_own);
+        ext_load_rev(P, t0, t1, cb, n_prev, j, g_prev);
         ScanRule rule;
         rule.n_own = ce - cb;
-        rule.e_own = last ? 0 : ext_len_rev(P, t0, t1, ce, ce - cb, j);
+        rule.e_own = last ? 0 : ext_sum(g_own, n_own);
         rule.lj = last ? 0 : 1;
         rule.dec = nullptr;
         rule.rerun = B.rrerun + sjh;
         rule.ext_ok = (last || P.dec[sjh] >= 0) ? 1 : 0;
-        const int e_prev = lj >= 1 ? ext_len_rev(P, t0, t1, cb, P.L, j) : 0;  // the previous segment is full
+        const int e_prev = lj >= 1 ? ext_sum(g_prev, n_prev) : 0;
         rule.x_mid = e_prev > 0 ? x_seg : nullptr;
         tc_bwd_scan<true>(B, maps.f, &maps.dO, sm, j, t0, t1, cb - e_prev, ce, x0,
-                          e_prev > 0 ? nullptr : x_seg, plan_chunk_off(P.plan, s), &rule);
+                          e_prev > 0 ? nullptr : x_seg, plan_chunk_off(P.plan, s), &rule, true);
         return;
     }
     if (mode == 2) {
@@ -1673,8 +1755,13 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_bwd_c(BwdProblem B, const __grid_
     }
     const float* x0 = last ? dht : B.dhb + (sjh + P.Hv) * KVN;
     float* x_out = (lj == 0) ? dh0 : nullptr;
-    if (ce <= cb) { copy_state(x0, x_out, false); return; }
-    tc_bwd_scan<true>(B, maps.f, &maps.dO, sm, j, t0, t1, cb, ce, x0, x_out, plan_chunk_off(P.plan, s));
+    if (ce <= cb) {
+        copy_state(x0, x_out, false);
+        tc_bwd_release(sm);
+        return;
+    }
+    tc_bwd_scan<true>(B, maps.f, &maps.dO, sm, j, t0, t1, cb, ce, x0, x_out, plan_chunk_off(P.plan, s),
+                      nullptr, true);
 }
 
 }  // namespace
@@ -1799,7 +1886,8 @@ cudaError_t launch_bwd_scan_tc(const BwdProblem& B, int which, int64_t T_total, 
     } else {
         e = smem_attr(k_tc_bwd_c, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        k_tc_bwd_c<<<dim3(P.total_segs, P.Hv), TCT, SMEM_BYTES, st>>>(B, maps, which - 1);
+        e = launch_pdl(k_tc_bwd_c, dim3(P.total_segs, P.Hv), dim3(TCT), SMEM_BYTES, st, B, maps, which - 1);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
