@@ -1148,9 +1148,9 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_phase_a(Problem P, const __grid_c
 // beta |k|^2 terms only raise a chunk's log-bound above its gate sum, chunks before e are
 // certainly not decoupled from the segment's entering state.  Every warp computes it with the
 // same code and summation order, so the CTA of segment lj (looking ahead) and that of lj + 1
-// (looking at itself) agree bit for bit.
+// (looking at itself) agree bit for bit.  In two steps (the gate loads, ext_load, then the sum,
+// ext_sum), so that a caller that needs two lengths issues all their loads at once.
 constexpr int EXT_MAX = 4;
-// (in two steps, so that a caller that needs two lengths issues all their loads at once)
 __device__ __forceinline__ void ext_load(const Problem& P, int64_t t0, int64_t t1, int cs, int n, int j,
                                          float (&gv)[EXT_MAX][2]) {
     const int lane = threadIdx.x & 31;
@@ -1177,11 +1177,6 @@ __device__ __forceinline__ int ext_sum(const float (&gv)[EXT_MAX][2], int n) {
     }
     return 0;
 }
-__device__ int ext_len(const Problem& P, int64_t t0, int64_t t1, int cs, int n, int j) {
-    float gv[EXT_MAX][2];
-    ext_load(P, t0, t1, cs, n, j, gv);
-    return ext_sum(gv, n);
-}
 
 // Output stage (KIND = TK_OUT) or the backward's recompute of the state entering every chunk
 // (TK_HIST), one CTA per (segment, v-head).  mode 0: every segment from its entering state
@@ -1195,9 +1190,11 @@ __device__ int ext_len(const Problem& P, int64_t t0, int64_t t1, int cs, int n, 
 // correction, reruns from its true entering state every segment with an unwritten result: one
 // flagged by its own CTA, one that follows a segment whose transition is not negligible, and
 // a last segment whose own transition is not negligible (its final state).
-template <int KIND>
-__global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_constant__ TcMaps maps,
-                                                      int mode) {
+// (mode is a template parameter: each kernel holds one copy of the scan, whose code is larger
+// than an SM's instruction cache)
+template <int KIND, int MODE>
+__global__ void __launch_bounds__(TCT, 1) k_tc_phase_c(Problem P, const __grid_constant__ TcMaps maps) {
+    constexpr int mode = MODE;
     if (mode != 2) CTRACE(1, 0);
     pdl_launch_dependents();
     unsigned char* sm = aligned_smem();
@@ -1667,8 +1664,8 @@ __global__ void __launch_bounds__(TCT, 1) k_tc_bwd_a(BwdProblem B, const __grid_
 
 // g-only extension length of the reverse scan into the segment ending at chunk ce (n chunks):
 // the smallest e in [1, min(n, EXT_MAX)] whose last e chunks' gate sum is below
-// LOG_NEGLIGIBLE, else 0 (the mirror image of ext_len, with the same guarantees).
-// (loads in ext_load_rev, the sum in ext_sum, as for ext_len)
+// LOG_NEGLIGIBLE, else 0 (the mirror image of the forward's extension length, with the same
+// guarantees; the loads here, the sum in ext_sum).
 __device__ __forceinline__ void ext_load_rev(const Problem& P, int64_t t0, int64_t t1, int ce, int n, int j,
                                              float (&gv)[EXT_MAX][2]) {
     const int lane = threadIdx.x & 31;
@@ -1821,10 +1818,11 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
     cudaError_t e;
     e = smem_attr(k_tc_phase_a, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = smem_attr(k_tc_phase_c<TK_OUT>, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = smem_attr(k_tc_phase_c<TK_HIST>, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    for (auto kern : {k_tc_phase_c<TK_OUT, 0>, k_tc_phase_c<TK_OUT, 1>, k_tc_phase_c<TK_OUT, 2>,
+                      k_tc_phase_c<TK_HIST, 0>, k_tc_phase_c<TK_HIST, 1>, k_tc_phase_c<TK_HIST, 2>}) {
+        e = smem_attr(kern, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+    }
 #ifdef GDN_CHECK
     launch_plan(P, CH, st);
 #else
@@ -1836,9 +1834,11 @@ cudaError_t launch_fwd_tc(const Problem& P, bool hist, int64_t T_total, cudaStre
     const dim3 grid(P.total_segs, P.Hv);
     auto out_pass = [&](const char* name, int mode) {
         timing_begin(name, st);
-        const cudaError_t r =
-            hist ? launch_pdl(k_tc_phase_c<TK_HIST>, grid, dim3(TCT), SMEM_BYTES, st, P, maps, mode)
-                 : launch_pdl(k_tc_phase_c<TK_OUT>, grid, dim3(TCT), SMEM_BYTES, st, P, maps, mode);
+        auto kern = hist ? (mode == 1 ? k_tc_phase_c<TK_HIST, 1> : mode == 2 ? k_tc_phase_c<TK_HIST, 2>
+                                                                          : k_tc_phase_c<TK_HIST, 0>)
+                         : (mode == 1 ? k_tc_phase_c<TK_OUT, 1> : mode == 2 ? k_tc_phase_c<TK_OUT, 2>
+                                                                          : k_tc_phase_c<TK_OUT, 0>);
+        const cudaError_t r = launch_pdl(kern, grid, dim3(TCT), SMEM_BYTES, st, P, maps);
         timing_end(st);
         return r;
     };
