@@ -228,6 +228,9 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
             }
             if (lane == 0) *sFlag = (last < -80.f || !(last == last)) ? 1 : 0;
         }
+        // the previous head's W' stores have read their staging tiles (waited for here, after
+        // this head's gates, rather than at the end of that head: the A/P phase reuses them)
+        if (tid == 0 && hh > 0) bulk_wait_read0();
         __syncthreads();  // gates visible; the previous head's staging has been read
         PTRACE(1);
 
@@ -469,9 +472,7 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
         __syncthreads();
         PTRACE(4);
         if (tid == 0) {
-            bulk_store(rec + PREP_TU, smem + S::oQ0, 8192);
-            bulk_commit();
-            // W'^T [dk][i] = K^T TW^T into TMEM columns [64, 128)
+            // W'^T [dk][i] = K^T TW^T into TMEM columns [64, 128), then TU's record copy
             constexpr uint32_t ID2 = make_idesc(128, 64, 1, 0);
             const uint64_t da = make_desc(kq, 16384, 1024);
             const uint64_t db = make_desc(smem_addr(smem + S::oQ1), 0, 1024);
@@ -479,6 +480,8 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
 #pragma unroll
             for (int st = 0; st < 4; ++st) mma_bf16(tm + 64, da + (st * 2048 >> 4), db + (st * 32 >> 4), ID2, st > 0);
             commit(&bars[2]);
+            bulk_store(rec + PREP_TU, smem + S::oQ0, 8192);
+            bulk_commit();
         }
         // T itself for the backward (the record's swizzled bf16 image) and for the low-level
         // output: 16-byte stores straight from the fp32 blocks while the W' product runs
@@ -542,10 +545,10 @@ __global__ void __launch_bounds__(PT, 4) k_prep(Problem P, const __grid_constant
             bulk_store(rec + PREP_W + 8192, smem + S::oQ1, 8192);
             bulk_commit();
             PTRACE(6);
-            bulk_wait_read0();  // the next head (or the CTA's exit) may reuse the staging tiles
             PTRACE(7);
         }
     }
+    if (tid == 0) bulk_wait_read0();  // the last head's stores have read their tiles
     __syncthreads();
     if (w == 0) {
         fence_after_sync();
