@@ -127,7 +127,12 @@ double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int wa
     if (bounded) {
         // exact mode with decay bounds, costed for decaying gates: one pass of L chunks plus
         // the ~2 chunks each segment scans into the next, and the three extra launches
-        // (transitions, fix-up, correction: ~3 us each, returning at once) when segmented
+        // (transitions, fix-up, correction: ~3 us each, returning at once) when segmented.
+        // Each wave of a scan launch also pays its start (set-up, the first chunks' tiles in
+        // flight) and its end (the last state out, the spread of its CTAs' ends): ~5 chunk
+        // steps, fitted to the forward at 32768 tokens x 8 / 24 heads, where one wave of
+        // 88-chunk scans ran 0.351 ms, two of 45 chunks 0.366 ms, three of 29 chunks 0.378 ms.
+        constexpr double tW = 5.0;
         long segs = 0;
         int maxn = 0;
         for (int s = 0; s < N; ++s) {
@@ -137,7 +142,7 @@ double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int wa
         }
         const long cw = (segs * Hv + sms - 1) / sms;
         const int Lc = std::min(L, *std::max_element(nts, nts + N));
-        return maxn > 1 ? double(cw) * (Lc + 2) * tC + 4.0 : double(cw) * Lc * tC;
+        return maxn > 1 ? double(cw) * (Lc + 2 + tW) * tC + 4.0 : double(cw) * (Lc + tW) * tC;
     }
     long segs = 0, actas = 0;
     int maxn = 0;
