@@ -174,7 +174,7 @@ double cp_cost(int L, const int* nts, int N, int Hv, int sms, bool exact, int wa
 // (N = chunks of a sequence); an explicit cp_lambda keeps that rule.  By default the planner
 // instead minimises cp_cost over L, which accounts for the wave quantisation of the launches
 // on this GPU's SM count.
-void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
+void plan(const gdn_problem* p, HostPlan& h, bool backward = false, int sms_override = 0) {
     h.C = gdn::fwd_chunk_size(p->dtype);
     h.N = p->cu_seqlens ? p->num_seqs : p->B;
     int nt_max = 0;
@@ -199,7 +199,7 @@ void plan(const gdn_problem* p, HostPlan& h, bool backward = false) {
                 const int len = p->cu_seqlens ? p->cu_seqlens_host[s + 1] - p->cu_seqlens_host[s] : p->T;
                 nts[s] = (len + h.C - 1) / h.C;
             }
-            const int sms = sm_count();
+            const int sms = sms_override > 0 ? sms_override : sm_count();
             const bool exact = p->cp_mode != GDN_CP_WARMUP;
             const bool bounded_cost = exact && p->cp_mode != GDN_CP_EXACT_FULL && p->dtype == GDN_BF16;
             double best = 1e300;
@@ -369,6 +369,20 @@ gdn_status gdn_device_status(const void* workspace, void* stream) {
                     unsigned(word));
     if (word != 0)
         return fail(GDN_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%08x)", unsigned(word));
+    return GDN_OK;
+}
+
+gdn_status gdn_debug_plan(const gdn_problem* p, int32_t sms, int32_t* chunks_per_segment,
+                          int32_t* segments) {
+    gdn_status st = validate_problem(p);
+    if (st != GDN_OK) return st;
+    if (!chunks_per_segment || !segments) return fail(GDN_ERR_INVALID_ARG, "output pointer is NULL");
+    if (sms <= 0) return fail(GDN_ERR_INVALID_ARG, "sms must be positive (got %d)", sms);
+    HostPlan h;
+    plan(p, h, false, sms);
+    *chunks_per_segment = h.L;
+    *segments = h.total_segs;
+    g_err[0] = 0;
     return GDN_OK;
 }
 

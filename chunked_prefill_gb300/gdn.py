@@ -70,6 +70,8 @@ def lib():
         L.gdn_chunk_bwd.argtypes = [P] + [vp] * 15 + [ctypes.c_size_t, vp]
         L.gdn_chunk_layout.argtypes = [P, ctypes.POINTER(ctypes.c_int32),
                                        ctypes.POINTER(ctypes.c_int64)]
+        L.gdn_debug_plan.argtypes = [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                     ctypes.POINTER(ctypes.c_int32)]
         L.gdn_chunk_fwd_saved.argtypes = [P] + [vp] * 12 + [ctypes.c_size_t, vp]
         L.gdn_chunk_bwd_saved.argtypes = [P] + [vp] * 15 + [ctypes.c_size_t, vp]
         L.gdn_prologue_fwd.argtypes = [P] + [vp] * 10 + [vp]
@@ -259,6 +261,13 @@ def gdn_chunk_layout(prob: Problem):
     c, n = ctypes.c_int32(0), ctypes.c_int64(0)
     _check(lib().gdn_chunk_layout(prob.ref(), ctypes.byref(c), ctypes.byref(n)))
     return c.value, n.value
+
+
+def gdn_debug_plan(prob: Problem, sms: int):
+    """Test hook: (chunks per segment, segments) the planner picks for `prob` on `sms` SMs."""
+    L, n = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().gdn_debug_plan(prob.ref(), int(sms), ctypes.byref(L), ctypes.byref(n)))
+    return L.value, n.value
 
 
 def gdn_chunk_fwd_saved(q, k, v, g, beta, scale, h0=None, output_final_state=True,

@@ -291,6 +291,14 @@ gdn_status gdn_noalloc_debug_wait_timeout(int32_t limit_us, void* stream);
  * ------------------------------------------------------------------------------------ */
 gdn_status gdn_device_status(const void* workspace, void* stream);
 
+/* Test hook of the planner (host only, no GPU work): the segmentation that gdn_chunk_fwd (and
+ * gdn_chunk_bwd) would use for `p` on a GPU with `sms` multiprocessors -- chunks per
+ * context-parallel segment and the number of segments over all sequences (one per sequence
+ * when the planner does not split them).  GDN_ERR_INVALID_ARG for an invalid problem, NULL
+ * outputs or sms <= 0. */
+gdn_status gdn_debug_plan(const gdn_problem* p, int32_t sms, int32_t* chunks_per_segment,
+                          int32_t* segments);
+
 /* Test hook of the failure report: one block waits on an mbarrier that no thread ever
  * completes, gives up after limit_us microseconds (1 .. 1000000) and sets its bit in the error
  * word of `workspace` (only those 4 bytes are touched).  Asynchronous on `stream`. */

@@ -136,3 +136,37 @@ def test_status_codes_match_the_header(L):
     assert {"GDN_OK", "GDN_ERR_TIMEOUT", "GDN_ERR_BOUNDS"} <= set(codes)
     for name, value in codes.items():
         assert getattr(L, name) == value, name
+
+
+# The planner's segmentation on a 152-SM GB300 for the benchmark shapes, pinned to the plans
+# measured fastest there (CUDA events, same GPU, the same workload forced to each segment
+# length): 1 x 32768 tokens at 8 / 24 heads took 0.351 ms with 86-chunk segments (one wave of
+# scan CTAs) against 0.366 ms with 43 and 0.378 ms with 27 (two and three waves); the training
+# step at 16 / 16 heads 1.409 ms with 57 (one wave) against 1.466 ms with 27 (two waves) and
+# 1.436 ms with 64; at 2 / 8 heads 27-chunk segments fill the 152 SMs once (54: 0.177 against
+# 0.141 ms); 16 packed sequences of 64 chunks at 4 / 16 heads ran best unsplit.
+@pytest.mark.parametrize("shape, expect", [
+    (dict(B=1, T=32768, Hqk=2, Hv=8), (27, 19)),
+    (dict(B=1, T=32768, Hqk=8, Hv=24), (86, 6)),
+    (dict(B=1, T=32768, Hqk=16, Hv=16), (57, 9)),
+    (dict(B=1, T=256, Hqk=2, Hv=4), (4, 1)),
+])
+def test_planner_choice_on_152_sms(L, shape, expect):
+    p = problem(L, cp_mode=L.CP_AUTO, **shape)
+    seg_len, segs = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert L.lib().gdn_debug_plan(ctypes.byref(p), 152, ctypes.byref(seg_len), ctypes.byref(segs)) == 0
+    assert (seg_len.value, segs.value) == expect
+
+
+def test_planner_choice_packed_sequences(L):
+    import torch
+    cu = torch.arange(0, 16 * 4096 + 1, 4096, dtype=torch.int32)
+    p = problem(L, B=1, T=16 * 4096, Hqk=4, Hv=16, cp_mode=L.CP_AUTO, num_seqs=16,
+                cu_seqlens=0x10000, cu_seqlens_host=cu.data_ptr())
+    seg_len, segs = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert L.lib().gdn_debug_plan(ctypes.byref(p), 152, ctypes.byref(seg_len), ctypes.byref(segs)) == 0
+    assert (seg_len.value, segs.value) == (64, 16)
+    # the binding's wrapper, and the hook's argument checks
+    q = torch.empty(1, 32768, 16, 128, dtype=torch.bfloat16)
+    assert L.gdn_debug_plan(L.Problem(q, q, 128 ** -0.5), 152) == (57, 9)
+    assert L.lib().gdn_debug_plan(ctypes.byref(p), 0, ctypes.byref(seg_len), ctypes.byref(segs)) == 1
