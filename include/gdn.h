@@ -30,6 +30,12 @@
  *     been written and gdn_last_error() (thread-local) says why.
  *   - Results are deterministic: repeated calls give bitwise-identical outputs.
  *   - K = V = 128 only (GDN_ERR_UNSUPPORTED otherwise).
+ *   - Stream order holds as for any launch.  Inside a call, kernels overlap their
+ *     predecessors' ends by programmatic dependent launch, each waiting for its predecessor
+ *     (griddepcontrol.wait) before it reads anything that one wrote; the library's kernels
+ *     signal their dependents early, so a caller's kernel launched right after a call WITH
+ *     programmatic stream serialisation must itself wait (cudaGridDependencySynchronize)
+ *     before it reads the call's outputs.  Ordinary launches, copies and events need nothing.
  */
 #ifndef GDN_H
 #define GDN_H
