@@ -9,11 +9,8 @@
 // K and Q arrive by TMA; W' and TU leave by bulk copies from shared-memory tiles already in
 // the 128-byte-swizzled layout the scan's tensor-core operands use, P and T (for the backward)
 // by 16-byte stores of the same image from registers.  (P staged for a bulk copy instead cost
-// the inverse a wait for the copy's reads, and the backward's local-gradient kernel, which
-// reads the records later, ran 4 % slower when the backward's own preparation wrote P that
-// way; TU written by 16-byte stores instead made both the preparation and that kernel slower:
-// measured, cause not found.)  Rows past the end of a
-// sequence hold whatever tokens follow (finite); beta = g = 0 there makes T's rows and the
+// the inverse a wait for the copy's reads; TU written by 16-byte stores instead made the
+// preparation slower.)  Rows past the end of a sequence hold whatever tokens follow (finite); beta = g = 0 there makes T's rows and the
 // columns of TU and W' for them exactly zero, and P's rows for them are written as zeros (the
 // backward's dO^T P must not see them).
 #include <cuda.h>
