@@ -615,11 +615,13 @@ FWDBWD_WORKLOAD = "fwdbwd_t32k_hqk16_hv16"
 
 
 def sub_measure(name, args, dev, world, local, save):
-    """A sub-record of the line, measured as if alone.  Where a workload's buffers land in
-    device memory depends on what the process allocated before, and the training step's local
-    gradients ran ~6 % slower (and the forward ~2 % faster) after another workload in the same
-    process; so on one GPU each sub-record runs in a fresh child process (the same bench.py,
-    its JSON line parsed back).  Several ranks measure it in-process, as the ranks must."""
+    """A sub-record of the line, measured as if alone.  Kernels load on first use, so where a
+    kernel's code lands in device memory depends on what the process ran before; the training
+    step's local gradients once ran ~6 % slower after another workload in the same process (an
+    instruction-fetch effect, gone since that kernel's code was compacted).  On one GPU each
+    sub-record therefore still runs in a fresh child process (the same bench.py, its JSON line
+    parsed back), loading and allocating as it would alone.  Several ranks measure it
+    in-process, as the ranks must."""
     if world > 1:
         r = measure(name, args, dev, world, local, clocks=True, save=save)
         r["process"] = "in-process (ranks)"
