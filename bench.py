@@ -706,7 +706,10 @@ def measure(name, args, dev, world, local, clocks=True, save=False, fwd_kw=None)
             "frac": achieved / pk["hbm_gbs"], "peak_kind": pk_kind,
             "traffic": NCU_STEP_TRAFFIC.get(key),
             "algorithmic_bytes_per_step": by,
-            "bytes_counted": "+".join(step_tensors(w.backward)) + " (each read or written once)",
+            "bytes_counted": ("forward call: q+k+v+g+beta+h0 read, o+ht written; backward call: "
+                              "q+k+v+dO+g+beta+h0+dht read, dq+dk+dv+dg+dbeta+dh0 written "
+                              "(each once per call)") if w.backward else
+                             "+".join(step_tensors(False)) + " (each read or written once)",
             "algorithmic_flops_per_step": fl,
             "roofline_ms": max(t_tc, t_hbm) * 1000.0,
             "dominant_kernel": dom, "kernels": kernels}
